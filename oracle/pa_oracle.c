@@ -69,6 +69,21 @@ double oracle_half_to_double(uint16_t bits)
     return sign ? -mag : mag;
 }
 
+/* All 65536 binary16 values widened by oracle_half_to_double, filled once so
+ * that full-size checks finish in seconds; every lookup returns exactly what
+ * the function above returns. */
+static double g_half_table[1 << 16];
+static int g_half_table_ready = 0;
+
+static void fill_half_table(void)
+{
+    if (g_half_table_ready) return;
+    for (int i = 0; i < (1 << 16); ++i) g_half_table[i] = oracle_half_to_double((uint16_t)i);
+    g_half_table_ready = 1;
+}
+
+#define H2D(bits) (g_half_table[(bits)])
+
 typedef struct {
     const uint16_t *q, *k_cache, *v_cache;
     const int32_t *block_tables, *seq_lens;
@@ -119,7 +134,7 @@ static int scores_of(const oracle_problem* P, int b, int h, double* s)
         if (!k) return -2;
         double dot = 0.0;
         for (int d = 0; d < P->head_dim; ++d)
-            dot += oracle_half_to_double(qv[d]) * oracle_half_to_double(k[d]);
+            dot += H2D(qv[d]) * H2D(k[d]);
         s[t] = P->scale * dot;
     }
     return 0;
@@ -144,7 +159,7 @@ static int decode_one(const oracle_problem* P, int b, int h, double* out, double
         double w = exp(s[t] - M);
         const uint16_t* v = token_row(P, P->v_cache, b, g, t);
         denom += w;
-        for (int d = 0; d < D; ++d) out[d] += w * oracle_half_to_double(v[d]);
+        for (int d = 0; d < D; ++d) out[d] += w * H2D(v[d]);
     }
     for (int d = 0; d < D; ++d) out[d] /= denom;
     return 0;
@@ -156,6 +171,7 @@ static oracle_problem make_problem(const uint16_t* q, const uint16_t* k_cache, c
                                    int block_size, long long num_blocks, double scale)
 {
     oracle_problem P;
+    fill_half_table();
     P.q = q; P.k_cache = k_cache; P.v_cache = v_cache;
     P.block_tables = block_tables; P.seq_lens = seq_lens;
     P.num_seqs = num_seqs; P.max_blocks_per_seq = max_blocks_per_seq;
@@ -282,7 +298,7 @@ int oracle_partition_partials(double* m_out, double* l_out, double* acc_out, con
             for (int t = a; t < e; ++t) {
                 const uint16_t* v = token_row(&P, P.v_cache, b, g, t);
                 if (!v) { free(s); free(pv); free(p_tile); return -2; }
-                for (int d = 0; d < D; ++d) pv[d] += p_tile[t - a] * oracle_half_to_double(v[d]);
+                for (int d = 0; d < D; ++d) pv[d] += p_tile[t - a] * H2D(v[d]);
             }
             /* acc = acc * (alpha * l_i / l_new) + (beta / l_new) * (p @ V) */
             double keep = alpha * l_i / l_new;
