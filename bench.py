@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of split-KV paged-attention decode on GB300.
+
+A step is one decode call over the whole batch: the partition kernel and the
+log-sum-exp reduce, through the library's C ABI, with q, the K/V pool, the
+block tables and the sequence lengths already resident in HBM.  The default
+workload is the 100K-token long-context decode: batch 1, seq_len 102400
+(200 partitions of 512), 24 query / 4 kv heads, head_dim 256, block_size 16,
+fp16 N(0,1) data, scale 1/16; its 419 MB of K/V exceed the 129 MB L2, so
+back-to-back steps read from HBM.
+
+Prints one JSON line: KV-cache GB/s read (sum_b L_b * 4096 B per call / time),
+with the fraction of the measured HBM peak, calls/s, tokens/s, a roofline
+entry for the partition kernel, the float64 oracle timed on the host cores as
+a CPU baseline, an end-to-end figure through the public call with host
+buffers, and the SM clocks sampled during the timed region.
+
+`--impl reference` times the float64 CPU oracle on the same workload instead
+(the only reference implementation of this method).  Under torchrun the
+GPU arm runs one replica per rank (the path needs no exchange between GPUs:
+replicas only) and reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_cache_308_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode-attention KV-cache GB/s"
+DEFAULT_WORKLOAD = "b1_l102400"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic_partition_b1_l102400.json")
+KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_308_gb300", "csrc", "pa_kernels.cu")
+
+WORKLOAD_TEXT = {
+    "b1_l2048": "batch 1, seq_len 2048, heads 24/4, head_dim 256, block_size 16, partition 512",
+    "b8_u8192": "batch 8, seq_lens uniform [1, 8192], heads 24/4, head_dim 256, block_size 16, pool 8192 blocks",
+    "b4_l32768_peaked": "batch 4, seq_len 32768, 1% of keys x8, heads 24/4, head_dim 256, block_size 16, partition 512",
+    "b1_l102400": "batch 1, seq_len 102400 (200 partitions of 512), heads 24/4, head_dim 256, block_size 16",
+    "b64_loguniform": "batch 64, seq_lens log-uniform [16, 65536], heads 24/4, head_dim 256, block_size 16, "
+                      "pool 98304 blocks",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.CONFIG_NAMES)
+    ap.add_argument("--all-configs", action="store_true", help="also time the other four workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken during the timed region."""
+
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == 0:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        time.sleep(0.15)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((t, parts))
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.06 <= r[0] <= self.t1 + 0.06]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        mhz = [float(p[1]) for _, p in use if p[1].replace(".", "", 1).isdigit()]
+        mx = [float(p[2]) for _, p in use if p[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, p in use for n, v in zip(names, p[5:9]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(use), "in_region": bool(inside)}
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for p in (KERNEL_SRC, os.path.join(ROOT, "paged_kv_cache_308_gb300", "csrc", "pa_internal.h")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per partition-kernel launch from the committed ncu summary,
+    or None when the kernel source changed since it was captured."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+        if d.get("kernel_sha") == kernel_hash() and d.get("workload") == workload:
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def host_bits(t):
+    import numpy as np
+    a = t.detach().cpu().contiguous().numpy()
+    return a.view(np.uint16) if a.dtype == np.float16 else a
+
+
+def cpu_baseline(w, budget_s: float):
+    """The float64 oracle as it stands, on the host cores, over whole decode
+    calls of the workload: repeated until `budget_s` of work (at least one)."""
+    import oracle
+    q, k, v = host_bits(w.q), host_bits(w.k_cache), host_bits(w.v_cache)
+    bt, sl = host_bits(w.block_tables), host_bits(w.seq_lens)
+    cores = os.cpu_count() or 1
+    oracle.build()
+    calls = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.paged_decode(q, k, v, bt, sl, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, w.scale,
+                            threads=cores)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (calls >= 1 and el * (calls + 1) / calls > 3 * budget_s):
+            break
+    gbs = w.kv_bytes * calls / el / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{calls} whole decode call(s) of {w.name} ({w.total_tokens} tokens, {w.num_heads} heads), "
+                      f"{el:.1f} s, float64, OpenMP over (seq, head) pairs"}, calls / el
+
+
+def time_steps(fn, steps, stream):
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        fn()
+    e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e) / 1e3
+
+
+def run_reference(args):
+    """The float64 oracle on the host cores.  Each step is a bounded sample of
+    the workload: every (sequence, head) pair over the first L' tokens of its
+    sequence, L' calibrated so that the whole run ends within a few minutes;
+    the step is credited with the K/V bytes of those tokens (4096 B each)."""
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    w = W.make_config(args.workload, device="cpu", seed=args.seed)
+    oracle.build()
+    q, k, v = host_bits(w.q), host_bits(w.k_cache), host_bits(w.v_cache)
+    bt = host_bits(w.block_tables)
+    lens = np.array(w.seq_lens_host, dtype=np.int32)
+    cores = os.cpu_count() or 1
+    per_token = w.num_kv_heads * w.head_dim * 2 * 2
+
+    def call(cap):
+        sl = np.minimum(lens, cap).astype(np.int32)
+        oracle.paged_decode(q, k, v, bt, sl, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, w.scale,
+                            threads=cores)
+        return int(sl.sum())
+
+    target = max(0.002, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    cap, t = 16, 0.0
+    while cap < int(lens.max()):
+        t0 = time.perf_counter()
+        call(cap)
+        t = time.perf_counter() - t0
+        if t >= target:
+            break
+        cap = min(int(lens.max()), cap * 2)
+    if t > target and cap > 16:
+        cap = max(16, int(cap * target / t))
+    for _ in range(args.warmup):
+        call(cap)
+    tokens = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        tokens += call(cap)
+    el = time.perf_counter() - t0
+    gbs = tokens * per_token / el / 1e9
+    sample = (f"each step: all {w.num_seqs}x{w.num_heads} (seq, head) pairs of {args.workload} over the first "
+              f"{cap} tokens of each sequence ({tokens // max(1, args.steps)} of {w.total_tokens} cache tokens), "
+              f"float64, OpenMP over pairs")
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}", "parallelism": "none (CPU)"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (use --impl reference for the CPU oracle)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    from paged_kv_cache_308_gb300 import binding as pb
+
+    w = W.make_config(args.workload, device=dev, seed=args.seed)
+    out = torch.empty_like(w.q)
+    stream = torch.cuda.current_stream()
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len)
+    launches_per_step = 1 + plan["launch_reduce"]
+
+    def step():
+        pb.pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
+                     w.head_dim, w.block_size, w.scale, stream, max_seq_len=w.max_seq_len)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler.mark(0)
+    elapsed = time_steps(step, args.steps, stream)
+    torch.cuda.synchronize()
+    sampler.mark(1)
+    if pg:
+        pg.barrier()
+    sampler.stop()
+    if pg:
+        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed = float(t.item())
+    assert pb.pa_get_device_status() == 0
+
+    peak, peak_kind = hbm_peak()
+    kv = w.kv_bytes
+    value = world * kv * args.steps / elapsed / 1e9
+    per_gpu = kv * args.steps / elapsed / 1e9
+
+    # roofline: the partition kernel alone, timed by events the library records
+    # on this stream around its launch
+    ws = pb.alloc_workspace(plan, dev)
+    nrep = max(20, min(args.steps, 500))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
+    for e0, e1 in evs:
+        pb.pa_decode_ex(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
+                        w.head_dim, w.block_size, w.scale, stream, max_seq_len=w.max_seq_len, workspace=ws,
+                        events=(e0, e1))
+    torch.cuda.synchronize()
+    part_s = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+    achieved = kv / part_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(args.workload), "kernel": "pa_partition_kernel<256>",
+                "algorithmic_bytes_per_launch": kv, "launch_us": part_s * 1e6,
+                "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)"}
+
+    # end to end through the public call with host buffers: per step the step's
+    # inputs (q, block tables, sequence lengths) go host->device from pinned
+    # memory and the output comes back; the K/V cache stays resident in HBM.
+    h_q = w.q.cpu().pin_memory()
+    h_bt = w.block_tables.cpu().pin_memory()
+    h_sl = w.seq_lens.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+    def e2e_step():
+        w.q.copy_(h_q, non_blocking=True)
+        w.block_tables.copy_(h_bt, non_blocking=True)
+        w.seq_lens.copy_(h_sl, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(10, min(args.steps, 2000))
+    e2e_el = time_steps(e2e_step, e2e_steps, stream)
+    torch.cuda.synchronize()
+    e2e = {"value": world * kv * e2e_steps / e2e_el / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": h_q.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4,
+           "d2h_bytes_per_step": h_out.numel() * 2, "ms_per_step": e2e_el / e2e_steps * 1e3}
+
+    per_config = None
+    if args.all_configs and rank == 0:
+        per_config = {}
+        for name in W.CONFIG_NAMES:
+            if name == args.workload:
+                continue
+            wc = W.make_config(name, device=dev, seed=args.seed)
+            oc = torch.empty_like(wc.q)
+            fn = lambda: pb.pa_decode(oc, wc.q, wc.k_cache, wc.v_cache, wc.block_tables, wc.seq_lens,
+                                      wc.num_heads, wc.num_kv_heads, wc.head_dim, wc.block_size, wc.scale, stream,
+                                      max_seq_len=wc.max_seq_len)
+            for _ in range(20):
+                fn()
+            torch.cuda.synchronize()
+            n = 500
+            el = time_steps(fn, n, stream)
+            per_config[name] = {"kv_bytes": wc.kv_bytes, "us_per_call": el / n * 1e6,
+                                "GB_per_s": wc.kv_bytes * n / el / 1e9,
+                                "pct_of_hbm_peak": 100 * wc.kv_bytes * n / el / 1e9 / peak,
+                                "calls_per_s": n / el, "tokens_per_s": wc.num_seqs * n / el,
+                                "l2": "larger than L2" if wc.kv_bytes > 129e6 else "fits in L2 (warm)"}
+            del wc, oc
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu, _ = cpu_baseline(W.make_config(args.workload, device="cpu", seed=args.seed), args.cpu_seconds)
+
+    if rank == 0:
+        clocks = sampler.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
+                       "kv_bytes_per_step": kv, "tokens_in_cache": w.total_tokens,
+                       "mode": "split" if plan["launch_reduce"] else "single",
+                       "partition_size": plan["partition_size"],
+                       "l2": f"inputs larger than L2 ({kv / 1e6:.0f} MB of K/V vs 129 MB L2), no flush",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_hbm_peak": 100 * per_gpu / peak,
+            "calls_per_s": world * args.steps / elapsed,
+            "tokens_per_s": world * w.num_seqs * args.steps / elapsed,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        if per_config is not None:
+            line["per_config"] = per_config
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,181 @@
+/*
+ * pa_decode.h -- C ABI of the GB300 (sm_103a) paged-attention decode library.
+ *
+ * One decode call: every sequence b contributes one query token per query
+ * head h, which attends over the first seq_lens[b] tokens of its K/V, stored
+ * in a paged pool and found through the block table:
+ *
+ *     out[b, h, :] = softmax(scale * q[b, h, :] . K_b^T) V_b
+ *     token t of sequence b: physical block block_tables[b][t / block_size],
+ *                            slot t % block_size
+ *     query head h reads kv head  h / (num_heads / num_kv_heads)
+ *
+ * Method (split-KV, "V2"): the tokens of a sequence are cut into partitions;
+ * one CTA per (partition, kv head, sequence) loads each K/V block of its
+ * partition once for all query heads of the GQA group and produces the
+ * online-softmax partial (max score, exp sum, weighted V); a second kernel
+ * merges the partials of each (sequence, head) by a log-sum-exp reduce.
+ * Sources: "docs" commit page (GQA-aware grid on kv heads; Phase 1 partition
+ * kernel, Phase 2 reduce kernel; the compound partial), the
+ * "paged_attention_v2_triton.py" commit page (alpha/beta online-softmax
+ * update), the "qwen3_6_scripts/paged_attn.py" commit page (decode dispatch
+ * between a single-pass and a partitioned kernel by sequence length;
+ * allocate-once buffer reuse).
+ *
+ * Layouts (all row-major, contiguous):
+ *   q, out         fp16 [num_seqs][num_heads][head_dim]
+ *   k_cache,
+ *   v_cache        fp16 [num_blocks][num_kv_heads][block_size][head_dim]
+ *                  (one (block, kv head) is block_size*head_dim contiguous
+ *                  halves; the pages do not print a layout, this is the
+ *                  library's choice)
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                  ceil(seq_lens[b] / block_size) are never read
+ *   seq_lens       int32 [num_seqs]
+ * Every pointer argument named above is a DEVICE pointer; out, q, k_cache and
+ * v_cache must be 16-byte aligned, block_tables and seq_lens 4-byte aligned.
+ *
+ * Supported: head_dim in {64, 128, 256}; block_size 16; num_heads a multiple
+ * of num_kv_heads with a GQA ratio of 1..8.  Other shapes return
+ * PA_ERR_UNSUPPORTED.
+ *
+ * Ownership: the caller owns every buffer it passes and orders it with
+ * `stream`; the library never frees caller memory.  Calls are asynchronous on
+ * `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *
+ * Errors: functions return PA_OK (0) or a negative pa_status; nothing is
+ * printed and nothing aborts.  Problems only the device can see (a block id
+ * outside [0, num_blocks), a sequence length above max_seq_len or above
+ * max_blocks_per_seq * block_size, a wait that gave up) set bits of a
+ * per-device status word read by pa_get_device_status(); the affected outputs
+ * are then unspecified, and no kernel traps.
+ */
+#ifndef PA_DECODE_H
+#define PA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t; /* same type as cudaStream_t */
+
+/* Return codes. */
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,  /* null or misaligned pointer, bad size, non-finite scale, ... */
+    PA_ERR_UNSUPPORTED = -2,  /* head_dim, block_size or GQA ratio not compiled in */
+    PA_ERR_CUDA = -3,         /* a CUDA runtime call or a kernel launch failed */
+    PA_ERR_OOM = -4,          /* the library-owned workspace could not be allocated */
+    PA_ERR_WORKSPACE = -5     /* caller workspace too small or not 256-byte aligned */
+};
+
+/* Bits of the device status word (pa_get_device_status). */
+enum {
+    PA_DEV_BAD_BLOCK_ID = 1,  /* a block id read from block_tables was outside [0, num_blocks) */
+    PA_DEV_BAD_SEQ_LEN = 2,   /* seq_lens[b] < 0, > max_seq_len or > max_blocks_per_seq*block_size */
+    PA_DEV_TIMEOUT = 4        /* a shared-memory copy wait gave up (bounded wait, see opts.wait_limit) */
+};
+
+/* Execution modes. */
+enum {
+    PA_MODE_AUTO = 0,   /* library picks SINGLE or SPLIT from the sizes (see pa_decode_plan) */
+    PA_MODE_SINGLE = 1, /* one CTA per (kv head, sequence) covers the whole sequence; no reduce */
+    PA_MODE_SPLIT = 2   /* partitions of partition_size tokens + log-sum-exp reduce */
+};
+
+/* Option flags. */
+enum {
+    PA_FLAG_FORCE_TIMEOUT = 1 /* test hook: every copy wait gives up before its first poll; the
+                                 kernel then drains its copies, sets PA_DEV_TIMEOUT and returns */
+};
+
+/* All inputs of one decode call (device pointers; see the layouts above). */
+typedef struct {
+    void* out;
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    int num_seqs;           /* 0..65535 */
+    int max_blocks_per_seq; /* row stride of block_tables */
+    int max_seq_len;        /* host-side bound, >= every seq_lens[b]; sizes the grid */
+    int64_t num_blocks;     /* blocks in the pool; num_blocks*num_kv_heads*block_size < 2^31 */
+    int num_heads;
+    int num_kv_heads;
+    int head_dim;
+    int block_size;
+    float scale;            /* multiplies q.k before the softmax (finite) */
+} pa_decode_args;
+
+/* Tuning and debug options; an all-zero struct means "defaults". */
+typedef struct {
+    int mode;                    /* PA_MODE_* */
+    int partition_size;          /* tokens per partition in SPLIT mode, multiple of block_size; 0 = 512 */
+    int flags;                   /* PA_FLAG_* */
+    unsigned int wait_limit;     /* polls before a copy wait gives up; 0 = library default (2^20) */
+    void* event_partition_begin; /* optional cudaEvent_t recorded on `stream` right before ... */
+    void* event_partition_end;   /* ... and right after the partition kernel (timing only) */
+} pa_decode_opts;
+
+/* What a call will launch (filled by pa_decode_plan; host-only, no CUDA calls). */
+typedef struct {
+    int mode;              /* PA_MODE_SINGLE or PA_MODE_SPLIT */
+    int partition_size;    /* tokens per CTA (SINGLE: max_seq_len rounded up to block_size) */
+    int grid_x, grid_y, grid_z;          /* partition kernel: partitions, kv heads, sequences */
+    int threads;           /* threads per partition CTA */
+    int smem_bytes;        /* dynamic shared memory per partition CTA */
+    int launch_reduce;     /* 1 if the reduce kernel runs */
+    int reduce_grid_x, reduce_grid_y, reduce_grid_z; /* heads, sequences, head_dim/64 */
+    size_t workspace_bytes; /* caller workspace pa_decode_ex needs (0 when no reduce) */
+} pa_decode_plan_t;
+
+/* Decode attention with a library-owned workspace.
+ * The workspace for the partials is cached per device and grown on demand
+ * (allocate once, reuse across calls); growing it synchronises the device, so
+ * the first call with a larger size must not be inside a stream capture, and
+ * calls on different streams that overlap in time share (and race on) it.
+ * num_blocks is the pool size (k_cache.shape[0]); it bounds the block ids the
+ * kernel will follow. */
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+              int max_blocks_per_seq, int max_seq_len, int64_t num_blocks, int num_heads,
+              int num_kv_heads, int head_dim, int block_size, float scale, pa_stream_t stream);
+
+/* Decode attention with caller-owned workspace (device memory, 256-byte
+ * aligned, at least plan.workspace_bytes; may be NULL when that is 0).
+ * Allocates nothing, so it can be captured in a CUDA graph.  opts may be NULL. */
+int pa_decode_ex(const pa_decode_args* args, const pa_decode_opts* opts, void* workspace,
+                 size_t workspace_bytes, pa_stream_t stream);
+
+/* Validate the arguments and fill *plan with the launches a call would make.
+ * num_sms > 0 is the SM count to plan for; 0 asks the current device.  Pure
+ * host logic when num_sms > 0.  Returns the same codes a call would. */
+int pa_decode_plan(const pa_decode_args* args, const pa_decode_opts* opts, int num_sms,
+                   pa_decode_plan_t* plan);
+
+/* Workspace bytes of a SPLIT call with these sizes (an upper bound for AUTO). */
+size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim,
+                                int partition_size);
+
+/* Synchronise `stream`, then read and clear the current device's status word
+ * into *status (PA_DEV_* bits).  Returns PA_OK or PA_ERR_CUDA. */
+int pa_get_device_status(pa_stream_t stream, int* status);
+
+/* Static English text for a return code. */
+const char* pa_status_string(int status);
+
+/* Free the library-owned workspaces of every device (synchronises them). */
+void pa_release_workspace(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_DECODE_H */

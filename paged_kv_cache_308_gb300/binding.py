@@ -1,0 +1,248 @@
+"""ctypes binding of libpa_decode.so (include/pa_decode.h), same names as the C ABI.
+
+Argument marshalling only: every step of the decode runs in the library's
+CUDA kernels.  Tensors are torch tensors on the GPU; their device pointers,
+sizes and the current CUDA stream are handed to the C functions.  If the
+shared library is missing the import of this module fails loudly -- there is
+no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpa_decode.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "pa_decode.h")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = -1
+PA_ERR_UNSUPPORTED = -2
+PA_ERR_CUDA = -3
+PA_ERR_OOM = -4
+PA_ERR_WORKSPACE = -5
+
+PA_DEV_BAD_BLOCK_ID = 1
+PA_DEV_BAD_SEQ_LEN = 2
+PA_DEV_TIMEOUT = 4
+
+PA_MODE_AUTO = 0
+PA_MODE_SINGLE = 1
+PA_MODE_SPLIT = 2
+MODES = {"auto": PA_MODE_AUTO, "single": PA_MODE_SINGLE, "split": PA_MODE_SPLIT}
+
+PA_FLAG_FORCE_TIMEOUT = 1
+
+
+class pa_decode_args(ctypes.Structure):
+    _fields_ = [
+        ("out", ctypes.c_void_p), ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p),
+        ("v_cache", ctypes.c_void_p), ("block_tables", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+        ("num_seqs", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int), ("max_seq_len", ctypes.c_int),
+        ("num_blocks", ctypes.c_int64), ("num_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int), ("scale", ctypes.c_float),
+    ]
+
+
+class pa_decode_opts(ctypes.Structure):
+    _fields_ = [
+        ("mode", ctypes.c_int), ("partition_size", ctypes.c_int), ("flags", ctypes.c_int),
+        ("wait_limit", ctypes.c_uint), ("event_partition_begin", ctypes.c_void_p),
+        ("event_partition_end", ctypes.c_void_p),
+    ]
+
+
+class pa_decode_plan_t(ctypes.Structure):
+    _fields_ = [
+        ("mode", ctypes.c_int), ("partition_size", ctypes.c_int), ("grid_x", ctypes.c_int),
+        ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int), ("threads", ctypes.c_int),
+        ("smem_bytes", ctypes.c_int), ("launch_reduce", ctypes.c_int), ("reduce_grid_x", ctypes.c_int),
+        ("reduce_grid_y", ctypes.c_int), ("reduce_grid_z", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class PaDecodeError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})" if what else f"{status_string(code)} ({code})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_308_gb300.build` "
+                          "(or __graft_entry__.build()); there is no fallback implementation")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    lib.pa_decode.restype = i32
+    lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, i32, i32, i32, f32, vp]
+    lib.pa_decode_ex.restype = i32
+    lib.pa_decode_ex.argtypes = [ctypes.POINTER(pa_decode_args), ctypes.POINTER(pa_decode_opts), vp,
+                                 ctypes.c_size_t, vp]
+    lib.pa_decode_plan.restype = i32
+    lib.pa_decode_plan.argtypes = [ctypes.POINTER(pa_decode_args), ctypes.POINTER(pa_decode_opts), i32,
+                                   ctypes.POINTER(pa_decode_plan_t)]
+    lib.pa_decode_workspace_size.restype = ctypes.c_size_t
+    lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.pa_get_device_status.restype = i32
+    lib.pa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_status_string.argtypes = [i32]
+    lib.pa_release_workspace.restype = None
+    lib.pa_release_workspace.argtypes = []
+    lib.pa_version.restype = i32
+    lib.pa_version.argtypes = []
+    return lib
+
+
+lib = _load()
+
+
+def header_functions() -> list:
+    """Names of the functions include/pa_decode.h declares."""
+    text = open(HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def status_string(code: int) -> str:
+    return lib.pa_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return lib.pa_version()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def make_args(out, q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_kv_heads, head_dim,
+              block_size, scale, max_seq_len) -> pa_decode_args:
+    return pa_decode_args(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens),
+        int(seq_lens.shape[0]), int(block_tables.shape[1]) if block_tables.dim() == 2 else 0,
+        int(max_seq_len), int(k_cache.shape[0]), int(num_heads), int(num_kv_heads), int(head_dim),
+        int(block_size), float(scale))
+
+
+def make_opts(mode="auto", partition_size: int = 0, flags: int = 0, wait_limit: int = 0,
+              events=None) -> pa_decode_opts:
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    ev0 = ev1 = None
+    if events is not None:
+        ev0, ev1 = (e.cuda_event if hasattr(e, "cuda_event") else e for e in events)
+    return pa_decode_opts(m, int(partition_size), int(flags), int(wait_limit), ev0, ev1)
+
+
+def _check_tensors(out, q, k_cache, v_cache, block_tables, seq_lens):
+    for name, t, dt in (("out", out, torch.float16), ("q", q, torch.float16), ("k_cache", k_cache, torch.float16),
+                        ("v_cache", v_cache, torch.float16), ("block_tables", block_tables, torch.int32),
+                        ("seq_lens", seq_lens, torch.int32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_kv_heads, head_dim,
+              block_size, scale, stream=None, *, max_seq_len: int) -> None:
+    """The library-owned-workspace call; raises PaDecodeError on a non-zero code."""
+    _check_tensors(out, q, k_cache, v_cache, block_tables, seq_lens)
+    rc = lib.pa_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                       block_tables.data_ptr(), seq_lens.data_ptr(), int(seq_lens.shape[0]),
+                       int(block_tables.shape[1]), int(max_seq_len), int(k_cache.shape[0]), int(num_heads),
+                       int(num_kv_heads), int(head_dim), int(block_size), float(scale), _stream_handle(stream))
+    if rc != PA_OK:
+        raise PaDecodeError(rc, "pa_decode")
+
+
+def pa_decode_plan(out, q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_kv_heads, head_dim,
+                   block_size, scale, *, max_seq_len: int, num_sms: int = 0, **opt) -> dict:
+    args = make_args(out, q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_kv_heads, head_dim,
+                     block_size, scale, max_seq_len)
+    plan = pa_decode_plan_t()
+    rc = lib.pa_decode_plan(ctypes.byref(args), ctypes.byref(make_opts(**opt)), int(num_sms), ctypes.byref(plan))
+    if rc != PA_OK:
+        raise PaDecodeError(rc, "pa_decode_plan")
+    return plan.as_dict()
+
+
+def pa_decode_ex(out, q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_kv_heads, head_dim,
+                 block_size, scale, stream=None, *, max_seq_len: int, workspace: Optional[torch.Tensor] = None,
+                 **opt) -> None:
+    """Caller-workspace call (graph-capturable).  `workspace` is a uint8 CUDA tensor or None."""
+    _check_tensors(out, q, k_cache, v_cache, block_tables, seq_lens)
+    args = make_args(out, q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_kv_heads, head_dim,
+                     block_size, scale, max_seq_len)
+    opts = make_opts(**opt)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.pa_decode_ex(ctypes.byref(args), ctypes.byref(opts), ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != PA_OK:
+        raise PaDecodeError(rc, "pa_decode_ex")
+
+
+def alloc_workspace(plan: dict, device) -> Optional[torch.Tensor]:
+    """A device buffer of plan['workspace_bytes'] (256-byte aligned by the caching allocator)."""
+    n = int(plan["workspace_bytes"])
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def pa_decode_workspace_size(num_seqs, max_seq_len, num_heads, head_dim, partition_size=0) -> int:
+    return lib.pa_decode_workspace_size(int(num_seqs), int(max_seq_len), int(num_heads), int(head_dim),
+                                        int(partition_size))
+
+
+def pa_get_device_status(stream=None) -> int:
+    st = ctypes.c_int(0)
+    rc = lib.pa_get_device_status(_stream_handle(stream), ctypes.byref(st))
+    if rc != PA_OK:
+        raise PaDecodeError(rc, "pa_get_device_status")
+    return st.value
+
+
+def pa_status_string(code: int) -> str:
+    return status_string(code)
+
+
+def pa_release_workspace() -> None:
+    lib.pa_release_workspace()
+
+
+def pa_version() -> int:
+    return lib.pa_version()
+
+
+def decode_workload(w, out: Optional[torch.Tensor] = None, stream=None, **opt) -> torch.Tensor:
+    """Run one decode call on a workloads.Workload (tensors already on the GPU)."""
+    if out is None:
+        out = torch.empty_like(w.q)
+    if opt:
+        plan = pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                              w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len, **opt)
+        ws = alloc_workspace(plan, w.q.device)
+        if ws is not None and stream is not None:
+            ws.record_stream(stream)  # keep the buffer alive until that stream's work is done
+        pa_decode_ex(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
+                     w.head_dim, w.block_size, w.scale, stream, max_seq_len=w.max_seq_len, workspace=ws, **opt)
+    else:
+        pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
+                  w.head_dim, w.block_size, w.scale, stream, max_seq_len=w.max_seq_len)
+    return out

@@ -1,0 +1,329 @@
+// C-ABI layer of the paged-attention decode library: argument validation,
+// host dispatch (single-pass vs split-KV), the cached workspace, tensor maps
+// and kernel launches.  The public contract is include/pa_decode.h.
+//
+// Dispatch follows the decode dispatch of the "qwen3_6_scripts/paged_attn.py"
+// commit page (a single-CTA kernel for short sequences, the partitioned kernel
+// plus a reduce for long ones); the thresholds are this library's own, set
+// from GB300 measurements rather than the page's 8192-token rule.  The cached
+// workspace follows that page's allocate-once, reuse-across-calls advice.
+#include "pa_decode.h"
+
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace {
+
+constexpr int kDefaultPartition = 512;
+constexpr int kMaxDevices = 64;
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t split_workspace_bytes(long long num_seqs, long long num_heads, long long max_partitions, long long head_dim) {
+    if (max_partitions <= 1) return 0;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_heads * max_partitions;
+    return align_up(rows * 4, kWsAlign) * 2 + align_up(rows * head_dim * 4, kWsAlign);
+}
+
+int query_sm_count(int* num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+int validate(const pa_decode_args* a, const pa_decode_opts* o) {
+    if (!a) return PA_ERR_INVALID_ARG;
+    if (a->num_seqs < 0 || a->num_seqs > 65535) return PA_ERR_INVALID_ARG;
+    if (a->num_heads <= 0 || a->num_kv_heads <= 0 || a->head_dim <= 0 || a->block_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (a->num_heads % a->num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (!isfinite(a->scale)) return PA_ERR_INVALID_ARG;
+    if (a->max_seq_len < 0 || a->max_blocks_per_seq < 0 || a->num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (o && (o->mode < PA_MODE_AUTO || o->mode > PA_MODE_SPLIT)) return PA_ERR_INVALID_ARG;
+    if (o && o->partition_size < 0) return PA_ERR_INVALID_ARG;
+    if (o && o->partition_size % a->block_size) return PA_ERR_INVALID_ARG;
+    if (a->head_dim != 64 && a->head_dim != 128 && a->head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (a->block_size != pa::kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (a->num_heads / a->num_kv_heads > pa::kMaxGroup) return PA_ERR_UNSUPPORTED;
+    // the grid must cover every sequence the block table can describe
+    if ((long long)a->max_seq_len > (long long)a->max_blocks_per_seq * a->block_size) return PA_ERR_INVALID_ARG;
+    // TMA row coordinates are 32-bit
+    if (a->num_blocks * a->num_kv_heads * a->block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    if (a->num_seqs == 0) return PA_OK;
+    if (!a->out || !a->q || !a->k_cache || !a->v_cache || !a->block_tables || !a->seq_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned(a->out, 16) || !aligned(a->q, 16) || !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) ||
+        !aligned(a->block_tables, 4) || !aligned(a->seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (a->num_blocks == 0 && a->max_seq_len > 0) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_decode_plan_t* plan) {
+    int rc = validate(a, o);
+    if (rc) return rc;
+    memset(plan, 0, sizeof(*plan));
+    const int bs = a->block_size;
+    const int part = (o && o->partition_size > 0) ? o->partition_size : kDefaultPartition;
+    const int split_parts = (a->max_seq_len + part - 1) / part;
+    int mode = o ? o->mode : PA_MODE_AUTO;
+    if (mode == PA_MODE_AUTO) {
+        // A sequence that fits one partition needs no reduce.  Otherwise split:
+        // with few (sequence, kv head) pairs a single-pass grid leaves most of
+        // the SMs idle, and with many its time is set by the longest sequence.
+        (void)num_sms;
+        mode = split_parts <= 1 ? PA_MODE_SINGLE : PA_MODE_SPLIT;
+    }
+    plan->mode = mode;
+    if (mode == PA_MODE_SINGLE) {
+        const int whole = ((a->max_seq_len + bs - 1) / bs) * bs;
+        plan->partition_size = whole > 0 ? whole : bs;
+        plan->grid_x = 1;
+    } else {
+        plan->partition_size = part;
+        plan->grid_x = split_parts > 0 ? split_parts : 1;
+    }
+    plan->grid_y = a->num_kv_heads;
+    plan->grid_z = a->num_seqs;
+    plan->threads = pa::kWarps * 32;
+    plan->smem_bytes = pa::partition_smem_bytes(a->head_dim);
+    plan->launch_reduce = (mode == PA_MODE_SPLIT && plan->grid_x > 1) ? 1 : 0;
+    if (plan->launch_reduce) {
+        plan->reduce_grid_x = a->num_heads;
+        plan->reduce_grid_y = a->num_seqs;
+        plan->reduce_grid_z = a->head_dim / pa::kReduceSlice;
+        plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->grid_x, a->head_dim);
+    }
+    return PA_OK;
+}
+
+// cuTensorMapEncodeTiled, reached through the runtime so the library needs no
+// link-time dependency on the driver (it still loads on machines without one).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// A cache viewed as a 2-D tensor of (num_blocks * num_kv_heads * block_size)
+// rows by head_dim halves; a box is block_size rows by 64 halves (128 bytes),
+// stored with the 128-byte swizzle.  Rows past the pool read as zero.
+int make_cache_map(CUtensorMap* map, const void* base, const pa_decode_args* a) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PA_ERR_CUDA;
+    const cuuint64_t rows = static_cast<cuuint64_t>(a->num_blocks) * a->num_kv_heads * a->block_size;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(a->head_dim), rows > 0 ? rows : 1};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(a->head_dim) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(a->block_size)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_bytes, cudaStream_t stream,
+        const pa_decode_plan_t& plan) {
+    if (a->num_seqs == 0) return PA_OK;
+    if (plan.workspace_bytes > 0 && (!ws || ws_bytes < plan.workspace_bytes || !aligned(ws, kWsAlign)))
+        return PA_ERR_WORKSPACE;
+
+    CUtensorMap tk, tv;
+    int rc = make_cache_map(&tk, a->k_cache, a);
+    if (rc) return rc;
+    rc = make_cache_map(&tv, a->v_cache, a);
+    if (rc) return rc;
+
+    const size_t rows = static_cast<size_t>(a->num_seqs) * a->num_heads * plan.grid_x;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    pa::PartitionParams prm;
+    prm.out = static_cast<__half*>(a->out);
+    prm.q = static_cast<const __half*>(a->q);
+    prm.block_tables = a->block_tables;
+    prm.seq_lens = a->seq_lens;
+    prm.max_logits = plan.launch_reduce ? reinterpret_cast<float*>(w) : nullptr;
+    prm.exp_sums = plan.launch_reduce ? reinterpret_cast<float*>(w + align_up(rows * 4, kWsAlign)) : nullptr;
+    prm.tmp_out = plan.launch_reduce ? reinterpret_cast<float*>(w + 2 * align_up(rows * 4, kWsAlign)) : nullptr;
+    prm.num_blocks = a->num_blocks;
+    prm.num_heads = a->num_heads;
+    prm.num_kv_heads = a->num_kv_heads;
+    prm.group = a->num_heads / a->num_kv_heads;
+    prm.max_blocks_per_seq = a->max_blocks_per_seq;
+    prm.max_seq_len = a->max_seq_len;
+    prm.partition_size = plan.partition_size;
+    prm.max_partitions = plan.grid_x;
+    prm.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+    prm.wait_limit = (o && o->wait_limit) ? o->wait_limit : pa::kDefaultWaitLimit;
+    prm.force_timeout = (o && (o->flags & PA_FLAG_FORCE_TIMEOUT)) ? 1 : 0;
+
+    if (o && o->event_partition_begin &&
+        cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_begin), stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (pa::launch_partition(a->head_dim, prm, tk, tv, dim3(plan.grid_x, plan.grid_y, plan.grid_z), stream) !=
+        cudaSuccess)
+        return PA_ERR_CUDA;
+    if (o && o->event_partition_end &&
+        cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_end), stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (plan.launch_reduce) {
+        pa::ReduceParams rp;
+        rp.out = prm.out;
+        rp.max_logits = prm.max_logits;
+        rp.exp_sums = prm.exp_sums;
+        rp.tmp_out = prm.tmp_out;
+        rp.seq_lens = a->seq_lens;
+        rp.num_heads = a->num_heads;
+        rp.max_blocks_per_seq = a->max_blocks_per_seq;
+        rp.max_seq_len = a->max_seq_len;
+        rp.partition_size = plan.partition_size;
+        rp.max_partitions = plan.grid_x;
+        if (pa::launch_reduce(a->head_dim, rp, dim3(plan.reduce_grid_x, plan.reduce_grid_y, plan.reduce_grid_z),
+                              stream) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+// Library-owned workspace, one per device, grown on demand.
+std::mutex g_ws_mutex;
+void* g_ws[kMaxDevices];
+size_t g_ws_bytes[kMaxDevices];
+
+int ensure_workspace(size_t need, void** out) {
+    *out = nullptr;
+    if (need == 0) return PA_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    if (g_ws_bytes[dev] < need) {
+        if (g_ws[dev]) {
+            // earlier calls may still read the old buffer
+            if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+            cudaFree(g_ws[dev]);
+            g_ws[dev] = nullptr;
+            g_ws_bytes[dev] = 0;
+        }
+        const size_t grow = align_up(need + need / 4, 1 << 20);
+        if (cudaMalloc(&g_ws[dev], grow) != cudaSuccess) {
+            cudaGetLastError();
+            g_ws[dev] = nullptr;
+            return PA_ERR_OOM;
+        }
+        g_ws_bytes[dev] = grow;
+    }
+    *out = g_ws[dev];
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode_plan(const pa_decode_args* args, const pa_decode_opts* opts, int num_sms, pa_decode_plan_t* plan) {
+    if (!plan || num_sms < 0) return PA_ERR_INVALID_ARG;
+    if (num_sms == 0) {
+        int rc = query_sm_count(&num_sms);
+        if (rc) return rc;
+    }
+    return make_plan(args, opts, num_sms, plan);
+}
+
+int pa_decode_ex(const pa_decode_args* args, const pa_decode_opts* opts, void* workspace, size_t workspace_bytes,
+                 pa_stream_t stream) {
+    pa_decode_plan_t plan;
+    int rc = make_plan(args, opts, 0, &plan);
+    if (rc) return rc;
+    return run(args, opts, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), plan);
+}
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq, int max_seq_len, int64_t num_blocks,
+              int num_heads, int num_kv_heads, int head_dim, int block_size, float scale, pa_stream_t stream) {
+    pa_decode_args a;
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.max_seq_len = max_seq_len;
+    a.num_blocks = num_blocks;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.scale = scale;
+    pa_decode_plan_t plan;
+    int rc = make_plan(&a, nullptr, 0, &plan);
+    if (rc) return rc;
+    void* ws = nullptr;
+    rc = ensure_workspace(plan.workspace_bytes, &ws);
+    if (rc) return rc;
+    return run(&a, nullptr, ws, plan.workspace_bytes, reinterpret_cast<cudaStream_t>(stream), plan);
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim, int partition_size) {
+    if (num_seqs <= 0 || max_seq_len <= 0 || num_heads <= 0 || head_dim <= 0) return 0;
+    const int part = partition_size > 0 ? partition_size : kDefaultPartition;
+    return split_workspace_bytes(num_seqs, num_heads, (max_seq_len + part - 1) / part, head_dim);
+}
+
+int pa_get_device_status(pa_stream_t stream, int* status) {
+    if (!status) return PA_ERR_INVALID_ARG;
+    return pa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), status) == cudaSuccess ? PA_OK
+                                                                                                      : PA_ERR_CUDA;
+}
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape (head_dim, block_size or GQA ratio)";
+        case PA_ERR_CUDA: return "CUDA runtime error or launch failure";
+        case PA_ERR_OOM: return "workspace allocation failed";
+        case PA_ERR_WORKSPACE: return "workspace too small or misaligned";
+        default: return "unknown status";
+    }
+}
+
+void pa_release_workspace(void) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    int cur = 0;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (!g_ws[d]) continue;
+        if (cudaSetDevice(d) == cudaSuccess) {
+            cudaDeviceSynchronize();
+            cudaFree(g_ws[d]);
+        }
+        g_ws[d] = nullptr;
+        g_ws_bytes[d] = 0;
+    }
+    if (have_cur) cudaSetDevice(cur);
+}
+
+int pa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// Internal interface between the C-ABI layer (pa_api.cpp) and the kernels
+// (pa_kernels.cu).  Not installed; the public interface is include/pa_decode.h.
+#pragma once
+
+#include <cuda.h>          // CUtensorMap (header only; the driver is reached at run time)
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kBlockSize = 16;    // tokens per KV block (one MMA M-tile of tokens)
+constexpr int kWarps = 4;         // warps per partition CTA; each owns a ring of stages
+constexpr int kStages = 2;        // stages per warp; one stage = K and V of one block
+constexpr int kMaxGroup = 8;      // query heads per kv head: the MMA N dimension
+constexpr int kReduceThreads = 256;
+constexpr int kReduceSlice = 64;  // head_dim elements per reduce CTA
+constexpr unsigned kDefaultWaitLimit = 1u << 20;
+
+struct PartitionParams {
+    __half* out;
+    const __half* q;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    float* max_logits;  // [B][H][max_partitions], log2 domain
+    float* exp_sums;    // [B][H][max_partitions]
+    float* tmp_out;     // [B][H][max_partitions][D], normalised partial outputs
+    long long num_blocks;
+    int num_heads, num_kv_heads, group;
+    int max_blocks_per_seq, max_seq_len;
+    int partition_size, max_partitions;
+    float scale_log2;   // scale * log2(e)
+    unsigned wait_limit;
+    int force_timeout;
+};
+
+struct ReduceParams {
+    __half* out;
+    const float* max_logits;
+    const float* exp_sums;
+    const float* tmp_out;
+    const int32_t* seq_lens;
+    int num_heads, max_blocks_per_seq, max_seq_len;
+    int partition_size, max_partitions;
+};
+
+// Dynamic shared memory of a partition CTA for head_dim D (includes 1 KB of
+// alignment slack for the 128-byte swizzle).
+int partition_smem_bytes(int head_dim);
+
+cudaError_t launch_partition(int head_dim, const PartitionParams& prm, const CUtensorMap& tmap_k,
+                             const CUtensorMap& tmap_v, dim3 grid, cudaStream_t stream);
+
+// Launched with programmatic dependent launch so its start-up overlaps the
+// tail of the partition kernel; the kernel waits on the dependency before it
+// reads any partial.
+cudaError_t launch_reduce(int head_dim, const ReduceParams& prm, dim3 grid, cudaStream_t stream);
+
+// Read and clear the status word of the current device (synchronises stream).
+cudaError_t read_and_clear_status(cudaStream_t stream, int* status);
+
+}  // namespace pa

@@ -1,0 +1,539 @@
+// Split-KV paged-attention decode kernels for GB300 (sm_103a).
+//
+// pa_partition_kernel -- Phase 1 of the "docs" commit page (partition kernel
+//   gridded on kv heads): one CTA per (partition, kv head, sequence).  Every
+//   K/V block of the partition is fetched once from HBM by TMA and used by
+//   all query heads of the GQA group.  It writes the compound partial
+//   (max score, exp sum, normalised weighted V) of the "docs" commit page, or
+//   the final output when the sequence has a single partition.
+// pa_reduce_kernel -- Phase 2 of the same page: merges the partials of each
+//   (sequence, head) with a log-sum-exp reduce.
+//
+// Hardware mapping (written for sm_103a, not translated from the pages' Triton):
+// * Cache layout [block][kv_head][16 tokens][D]: one (block, kv head) is 16
+//   rows of D halves.  A 2-D tensor map views a cache as rows x D; each block
+//   arrives as D/64 TMA boxes of 16 rows x 64 halves (128 B) with the 128-byte
+//   swizzle, so the ldmatrix reads below hit 8 distinct bank groups.
+// * Each of the 4 warps owns kStages shared-memory stages (K and V of one
+//   block each), an mbarrier per stage, and a private online-softmax state;
+//   blocks of the partition are dealt round-robin to the warps.  Lane 0
+//   issues the copies; every wait is bounded (no spin can hang the GPU).
+// * Scores and PV run on the tensor cores as m16n8k16 MMAs in swapped form:
+//   S^T[16 tokens x 8 heads] = K[16 x D] . Q^T[D x 8] and
+//   O^T[D x 8 heads] += V^T[D x 16] . P^T[16 x 8], so the <= 8 heads of a
+//   GQA group sit in the N dimension.  P^T reaches the B-operand layout with
+//   movmatrix (an in-register 8x8 transpose), with no shared-memory round trip.
+// * Softmax state is kept in the log2 domain (scores pre-multiplied by
+//   scale*log2 e and exponentiated with exp2f).  Inside a warp the running
+//   max is updated per block and the accumulator rescaled by
+//   alpha = 2^(m_old - m_new), with the block probabilities taken relative to
+//   the new max; this is the alpha/beta update of the
+//   "paged_attention_v2_triton.py" commit page with beta folded into p.
+#include "pa_internal.h"
+
+#include <math.h>
+
+#include "pa_decode.h"
+
+namespace pa {
+
+__device__ unsigned int g_status;
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after `limit` polls and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t n = 0; n < limit; ++n)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// D[16x8] += A[16x16] . B[16x8], fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t half2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// Byte offset of 16-byte unit `unit` (0..7) of row `row` inside one swizzled
+// TMA box of 16 rows x 128 bytes (the 128-byte swizzle XORs the unit index
+// with the row index modulo 8).
+__device__ __forceinline__ uint32_t swz(int row, int unit) {
+    return static_cast<uint32_t>(row * 128 + ((unit ^ (row & 7)) << 4));
+}
+
+}  // namespace
+
+template <int D>
+struct PartitionShape {
+    static constexpr int kSteps = D / 16;                      // k-steps of QK, m-tiles of PV
+    static constexpr int kChunks = D / 64;                     // TMA boxes per K (or V) block
+    static constexpr int kBoxBytes = kBlockSize * 128;         // 16 rows x 64 halves
+    static constexpr int kTileBytes = kBlockSize * D * 2;      // K (or V) of one block
+    static constexpr int kStageBytes = 2 * kTileBytes;         // K + V
+    static constexpr int kStageArea = kWarps * kStages * kStageBytes;
+    static constexpr int kRedStride = D + 4;                   // padded row of the cross-warp reduce
+    static constexpr int kRedBytes = kWarps * kMaxGroup * kRedStride * 4;
+    static constexpr int kCtrlBytes = kWarps * kStages * 8 + 2 * kWarps * kMaxGroup * 4 + 16;
+    static constexpr int kSmemBytes = 1024 + kStageArea + kCtrlBytes;
+    static_assert(kRedBytes <= kStageArea, "cross-warp reduce must fit in the stage area");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    pa_partition_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                        const PartitionParams prm) {
+    using S = PartitionShape<D>;
+    // Let a dependent reduce launch start its CTAs as soon as the SMs free up;
+    // it still waits for this grid's completion before touching the partials.
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStageArea);
+    float* sm_m = reinterpret_cast<float*>(bars + kWarps * kStages);
+    float* sm_l = sm_m + kWarps * kMaxGroup;
+    int* sm_abort = reinterpret_cast<int*>(sm_l + kWarps * kMaxGroup);
+
+    const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = prm.group, H = prm.num_heads;
+
+    const int L = prm.seq_lens[b];
+    if (L < 0 || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) {
+        if (p == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(&g_status, PA_DEV_BAD_SEQ_LEN);
+        return;
+    }
+    if (L == 0) {  // empty sequence: the output is zero
+        if (p == 0)
+            for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+                prm.out[((size_t)b * H + kvh * G) * D + i] = __float2half_rn(0.f);
+        return;
+    }
+    const int n_part = (L + prm.partition_size - 1) / prm.partition_size;
+    if (p >= n_part) return;
+    const int blocks_per_part = prm.partition_size / kBlockSize;
+    const int blk0 = p * blocks_per_part;
+    const int nblk = min(blocks_per_part, (L + kBlockSize - 1) / kBlockSize - blk0);
+
+    const uint32_t stage0 = smem_addr(smem) + warp * kStages * S::kStageBytes;
+    const uint32_t bar0 = smem_addr(bars) + warp * kStages * 8;
+    if (threadIdx.x == 0) *sm_abort = 0;
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int g = lane >> 2, c = lane & 3;  // MMA fragment row group / column pair
+
+    // Q^T as the B operand of S^T = K . Q^T: lane holds head g, dims 16ks + 2c (+1) and +8.
+    uint32_t qb[S::kSteps][2];
+    {
+        const int hq = g < G ? g : 0;  // lanes of padding heads load nothing
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(prm.q + ((size_t)b * H + kvh * G + hq) * D);
+#pragma unroll
+        for (int ks = 0; ks < S::kSteps; ++ks) {
+            qb[ks][0] = g < G ? __ldg(qrow + 8 * ks + c) : 0u;
+            qb[ks][1] = g < G ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
+        }
+    }
+
+    float o[S::kSteps][4];
+#pragma unroll
+    for (int i = 0; i < S::kSteps; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 domain) of heads 2c, 2c+1
+    float l0 = 0.f, l1 = 0.f;              // this lane's share of the exp sums
+
+    // Blocks j = warp, warp + kWarps, ... of the partition belong to this warp.
+    const int nmine = warp < nblk ? (nblk - warp + kWarps - 1) / kWarps : 0;
+    const int32_t* bt = prm.block_tables + (size_t)b * prm.max_blocks_per_seq + blk0;
+    int ids = -1;             // lane k holds the block id of this warp's iteration 32*(it/32) + k
+    uint32_t valid_bits = 0;  // stage s holds a block with a legal id
+
+    auto issue = [&](int it) {
+        if ((it & 31) == 0) {
+            const int j = warp + (it + lane) * kWarps;
+            ids = j < nblk ? __ldg(bt + j) : -1;
+        }
+        const int phys = __shfl_sync(kFull, ids, it & 31);
+        const int s = it % kStages;
+        const uint32_t bar = bar0 + 8 * s;
+        const bool ok = phys >= 0 && (long long)phys < prm.num_blocks;
+        valid_bits = ok ? (valid_bits | (1u << s)) : (valid_bits & ~(1u << s));
+        if (lane == 0) {
+            if (ok) {
+                mbar_arrive_expect_tx(bar, S::kStageBytes);
+                const int row = (phys * prm.num_kv_heads + kvh) * kBlockSize;
+                const uint32_t kdst = stage0 + s * S::kStageBytes, vdst = kdst + S::kTileBytes;
+#pragma unroll
+                for (int ch = 0; ch < S::kChunks; ++ch) {
+                    tma_load_2d(kdst + ch * S::kBoxBytes, &tmap_k, ch * 64, row, bar);
+                    tma_load_2d(vdst + ch * S::kBoxBytes, &tmap_v, ch * 64, row, bar);
+                }
+            } else {
+                atomicOr(&g_status, PA_DEV_BAD_BLOCK_ID);
+                mbar_arrive(bar);  // complete the phase so the wait below stays in step
+            }
+        }
+    };
+
+    for (int it = 0; it < kStages && it < nmine; ++it) issue(it);
+
+    const float sl2 = prm.scale_log2;
+    const int mi = lane >> 3, r8 = lane & 7;
+    const int rq = r8 + ((mi & 1) << 3);  // ldmatrix row (token) for K . Q^T
+    const int rv = r8 + ((mi >> 1) << 3);  // ldmatrix row (token) for V^T . P^T
+    int i = 0;
+    bool timed_out = false;
+    for (; i < nmine; ++i) {
+        const int s = i % kStages;
+        const uint32_t bar = bar0 + 8 * s;
+        if (prm.force_timeout || !mbar_wait(bar, (i / kStages) & 1, prm.wait_limit)) {
+            timed_out = true;
+            break;
+        }
+        if ((valid_bits >> s) & 1u) {
+            const int tok0 = (blk0 + warp + i * kWarps) * kBlockSize;
+            const int nvalid = min(kBlockSize, L - tok0);
+            const uint32_t kst = stage0 + s * S::kStageBytes, vst = kst + S::kTileBytes;
+
+            // S^T = K . Q^T  (two accumulators for instruction-level parallelism)
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < S::kSteps; ++ks) {
+                uint32_t a[4];
+                ldsm_x4(a, kst + (ks >> 2) * S::kBoxBytes + swz(rq, ((ks & 3) << 1) + (mi >> 1)));
+                if (ks & 1)
+                    mma_16816(sb, a, qb[ks][0], qb[ks][1]);
+                else
+                    mma_16816(sa, a, qb[ks][0], qb[ks][1]);
+            }
+            // lane holds tokens g (s0, s1) and g + 8 (s2, s3) of heads 2c, 2c + 1
+            float s0 = (sa[0] + sb[0]) * sl2, s1 = (sa[1] + sb[1]) * sl2;
+            float s2 = (sa[2] + sb[2]) * sl2, s3 = (sa[3] + sb[3]) * sl2;
+            if (g >= nvalid) s0 = s1 = -INFINITY;      // tokens past the end are excluded
+            if (g + 8 >= nvalid) s2 = s3 = -INFINITY;
+
+            float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            const __half2 p01 = __floats2half2_rn(exp2f(s0 - mn0), exp2f(s1 - mn1));
+            const __half2 p23 = __floats2half2_rn(exp2f(s2 - mn0), exp2f(s3 - mn1));
+            // the exp sums use the rounded probabilities that enter P.V
+            const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
+            l0 = l0 * al0 + (f01.x + f23.x);
+            l1 = l1 * al1 + (f01.y + f23.y);
+            if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                for (int mt = 0; mt < S::kSteps; ++mt) {
+                    o[mt][0] *= al0;
+                    o[mt][1] *= al1;
+                    o[mt][2] *= al0;
+                    o[mt][3] *= al1;
+                }
+            }
+            const uint32_t pb0 = movmatrix_trans(half2_bits(p01));  // P^T rows: heads; cols: tokens 0..7
+            const uint32_t pb1 = movmatrix_trans(half2_bits(p23));  // tokens 8..15
+
+            if (nvalid < kBlockSize) {
+                // Slots past the end may hold anything (even NaN); 0 * NaN would
+                // poison P.V, so clear those V rows before the MMA reads them.
+                uint8_t* vgen = smem + (vst - smem_addr(smem));
+                const int units = (kBlockSize - nvalid) * S::kChunks * 8;
+                for (int u = lane; u < units; u += 32) {
+                    const int r = nvalid + u / (S::kChunks * 8), rem = u % (S::kChunks * 8);
+                    *reinterpret_cast<uint4*>(vgen + (rem >> 3) * S::kBoxBytes + r * 128 + (rem & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+            }
+
+            // O^T += V^T . P^T
+#pragma unroll
+            for (int mt = 0; mt < S::kSteps; ++mt) {
+                uint32_t a[4];
+                ldsm_x4_trans(a, vst + (mt >> 2) * S::kBoxBytes + swz(rv, ((mt & 3) << 1) + (mi & 1)));
+                mma_16816(o[mt], a, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (i + kStages < nmine) issue(i + kStages);
+    }
+
+    if (timed_out) {
+        // Drain this warp's copies still in flight before the CTA may exit.
+        for (int k = i; k < nmine && k < i + kStages; ++k)
+            mbar_wait(bar0 + 8 * (k % kStages), (k / kStages) & 1, kDefaultWaitLimit);
+        if (lane == 0) {
+            atomicOr(&g_status, PA_DEV_TIMEOUT);
+            atomicExch(sm_abort, 1);
+        }
+    }
+
+    // Finish this warp's exp sums: add the shares of the 8 lanes holding the same heads.
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, off);
+        l1 += __shfl_xor_sync(kFull, l1, off);
+    }
+    __syncthreads();  // all stages consumed; the stage area is reused below
+    if (*sm_abort) return;
+
+    // Merge the kWarps partial states of this CTA (same rule, across warps).
+    float* red = reinterpret_cast<float*>(smem);
+    {
+        float* rw = red + warp * kMaxGroup * S::kRedStride;
+#pragma unroll
+        for (int mt = 0; mt < S::kSteps; ++mt) {
+            const int d = 16 * mt + g;
+            rw[(2 * c) * S::kRedStride + d] = o[mt][0];
+            rw[(2 * c + 1) * S::kRedStride + d] = o[mt][1];
+            rw[(2 * c) * S::kRedStride + d + 8] = o[mt][2];
+            rw[(2 * c + 1) * S::kRedStride + d + 8] = o[mt][3];
+        }
+        if (g == 0) {
+            sm_m[warp * kMaxGroup + 2 * c] = m0;
+            sm_m[warp * kMaxGroup + 2 * c + 1] = m1;
+            sm_l[warp * kMaxGroup + 2 * c] = l0;
+            sm_l[warp * kMaxGroup + 2 * c + 1] = l1;
+        }
+    }
+    __syncthreads();
+
+    const bool direct = n_part == 1;
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const int h = idx / D, d = idx - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * kMaxGroup + h]);
+        float lsum = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = sm_m[w * kMaxGroup + h];
+            const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);  // warps without blocks add nothing
+            lsum += f * sm_l[w * kMaxGroup + h];
+            acc += f * red[(w * kMaxGroup + h) * S::kRedStride + d];
+        }
+        const float v = acc / lsum;
+        const size_t head = (size_t)b * H + kvh * G + h;
+        if (direct) {
+            prm.out[head * D + d] = __float2half_rn(v);
+        } else {
+            const size_t pi = head * prm.max_partitions + p;
+            prm.tmp_out[pi * D + d] = v;
+            if (d == 0) {
+                prm.max_logits[pi] = M;
+                prm.exp_sums[pi] = lsum;
+            }
+        }
+    }
+}
+
+// Phase 2: out[b, h] = sum_p w_p acc_p / sum_p w_p with w_p = l_p 2^(m_p - M),
+// M = max_p m_p (the log-sum-exp merge of the partials).  One CTA per
+// (head, sequence, 64-wide slice of head_dim); 16 threads cover the slice with
+// float4 loads and 16 groups stride over the partitions; the summation order
+// is fixed, so results are deterministic.
+template <int D>
+__global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceParams prm) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int h = blockIdx.x, b = blockIdx.y, slice = blockIdx.z;
+    const int L = prm.seq_lens[b];
+    // single-partition, empty and invalid sequences were finished by the partition kernel
+    if (L <= prm.partition_size || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) return;
+    const int n = (L + prm.partition_size - 1) / prm.partition_size;
+    const size_t base = ((size_t)b * prm.num_heads + h) * prm.max_partitions;
+    const float* ml = prm.max_logits + base;
+    const float* el = prm.exp_sums + base;
+
+    __shared__ float red_max[kReduceThreads / 32];
+    __shared__ float4 red_acc[16][16];
+    __shared__ float red_w[16];
+
+    float M = -INFINITY;
+    for (int p = threadIdx.x; p < n; p += kReduceThreads) M = fmaxf(M, ml[p]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    if ((threadIdx.x & 31) == 0) red_max[threadIdx.x >> 5] = M;
+    __syncthreads();
+    M = red_max[0];
+#pragma unroll
+    for (int w = 1; w < kReduceThreads / 32; ++w) M = fmaxf(M, red_max[w]);
+
+    const int lane16 = threadIdx.x & 15, pg = threadIdx.x >> 4;
+    const float4* tp = reinterpret_cast<const float4*>(prm.tmp_out + base * D + slice * kReduceSlice) + lane16;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+#pragma unroll 4
+    for (int p = pg; p < n; p += 16) {
+        const float w = el[p] * exp2f(ml[p] - M);
+        const float4 t = tp[(size_t)p * (D / 4)];
+        wsum += w;
+        acc.x += w * t.x;
+        acc.y += w * t.y;
+        acc.z += w * t.z;
+        acc.w += w * t.w;
+    }
+    red_acc[pg][lane16] = acc;
+    if (lane16 == 0) red_w[pg] = wsum;
+    __syncthreads();
+    if (threadIdx.x < kReduceSlice) {
+        const int dl = threadIdx.x;
+        float sum = 0.f, W = 0.f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float4 v = red_acc[q][dl >> 2];
+            sum += (dl & 3) == 0 ? v.x : (dl & 3) == 1 ? v.y : (dl & 3) == 2 ? v.z : v.w;
+            W += red_w[q];
+        }
+        prm.out[((size_t)b * prm.num_heads + h) * D + slice * kReduceSlice + dl] = __float2half_rn(sum / W);
+    }
+}
+
+int partition_smem_bytes(int head_dim) {
+    switch (head_dim) {
+        case 64: return PartitionShape<64>::kSmemBytes;
+        case 128: return PartitionShape<128>::kSmemBytes;
+        case 256: return PartitionShape<256>::kSmemBytes;
+        default: return -1;
+    }
+}
+
+namespace {
+
+template <int D>
+cudaError_t launch_partition_t(const PartitionParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
+                               cudaStream_t stream) {
+    const int smem = PartitionShape<D>::kSmemBytes;
+    // The attribute is per device; setting it on every call costs little and
+    // keeps multi-device processes correct.
+    cudaError_t e = cudaFuncSetAttribute(pa_partition_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    pa_partition_kernel<D><<<grid, kWarps * 32, smem, stream>>>(tk, tv, prm);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_reduce_t(const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, pa_reduce_kernel<D>, prm);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_partition(int head_dim, const PartitionParams& prm, const CUtensorMap& tk, const CUtensorMap& tv,
+                             dim3 grid, cudaStream_t stream) {
+    switch (head_dim) {
+        case 64: return launch_partition_t<64>(prm, tk, tv, grid, stream);
+        case 128: return launch_partition_t<128>(prm, tk, tv, grid, stream);
+        case 256: return launch_partition_t<256>(prm, tk, tv, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_reduce(int head_dim, const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
+    switch (head_dim) {
+        case 64: return launch_reduce_t<64>(prm, grid, stream);
+        case 128: return launch_reduce_t<128>(prm, grid, stream);
+        case 256: return launch_reduce_t<256>(prm, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t read_and_clear_status(cudaStream_t stream, int* status) {
+    unsigned int v = 0;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
+    if (e != cudaSuccess) return e;
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+    *status = static_cast<int>(v);
+    return cudaSuccess;
+}
+
+}  // namespace pa

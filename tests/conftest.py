@@ -8,4 +8,7 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
-    config.addinivalue_line("markers", "slow: takes more than a few seconds")
+    # The binding loads the compiled library at import; build it first if it is
+    # missing or stale (nvcc is present wherever the tests run).
+    from paged_kv_cache_308_gb300 import build
+    build.build()

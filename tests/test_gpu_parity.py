@@ -1,0 +1,238 @@
+"""GPU parity of the CUDA decode path against the float64 oracle, through the C ABI.
+
+Small shapes cover several tiles and ragged tails in every mode; the five
+named workloads run at full size in the launch configuration the benchmark
+times (the mixed 64-sequence batch is checked on sampled sequences).  Gather
+exactness (permuted pool, sequence alone vs in a batch, repeat runs) must be
+bit-identical.  Device-side error paths are exercised without faulting: bad
+block ids and lengths are caught by the kernel's own checks, and the forced
+timeout makes the bounded waits give up.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_308_gb300 import binding as pb
+from paged_kv_cache_308_gb300 import workloads as W
+from parity_helpers import assert_parity, compare, oracle_ref, oracle_ref_subset
+
+pytestmark = pytest.mark.gpu
+THREADS = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+def run(w, **opt):
+    out = pb.decode_workload(w, **opt)
+    torch.cuda.synchronize()
+    st = pb.pa_get_device_status()
+    assert st == 0, f"device status {st}"
+    return out
+
+
+SMALL_LENS = [[1], [15], [16], [17], [511], [512], [513], [1, 16, 17, 511, 512, 513, 1029], [2048, 3, 700]]
+MODES = [dict(), dict(mode="single"), dict(mode="split", partition_size=16), dict(mode="split", partition_size=64),
+         dict(mode="split", partition_size=512), dict(mode="split", partition_size=1024)]
+
+
+@pytest.mark.parametrize("lens", SMALL_LENS, ids=lambda x: "L" + "-".join(map(str, x)))
+@pytest.mark.parametrize("opt", MODES, ids=lambda o: "-".join(f"{v}" for v in o.values()) or "default")
+def test_small_gqa6_d256(dev, lens, opt):
+    w = W.make_workload("small", lens, num_blocks=sum((L + 15) // 16 for L in lens) + 7, seed=len(lens) + lens[0],
+                        device=dev, tail_fill=float("nan"))
+    out = run(w, **opt)
+    assert_parity(out, oracle_ref(w), f"lens={lens} {opt}")
+
+
+@pytest.mark.parametrize("H,Hkv,D", [(4, 4, 64), (8, 4, 128), (16, 2, 256), (12, 4, 64), (12, 2, 128),
+                                     (16, 4, 256), (5, 5, 128), (7, 1, 256)])
+@pytest.mark.parametrize("mode", ["single", "split"])
+def test_group_sizes_and_head_dims(dev, H, Hkv, D, mode):
+    lens = [1, 37, 700, 1500, 16 * 33]
+    w = W.make_workload("shape", lens, num_heads=H, num_kv_heads=Hkv, head_dim=D, num_blocks=300, seed=H * D,
+                        device=dev, scale=1 / math.sqrt(D), tail_fill=float("inf"))
+    out = run(w, mode=mode, partition_size=256 if mode == "split" else 0)
+    assert_parity(out, oracle_ref(w), f"H={H} Hkv={Hkv} D={D} {mode}")
+
+
+@pytest.mark.parametrize("name,opt", [
+    ("b1_l2048", dict()),
+    ("b1_l2048", dict(mode="single")),
+    ("b8_u8192", dict(mode="single")),
+    ("b8_u8192", dict(mode="split")),
+    ("b8_u8192", dict()),
+    ("b4_l32768_peaked", dict()),
+    ("b1_l102400", dict()),
+])
+def test_named_workload_full(dev, name, opt):
+    w = W.make_config(name, device=dev)
+    out = run(w, **opt) if opt else pb.decode_workload(w)  # the benchmark's call: library workspace, AUTO
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    r = assert_parity(out, oracle_ref(w, THREADS), f"{name} {opt}")
+    print(name, opt, r)
+
+
+def test_mixed_batch_sampled(dev):
+    w = W.make_config("b64_loguniform", device=dev)
+    out = pb.decode_workload(w)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    lens = np.array(w.seq_lens_host)
+    rng = np.random.default_rng(0)
+    seqs = sorted(set([int(lens.argmax()), int(lens.argmin())] + rng.choice(len(lens), 10, replace=False).tolist()))
+    ref = oracle_ref_subset(w, seqs, THREADS)
+    assert_parity(out[seqs], ref, "b64_loguniform sampled")
+    # the rest of the batch: finite, and each row a convex combination of V (bounded by max |V|)
+    assert torch.isfinite(out).all()
+    assert out.abs().max().item() <= w.v_cache.abs().max().item() + 1e-3
+
+
+def test_peaked_keys_both_modes(dev):
+    w = W.make_workload("peaked", [4096, 777], num_blocks=400, seed=3, device=dev, peaked_fraction=0.01)
+    ref = oracle_ref(w)
+    for opt in (dict(mode="single"), dict(mode="split", partition_size=512), dict(mode="split", partition_size=32)):
+        assert_parity(run(w, **opt), ref, f"peaked {opt}")
+
+
+def _permuted_pool(w, seed):
+    g = torch.Generator(device=w.k_cache.device).manual_seed(seed)
+    perm = torch.randperm(w.num_blocks, generator=g, device=w.k_cache.device)
+    k2 = torch.empty_like(w.k_cache)
+    v2 = torch.empty_like(w.v_cache)
+    k2[perm] = w.k_cache
+    v2[perm] = w.v_cache
+    bt = w.block_tables.long()
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0)], bt).to(torch.int32)
+    return W.Workload(w.name, w.q, k2, v2, bt2, w.seq_lens, w.seq_lens_host, w.num_heads, w.num_kv_heads,
+                      w.head_dim, w.block_size, w.scale, w.partition_size)
+
+
+@pytest.mark.parametrize("opt", [dict(mode="single"), dict(mode="split", partition_size=512),
+                                 dict(mode="split", partition_size=48)])
+def test_permuted_block_table_is_bit_identical(dev, opt):
+    w = W.make_workload("perm", [3000, 517, 8000, 1], num_blocks=900, seed=5, device=dev)
+    a = run(w, **opt)
+    b = run(_permuted_pool(w, 11), **opt)
+    assert torch.equal(a, b)
+    # the identity table over a freshly laid out pool gives the same bits too
+    assert torch.equal(a, run(_permuted_pool(w, 12), **opt))
+
+
+def test_sequence_alone_and_in_batch_are_bit_identical(dev):
+    w = W.make_workload("batch", [5000, 123, 2048, 999], num_blocks=700, seed=6, device=dev)
+    full = run(w, mode="split", partition_size=512)
+    for b in range(w.num_seqs):
+        one = W.Workload(w.name, w.q[b:b + 1].contiguous(), w.k_cache, w.v_cache,
+                         w.block_tables[b:b + 1].contiguous(), w.seq_lens[b:b + 1].contiguous(),
+                         [w.seq_lens_host[b]], w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, w.scale)
+        assert torch.equal(full[b:b + 1], run(one, mode="split", partition_size=512))
+
+
+def test_repeat_runs_are_bit_identical(dev):
+    w = W.make_config("b8_u8192", device=dev)
+    a = run(w)
+    for _ in range(3):
+        assert torch.equal(a, run(w))
+
+
+def test_single_key_returns_v_exactly(dev):
+    w = W.make_workload("one", [1, 1, 1], num_blocks=9, seed=7, device=dev, tail_fill=float("nan"))
+    for opt in (dict(mode="single"), dict(mode="split", partition_size=16)):
+        out = run(w, **opt)
+        for b in range(3):
+            phys = int(w.block_tables[b, 0])
+            for h in range(w.num_heads):
+                assert torch.equal(out[b, h], w.v_cache[phys, h // 6, 0])
+
+
+def test_empty_sequences_give_zero(dev):
+    w = W.make_workload("empty", [0, 600, 0, 17], num_blocks=50, seed=8, device=dev)
+    for opt in (dict(mode="single"), dict(mode="split", partition_size=128)):
+        out = run(w, **opt)
+        assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[2]) == 0
+        assert_parity(out, oracle_ref(w), f"empty {opt}")
+    allempty = W.make_workload("allempty", [0, 0], num_blocks=4, seed=9, device=dev)
+    assert torch.count_nonzero(run(allempty)) == 0
+
+
+def test_library_and_caller_workspace_calls_agree(dev):
+    w = W.make_config("b1_l2048", device=dev)
+    a = pb.decode_workload(w)
+    b = run(w, mode="auto")
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_graph_capture_of_caller_workspace_call(dev):
+    w = W.make_workload("graph", [4000, 100, 2500], num_blocks=500, seed=10, device=dev)
+    out = torch.empty_like(w.q)
+    kw = dict(max_seq_len=w.max_seq_len, mode="split", partition_size=512)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, **kw)
+    ws = pb.alloc_workspace(plan, dev)
+    args = (out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads, w.head_dim,
+            w.block_size, w.scale)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pb.pa_decode_ex(*args, s, workspace=ws, **kw)  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pb.pa_decode_ex(*args, torch.cuda.current_stream(), workspace=ws, **kw)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+
+
+def test_bad_block_id_sets_device_status(dev):
+    w = W.make_workload("badid", [100, 40], num_blocks=20, seed=11, device=dev)
+    pb.pa_get_device_status()  # clear
+    w.block_tables[0, 2] = w.num_blocks + 3
+    w.block_tables[1, 0] = -5
+    pb.decode_workload(w, mode="split", partition_size=32)
+    assert pb.pa_get_device_status() & pb.PA_DEV_BAD_BLOCK_ID
+    assert pb.pa_get_device_status() == 0  # reading clears it
+
+
+def test_bad_seq_len_sets_device_status(dev):
+    w = W.make_workload("badlen", [100, 40], num_blocks=20, seed=12, device=dev, extra_table_cols=4)
+    pb.pa_get_device_status()
+    out = torch.empty_like(w.q)
+    w.seq_lens[1] = 101  # above the max_seq_len hint of 100
+    pb.pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
+                 w.head_dim, w.block_size, w.scale, max_seq_len=100)
+    assert pb.pa_get_device_status() & pb.PA_DEV_BAD_SEQ_LEN
+
+
+def test_forced_timeout_returns_status_and_context_survives(dev):
+    w = W.make_workload("timeout", [3000, 64], num_blocks=200, seed=13, device=dev)
+    pb.pa_get_device_status()
+    for mode in ("single", "split"):
+        pb.decode_workload(w, mode=mode, partition_size=512 if mode == "split" else 0,
+                           flags=pb.PA_FLAG_FORCE_TIMEOUT)
+        assert pb.pa_get_device_status() & pb.PA_DEV_TIMEOUT
+    # the context is still healthy: a normal call afterwards is correct
+    assert_parity(run(w), oracle_ref(w), "after forced timeout")
+
+
+def test_caller_workspace_too_small_is_rejected(dev):
+    w = W.make_workload("ws", [2000], num_blocks=200, seed=14, device=dev)
+    out = torch.empty_like(w.q)
+    small = torch.empty(64, dtype=torch.uint8, device=dev)
+    with pytest.raises(pb.PaDecodeError) as e:
+        pb.pa_decode_ex(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
+                        w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len, mode="split",
+                        workspace=small)
+    assert e.value.code == pb.PA_ERR_WORKSPACE

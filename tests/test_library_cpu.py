@@ -1,0 +1,132 @@
+"""The C-ABI library without a GPU: it loads, exports every declared function,
+and its host logic (validation, dispatch plan, workspace sizing, status text)
+answers without touching a device."""
+import ctypes
+import math
+
+import pytest
+
+from paged_kv_cache_308_gb300 import binding as pb
+
+SMS = 152
+FAKE = 0x10000  # a 16-byte aligned non-null address; the plan never dereferences it
+
+
+def args(num_seqs=1, max_seq_len=102400, H=24, Hkv=4, D=256, bs=16, num_blocks=6400, mbps=None, scale=1 / 16,
+         **ptrs):
+    mbps = mbps if mbps is not None else (max_seq_len + bs - 1) // bs
+    p = dict(out=FAKE, q=FAKE, k_cache=FAKE, v_cache=FAKE, block_tables=FAKE, seq_lens=FAKE)
+    p.update(ptrs)
+    return pb.pa_decode_args(p["out"], p["q"], p["k_cache"], p["v_cache"], p["block_tables"], p["seq_lens"],
+                             num_seqs, mbps, max_seq_len, num_blocks, H, Hkv, D, bs, scale)
+
+
+def plan(a, mode=0, partition_size=0):
+    o = pb.pa_decode_opts(mode, partition_size, 0, 0, None, None)
+    pl = pb.pa_decode_plan_t()
+    rc = pb.lib.pa_decode_plan(ctypes.byref(a), ctypes.byref(o), SMS, ctypes.byref(pl))
+    return rc, pl.as_dict()
+
+
+def test_library_exports_every_declared_function():
+    names = pb.header_functions()
+    assert {"pa_decode", "pa_decode_ex", "pa_decode_plan", "pa_decode_workspace_size", "pa_get_device_status",
+            "pa_status_string", "pa_release_workspace", "pa_version"} <= set(names)
+    for n in names:
+        assert hasattr(pb.lib, n), n
+
+
+def test_status_strings():
+    for code in (pb.PA_OK, pb.PA_ERR_INVALID_ARG, pb.PA_ERR_UNSUPPORTED, pb.PA_ERR_CUDA, pb.PA_ERR_OOM,
+                 pb.PA_ERR_WORKSPACE):
+        s = pb.status_string(code)
+        assert s and s != "unknown status"
+    assert pb.status_string(-99) == "unknown status"
+    assert pb.version() >= 100
+
+
+def ws_bytes(B, H, parts, D):
+    a = lambda x: (x + 255) // 256 * 256
+    return 2 * a(B * H * parts * 4) + a(B * H * parts * D * 4)
+
+
+def test_plan_long_context_splits_into_512_token_partitions():
+    rc, pl = plan(args())
+    assert rc == pb.PA_OK
+    assert pl["mode"] == pb.PA_MODE_SPLIT and pl["partition_size"] == 512
+    assert (pl["grid_x"], pl["grid_y"], pl["grid_z"]) == (200, 4, 1)      # 800 CTAs on kv heads
+    assert pl["launch_reduce"] == 1
+    assert (pl["reduce_grid_x"], pl["reduce_grid_y"], pl["reduce_grid_z"]) == (24, 1, 4)
+    assert pl["workspace_bytes"] == ws_bytes(1, 24, 200, 256)
+    assert pl["workspace_bytes"] == pb.pa_decode_workspace_size(1, 102400, 24, 256, 512)
+
+
+def test_plan_modes():
+    rc, pl = plan(args(max_seq_len=2048, num_blocks=128), mode=pb.PA_MODE_SINGLE)
+    assert rc == 0 and pl["mode"] == pb.PA_MODE_SINGLE and pl["grid_x"] == 1 and pl["partition_size"] == 2048
+    assert pl["launch_reduce"] == 0 and pl["workspace_bytes"] == 0
+    rc, pl = plan(args(max_seq_len=1000, num_blocks=128), mode=pb.PA_MODE_SINGLE)
+    assert pl["partition_size"] == 1008                                   # rounded up to whole blocks
+    rc, pl = plan(args(max_seq_len=512, num_blocks=128))
+    assert rc == 0 and pl["mode"] == pb.PA_MODE_SINGLE                    # one partition: no reduce
+    rc, pl = plan(args(max_seq_len=513, num_blocks=128), mode=pb.PA_MODE_SPLIT, partition_size=64)
+    assert rc == 0 and pl["grid_x"] == math.ceil(513 / 64) and pl["launch_reduce"] == 1
+    rc, pl = plan(args(num_seqs=0))
+    assert rc == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), pb.PA_ERR_INVALID_ARG),
+    (dict(out=FAKE + 2), pb.PA_ERR_INVALID_ARG),
+    (dict(k_cache=FAKE + 8), pb.PA_ERR_INVALID_ARG),
+    (dict(block_tables=FAKE + 2), pb.PA_ERR_INVALID_ARG),
+    (dict(H=24, Hkv=5), pb.PA_ERR_INVALID_ARG),
+    (dict(D=100), pb.PA_ERR_UNSUPPORTED),
+    (dict(D=96), pb.PA_ERR_UNSUPPORTED),
+    (dict(bs=32), pb.PA_ERR_UNSUPPORTED),
+    (dict(H=48, Hkv=4), pb.PA_ERR_UNSUPPORTED),     # GQA ratio 12 > 8
+    (dict(scale=float("nan")), pb.PA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), pb.PA_ERR_INVALID_ARG),
+    (dict(mbps=10), pb.PA_ERR_INVALID_ARG),         # max_seq_len beyond the block table
+    (dict(num_seqs=-1), pb.PA_ERR_INVALID_ARG),
+    (dict(num_seqs=70000), pb.PA_ERR_INVALID_ARG),
+    (dict(num_blocks=0), pb.PA_ERR_INVALID_ARG),
+    (dict(num_blocks=1 << 26), pb.PA_ERR_UNSUPPORTED),  # rows past 32-bit TMA coordinates
+])
+def test_plan_rejects_bad_arguments(kw, code):
+    rc, _ = plan(args(**kw))
+    assert rc == code
+
+
+def test_plan_rejects_bad_options():
+    assert plan(args(), mode=7)[0] == pb.PA_ERR_INVALID_ARG
+    assert plan(args(), partition_size=100)[0] == pb.PA_ERR_INVALID_ARG   # not a multiple of 16
+    assert plan(args(), partition_size=-16)[0] == pb.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 6, 8])
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_plan_accepts_supported_shapes(G, D):
+    rc, pl = plan(args(H=4 * G, Hkv=4, D=D))
+    assert rc == 0 and pl["threads"] == 128 and 0 < pl["smem_bytes"] <= 227 * 1024
+
+
+def test_decode_ex_checks_workspace_before_any_cuda_call():
+    a = args()
+    o = pb.pa_decode_opts(0, 0, 0, 0, None, None)
+    rc = pb.lib.pa_decode_ex(ctypes.byref(a), ctypes.byref(o), None, 0, None)
+    assert rc == pb.PA_ERR_WORKSPACE
+    rc = pb.lib.pa_decode_ex(ctypes.byref(a), ctypes.byref(o), FAKE + 64, 1 << 30, None)  # misaligned
+    assert rc == pb.PA_ERR_WORKSPACE
+
+
+def test_calls_fail_cleanly_without_a_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    a = args(max_seq_len=256, num_blocks=16)
+    o = pb.pa_decode_opts(pb.PA_MODE_SINGLE, 0, 0, 0, None, None)
+    assert pb.lib.pa_decode_ex(ctypes.byref(a), ctypes.byref(o), None, 0, None) == pb.PA_ERR_CUDA
+    st = ctypes.c_int(0)
+    assert pb.lib.pa_get_device_status(None, ctypes.byref(st)) == pb.PA_ERR_CUDA
+    pb.pa_release_workspace()  # nothing allocated: a no-op
