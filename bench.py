@@ -146,6 +146,18 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(use), "in_region": bool(inside)}
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The slowest rank's time: every rank passes its own, all get the max."""
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_step: int, steps: int, world: int, elapsed_max: float) -> float:
+    """Whole-job K/V GB/s: every rank runs the same workload (replicas)."""
+    return world * bytes_per_step * steps / elapsed_max / 1e9
+
+
 def kernel_hash():
     h = hashlib.sha256()
     for p in (KERNEL_SRC, os.path.join(ROOT, "paged_kv_cache_308_gb300", "csrc", "pa_internal.h")):
@@ -307,14 +319,12 @@ def run_gpu(args):
         pg.barrier()
     sampler.stop()
     if pg:
-        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed = float(t.item())
+        elapsed = max_over_ranks(elapsed, pg, dev)
     assert pb.pa_get_device_status() == 0
 
     peak, peak_kind = hbm_peak()
     kv = w.kv_bytes
-    value = world * kv * args.steps / elapsed / 1e9
+    value = aggregate_gbs(kv, args.steps, world, elapsed)
     per_gpu = kv * args.steps / elapsed / 1e9
 
     # roofline: the partition kernel alone, timed by events the library records
@@ -322,6 +332,10 @@ def run_gpu(args):
     ws = pb.alloc_workspace(plan, dev)
     nrep = max(20, min(args.steps, 500))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
+    for e0, e1 in evs:  # torch creates the CUDA event on its first record
+        e0.record(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
     for e0, e1 in evs:
         pb.pa_decode_ex(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
                         w.head_dim, w.block_size, w.scale, stream, max_seq_len=w.max_seq_len, workspace=ws,

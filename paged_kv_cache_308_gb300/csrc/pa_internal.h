@@ -10,8 +10,14 @@
 namespace pa {
 
 constexpr int kBlockSize = 16;    // tokens per KV block (one MMA M-tile of tokens)
-constexpr int kWarps = 4;         // warps per partition CTA; each owns a ring of stages
-constexpr int kStages = 2;        // stages per warp; one stage = K and V of one block
+#ifndef PA_WARPS
+#define PA_WARPS 4
+#endif
+#ifndef PA_STAGES
+#define PA_STAGES 2
+#endif
+constexpr int kWarps = PA_WARPS;    // warps per partition CTA; each owns a ring of stages
+constexpr int kStages = PA_STAGES;  // stages per warp; one stage = K and V of one block
 constexpr int kMaxGroup = 8;      // query heads per kv head: the MMA N dimension
 constexpr int kReduceThreads = 256;
 constexpr int kReduceSlice = 64;  // head_dim elements per reduce CTA
