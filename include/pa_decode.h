@@ -171,6 +171,35 @@ const char* pa_status_string(int status);
 /* Free the library-owned workspaces of every device (synchronises them). */
 void pa_release_workspace(void);
 
+/* Size of the fixed device scratch that pa_decode_noalloc uses (16 MiB). */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Decode attention without any device allocation, for callers that cannot
+ * call cudaMalloc: a framework that owns every byte of device memory through
+ * its own pool, a decode loop that cannot pay the synchronisation of an
+ * allocation, code running where allocating CUDA calls are not allowed.  The
+ * pages this library follows have no counterpart to this call.
+ *
+ * Arguments, layouts, modes (AUTO) and results are those of pa_decode.  The
+ * split-KV partials go to a file-scope device array of
+ * PA_NOALLOC_SCRATCH_BYTES that each GPU loading the library holds until the
+ * process exits.
+ *  - A call whose partials need more (see pa_decode_plan's workspace_bytes)
+ *    returns PA_ERR_WORKSPACE without launching anything.  At the 24-head,
+ *    head_dim-256, 512-token-partition shape that is about 64 sequence-
+ *    partitions per MiB, e.g. one 100K-token sequence needs 4.95 MB.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current, so make that first call before any stream capture.
+ *  - All calls on a device share the one array: calls that overlap on the
+ *    GPU (other streams, other host threads) race and give wrong outputs.
+ *    Calls queued on a single stream are safe.
+ *  - Nothing in the array has to start at zero: each call writes every partial
+ *    it reads. */
+int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                      int max_blocks_per_seq, int max_seq_len, int64_t num_blocks, int num_heads,
+                      int num_kv_heads, int head_dim, int block_size, float scale, pa_stream_t stream);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int pa_version(void);
 

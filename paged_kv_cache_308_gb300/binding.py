@@ -246,3 +246,20 @@ def decode_workload(w, out: Optional[torch.Tensor] = None, stream=None, **opt) -
         pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
                   w.head_dim, w.block_size, w.scale, stream, max_seq_len=w.max_seq_len)
     return out
+
+
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_kv_heads, head_dim,
+                      block_size, scale, stream=None, *, max_seq_len: int) -> None:
+    """The no-allocation call: the partials live in the library's fixed device
+    scratch (PA_NOALLOC_SCRATCH_BYTES); raises PaDecodeError on a non-zero code."""
+    fn = lib.pa_decode_noalloc
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    fn.restype = i32
+    fn.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int64, i32, i32, i32, i32, ctypes.c_float, vp]
+    _check_tensors(out, q, k_cache, v_cache, block_tables, seq_lens)
+    rc = fn(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+            seq_lens.data_ptr(), int(seq_lens.shape[0]), int(block_tables.shape[1]), int(max_seq_len),
+            int(k_cache.shape[0]), int(num_heads), int(num_kv_heads), int(head_dim), int(block_size), float(scale),
+            _stream_handle(stream))
+    if rc != PA_OK:
+        raise PaDecodeError(rc, "pa_decode_noalloc")
