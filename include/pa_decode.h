@@ -129,7 +129,7 @@ typedef struct {
     int threads;           /* threads per partition CTA */
     int smem_bytes;        /* dynamic shared memory per partition CTA */
     int launch_reduce;     /* 1 if the reduce kernel runs */
-    int reduce_grid_x, reduce_grid_y, reduce_grid_z; /* heads, sequences, head_dim/64 */
+    int reduce_grid_x, reduce_grid_y, reduce_grid_z; /* heads, sequences, head_dim/32 */
     size_t workspace_bytes; /* caller workspace pa_decode_ex needs (0 when no reduce) */
 } pa_decode_plan_t;
 

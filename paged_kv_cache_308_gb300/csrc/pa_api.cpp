@@ -33,11 +33,28 @@ size_t split_workspace_bytes(long long num_seqs, long long num_heads, long long 
     return align_up(rows * 4, kWsAlign) * 2 + align_up(rows * head_dim * 4, kWsAlign);
 }
 
+// SM count of the current device, cached per device.
 int query_sm_count(int* num_sms) {
+    static int cached[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices && cached[dev] > 0) {
+        *num_sms = cached[dev];
+        return PA_OK;
+    }
     if (cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) cached[dev] = *num_sms;
     return PA_OK;
+}
+
+// Head_dim slice of one reduce CTA: the widest slice that still gives the
+// reduce grid about four CTAs per SM, so a large batch runs few, wide CTAs
+// (short launch and latency chains) and a single long sequence runs narrow
+// ones (more loads in flight per partial).
+int reduce_slice(int head_dim, long long pairs, int num_sms) {
+    for (int w = head_dim; w > pa::kReduceMinSlice; w /= 2)
+        if (pairs * (head_dim / w) >= 4ll * num_sms) return w;
+    return pa::kReduceMinSlice;
 }
 
 int validate(const pa_decode_args* a, const pa_decode_opts* o) {
@@ -70,6 +87,9 @@ int validate(const pa_decode_args* a, const pa_decode_opts* o) {
 int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_decode_plan_t* plan) {
     int rc = validate(a, o);
     if (rc) return rc;
+    // The SM count only shapes the reduce grid; without a device the launch
+    // reports the error later, so a failed query just plans for one SM.
+    if (num_sms <= 0 && query_sm_count(&num_sms) != PA_OK) num_sms = 1;
     memset(plan, 0, sizeof(*plan));
     const int bs = a->block_size;
     const int part = (o && o->partition_size > 0) ? o->partition_size : kDefaultPartition;
@@ -79,7 +99,6 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         // A sequence that fits one partition needs no reduce.  Otherwise split:
         // with few (sequence, kv head) pairs a single-pass grid leaves most of
         // the SMs idle, and with many its time is set by the longest sequence.
-        (void)num_sms;
         mode = split_parts <= 1 ? PA_MODE_SINGLE : PA_MODE_SPLIT;
     }
     plan->mode = mode;
@@ -99,7 +118,7 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     if (plan->launch_reduce) {
         plan->reduce_grid_x = a->num_heads;
         plan->reduce_grid_y = a->num_seqs;
-        plan->reduce_grid_z = a->head_dim / pa::kReduceSlice;
+        plan->reduce_grid_z = a->head_dim / reduce_slice(a->head_dim, (long long)a->num_seqs * a->num_heads, num_sms);
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->grid_x, a->head_dim);
     }
     return PA_OK;
@@ -159,6 +178,8 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     pa::PartitionParams prm;
     prm.out = static_cast<__half*>(a->out);
     prm.q = static_cast<const __half*>(a->q);
+    prm.k_cache = static_cast<const __half*>(a->k_cache);
+    prm.v_cache = static_cast<const __half*>(a->v_cache);
     prm.block_tables = a->block_tables;
     prm.seq_lens = a->seq_lens;
     prm.max_logits = plan.launch_reduce ? reinterpret_cast<float*>(w) : nullptr;
@@ -197,8 +218,8 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
         rp.max_seq_len = a->max_seq_len;
         rp.partition_size = plan.partition_size;
         rp.max_partitions = plan.grid_x;
-        if (pa::launch_reduce(a->head_dim, rp, dim3(plan.reduce_grid_x, plan.reduce_grid_y, plan.reduce_grid_z),
-                              stream) != cudaSuccess)
+        if (pa::launch_reduce(a->head_dim, a->head_dim / plan.reduce_grid_z, rp,
+                              dim3(plan.reduce_grid_x, plan.reduce_grid_y, plan.reduce_grid_z), stream) != cudaSuccess)
             return PA_ERR_CUDA;
     }
     return PA_OK;
@@ -241,10 +262,6 @@ extern "C" {
 
 int pa_decode_plan(const pa_decode_args* args, const pa_decode_opts* opts, int num_sms, pa_decode_plan_t* plan) {
     if (!plan || num_sms < 0) return PA_ERR_INVALID_ARG;
-    if (num_sms == 0) {
-        int rc = query_sm_count(&num_sms);
-        if (rc) return rc;
-    }
     return make_plan(args, opts, num_sms, plan);
 }
 

@@ -11,21 +11,27 @@ namespace pa {
 
 constexpr int kBlockSize = 16;    // tokens per KV block (one MMA M-tile of tokens)
 #ifndef PA_WARPS
-#define PA_WARPS 4
+#define PA_WARPS 2
 #endif
 #ifndef PA_STAGES
 #define PA_STAGES 2
 #endif
-constexpr int kWarps = PA_WARPS;    // warps per partition CTA; each owns a ring of stages
-constexpr int kStages = PA_STAGES;  // stages per warp; one stage = K and V of one block
+#ifndef PA_PREFETCH
+#define PA_PREFETCH 0
+#endif
+constexpr int kWarps = PA_WARPS;       // warps per partition CTA; each owns a ring of stages
+constexpr int kStages = PA_STAGES;     // stages per warp; one stage = K and V of one block
+constexpr int kPrefetch = PA_PREFETCH; // blocks per warp prefetched into L2 beyond the staged ones
 constexpr int kMaxGroup = 8;      // query heads per kv head: the MMA N dimension
 constexpr int kReduceThreads = 256;
-constexpr int kReduceSlice = 64;  // head_dim elements per reduce CTA
+constexpr int kReduceMinSlice = 32;  // narrowest head_dim slice of a reduce CTA
 constexpr unsigned kDefaultWaitLimit = 1u << 20;
 
 struct PartitionParams {
     __half* out;
     const __half* q;
+    const __half* k_cache;  // for L2 prefetches (the staged copies go through the tensor maps)
+    const __half* v_cache;
     const int32_t* block_tables;
     const int32_t* seq_lens;
     float* max_logits;  // [B][H][max_partitions], log2 domain
@@ -57,10 +63,11 @@ int partition_smem_bytes(int head_dim);
 cudaError_t launch_partition(int head_dim, const PartitionParams& prm, const CUtensorMap& tmap_k,
                              const CUtensorMap& tmap_v, dim3 grid, cudaStream_t stream);
 
-// Launched with programmatic dependent launch so its start-up overlaps the
-// tail of the partition kernel; the kernel waits on the dependency before it
-// reads any partial.
-cudaError_t launch_reduce(int head_dim, const ReduceParams& prm, dim3 grid, cudaStream_t stream);
+// Both kernels are launched as programmatic dependents of the preceding work
+// on the stream, so their start-up overlaps its tail; each waits on the
+// dependency before it reads any memory.  `width` is the head_dim slice of a
+// reduce CTA (32, 64, 128 or 256, at most head_dim).
+cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3 grid, cudaStream_t stream);
 
 // Read and clear the status word of the current device (synchronises stream).
 cudaError_t read_and_clear_status(cudaStream_t stream, int* status);

@@ -85,6 +85,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) at `src` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -146,8 +151,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     pa_partition_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         const PartitionParams prm) {
     using S = PartitionShape<D>;
-    // Let a dependent reduce launch start its CTAs as soon as the SMs free up;
-    // it still waits for this grid's completion before touching the partials.
+    // Launched as a programmatic dependent of whatever precedes it on the
+    // stream: the CTAs may become resident early, but nothing is read before
+    // the preceding grid has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Let the dependent reduce launch its CTAs as soon as SMs free up; it
+    // still waits for this grid's completion before touching the partials.
     asm volatile("griddepcontrol.launch_dependents;");
 
     extern __shared__ uint8_t smem_raw[];
@@ -161,8 +170,27 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = prm.group, H = prm.num_heads;
+    const int blocks_per_part = prm.partition_size / kBlockSize;
+    const int blk0 = p * blocks_per_part;
+    const int32_t* bt = prm.block_tables + (size_t)b * prm.max_blocks_per_seq + blk0;
 
-    const int L = prm.seq_lens[b];
+    // Block ids of this warp's iterations, 32 at a time: lane k of batch n holds
+    // the id of iteration 32n + k (block j = warp + it * kWarps of the partition).
+    // The first batch is read before the sequence length is known, bounded by
+    // the block-table row, so the two loads overlap.
+    const int jmax = max(0, min(blocks_per_part, prm.max_blocks_per_seq - blk0));
+    int ids_copy = (warp + lane * kWarps) < jmax ? __ldg(bt + warp + lane * kWarps) : -1;
+    const int L = __ldg(prm.seq_lens + b);
+    int ids_pf = ids_copy, batch_copy = 0, batch_pf = 0;
+    auto block_id = [&](int& ids, int& batch, int it) {
+        if ((it >> 5) != batch) {
+            batch = it >> 5;
+            const int j = warp + ((it & ~31) + lane) * kWarps;
+            ids = j < jmax ? __ldg(bt + j) : -1;
+        }
+        return __shfl_sync(kFull, ids, it & 31);
+    };
+
     if (L < 0 || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) {
         if (p == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(&g_status, PA_DEV_BAD_SEQ_LEN);
         return;
@@ -175,8 +203,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     const int n_part = (L + prm.partition_size - 1) / prm.partition_size;
     if (p >= n_part) return;
-    const int blocks_per_part = prm.partition_size / kBlockSize;
-    const int blk0 = p * blocks_per_part;
     const int nblk = min(blocks_per_part, (L + kBlockSize - 1) / kBlockSize - blk0);
 
     const uint32_t stage0 = smem_addr(smem) + warp * kStages * S::kStageBytes;
@@ -188,38 +214,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     __syncthreads();
 
-    const int g = lane >> 2, c = lane & 3;  // MMA fragment row group / column pair
-
-    // Q^T as the B operand of S^T = K . Q^T: lane holds head g, dims 16ks + 2c (+1) and +8.
-    uint32_t qb[S::kSteps][2];
-    {
-        const int hq = g < G ? g : 0;  // lanes of padding heads load nothing
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(prm.q + ((size_t)b * H + kvh * G + hq) * D);
-#pragma unroll
-        for (int ks = 0; ks < S::kSteps; ++ks) {
-            qb[ks][0] = g < G ? __ldg(qrow + 8 * ks + c) : 0u;
-            qb[ks][1] = g < G ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
-        }
-    }
-
-    float o[S::kSteps][4];
-#pragma unroll
-    for (int i = 0; i < S::kSteps; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 domain) of heads 2c, 2c+1
-    float l0 = 0.f, l1 = 0.f;              // this lane's share of the exp sums
-
     // Blocks j = warp, warp + kWarps, ... of the partition belong to this warp.
     const int nmine = warp < nblk ? (nblk - warp + kWarps - 1) / kWarps : 0;
-    const int32_t* bt = prm.block_tables + (size_t)b * prm.max_blocks_per_seq + blk0;
-    int ids = -1;             // lane k holds the block id of this warp's iteration 32*(it/32) + k
     uint32_t valid_bits = 0;  // stage s holds a block with a legal id
 
+    // Stage the K and V of iteration `it` into stage it % kStages.
     auto issue = [&](int it) {
-        if ((it & 31) == 0) {
-            const int j = warp + (it + lane) * kWarps;
-            ids = j < nblk ? __ldg(bt + j) : -1;
-        }
-        const int phys = __shfl_sync(kFull, ids, it & 31);
+        const int phys = block_id(ids_copy, batch_copy, it);
         const int s = it % kStages;
         const uint32_t bar = bar0 + 8 * s;
         const bool ok = phys >= 0 && (long long)phys < prm.num_blocks;
@@ -240,8 +241,39 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             }
         }
     };
+    // Pull the K and V of iteration `it` from HBM into L2 ahead of its copy, so
+    // more bytes are in flight than the shared-memory stages alone allow.
+    auto prefetch = [&](int it) {
+        const int phys = block_id(ids_pf, batch_pf, it);
+        if (lane == 1 && phys >= 0 && (long long)phys < prm.num_blocks) {
+            const size_t off = ((size_t)phys * prm.num_kv_heads + kvh) * (kBlockSize * D);
+            prefetch_l2(prm.k_cache + off, S::kTileBytes);
+            prefetch_l2(prm.v_cache + off, S::kTileBytes);
+        }
+    };
 
     for (int it = 0; it < kStages && it < nmine; ++it) issue(it);
+    for (int it = kStages; it < kStages + kPrefetch && it < nmine; ++it) prefetch(it);
+
+    const int g = lane >> 2, c = lane & 3;  // MMA fragment row group / column pair
+
+    // Q^T as the B operand of S^T = K . Q^T: lane holds head g, dims 16ks + 2c (+1) and +8.
+    uint32_t qb[S::kSteps][2];
+    {
+        const int hq = g < G ? g : 0;  // lanes of padding heads load nothing
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(prm.q + ((size_t)b * H + kvh * G + hq) * D);
+#pragma unroll
+        for (int ks = 0; ks < S::kSteps; ++ks) {
+            qb[ks][0] = g < G ? __ldg(qrow + 8 * ks + c) : 0u;
+            qb[ks][1] = g < G ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
+        }
+    }
+
+    float o[S::kSteps][4];
+#pragma unroll
+    for (int i = 0; i < S::kSteps; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 domain) of heads 2c, 2c+1
+    float l0 = 0.f, l1 = 0.f;              // this lane's share of the exp sums
 
     const float sl2 = prm.scale_log2;
     const int mi = lane >> 3, r8 = lane & 7;
@@ -330,6 +362,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         }
         __syncwarp();
         if (i + kStages < nmine) issue(i + kStages);
+        if (kPrefetch > 0 && i + kStages + kPrefetch < nmine) prefetch(i + kStages + kPrefetch);
     }
 
     if (timed_out) {
@@ -401,14 +434,23 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
 }
 
-// Phase 2: out[b, h] = sum_p w_p acc_p / sum_p w_p with w_p = l_p 2^(m_p - M),
-// M = max_p m_p (the log-sum-exp merge of the partials).  One CTA per
-// (head, sequence, 64-wide slice of head_dim); 16 threads cover the slice with
-// float4 loads and 16 groups stride over the partitions; the summation order
-// is fixed, so results are deterministic.
-template <int D>
+// Phase 2: merge the partials of each (sequence, head).  With M = max_p m_p,
+// out = sum_p w_p acc_p / sum_p w_p and w_p = l_p 2^(m_p - M): the
+// log-sum-exp merge.  One CTA per (head, sequence, W-wide slice of head_dim);
+// W/4 threads cover the slice with float4 loads and the remaining factor of
+// the 256 threads strides over the partitions.  Each thread folds its
+// partitions in order with the alpha/beta rescale of the
+// "paged_attention_v2_triton.py" commit page (running max m, alpha =
+// 2^(m_old - m_new), beta = l_p 2^(m_p - m_new)), so no separate pass for
+// the max is needed; the groups are then merged by the same rule in a fixed
+// order, which keeps results deterministic.
+template <int D, int W>
 __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceParams prm) {
+    constexpr int kLanes = W / 4;                    // float4 columns of a slice
+    constexpr int kGroups = kReduceThreads / kLanes; // partition groups
+    static_assert(W <= D && D % W == 0 && kLanes <= kReduceThreads, "slice width");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int h = blockIdx.x, b = blockIdx.y, slice = blockIdx.z;
     const int L = prm.seq_lens[b];
     // single-partition, empty and invalid sequences were finished by the partition kernel
@@ -418,47 +460,47 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
     const float* ml = prm.max_logits + base;
     const float* el = prm.exp_sums + base;
 
-    __shared__ float red_max[kReduceThreads / 32];
-    __shared__ float4 red_acc[16][16];
-    __shared__ float red_w[16];
+    __shared__ float4 red_acc[kGroups][kLanes];
+    __shared__ float red_m[kGroups];
+    __shared__ float red_w[kGroups];
 
-    float M = -INFINITY;
-    for (int p = threadIdx.x; p < n; p += kReduceThreads) M = fmaxf(M, ml[p]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    if ((threadIdx.x & 31) == 0) red_max[threadIdx.x >> 5] = M;
-    __syncthreads();
-    M = red_max[0];
-#pragma unroll
-    for (int w = 1; w < kReduceThreads / 32; ++w) M = fmaxf(M, red_max[w]);
-
-    const int lane16 = threadIdx.x & 15, pg = threadIdx.x >> 4;
-    const float4* tp = reinterpret_cast<const float4*>(prm.tmp_out + base * D + slice * kReduceSlice) + lane16;
+    const int col = threadIdx.x % kLanes, pg = threadIdx.x / kLanes;
+    const float4* tp = reinterpret_cast<const float4*>(prm.tmp_out + base * D + slice * W) + col;
+    float m = -INFINITY, wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
 #pragma unroll 4
-    for (int p = pg; p < n; p += 16) {
-        const float w = el[p] * exp2f(ml[p] - M);
+    for (int p = pg; p < n; p += kGroups) {
+        const float mp = ml[p], lp = el[p];
         const float4 t = tp[(size_t)p * (D / 4)];
-        wsum += w;
-        acc.x += w * t.x;
-        acc.y += w * t.y;
-        acc.z += w * t.z;
-        acc.w += w * t.w;
+        const float mn = fmaxf(m, mp);
+        const float alpha = exp2f(m - mn);  // 0 on the first partition (m = -inf)
+        const float beta = lp * exp2f(mp - mn);
+        wsum = wsum * alpha + beta;
+        acc.x = acc.x * alpha + beta * t.x;
+        acc.y = acc.y * alpha + beta * t.y;
+        acc.z = acc.z * alpha + beta * t.z;
+        acc.w = acc.w * alpha + beta * t.w;
+        m = mn;
     }
-    red_acc[pg][lane16] = acc;
-    if (lane16 == 0) red_w[pg] = wsum;
+    red_acc[pg][col] = acc;
+    if (col == 0) {
+        red_m[pg] = m;
+        red_w[pg] = wsum;
+    }
     __syncthreads();
-    if (threadIdx.x < kReduceSlice) {
+    if (threadIdx.x < W) {
         const int dl = threadIdx.x;
-        float sum = 0.f, W = 0.f;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            const float4 v = red_acc[q][dl >> 2];
-            sum += (dl & 3) == 0 ? v.x : (dl & 3) == 1 ? v.y : (dl & 3) == 2 ? v.z : v.w;
-            W += red_w[q];
+        float M = -INFINITY;
+#pragma unroll 8
+        for (int q = 0; q < kGroups; ++q) M = fmaxf(M, red_m[q]);
+        float sum = 0.f, wt = 0.f;
+#pragma unroll 8
+        for (int q = 0; q < kGroups; ++q) {
+            const float f = red_m[q] == -INFINITY ? 0.f : exp2f(red_m[q] - M);  // groups without partitions
+            sum += f * reinterpret_cast<const float*>(red_acc[q])[dl];
+            wt += f * red_w[q];
         }
-        prm.out[((size_t)b * prm.num_heads + h) * D + slice * kReduceSlice + dl] = __float2half_rn(sum / W);
+        prm.out[((size_t)b * prm.num_heads + h) * D + slice * W + dl] = __float2half_rn(sum / wt);
     }
 }
 
@@ -473,6 +515,13 @@ int partition_smem_bytes(int head_dim) {
 
 namespace {
 
+cudaLaunchAttribute pdl_attribute() {
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
 template <int D>
 cudaError_t launch_partition_t(const PartitionParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                                cudaStream_t stream) {
@@ -481,25 +530,44 @@ cudaError_t launch_partition_t(const PartitionParams& prm, const CUtensorMap& tk
     // keeps multi-device processes correct.
     cudaError_t e = cudaFuncSetAttribute(pa_partition_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    pa_partition_kernel<D><<<grid, kWarps * 32, smem, stream>>>(tk, tv, prm);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, pa_partition_kernel<D>, tk, tv, prm);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, int W>
 cudaError_t launch_reduce_t(const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kReduceThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, pa_reduce_kernel<D>, prm);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, pa_reduce_kernel<D, W>, prm);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_reduce_d(int width, const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
+    switch (width) {
+        case 32: return launch_reduce_t<D, 32>(prm, grid, stream);
+        case 64: return launch_reduce_t<D, 64>(prm, grid, stream);
+        case 128: if constexpr (D >= 128) return launch_reduce_t<D, 128>(prm, grid, stream); else break;
+        case 256: if constexpr (D >= 256) return launch_reduce_t<D, 256>(prm, grid, stream); else break;
+        default: break;
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -514,11 +582,11 @@ cudaError_t launch_partition(int head_dim, const PartitionParams& prm, const CUt
     }
 }
 
-cudaError_t launch_reduce(int head_dim, const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
+cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
     switch (head_dim) {
-        case 64: return launch_reduce_t<64>(prm, grid, stream);
-        case 128: return launch_reduce_t<128>(prm, grid, stream);
-        case 256: return launch_reduce_t<256>(prm, grid, stream);
+        case 64: return launch_reduce_d<64>(width, prm, grid, stream);
+        case 128: return launch_reduce_d<128>(width, prm, grid, stream);
+        case 256: return launch_reduce_d<256>(width, prm, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

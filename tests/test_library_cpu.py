@@ -56,7 +56,7 @@ def test_plan_long_context_splits_into_512_token_partitions():
     assert pl["mode"] == pb.PA_MODE_SPLIT and pl["partition_size"] == 512
     assert (pl["grid_x"], pl["grid_y"], pl["grid_z"]) == (200, 4, 1)      # 800 CTAs on kv heads
     assert pl["launch_reduce"] == 1
-    assert (pl["reduce_grid_x"], pl["reduce_grid_y"], pl["reduce_grid_z"]) == (24, 1, 4)
+    assert (pl["reduce_grid_x"], pl["reduce_grid_y"], pl["reduce_grid_z"]) == (24, 1, 8)
     assert pl["workspace_bytes"] == ws_bytes(1, 24, 200, 256)
     assert pl["workspace_bytes"] == pb.pa_decode_workspace_size(1, 102400, 24, 256, 512)
 
@@ -108,7 +108,7 @@ def test_plan_rejects_bad_options():
 @pytest.mark.parametrize("D", [64, 128, 256])
 def test_plan_accepts_supported_shapes(G, D):
     rc, pl = plan(args(H=4 * G, Hkv=4, D=D))
-    assert rc == 0 and pl["threads"] == 128 and 0 < pl["smem_bytes"] <= 227 * 1024
+    assert rc == 0 and pl["threads"] % 32 == 0 and 0 < pl["smem_bytes"] <= 227 * 1024
 
 
 def test_decode_ex_checks_workspace_before_any_cuda_call():
@@ -130,3 +130,11 @@ def test_calls_fail_cleanly_without_a_device():
     st = ctypes.c_int(0)
     assert pb.lib.pa_get_device_status(None, ctypes.byref(st)) == pb.PA_ERR_CUDA
     pb.pa_release_workspace()  # nothing allocated: a no-op
+
+
+@pytest.mark.parametrize("B,L,z", [(1, 102400, 8), (4, 32768, 8), (8, 8192, 4), (64, 65536, 1), (16, 4096, 2)])
+def test_reduce_slice_follows_the_batch(B, L, z):
+    # the widest head_dim slice that still gives >= 4 reduce CTAs per SM
+    rc, pl = plan(args(num_seqs=B, max_seq_len=L, num_blocks=B * L // 16))
+    assert rc == 0 and pl["launch_reduce"] == 1
+    assert pl["reduce_grid_z"] == z and (pl["reduce_grid_x"], pl["reduce_grid_y"]) == (24, B)
