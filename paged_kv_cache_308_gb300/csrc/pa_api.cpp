@@ -161,6 +161,10 @@ int make_cache_map(CUtensorMap* map, const void* base, const pa_decode_args* a) 
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// Diagnostic builds (-DPA_TRACE): device buffer for per-CTA timestamps of
+// the partition kernel, 5 x 8 bytes per CTA, set by pa_debug_set_trace.
+unsigned long long* g_trace = nullptr;
+
 int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_bytes, cudaStream_t stream,
         const pa_decode_plan_t& plan) {
     if (a->num_seqs == 0) return PA_OK;
@@ -196,6 +200,7 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
     prm.wait_limit = (o && o->wait_limit) ? o->wait_limit : pa::kDefaultWaitLimit;
     prm.force_timeout = (o && (o->flags & PA_FLAG_FORCE_TIMEOUT)) ? 1 : 0;
+    prm.trace = g_trace;
 
     if (o && o->event_partition_begin &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_begin), stream) != cudaSuccess)
@@ -342,5 +347,10 @@ void pa_release_workspace(void) {
 }
 
 int pa_version(void) { return 100; }
+
+#ifdef PA_TRACE
+// Diagnostic builds only (not part of the public header).
+void pa_debug_set_trace(void* device_buffer) { g_trace = static_cast<unsigned long long*>(device_buffer); }
+#endif
 
 }  // extern "C"

@@ -44,6 +44,9 @@ struct PartitionParams {
     float scale_log2;   // scale * log2(e)
     unsigned wait_limit;
     int force_timeout;
+    // Diagnostic builds (-DPA_TRACE) only: per-CTA records of
+    // {sm id, entry, first block ready, main loop done, exit} in globaltimer ns.
+    unsigned long long* trace;
 };
 
 struct ReduceParams {

@@ -43,6 +43,25 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+#ifdef PA_TRACE
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+#define PA_TRACE_MARK(slot)                                                                              \
+    do {                                                                                                 \
+        if (prm.trace && threadIdx.x == 0) {                                                             \
+            const size_t cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;   \
+            prm.trace[cta * 5 + (slot)] = global_ns();                                                   \
+        }                                                                                                \
+    } while (0)
+#else
+#define PA_TRACE_MARK(slot) \
+    do {                    \
+    } while (0)
+#endif
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -158,6 +177,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     // Let the dependent reduce launch its CTAs as soon as SMs free up; it
     // still waits for this grid's completion before touching the partials.
     asm volatile("griddepcontrol.launch_dependents;");
+#ifdef PA_TRACE
+    if (prm.trace && threadIdx.x == 0) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %smid;" : "=r"(smid));
+        const size_t cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        prm.trace[cta * 5 + 0] = smid;
+    }
+    PA_TRACE_MARK(1);
+#endif
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -288,6 +316,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             timed_out = true;
             break;
         }
+        if (i == 0) PA_TRACE_MARK(2);
         if ((valid_bits >> s) & 1u) {
             const int tok0 = (blk0 + warp + i * kWarps) * kBlockSize;
             const int nvalid = min(kBlockSize, L - tok0);
@@ -382,6 +411,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         l1 += __shfl_xor_sync(kFull, l1, off);
     }
     __syncthreads();  // all stages consumed; the stage area is reused below
+    PA_TRACE_MARK(3);
     if (*sm_abort) return;
 
     // Merge the kWarps partial states of this CTA (same rule, across warps).
@@ -432,6 +462,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             }
         }
     }
+    PA_TRACE_MARK(4);
 }
 
 // Phase 2: merge the partials of each (sequence, head).  With M = max_p m_p,
