@@ -414,10 +414,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     PA_TRACE_MARK(3);
     if (*sm_abort) return;
 
-    // Merge the kWarps partial states of this CTA (same rule, across warps).
-    float* red = reinterpret_cast<float*>(smem);
-    {
-        float* rw = red + warp * kMaxGroup * S::kRedStride;
+    // Merge the kWarps partial states of this CTA by the same max/rescale
+    // rule: warps 1.. leave theirs in shared memory, warp 0 folds them into its
+    // own MMA fragments with per-head factors and stores straight from registers.
+    float* red = reinterpret_cast<float*>(smem);  // [kWarps - 1][kMaxGroup][kRedStride]
+    if (warp > 0) {
+        float* rw = red + (warp - 1) * kMaxGroup * S::kRedStride;
 #pragma unroll
         for (int mt = 0; mt < S::kSteps; ++mt) {
             const int d = 16 * mt + g;
@@ -434,32 +436,80 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         }
     }
     __syncthreads();
+    if (warp != 0) return;
 
+    // Per-head factors for heads 2c and 2c + 1: M = max over warps,
+    // f_w = 2^(m_w - M) / L with L = sum_w 2^(m_w - M) l_w (warps without
+    // blocks have m_w = -inf and contribute nothing).
+    float M0 = m0, M1 = m1;
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) {
+        M0 = fmaxf(M0, sm_m[w * kMaxGroup + 2 * c]);
+        M1 = fmaxf(M1, sm_m[w * kMaxGroup + 2 * c + 1]);
+    }
+    float f0[kWarps], f1[kWarps];
+    f0[0] = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
+    f1[0] = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
+    float L0 = f0[0] * l0, L1 = f1[0] * l1;
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) {
+        const float mw0 = sm_m[w * kMaxGroup + 2 * c], mw1 = sm_m[w * kMaxGroup + 2 * c + 1];
+        f0[w] = mw0 == -INFINITY ? 0.f : exp2f(mw0 - M0);
+        f1[w] = mw1 == -INFINITY ? 0.f : exp2f(mw1 - M1);
+        L0 += f0[w] * sm_l[w * kMaxGroup + 2 * c];
+        L1 += f1[w] * sm_l[w * kMaxGroup + 2 * c + 1];
+    }
+    const float inv0 = 1.f / L0, inv1 = 1.f / L1;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        f0[w] *= inv0;
+        f1[w] *= inv1;
+    }
+    const bool has0 = 2 * c < G, has1 = 2 * c + 1 < G;  // padding heads are not written
+    const size_t head0 = (size_t)b * H + kvh * G + 2 * c;
     const bool direct = n_part == 1;
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int h = idx / D, d = idx - h * D;
-        float M = -INFINITY;
+    const size_t pi0 = head0 * prm.max_partitions + p, pi1 = pi0 + prm.max_partitions;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * kMaxGroup + h]);
-        float lsum = 0.f, acc = 0.f;
+    for (int mt = 0; mt < S::kSteps; ++mt) {
+        const int d = 16 * mt + g;
+        float v00 = f0[0] * o[mt][0], v10 = f1[0] * o[mt][1];  // (head 2c, d), (head 2c+1, d)
+        float v08 = f0[0] * o[mt][2], v18 = f1[0] * o[mt][3];  // ... at d + 8
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float mw = sm_m[w * kMaxGroup + h];
-            const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);  // warps without blocks add nothing
-            lsum += f * sm_l[w * kMaxGroup + h];
-            acc += f * red[(w * kMaxGroup + h) * S::kRedStride + d];
+        for (int w = 1; w < kWarps; ++w) {
+            const float* rw = red + (w - 1) * kMaxGroup * S::kRedStride;
+            v00 += f0[w] * rw[(2 * c) * S::kRedStride + d];
+            v10 += f1[w] * rw[(2 * c + 1) * S::kRedStride + d];
+            v08 += f0[w] * rw[(2 * c) * S::kRedStride + d + 8];
+            v18 += f1[w] * rw[(2 * c + 1) * S::kRedStride + d + 8];
         }
-        const float v = acc / lsum;
-        const size_t head = (size_t)b * H + kvh * G + h;
         if (direct) {
-            prm.out[head * D + d] = __float2half_rn(v);
-        } else {
-            const size_t pi = head * prm.max_partitions + p;
-            prm.tmp_out[pi * D + d] = v;
-            if (d == 0) {
-                prm.max_logits[pi] = M;
-                prm.exp_sums[pi] = lsum;
+            if (has0) {
+                prm.out[head0 * D + d] = __float2half_rn(v00);
+                prm.out[head0 * D + d + 8] = __float2half_rn(v08);
             }
+            if (has1) {
+                prm.out[(head0 + 1) * D + d] = __float2half_rn(v10);
+                prm.out[(head0 + 1) * D + d + 8] = __float2half_rn(v18);
+            }
+        } else {
+            if (has0) {
+                prm.tmp_out[pi0 * D + d] = v00;
+                prm.tmp_out[pi0 * D + d + 8] = v08;
+            }
+            if (has1) {
+                prm.tmp_out[pi1 * D + d] = v10;
+                prm.tmp_out[pi1 * D + d + 8] = v18;
+            }
+        }
+    }
+    if (!direct && g == 0) {
+        if (has0) {
+            prm.max_logits[pi0] = M0;
+            prm.exp_sums[pi0] = L0;
+        }
+        if (has1) {
+            prm.max_logits[pi1] = M1;
+            prm.exp_sums[pi1] = L1;
         }
     }
     PA_TRACE_MARK(4);
