@@ -66,7 +66,7 @@ typedef struct CUstream_st* pa_stream_t; /* same type as cudaStream_t */
 enum {
     PA_OK = 0,
     PA_ERR_INVALID_ARG = -1,  /* null or misaligned pointer, bad size, non-finite scale, ... */
-    PA_ERR_UNSUPPORTED = -2,  /* head_dim, block_size or GQA ratio not compiled in */
+    PA_ERR_UNSUPPORTED = -2,  /* head_dim, block_size, GQA ratio or CTA shape not compiled in */
     PA_ERR_CUDA = -3,         /* a CUDA runtime call or a kernel launch failed */
     PA_ERR_OOM = -4,          /* the library-owned workspace could not be allocated */
     PA_ERR_WORKSPACE = -5     /* caller workspace too small or not 256-byte aligned */
@@ -119,6 +119,8 @@ typedef struct {
     unsigned int wait_limit;     /* polls before a copy wait gives up; 0 = library default (2^20) */
     void* event_partition_begin; /* optional cudaEvent_t recorded on `stream` right before ... */
     void* event_partition_end;   /* ... and right after the partition kernel (timing only) */
+    int warps;                   /* partition CTA shape: warps per CTA and shared-memory stages per */
+    int stages;                  /* warp; 0/0 = library choice; compiled: 2x2, 1x2, 1x3, 4x2 */
 } pa_decode_opts;
 
 /* What a call will launch (filled by pa_decode_plan; host-only, no CUDA calls). */
@@ -131,6 +133,7 @@ typedef struct {
     int launch_reduce;     /* 1 if the reduce kernel runs */
     int reduce_grid_x, reduce_grid_y, reduce_grid_z; /* heads, sequences, head_dim/32 */
     size_t workspace_bytes; /* caller workspace pa_decode_ex needs (0 when no reduce) */
+    int stages;            /* shared-memory stages per warp of the partition CTA */
 } pa_decode_plan_t;
 
 /* Decode attention with a library-owned workspace.

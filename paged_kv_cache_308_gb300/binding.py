@@ -52,7 +52,7 @@ class pa_decode_opts(ctypes.Structure):
     _fields_ = [
         ("mode", ctypes.c_int), ("partition_size", ctypes.c_int), ("flags", ctypes.c_int),
         ("wait_limit", ctypes.c_uint), ("event_partition_begin", ctypes.c_void_p),
-        ("event_partition_end", ctypes.c_void_p),
+        ("event_partition_end", ctypes.c_void_p), ("warps", ctypes.c_int), ("stages", ctypes.c_int),
     ]
 
 
@@ -62,6 +62,7 @@ class pa_decode_plan_t(ctypes.Structure):
         ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int), ("threads", ctypes.c_int),
         ("smem_bytes", ctypes.c_int), ("launch_reduce", ctypes.c_int), ("reduce_grid_x", ctypes.c_int),
         ("reduce_grid_y", ctypes.c_int), ("reduce_grid_z", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
+        ("stages", ctypes.c_int),
     ]
 
     def as_dict(self):
@@ -141,12 +142,12 @@ def make_args(out, q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_k
 
 
 def make_opts(mode="auto", partition_size: int = 0, flags: int = 0, wait_limit: int = 0,
-              events=None) -> pa_decode_opts:
+              events=None, warps: int = 0, stages: int = 0) -> pa_decode_opts:
     m = MODES[mode] if isinstance(mode, str) else int(mode)
     ev0 = ev1 = None
     if events is not None:
         ev0, ev1 = (e.cuda_event if hasattr(e, "cuda_event") else e for e in events)
-    return pa_decode_opts(m, int(partition_size), int(flags), int(wait_limit), ev0, ev1)
+    return pa_decode_opts(m, int(partition_size), int(flags), int(wait_limit), ev0, ev1, int(warps), int(stages))
 
 
 def _check_tensors(out, q, k_cache, v_cache, block_tables, seq_lens):

@@ -68,6 +68,10 @@ int validate(const pa_decode_args* a, const pa_decode_opts* o) {
     if (o && (o->mode < PA_MODE_AUTO || o->mode > PA_MODE_SPLIT)) return PA_ERR_INVALID_ARG;
     if (o && o->partition_size < 0) return PA_ERR_INVALID_ARG;
     if (o && o->partition_size % a->block_size) return PA_ERR_INVALID_ARG;
+    if (o && (o->warps < 0 || o->stages < 0)) return PA_ERR_INVALID_ARG;
+    // every head_dim is compiled with the same set of CTA shapes
+    if (o && (o->warps || o->stages) && pa::partition_smem_bytes(256, o->warps, o->stages) < 0)
+        return PA_ERR_UNSUPPORTED;
     if (a->head_dim != 64 && a->head_dim != 128 && a->head_dim != 256) return PA_ERR_UNSUPPORTED;
     if (a->block_size != pa::kBlockSize) return PA_ERR_UNSUPPORTED;
     if (a->num_heads / a->num_kv_heads > pa::kMaxGroup) return PA_ERR_UNSUPPORTED;
@@ -84,11 +88,70 @@ int validate(const pa_decode_args* a, const pa_decode_opts* o) {
     return PA_OK;
 }
 
+// Partition CTA shape (warps, stages per warp), picked with a wave model fitted
+// to GB300 measurements.  A CTA keeps warps * stages blocks in flight, so on
+// its own it streams at most that many bytes per HBM round trip (~1.6 us);
+// the slots per SM follow from its shared memory; every wave of CTAs shares
+// the HBM bandwidth and pays ~4 us of start-up and epilogue.  The shape with
+// the smallest predicted time wins; ties go to more bytes in flight per CTA.
+// The CTA count is exact for one sequence; for a batch, whose lengths the
+// host does not see, half the grid is assumed (lengths spread up to the max).
+struct CtaShape {
+    int warps, stages;
+};
+constexpr CtaShape kShapes[] = {{2, 2}, {1, 2}, {1, 3}, {4, 2}};
+constexpr double kHbmBytesPerUs = 6.8e6;
+constexpr double kRoundTripUs = 1.6;
+constexpr double kCtaOverheadUs = 4.0;
+constexpr long long kSmemPerSm = 228 * 1024;
+
+double predict_us(int head_dim, CtaShape sh, long long ctas, double bytes_per_cta, int num_sms) {
+    const long long smem = pa::partition_smem_bytes(head_dim, sh.warps, sh.stages) + 1024;
+    long long per_sm = kSmemPerSm / smem;
+    if (per_sm > 2048 / (32 * sh.warps)) per_sm = 2048 / (32 * sh.warps);
+    if (per_sm > 32) per_sm = 32;
+    if (per_sm < 1) per_sm = 1;
+    const long long slots = per_sm * num_sms;
+    const double in_flight = (double)sh.warps * sh.stages * 2 * pa::kBlockSize * head_dim * 2;
+    const double cta_rate = in_flight / kRoundTripUs;
+    double t = 0;
+    for (long long left = ctas; left > 0; left -= slots) {
+        const long long k = left < slots ? left : slots;
+        const double share = kHbmBytesPerUs / (double)k;
+        t += bytes_per_cta / (share < cta_rate ? share : cta_rate) + kCtaOverheadUs;
+    }
+    return t;
+}
+
+void choose_shape(const pa_decode_args* a, const pa_decode_plan_t* plan, int num_sms, int* warps, int* stages) {
+    const long long grid = (long long)plan->grid_x * plan->grid_y * plan->grid_z;
+    long long ctas = a->num_seqs == 1 ? grid : grid / 2;
+    if (ctas < (long long)a->num_seqs * a->num_kv_heads) ctas = (long long)a->num_seqs * a->num_kv_heads;
+    const int tokens = plan->partition_size < a->max_seq_len ? plan->partition_size : a->max_seq_len;
+    const double bytes = (double)(tokens > 0 ? tokens : 1) * a->head_dim * 2 * 2;
+    constexpr int n = (int)(sizeof(kShapes) / sizeof(kShapes[0]));
+    double t[n], best = 0;
+    for (int i = 0; i < n; ++i) {
+        t[i] = predict_us(a->head_dim, kShapes[i], ctas, bytes, num_sms > 0 ? num_sms : 1);
+        if (i == 0 || t[i] < best) best = t[i];
+    }
+    int pick = -1;
+    for (int i = 0; i < n; ++i) {
+        if (t[i] > best + 0.1) continue;
+        const int fl = kShapes[i].warps * kShapes[i].stages;
+        if (pick < 0 || fl > kShapes[pick].warps * kShapes[pick].stages ||
+            (fl == kShapes[pick].warps * kShapes[pick].stages && kShapes[i].warps > kShapes[pick].warps))
+            pick = i;
+    }
+    *warps = kShapes[pick].warps;
+    *stages = kShapes[pick].stages;
+}
+
 int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_decode_plan_t* plan) {
     int rc = validate(a, o);
     if (rc) return rc;
-    // The SM count only shapes the reduce grid; without a device the launch
-    // reports the error later, so a failed query just plans for one SM.
+    // The SM count only shapes the CTA choice and the reduce grid; without a
+    // device the launch reports the error later, so a failed query plans for one SM.
     if (num_sms <= 0 && query_sm_count(&num_sms) != PA_OK) num_sms = 1;
     memset(plan, 0, sizeof(*plan));
     const int bs = a->block_size;
@@ -112,8 +175,11 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     }
     plan->grid_y = a->num_kv_heads;
     plan->grid_z = a->num_seqs;
-    plan->threads = pa::kWarps * 32;
-    plan->smem_bytes = pa::partition_smem_bytes(a->head_dim);
+    int warps = o ? o->warps : 0, stages = o ? o->stages : 0;
+    if (!warps) choose_shape(a, plan, num_sms, &warps, &stages);
+    plan->threads = warps * 32;
+    plan->stages = stages;
+    plan->smem_bytes = pa::partition_smem_bytes(a->head_dim, warps, stages);
     plan->launch_reduce = (mode == PA_MODE_SPLIT && plan->grid_x > 1) ? 1 : 0;
     if (plan->launch_reduce) {
         plan->reduce_grid_x = a->num_heads;
@@ -182,8 +248,6 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     pa::PartitionParams prm;
     prm.out = static_cast<__half*>(a->out);
     prm.q = static_cast<const __half*>(a->q);
-    prm.k_cache = static_cast<const __half*>(a->k_cache);
-    prm.v_cache = static_cast<const __half*>(a->v_cache);
     prm.block_tables = a->block_tables;
     prm.seq_lens = a->seq_lens;
     prm.max_logits = plan.launch_reduce ? reinterpret_cast<float*>(w) : nullptr;
@@ -205,7 +269,8 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     if (o && o->event_partition_begin &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_begin), stream) != cudaSuccess)
         return PA_ERR_CUDA;
-    if (pa::launch_partition(a->head_dim, prm, tk, tv, dim3(plan.grid_x, plan.grid_y, plan.grid_z), stream) !=
+    if (pa::launch_partition(a->head_dim, plan.threads / 32, plan.stages, prm, tk, tv,
+                             dim3(plan.grid_x, plan.grid_y, plan.grid_z), stream) !=
         cudaSuccess)
         return PA_ERR_CUDA;
     if (o && o->event_partition_end &&

@@ -10,18 +10,6 @@
 namespace pa {
 
 constexpr int kBlockSize = 16;    // tokens per KV block (one MMA M-tile of tokens)
-#ifndef PA_WARPS
-#define PA_WARPS 2
-#endif
-#ifndef PA_STAGES
-#define PA_STAGES 2
-#endif
-#ifndef PA_PREFETCH
-#define PA_PREFETCH 0
-#endif
-constexpr int kWarps = PA_WARPS;       // warps per partition CTA; each owns a ring of stages
-constexpr int kStages = PA_STAGES;     // stages per warp; one stage = K and V of one block
-constexpr int kPrefetch = PA_PREFETCH; // blocks per warp prefetched into L2 beyond the staged ones
 constexpr int kMaxGroup = 8;      // query heads per kv head: the MMA N dimension
 constexpr int kReduceThreads = 256;
 constexpr int kReduceMinSlice = 32;  // narrowest head_dim slice of a reduce CTA
@@ -30,8 +18,6 @@ constexpr unsigned kDefaultWaitLimit = 1u << 20;
 struct PartitionParams {
     __half* out;
     const __half* q;
-    const __half* k_cache;  // for L2 prefetches (the staged copies go through the tensor maps)
-    const __half* v_cache;
     const int32_t* block_tables;
     const int32_t* seq_lens;
     float* max_logits;  // [B][H][max_partitions], log2 domain
@@ -59,12 +45,13 @@ struct ReduceParams {
     int partition_size, max_partitions;
 };
 
-// Dynamic shared memory of a partition CTA for head_dim D (includes 1 KB of
-// alignment slack for the 128-byte swizzle).
-int partition_smem_bytes(int head_dim);
+// Dynamic shared memory of a partition CTA of `warps` warps with `stages`
+// stages each (includes 1 KB of alignment slack for the 128-byte swizzle);
+// -1 for a shape that is not compiled.
+int partition_smem_bytes(int head_dim, int warps, int stages);
 
-cudaError_t launch_partition(int head_dim, const PartitionParams& prm, const CUtensorMap& tmap_k,
-                             const CUtensorMap& tmap_v, dim3 grid, cudaStream_t stream);
+cudaError_t launch_partition(int head_dim, int warps, int stages, const PartitionParams& prm,
+                             const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, dim3 grid, cudaStream_t stream);
 
 // Both kernels are launched as programmatic dependents of the preceding work
 // on the stream, so their start-up overlaps its tail; each waits on the

@@ -14,9 +14,10 @@
 //   rows of D halves.  A 2-D tensor map views a cache as rows x D; each block
 //   arrives as D/64 TMA boxes of 16 rows x 64 halves (128 B) with the 128-byte
 //   swizzle, so the ldmatrix reads below hit 8 distinct bank groups.
-// * Each of the 4 warps owns kStages shared-memory stages (K and V of one
+// * Each of the NW warps of a CTA owns NS shared-memory stages (K and V of one
 //   block each), an mbarrier per stage, and a private online-softmax state;
-//   blocks of the partition are dealt round-robin to the warps.  Lane 0
+//   blocks of the partition are dealt round-robin to the warps.  Several CTA
+//   shapes (NW, NS) are compiled; the host picks one per call.  Lane 0
 //   issues the copies; every wait is bounded (no spin can hang the GPU).
 // * Scores and PV run on the tensor cores as m16n8k16 MMAs in swapped form:
 //   S^T[16 tokens x 8 heads] = K[16 x D] . Q^T[D x 8] and
@@ -104,11 +105,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) at `src` into L2.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -149,27 +145,27 @@ __device__ __forceinline__ uint32_t swz(int row, int unit) {
 
 }  // namespace
 
-template <int D>
+template <int D, int NW, int NS>
 struct PartitionShape {
     static constexpr int kSteps = D / 16;                      // k-steps of QK, m-tiles of PV
     static constexpr int kChunks = D / 64;                     // TMA boxes per K (or V) block
     static constexpr int kBoxBytes = kBlockSize * 128;         // 16 rows x 64 halves
     static constexpr int kTileBytes = kBlockSize * D * 2;      // K (or V) of one block
     static constexpr int kStageBytes = 2 * kTileBytes;         // K + V
-    static constexpr int kStageArea = kWarps * kStages * kStageBytes;
+    static constexpr int kStageArea = NW * NS * kStageBytes;
     static constexpr int kRedStride = D + 4;                   // padded row of the cross-warp reduce
-    static constexpr int kRedBytes = kWarps * kMaxGroup * kRedStride * 4;
-    static constexpr int kCtrlBytes = kWarps * kStages * 8 + 2 * kWarps * kMaxGroup * 4 + 16;
+    static constexpr int kRedBytes = NW * kMaxGroup * kRedStride * 4;
+    static constexpr int kCtrlBytes = NW * NS * 8 + 2 * NW * kMaxGroup * 4 + 16;
     static constexpr int kSmemBytes = 1024 + kStageArea + kCtrlBytes;
     static_assert(kRedBytes <= kStageArea, "cross-warp reduce must fit in the stage area");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
 };
 
-template <int D>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+template <int D, int NW, int NS>
+__global__ void __launch_bounds__(NW * 32, 1)
     pa_partition_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         const PartitionParams prm) {
-    using S = PartitionShape<D>;
+    using S = PartitionShape<D, NW, NS>;
     // Launched as a programmatic dependent of whatever precedes it on the
     // stream: the CTAs may become resident early, but nothing is read before
     // the preceding grid has completed and its writes are visible.
@@ -191,9 +187,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStageArea);
-    float* sm_m = reinterpret_cast<float*>(bars + kWarps * kStages);
-    float* sm_l = sm_m + kWarps * kMaxGroup;
-    int* sm_abort = reinterpret_cast<int*>(sm_l + kWarps * kMaxGroup);
+    float* sm_m = reinterpret_cast<float*>(bars + NW * NS);
+    float* sm_l = sm_m + NW * kMaxGroup;
+    int* sm_abort = reinterpret_cast<int*>(sm_l + NW * kMaxGroup);
 
     const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,17 +199,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int32_t* bt = prm.block_tables + (size_t)b * prm.max_blocks_per_seq + blk0;
 
     // Block ids of this warp's iterations, 32 at a time: lane k of batch n holds
-    // the id of iteration 32n + k (block j = warp + it * kWarps of the partition).
+    // the id of iteration 32n + k (block j = warp + it * NW of the partition).
     // The first batch is read before the sequence length is known, bounded by
     // the block-table row, so the two loads overlap.
     const int jmax = max(0, min(blocks_per_part, prm.max_blocks_per_seq - blk0));
-    int ids_copy = (warp + lane * kWarps) < jmax ? __ldg(bt + warp + lane * kWarps) : -1;
+    int ids_copy = (warp + lane * NW) < jmax ? __ldg(bt + warp + lane * NW) : -1;
     const int L = __ldg(prm.seq_lens + b);
-    int ids_pf = ids_copy, batch_copy = 0, batch_pf = 0;
+    int batch_copy = 0;
     auto block_id = [&](int& ids, int& batch, int it) {
         if ((it >> 5) != batch) {
             batch = it >> 5;
-            const int j = warp + ((it & ~31) + lane) * kWarps;
+            const int j = warp + ((it & ~31) + lane) * NW;
             ids = j < jmax ? __ldg(bt + j) : -1;
         }
         return __shfl_sync(kFull, ids, it & 31);
@@ -233,23 +229,23 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     if (p >= n_part) return;
     const int nblk = min(blocks_per_part, (L + kBlockSize - 1) / kBlockSize - blk0);
 
-    const uint32_t stage0 = smem_addr(smem) + warp * kStages * S::kStageBytes;
-    const uint32_t bar0 = smem_addr(bars) + warp * kStages * 8;
+    const uint32_t stage0 = smem_addr(smem) + warp * NS * S::kStageBytes;
+    const uint32_t bar0 = smem_addr(bars) + warp * NS * 8;
     if (threadIdx.x == 0) *sm_abort = 0;
     if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
-    // Blocks j = warp, warp + kWarps, ... of the partition belong to this warp.
-    const int nmine = warp < nblk ? (nblk - warp + kWarps - 1) / kWarps : 0;
+    // Blocks j = warp, warp + NW, ... of the partition belong to this warp.
+    const int nmine = warp < nblk ? (nblk - warp + NW - 1) / NW : 0;
     uint32_t valid_bits = 0;  // stage s holds a block with a legal id
 
-    // Stage the K and V of iteration `it` into stage it % kStages.
+    // Stage the K and V of iteration `it` into stage it % NS.
     auto issue = [&](int it) {
         const int phys = block_id(ids_copy, batch_copy, it);
-        const int s = it % kStages;
+        const int s = it % NS;
         const uint32_t bar = bar0 + 8 * s;
         const bool ok = phys >= 0 && (long long)phys < prm.num_blocks;
         valid_bits = ok ? (valid_bits | (1u << s)) : (valid_bits & ~(1u << s));
@@ -269,19 +265,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             }
         }
     };
-    // Pull the K and V of iteration `it` from HBM into L2 ahead of its copy, so
-    // more bytes are in flight than the shared-memory stages alone allow.
-    auto prefetch = [&](int it) {
-        const int phys = block_id(ids_pf, batch_pf, it);
-        if (lane == 1 && phys >= 0 && (long long)phys < prm.num_blocks) {
-            const size_t off = ((size_t)phys * prm.num_kv_heads + kvh) * (kBlockSize * D);
-            prefetch_l2(prm.k_cache + off, S::kTileBytes);
-            prefetch_l2(prm.v_cache + off, S::kTileBytes);
-        }
-    };
-
-    for (int it = 0; it < kStages && it < nmine; ++it) issue(it);
-    for (int it = kStages; it < kStages + kPrefetch && it < nmine; ++it) prefetch(it);
+    for (int it = 0; it < NS && it < nmine; ++it) issue(it);
 
     const int g = lane >> 2, c = lane & 3;  // MMA fragment row group / column pair
 
@@ -310,15 +294,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     int i = 0;
     bool timed_out = false;
     for (; i < nmine; ++i) {
-        const int s = i % kStages;
+        const int s = i % NS;
         const uint32_t bar = bar0 + 8 * s;
-        if (prm.force_timeout || !mbar_wait(bar, (i / kStages) & 1, prm.wait_limit)) {
+        if (prm.force_timeout || !mbar_wait(bar, (i / NS) & 1, prm.wait_limit)) {
             timed_out = true;
             break;
         }
         if (i == 0) PA_TRACE_MARK(2);
         if ((valid_bits >> s) & 1u) {
-            const int tok0 = (blk0 + warp + i * kWarps) * kBlockSize;
+            const int tok0 = (blk0 + warp + i * NW) * kBlockSize;
             const int nvalid = min(kBlockSize, L - tok0);
             const uint32_t kst = stage0 + s * S::kStageBytes, vst = kst + S::kTileBytes;
 
@@ -390,14 +374,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             }
         }
         __syncwarp();
-        if (i + kStages < nmine) issue(i + kStages);
-        if (kPrefetch > 0 && i + kStages + kPrefetch < nmine) prefetch(i + kStages + kPrefetch);
+        if (i + NS < nmine) issue(i + NS);
     }
 
     if (timed_out) {
         // Drain this warp's copies still in flight before the CTA may exit.
-        for (int k = i; k < nmine && k < i + kStages; ++k)
-            mbar_wait(bar0 + 8 * (k % kStages), (k / kStages) & 1, kDefaultWaitLimit);
+        for (int k = i; k < nmine && k < i + NS; ++k)
+            mbar_wait(bar0 + 8 * (k % NS), (k / NS) & 1, kDefaultWaitLimit);
         if (lane == 0) {
             atomicOr(&g_status, PA_DEV_TIMEOUT);
             atomicExch(sm_abort, 1);
@@ -414,10 +397,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     PA_TRACE_MARK(3);
     if (*sm_abort) return;
 
-    // Merge the kWarps partial states of this CTA by the same max/rescale
+    // Merge the NW partial states of this CTA by the same max/rescale
     // rule: warps 1.. leave theirs in shared memory, warp 0 folds them into its
     // own MMA fragments with per-head factors and stores straight from registers.
-    float* red = reinterpret_cast<float*>(smem);  // [kWarps - 1][kMaxGroup][kRedStride]
+    float* red = reinterpret_cast<float*>(smem);  // [NW - 1][kMaxGroup][kRedStride]
     if (warp > 0) {
         float* rw = red + (warp - 1) * kMaxGroup * S::kRedStride;
 #pragma unroll
@@ -443,16 +426,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     // blocks have m_w = -inf and contribute nothing).
     float M0 = m0, M1 = m1;
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) {
+    for (int w = 1; w < NW; ++w) {
         M0 = fmaxf(M0, sm_m[w * kMaxGroup + 2 * c]);
         M1 = fmaxf(M1, sm_m[w * kMaxGroup + 2 * c + 1]);
     }
-    float f0[kWarps], f1[kWarps];
+    float f0[NW], f1[NW];
     f0[0] = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
     f1[0] = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
     float L0 = f0[0] * l0, L1 = f1[0] * l1;
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) {
+    for (int w = 1; w < NW; ++w) {
         const float mw0 = sm_m[w * kMaxGroup + 2 * c], mw1 = sm_m[w * kMaxGroup + 2 * c + 1];
         f0[w] = mw0 == -INFINITY ? 0.f : exp2f(mw0 - M0);
         f1[w] = mw1 == -INFINITY ? 0.f : exp2f(mw1 - M1);
@@ -461,7 +444,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     const float inv0 = 1.f / L0, inv1 = 1.f / L1;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
         f0[w] *= inv0;
         f1[w] *= inv1;
     }
@@ -475,7 +458,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         float v00 = f0[0] * o[mt][0], v10 = f1[0] * o[mt][1];  // (head 2c, d), (head 2c+1, d)
         float v08 = f0[0] * o[mt][2], v18 = f1[0] * o[mt][3];  // ... at d + 8
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) {
+        for (int w = 1; w < NW; ++w) {
             const float* rw = red + (w - 1) * kMaxGroup * S::kRedStride;
             v00 += f0[w] * rw[(2 * c) * S::kRedStride + d];
             v10 += f1[w] * rw[(2 * c + 1) * S::kRedStride + d];
@@ -585,13 +568,22 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
     }
 }
 
-int partition_smem_bytes(int head_dim) {
-    switch (head_dim) {
-        case 64: return PartitionShape<64>::kSmemBytes;
-        case 128: return PartitionShape<128>::kSmemBytes;
-        case 256: return PartitionShape<256>::kSmemBytes;
-        default: return -1;
+// The CTA shapes (warps, stages per warp) compiled for every head_dim.
+#define PA_FOR_EACH_SHAPE(X) X(2, 2) X(1, 2) X(1, 3) X(4, 2)
+
+int partition_smem_bytes(int head_dim, int warps, int stages) {
+#define PA_SMEM_CASE(W_, S_)                                                       \
+    if (warps == W_ && stages == S_) {                                            \
+        switch (head_dim) {                                                       \
+            case 64: return PartitionShape<64, W_, S_>::kSmemBytes;               \
+            case 128: return PartitionShape<128, W_, S_>::kSmemBytes;             \
+            case 256: return PartitionShape<256, W_, S_>::kSmemBytes;             \
+            default: return -1;                                                   \
+        }                                                                         \
     }
+    PA_FOR_EACH_SHAPE(PA_SMEM_CASE)
+#undef PA_SMEM_CASE
+    return -1;
 }
 
 namespace {
@@ -603,23 +595,24 @@ cudaLaunchAttribute pdl_attribute() {
     return a;
 }
 
-template <int D>
+template <int D, int NW, int NS>
 cudaError_t launch_partition_t(const PartitionParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                                cudaStream_t stream) {
-    const int smem = PartitionShape<D>::kSmemBytes;
+    const int smem = PartitionShape<D, NW, NS>::kSmemBytes;
     // The attribute is per device; setting it on every call costs little and
     // keeps multi-device processes correct.
-    cudaError_t e = cudaFuncSetAttribute(pa_partition_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kWarps * 32);
+    cfg.blockDim = dim3(NW * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, pa_partition_kernel<D>, tk, tv, prm);
+    e = cudaLaunchKernelEx(&cfg, pa_partition_kernel<D, NW, NS>, tk, tv, prm);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -653,14 +646,20 @@ cudaError_t launch_reduce_d(int width, const ReduceParams& prm, dim3 grid, cudaS
 
 }  // namespace
 
-cudaError_t launch_partition(int head_dim, const PartitionParams& prm, const CUtensorMap& tk, const CUtensorMap& tv,
-                             dim3 grid, cudaStream_t stream) {
-    switch (head_dim) {
-        case 64: return launch_partition_t<64>(prm, tk, tv, grid, stream);
-        case 128: return launch_partition_t<128>(prm, tk, tv, grid, stream);
-        case 256: return launch_partition_t<256>(prm, tk, tv, grid, stream);
-        default: return cudaErrorInvalidValue;
+cudaError_t launch_partition(int head_dim, int warps, int stages, const PartitionParams& prm, const CUtensorMap& tk,
+                             const CUtensorMap& tv, dim3 grid, cudaStream_t stream) {
+#define PA_LAUNCH_CASE(W_, S_)                                                          \
+    if (warps == W_ && stages == S_) {                                                 \
+        switch (head_dim) {                                                            \
+            case 64: return launch_partition_t<64, W_, S_>(prm, tk, tv, grid, stream);   \
+            case 128: return launch_partition_t<128, W_, S_>(prm, tk, tv, grid, stream); \
+            case 256: return launch_partition_t<256, W_, S_>(prm, tk, tv, grid, stream); \
+            default: return cudaErrorInvalidValue;                                     \
+        }                                                                              \
     }
+    PA_FOR_EACH_SHAPE(PA_LAUNCH_CASE)
+#undef PA_LAUNCH_CASE
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3 grid, cudaStream_t stream) {

@@ -236,3 +236,15 @@ def test_caller_workspace_too_small_is_rejected(dev):
                         w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len, mode="split",
                         workspace=small)
     assert e.value.code == pb.PA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("warps,stages", [(2, 2), (1, 2), (1, 3), (4, 2)])
+@pytest.mark.parametrize("mode", ["single", "split"])
+def test_every_cta_shape(dev, warps, stages, mode):
+    w = W.make_workload("shape", [1, 17, 513, 3000, 100], num_blocks=300, seed=warps * 10 + stages, device=dev,
+                        tail_fill=float("nan"))
+    out = run(w, mode=mode, partition_size=256 if mode == "split" else 0, warps=warps, stages=stages)
+    assert_parity(out, oracle_ref(w), f"{warps}x{stages} {mode}")
+    # the result does not depend on the CTA shape beyond rounding order
+    ref = run(w, mode=mode, partition_size=256 if mode == "split" else 0, warps=2, stages=2)
+    assert (out.float() - ref.float()).abs().max().item() < 2e-3

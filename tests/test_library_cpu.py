@@ -138,3 +138,30 @@ def test_reduce_slice_follows_the_batch(B, L, z):
     rc, pl = plan(args(num_seqs=B, max_seq_len=L, num_blocks=B * L // 16))
     assert rc == 0 and pl["launch_reduce"] == 1
     assert pl["reduce_grid_z"] == z and (pl["reduce_grid_x"], pl["reduce_grid_y"]) == (24, B)
+
+
+def test_cta_shape_option():
+    a = args()
+    for w, s in ((2, 2), (1, 2), (1, 3), (4, 2)):
+        o = pb.make_opts(warps=w, stages=s)
+        pl = pb.pa_decode_plan_t()
+        assert pb.lib.pa_decode_plan(ctypes.byref(a), ctypes.byref(o), SMS, ctypes.byref(pl)) == pb.PA_OK
+        assert (pl.threads, pl.stages) == (32 * w, s)
+        # one stage holds the K and V of a 16-token block: 2 x 16 x 256 x 2 B
+        assert pl.smem_bytes >= w * s * 16384
+    for w, s in ((3, 2), (2, 5), (0, 2)):
+        o = pb.make_opts(warps=w, stages=s)
+        pl = pb.pa_decode_plan_t()
+        assert pb.lib.pa_decode_plan(ctypes.byref(a), ctypes.byref(o), SMS, ctypes.byref(pl)) == pb.PA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("B,L,shape", [
+    (1, 2048, (4, 2)),       # 16 CTAs: the most bytes in flight per CTA
+    (8, 8192, (2, 2)),       # ~256 CTAs: one wave of 2-warp CTAs
+    (4, 32768, (1, 3)),      # ~512-1024 CTAs: two waves of 4 CTAs/SM
+    (1, 102400, (1, 2)),     # 800 CTAs: one wave at 6 CTAs/SM
+    (64, 65536, (1, 2)),     # many waves: the finest slots
+])
+def test_cta_shape_follows_the_wave_model(B, L, shape):
+    rc, pl = plan(args(num_seqs=B, max_seq_len=L, num_blocks=B * L // 16))
+    assert rc == 0 and (pl["threads"] // 32, pl["stages"]) == shape
