@@ -15,6 +15,9 @@ their uint16 bit patterns):
                             of the "paged_attention_v2_triton.py" commit page.
 * ``combine_lse`` / ``combine_fold`` -- the second pass over the partials
                             ("docs" commit page, Phase 2 reduce).
+* ``prefix_attention``   -- chunked-prefill attention: each new token attends to
+                            its sequence's paged context and causally to the chunk
+                            ("qwen3_6_scripts/paged_attn.py" commit page, prefix path).
 * ``half_to_double``     -- exact binary16 decode, written from the format.
 """
 from __future__ import annotations
@@ -66,6 +69,13 @@ def _load():
             lib.oracle_paged_decode_one.argtypes = [_dp] + common + [ctypes.c_int, ctypes.c_int]
             lib.oracle_partition_partials.restype = ctypes.c_int
             lib.oracle_partition_partials.argtypes = [_dp, _dp, _dp] + common + [ctypes.c_int] * 4
+            pre = [_u16p, _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_longlong,
+                   ctypes.c_double]
+            lib.oracle_prefix_attention.restype = ctypes.c_int
+            lib.oracle_prefix_attention.argtypes = [_dp] + pre + [ctypes.c_int]
+            lib.oracle_prefix_attention_one.restype = ctypes.c_int
+            lib.oracle_prefix_attention_one.argtypes = [_dp] + pre + [ctypes.c_int, ctypes.c_int]
             for name in ("oracle_combine_lse", "oracle_combine_fold"):
                 fn = getattr(lib, name)
                 fn.restype = ctypes.c_int
@@ -187,4 +197,44 @@ def split_decode(q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_kv_
                                            num_kv_heads, head_dim, block_size, scale, b, h,
                                            partition_size, tile_size)
             out[b, h] = comb(m, l, acc.reshape(len(m), head_dim)) if len(m) else 0.0
+    return out
+
+
+def _prefix_args(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_heads,
+                 num_kv_heads, head_dim, block_size, scale):
+    q, kn, vn, k, v = _bits(q), _bits(k_new), _bits(v_new), _bits(k_cache), _bits(v_cache)
+    bt, cl, qs = _i32(block_tables), _i32(context_lens), _i32(query_start_loc)
+    num_seqs = int(cl.shape[0])
+    num_tokens = int(qs[-1]) if qs.size else 0
+    mbps = int(bt.shape[1]) if bt.ndim == 2 else 0
+    row = num_kv_heads * block_size * head_dim
+    num_blocks = k.size // row if row else 0
+    if (q.size != num_tokens * num_heads * head_dim or kn.size != num_tokens * num_kv_heads * head_dim
+            or vn.size != kn.size or qs.size != num_seqs + 1 or k.size != v.size):
+        raise OracleError("shape mismatch")
+    keep = (q, kn, vn, k, v, bt, cl, qs)
+    args = [_ptr(q, _u16p), _ptr(kn, _u16p), _ptr(vn, _u16p), _ptr(k, _u16p), _ptr(v, _u16p), _ptr(bt, _i32p),
+            _ptr(cl, _i32p), _ptr(qs, _i32p), num_seqs, num_tokens, mbps, num_heads, num_kv_heads, head_dim,
+            block_size, num_blocks, float(scale)]
+    return keep, args, num_tokens
+
+
+def prefix_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_heads,
+                     num_kv_heads, head_dim, block_size, scale, threads: int = 0) -> np.ndarray:
+    """float64 [num_tokens, num_heads, head_dim] of chunked-prefill attention."""
+    keep, args, n = _prefix_args(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                                 num_heads, num_kv_heads, head_dim, block_size, scale)
+    out = np.zeros((n, num_heads, head_dim), dtype=np.float64)
+    _check(_load().oracle_prefix_attention(_ptr(out, _dp), *args, int(threads)))
+    del keep
+    return out
+
+
+def prefix_attention_one(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_heads,
+                         num_kv_heads, head_dim, block_size, scale, tok: int, h: int) -> np.ndarray:
+    keep, args, _ = _prefix_args(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                                 num_heads, num_kv_heads, head_dim, block_size, scale)
+    out = np.zeros((head_dim,), dtype=np.float64)
+    _check(_load().oracle_prefix_attention_one(_ptr(out, _dp), *args, int(tok), int(h)))
+    del keep
     return out

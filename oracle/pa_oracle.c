@@ -37,6 +37,16 @@
  *      and the same alpha/beta rule applied partition by partition.  The
  *      "docs" commit page calls this the Phase 2 reduce over partitions.
  *
+ *  oracle_prefix_attention -- chunked-prefill ("prefix") attention: sequence
+ *      b already has context_lens[b] tokens in the paged cache and brings a
+ *      chunk of q_len_b new tokens (rows query_start_loc[b] .. [b+1]-1 of q,
+ *      k_new, v_new).  Chunk token i attends to every context token and to
+ *      chunk tokens 0..i (causal inside the chunk):
+ *          out = softmax(scale * q . [K_ctx ; K_new[0..i]]^T) [V_ctx ; V_new[0..i]]
+ *      Source: "qwen3_6_scripts/paged_attn.py" commit page, prefix-path
+ *      paragraphs (online softmax over the pre-gathered paged context, then
+ *      over the current chunk with the same update).
+ *
  * fp16 inputs are widened to double exactly (IEEE 754 binary16 decode written
  * from the format's definition below); all arithmetic is double.
  *
@@ -353,4 +363,129 @@ int oracle_combine_fold(double* out, const double* m, const double* l, const dou
         l_i = l_new;
     }
     return 0;
+}
+
+
+/* Chunked-prefill attention, the definition, for one (new token, head).
+ * tok indexes the packed new tokens; its sequence b is the one whose
+ * [query_start_loc[b], query_start_loc[b+1]) range holds it. */
+static int prefix_one(double* out, double* s, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                      const oracle_problem* P, const int32_t* context_lens, const int32_t* query_start_loc,
+                      int b, int tok, int h)
+{
+    int G = P->num_heads / P->num_kv_heads, g = h / G, D = P->head_dim;
+    int C = context_lens[b];
+    int i = tok - query_start_loc[b];
+    const uint16_t* qv = q + ((long long)tok * P->num_heads + h) * D;
+    int n = C + i + 1;
+    for (int t = 0; t < n; ++t) {
+        const uint16_t* k;
+        if (t < C) {
+            k = token_row(P, P->k_cache, b, g, t);
+            if (!k) return -2;
+        } else {
+            k = k_new + ((long long)(query_start_loc[b] + (t - C)) * P->num_kv_heads + g) * D;
+        }
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += H2D(qv[d]) * H2D(k[d]);
+        s[t] = P->scale * dot;
+    }
+    double M = -INFINITY;
+    for (int t = 0; t < n; ++t)
+        if (s[t] > M) M = s[t];
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    double denom = 0.0;
+    for (int t = 0; t < n; ++t) {
+        double w = exp(s[t] - M);
+        const uint16_t* v = t < C ? token_row(P, P->v_cache, b, g, t)
+                                  : v_new + ((long long)(query_start_loc[b] + (t - C)) * P->num_kv_heads + g) * D;
+        denom += w;
+        for (int d = 0; d < D; ++d) out[d] += w * H2D(v[d]);
+    }
+    for (int d = 0; d < D; ++d) out[d] /= denom;
+    return 0;
+}
+
+static int check_prefix(const oracle_problem* P, const int32_t* context_lens, const int32_t* query_start_loc,
+                        int num_tokens, int* max_keys)
+{
+    if (!context_lens || !query_start_loc || num_tokens < 0) return -1;
+    if (query_start_loc[0] != 0 || query_start_loc[P->num_seqs] != num_tokens) return -1;
+    *max_keys = 1;
+    for (int b = 0; b < P->num_seqs; ++b) {
+        int C = context_lens[b], ql = query_start_loc[b + 1] - query_start_loc[b];
+        if (ql < 0) return -1;
+        if (C < 0 || (long long)C > (long long)P->max_blocks_per_seq * P->block_size) return -3;
+        if (C + ql > *max_keys) *max_keys = C + ql;
+    }
+    return 0;
+}
+
+/* out: double [num_tokens][num_heads][head_dim]. */
+int oracle_prefix_attention(double* out, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                            const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* block_tables,
+                            const int32_t* context_lens, const int32_t* query_start_loc, int num_seqs,
+                            int num_tokens, int max_blocks_per_seq, int num_heads, int num_kv_heads, int head_dim,
+                            int block_size, long long num_blocks, double scale, int threads)
+{
+    oracle_problem P = make_problem(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                    num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale);
+    if (!out || !k_new || !v_new || check_problem(&P)) return -1;
+    int max_keys = 1;
+    int rc = check_prefix(&P, context_lens, query_start_loc, num_tokens, &max_keys);
+    if (rc) return rc;
+    long long rows = (long long)num_tokens * num_heads;
+    int status = 0;
+    (void)threads;
+#ifdef _OPENMP
+    int nt = threads > 0 ? threads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)max_keys);
+        int local = s ? 0 : -1;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 4)
+#endif
+        for (long long r = 0; r < rows; ++r) {
+            int tok = (int)(r / num_heads), h = (int)(r % num_heads);
+            int b = 0;
+            while (b + 1 < num_seqs && query_start_loc[b + 1] <= tok) ++b;
+            int e = s ? prefix_one(out + r * head_dim, s, q, k_new, v_new, &P, context_lens, query_start_loc, b,
+                                   tok, h)
+                      : -1;
+            if (e) local = e;
+        }
+        free(s);
+        if (local) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            status = local;
+        }
+    }
+    return status;
+}
+
+/* One (new token, head) of the definition, for sampled checks at full size. */
+int oracle_prefix_attention_one(double* out, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* block_tables,
+                                const int32_t* context_lens, const int32_t* query_start_loc, int num_seqs,
+                                int num_tokens, int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                                int head_dim, int block_size, long long num_blocks, double scale, int tok, int h)
+{
+    oracle_problem P = make_problem(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                    num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale);
+    if (!out || !k_new || !v_new || check_problem(&P) || tok < 0 || tok >= num_tokens || h < 0 || h >= num_heads)
+        return -1;
+    int max_keys = 1;
+    int rc = check_prefix(&P, context_lens, query_start_loc, num_tokens, &max_keys);
+    if (rc) return rc;
+    int b = 0;
+    while (b + 1 < num_seqs && query_start_loc[b + 1] <= tok) ++b;
+    double* s = (double*)malloc(sizeof(double) * (size_t)max_keys);
+    if (!s) return -1;
+    rc = prefix_one(out, s, q, k_new, v_new, &P, context_lens, query_start_loc, b, tok, h);
+    free(s);
+    return rc;
 }
