@@ -174,6 +174,56 @@ const char* pa_status_string(int status);
 /* Free the library-owned workspaces of every device (synchronises them). */
 void pa_release_workspace(void);
 
+/* Chunked-prefill ("prefix") attention over the paged cache.
+ * Sequence b has context_lens[b] tokens already in the paged cache (found
+ * through block_tables as for decode) and brings a chunk of new tokens: rows
+ * query_start_loc[b] .. query_start_loc[b+1]-1 of q, k_new and v_new.  New
+ * token i of the chunk attends to every context token and to chunk tokens
+ * 0..i (causal inside the chunk):
+ *     out[tok, h, :] = softmax(scale * q[tok, h, :] . [K_ctx ; K_new[0..i]]^T) [V_ctx ; V_new[0..i]]
+ * Source: "qwen3_6_scripts/paged_attn.py" commit page, prefix path (online
+ * softmax over the pre-gathered paged context, then over the current chunk).
+ * Layouts: q, out fp16 [num_tokens][num_heads][head_dim]; k_new, v_new fp16
+ * [num_tokens][num_kv_heads][head_dim]; query_start_loc int32 [num_seqs + 1]
+ * (0 first, num_tokens last, non-decreasing); context_lens int32 [num_seqs];
+ * caches and block table as for pa_decode.  max_context_len and max_query_len
+ * are host-side bounds that size the grid.  The new tokens' K/V are read from
+ * k_new/v_new, not from the cache (the caller appends them afterwards).
+ * Same support, alignment, ownership and error rules as pa_decode; allocates
+ * nothing.  Device-detected bad lengths set PA_DEV_BAD_SEQ_LEN. */
+typedef struct {
+    void* out;
+    const void* q;
+    const void* k_new;
+    const void* v_new;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* query_start_loc;
+    int num_seqs;
+    int num_tokens;
+    int max_blocks_per_seq;
+    int max_context_len;
+    int max_query_len;
+    int64_t num_blocks;
+    int num_heads;
+    int num_kv_heads;
+    int head_dim;
+    int block_size;
+    float scale;
+} pa_prefix_args;
+
+int pa_prefix(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
+              const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+              const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_blocks_per_seq,
+              int max_context_len, int max_query_len, int64_t num_blocks, int num_heads, int num_kv_heads,
+              int head_dim, int block_size, float scale, pa_stream_t stream);
+
+/* The same with an argument struct and options (opts may be NULL; of the
+ * options only flags, wait_limit and the two timing events apply). */
+int pa_prefix_ex(const pa_prefix_args* args, const pa_decode_opts* opts, pa_stream_t stream);
+
 /* Size of the fixed device scratch that pa_decode_noalloc uses (16 MiB). */
 #define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
 

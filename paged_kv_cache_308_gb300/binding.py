@@ -69,6 +69,18 @@ class pa_decode_plan_t(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class pa_prefix_args(ctypes.Structure):
+    _fields_ = [
+        ("out", ctypes.c_void_p), ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("block_tables", ctypes.c_void_p),
+        ("context_lens", ctypes.c_void_p), ("query_start_loc", ctypes.c_void_p), ("num_seqs", ctypes.c_int),
+        ("num_tokens", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int), ("max_context_len", ctypes.c_int),
+        ("max_query_len", ctypes.c_int), ("num_blocks", ctypes.c_int64), ("num_heads", ctypes.c_int),
+        ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
+        ("scale", ctypes.c_float),
+    ]
+
+
 class PaDecodeError(RuntimeError):
     def __init__(self, code: int, what: str = ""):
         self.code = code
@@ -99,6 +111,10 @@ def _load() -> ctypes.CDLL:
     lib.pa_release_workspace.argtypes = []
     lib.pa_version.restype = i32
     lib.pa_version.argtypes = []
+    lib.pa_prefix.restype = i32
+    lib.pa_prefix.argtypes = [vp] * 9 + [i32] * 5 + [i64, i32, i32, i32, i32, f32, vp]
+    lib.pa_prefix_ex.restype = i32
+    lib.pa_prefix_ex.argtypes = [ctypes.POINTER(pa_prefix_args), ctypes.POINTER(pa_decode_opts), vp]
     return lib
 
 
@@ -264,3 +280,43 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, num_head
             _stream_handle(stream))
     if rc != PA_OK:
         raise PaDecodeError(rc, "pa_decode_noalloc")
+
+
+def pa_prefix(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_heads,
+              num_kv_heads, head_dim, block_size, scale, stream=None, *, max_context_len: int, max_query_len: int,
+              **opt) -> None:
+    """Chunked-prefill attention (see include/pa_decode.h); options as for pa_decode_ex."""
+    for name, t, dt in (("out", out, torch.float16), ("q", q, torch.float16), ("k_new", k_new, torch.float16),
+                        ("v_new", v_new, torch.float16), ("k_cache", k_cache, torch.float16),
+                        ("v_cache", v_cache, torch.float16), ("block_tables", block_tables, torch.int32),
+                        ("context_lens", context_lens, torch.int32),
+                        ("query_start_loc", query_start_loc, torch.int32)):
+        if t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    args = pa_prefix_args(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+                          v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
+                          query_start_loc.data_ptr(), int(context_lens.shape[0]), int(q.shape[0]),
+                          int(block_tables.shape[1]), int(max_context_len), int(max_query_len),
+                          int(k_cache.shape[0]), int(num_heads), int(num_kv_heads), int(head_dim), int(block_size),
+                          float(scale))
+    if opt:
+        rc = lib.pa_prefix_ex(ctypes.byref(args), ctypes.byref(make_opts(**opt)), _stream_handle(stream))
+    else:
+        rc = lib.pa_prefix(args.out, args.q, args.k_new, args.v_new, args.k_cache, args.v_cache, args.block_tables,
+                           args.context_lens, args.query_start_loc, args.num_seqs, args.num_tokens,
+                           args.max_blocks_per_seq, args.max_context_len, args.max_query_len, args.num_blocks,
+                           args.num_heads, args.num_kv_heads, args.head_dim, args.block_size, args.scale,
+                           _stream_handle(stream))
+    if rc != PA_OK:
+        raise PaDecodeError(rc, "pa_prefix")
+
+
+def prefix_workload(w, out: Optional[torch.Tensor] = None, stream=None, **opt) -> torch.Tensor:
+    """Run chunked-prefill attention on a workloads.PrefixWorkload (tensors on the GPU)."""
+    if out is None:
+        out = torch.empty_like(w.q)
+    pa_prefix(out, w.q, w.k_new, w.v_new, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+              w.query_start_loc, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, w.scale, stream,
+              max_context_len=w.max_context_len, max_query_len=w.max_query_len, **opt)
+    return out
+

@@ -295,6 +295,94 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     return PA_OK;
 }
 
+// New tokens' K or V viewed as a 3-D tensor [num_tokens][num_kv_heads][head_dim];
+// a box is 16 tokens x 1 kv head x 64 halves with the 128-byte swizzle, the
+// same shared-memory layout as a cache box.  Tokens past the end read as zero.
+int make_new_kv_map(CUtensorMap* map, const void* base, int num_tokens, int num_kv_heads, int head_dim) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PA_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)(num_tokens > 0 ? num_tokens : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_kv_heads * head_dim * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)pa::kBlockSize};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int validate_prefix(const pa_prefix_args* a, const pa_decode_opts* o) {
+    if (!a) return PA_ERR_INVALID_ARG;
+    if (a->num_seqs < 0 || a->num_seqs > 65535 || a->num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (a->num_heads <= 0 || a->num_kv_heads <= 0 || a->head_dim <= 0 || a->block_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (a->num_heads % a->num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (!isfinite(a->scale)) return PA_ERR_INVALID_ARG;
+    if (a->max_context_len < 0 || a->max_query_len < 0 || a->max_blocks_per_seq < 0 || a->num_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    if (o && (o->mode < PA_MODE_AUTO || o->mode > PA_MODE_SPLIT)) return PA_ERR_INVALID_ARG;
+    if (a->head_dim != 64 && a->head_dim != 128 && a->head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (a->block_size != pa::kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (a->num_heads / a->num_kv_heads > pa::kMaxGroup) return PA_ERR_UNSUPPORTED;
+    if ((long long)a->max_context_len > (long long)a->max_blocks_per_seq * a->block_size) return PA_ERR_INVALID_ARG;
+    if (a->num_blocks * a->num_kv_heads * a->block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    if (a->num_tokens > 0 && a->max_query_len == 0) return PA_ERR_INVALID_ARG;
+    if (a->num_seqs == 0 || a->num_tokens == 0) return PA_OK;
+    if (!a->out || !a->q || !a->k_new || !a->v_new || !a->k_cache || !a->v_cache || !a->block_tables ||
+        !a->context_lens || !a->query_start_loc)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(a->out, 16) || !aligned(a->q, 16) || !aligned(a->k_new, 16) || !aligned(a->v_new, 16) ||
+        !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->block_tables, 4) ||
+        !aligned(a->context_lens, 4) || !aligned(a->query_start_loc, 4))
+        return PA_ERR_INVALID_ARG;
+    if (a->num_blocks == 0 && a->max_context_len > 0) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t stream) {
+    int rc = validate_prefix(a, o);
+    if (rc) return rc;
+    if (a->num_seqs == 0 || a->num_tokens == 0) return PA_OK;
+    pa_decode_args ca;  // the cache part, for the shared tensor-map helper
+    memset(&ca, 0, sizeof(ca));
+    ca.num_blocks = a->num_blocks > 0 ? a->num_blocks : 1;
+    ca.num_kv_heads = a->num_kv_heads;
+    ca.head_dim = a->head_dim;
+    ca.block_size = a->block_size;
+    CUtensorMap maps[4];
+    if ((rc = make_cache_map(&maps[0], a->k_cache, &ca)) || (rc = make_cache_map(&maps[1], a->v_cache, &ca)) ||
+        (rc = make_new_kv_map(&maps[2], a->k_new, a->num_tokens, a->num_kv_heads, a->head_dim)) ||
+        (rc = make_new_kv_map(&maps[3], a->v_new, a->num_tokens, a->num_kv_heads, a->head_dim)))
+        return rc;
+    pa::PrefixParams prm;
+    prm.out = static_cast<__half*>(a->out);
+    prm.q = static_cast<const __half*>(a->q);
+    prm.block_tables = a->block_tables;
+    prm.context_lens = a->context_lens;
+    prm.query_start_loc = a->query_start_loc;
+    prm.num_blocks = a->num_blocks;
+    prm.num_heads = a->num_heads;
+    prm.num_kv_heads = a->num_kv_heads;
+    prm.group = a->num_heads / a->num_kv_heads;
+    prm.max_blocks_per_seq = a->max_blocks_per_seq;
+    prm.max_context_len = a->max_context_len;
+    prm.max_query_len = a->max_query_len;
+    prm.num_tokens = a->num_tokens;
+    prm.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+    prm.wait_limit = (o && o->wait_limit) ? o->wait_limit : pa::kDefaultWaitLimit;
+    prm.force_timeout = (o && (o->flags & PA_FLAG_FORCE_TIMEOUT)) ? 1 : 0;
+    const int tile_tokens = 64 / prm.group;
+    const dim3 grid((a->max_query_len + tile_tokens - 1) / tile_tokens, a->num_kv_heads, a->num_seqs);
+    if (o && o->event_partition_begin &&
+        cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_begin), stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (pa::launch_prefix(a->head_dim, prm, maps, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (o && o->event_partition_end &&
+        cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_end), stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
 // Library-owned workspace, one per device, grown on demand.
 std::mutex g_ws_mutex;
 void* g_ws[kMaxDevices];
@@ -369,6 +457,38 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
     rc = ensure_workspace(plan.workspace_bytes, &ws);
     if (rc) return rc;
     return run(&a, nullptr, ws, plan.workspace_bytes, reinterpret_cast<cudaStream_t>(stream), plan);
+}
+
+int pa_prefix_ex(const pa_prefix_args* args, const pa_decode_opts* opts, pa_stream_t stream) {
+    return run_prefix(args, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_prefix(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, const int32_t* query_start_loc, int num_seqs,
+              int num_tokens, int max_blocks_per_seq, int max_context_len, int max_query_len, int64_t num_blocks,
+              int num_heads, int num_kv_heads, int head_dim, int block_size, float scale, pa_stream_t stream) {
+    pa_prefix_args a;
+    a.out = out;
+    a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start_loc = query_start_loc;
+    a.num_seqs = num_seqs;
+    a.num_tokens = num_tokens;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.max_context_len = max_context_len;
+    a.max_query_len = max_query_len;
+    a.num_blocks = num_blocks;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.scale = scale;
+    return run_prefix(&a, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim, int partition_size) {

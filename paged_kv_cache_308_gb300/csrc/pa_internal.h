@@ -45,6 +45,26 @@ struct ReduceParams {
     int partition_size, max_partitions;
 };
 
+struct PrefixParams {
+    __half* out;                    // [num_tokens][H][D]
+    const __half* q;                // [num_tokens][H][D]
+    const int32_t* block_tables;    // context blocks
+    const int32_t* context_lens;    // [B]
+    const int32_t* query_start_loc; // [B + 1]
+    long long num_blocks;
+    int num_heads, num_kv_heads, group;
+    int max_blocks_per_seq, max_context_len, max_query_len, num_tokens;
+    float scale_log2;
+    unsigned wait_limit;
+    int force_timeout;
+};
+
+// Chunked-prefill kernel: grid (query tiles, kv heads, sequences); maps are
+// {K cache, V cache (2-D, as for decode), K new, V new (3-D [token][kv head][dim])}.
+int prefix_smem_bytes(int head_dim);
+cudaError_t launch_prefix(int head_dim, const PrefixParams& prm, const CUtensorMap* maps, dim3 grid,
+                          cudaStream_t stream);
+
 // Dynamic shared memory of a partition CTA of `warps` warps with `stages`
 // stages each (includes 1 KB of alignment slack for the 128-byte swizzle);
 // -1 for a shape that is not compiled.

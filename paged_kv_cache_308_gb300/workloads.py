@@ -191,3 +191,89 @@ def make_config(name: str, device="cpu", seed: int = 0, **kw) -> Workload:
     peaked = 0.01 if name == "b4_l32768_peaked" else 0.0
     return make_workload(name, lens, num_blocks=_POOL[name], seed=seed, device=device,
                          peaked_fraction=peaked, **kw)
+
+
+@dataclass
+class PrefixWorkload:
+    """Inputs of one chunked-prefill call: per sequence, context_lens[b]
+    cached tokens (paged, as for decode) and a chunk of new tokens packed
+    in q / k_new / v_new at rows query_start_loc[b] .. [b+1]-1."""
+    name: str
+    q: torch.Tensor                # fp16 [T, H, D]
+    k_new: torch.Tensor            # fp16 [T, Hkv, D]
+    v_new: torch.Tensor            # fp16 [T, Hkv, D]
+    k_cache: torch.Tensor          # fp16 [NB, Hkv, bs, D]
+    v_cache: torch.Tensor
+    block_tables: torch.Tensor     # int32 [B, max_blocks_per_seq]
+    context_lens: torch.Tensor     # int32 [B]
+    query_start_loc: torch.Tensor  # int32 [B + 1]
+    context_lens_host: List[int]
+    query_lens_host: List[int]
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    scale: float
+
+    @property
+    def num_tokens(self) -> int:
+        return int(sum(self.query_lens_host))
+
+    @property
+    def max_context_len(self) -> int:
+        return max(self.context_lens_host) if self.context_lens_host else 0
+
+    @property
+    def max_query_len(self) -> int:
+        return max(self.query_lens_host) if self.query_lens_host else 0
+
+    @property
+    def flops(self) -> int:
+        """Score and P.V multiply-adds x 2: per new token i of a sequence with
+        context C, (C + i + 1) keys x heads x head_dim x 2 products x 2."""
+        keys = sum(C * L + L * (L + 1) // 2 for C, L in zip(self.context_lens_host, self.query_lens_host))
+        return 4 * keys * self.num_heads * self.head_dim
+
+
+def make_prefix_workload(name: str, context_lens: List[int], query_lens: List[int], *, num_heads: int = NUM_HEADS,
+                         num_kv_heads: int = NUM_KV_HEADS, head_dim: int = HEAD_DIM, block_size: int = BLOCK_SIZE,
+                         num_blocks: Optional[int] = None, scale: float = SCALE, seed: int = 0, device="cpu",
+                         tail_fill: Optional[float] = None) -> PrefixWorkload:
+    base = make_workload(name, context_lens, num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                         block_size=block_size, num_blocks=num_blocks, scale=scale, seed=seed, device=device,
+                         tail_fill=tail_fill)
+    gen = _device_generator(device, seed + 7)
+    T = int(sum(query_lens))
+    qs = [0]
+    for L in query_lens:
+        qs.append(qs[-1] + int(L))
+    q = _normal_fp16((T, num_heads, head_dim), gen, device)
+    kn = _normal_fp16((T, num_kv_heads, head_dim), gen, device)
+    vn = _normal_fp16((T, num_kv_heads, head_dim), gen, device)
+    return PrefixWorkload(name, q, kn, vn, base.k_cache, base.v_cache, base.block_tables, base.seq_lens,
+                          torch.tensor(qs, dtype=torch.int32, device=device), list(base.seq_lens_host),
+                          [int(x) for x in query_lens], num_heads, num_kv_heads, head_dim, block_size, scale)
+
+
+PREFIX_CONFIG_NAMES = ["prefix_b4_c8192_q512", "prefix_b16_mixed"]
+
+
+def make_prefix_config(name: str, device="cpu", seed: int = 0) -> PrefixWorkload:
+    """Chunked-prefill workloads (24/4 heads, head_dim 256, block_size 16):
+
+    * ``prefix_b4_c8192_q512``  4 sequences, 8192 cached tokens each, chunks of 512;
+    * ``prefix_b16_mixed``      16 sequences, cached lengths log-uniform on
+                                [16, 32768] (0 for two of them), chunks uniform
+                                on [1, 1024]."""
+    if name == "prefix_b4_c8192_q512":
+        return make_prefix_workload(name, [8192] * 4, [512] * 4, seed=seed, device=device)
+    if name == "prefix_b16_mixed":
+        g = torch.Generator().manual_seed(seed)
+        u = torch.rand(16, generator=g, dtype=torch.float64)
+        lo, hi = math.log(16.0), math.log(32768.0)
+        ctx = [int(round(math.exp(lo + (hi - lo) * float(x)))) for x in u]
+        ctx[3] = ctx[11] = 0
+        ql = torch.randint(1, 1025, (16,), generator=g).tolist()
+        return make_prefix_workload(name, ctx, ql, seed=seed, device=device)
+    raise KeyError(name)
+
