@@ -88,8 +88,10 @@ enum {
 
 /* Option flags. */
 enum {
-    PA_FLAG_FORCE_TIMEOUT = 1 /* test hook: every copy wait gives up before its first poll; the
-                                 kernel then drains its copies, sets PA_DEV_TIMEOUT and returns */
+    PA_FLAG_FORCE_TIMEOUT = 1,   /* test hook: every copy wait gives up before its first poll; the
+                                    kernel then drains its copies, sets PA_DEV_TIMEOUT and returns */
+    PA_FLAG_PREFIX_WARP_MMA = 2  /* pa_prefix_ex: use the warp-level MMA kernel instead of the
+                                    tcgen05 (tensor-memory) one */
 };
 
 /* All inputs of one decode call (device pointers; see the layouts above). */

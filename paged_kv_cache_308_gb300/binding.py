@@ -36,6 +36,7 @@ PA_MODE_SPLIT = 2
 MODES = {"auto": PA_MODE_AUTO, "single": PA_MODE_SINGLE, "split": PA_MODE_SPLIT}
 
 PA_FLAG_FORCE_TIMEOUT = 1
+PA_FLAG_PREFIX_WARP_MMA = 2
 
 
 class pa_decode_args(ctypes.Structure):

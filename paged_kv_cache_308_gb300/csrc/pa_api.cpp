@@ -371,12 +371,16 @@ int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t st
     prm.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
     prm.wait_limit = (o && o->wait_limit) ? o->wait_limit : pa::kDefaultWaitLimit;
     prm.force_timeout = (o && (o->flags & PA_FLAG_FORCE_TIMEOUT)) ? 1 : 0;
-    const int tile_tokens = 64 / prm.group;
+    // tensor-core (tcgen05) kernel by default; the warp-level MMA kernel on request
+    const bool warp_mma = o && (o->flags & PA_FLAG_PREFIX_WARP_MMA);
+    const int tile_tokens = (warp_mma ? 64 : 128) / prm.group;
     const dim3 grid((a->max_query_len + tile_tokens - 1) / tile_tokens, a->num_kv_heads, a->num_seqs);
     if (o && o->event_partition_begin &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_begin), stream) != cudaSuccess)
         return PA_ERR_CUDA;
-    if (pa::launch_prefix(a->head_dim, prm, maps, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
+    const cudaError_t e = warp_mma ? pa::launch_prefix(a->head_dim, prm, maps, grid, stream)
+                                   : pa::launch_prefix_tc(a->head_dim, prm, maps, grid, stream);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
     if (o && o->event_partition_end &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_end), stream) != cudaSuccess)
         return PA_ERR_CUDA;

@@ -64,6 +64,10 @@ struct PrefixParams {
 int prefix_smem_bytes(int head_dim);
 cudaError_t launch_prefix(int head_dim, const PrefixParams& prm, const CUtensorMap* maps, dim3 grid,
                           cudaStream_t stream);
+// The tcgen05 version: 128-row tiles (floor(128 / G) tokens), same maps.
+int prefix_tc_smem_bytes(int head_dim);
+cudaError_t launch_prefix_tc(int head_dim, const PrefixParams& prm, const CUtensorMap* maps, dim3 grid,
+                             cudaStream_t stream);
 
 // Dynamic shared memory of a partition CTA of `warps` warps with `stages`
 // stages each (includes 1 KB of alignment slack for the 128-byte swizzle);

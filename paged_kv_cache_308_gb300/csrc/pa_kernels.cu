@@ -679,6 +679,7 @@ cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3
 }
 
 #include "pa_prefix_kernel.cuh"
+#include "pa_prefix_tc.cuh"
 
 cudaError_t read_and_clear_status(cudaStream_t stream, int* status) {
     unsigned int v = 0;

@@ -29,6 +29,15 @@ def dev():
     return torch.device("cuda:0")
 
 
+# the tcgen05 (tensor-memory) kernel is the default; the warp-level MMA kernel on request
+IMPLS = {"tcgen05": {}, "warp_mma": {"flags": pb.PA_FLAG_PREFIX_WARP_MMA}}
+
+
+@pytest.fixture(params=list(IMPLS))
+def impl(request):
+    return IMPLS[request.param]
+
+
 def _oracle(w, threads=THREADS):
     return oracle.prefix_attention(host_bits(w.q), host_bits(w.k_new), host_bits(w.v_new), host_bits(w.k_cache),
                                    host_bits(w.v_cache), host_bits(w.block_tables), host_bits(w.context_lens),
@@ -36,8 +45,8 @@ def _oracle(w, threads=THREADS):
                                    w.block_size, w.scale, threads=threads)
 
 
-def _run(w, **opt):
-    out = pb.prefix_workload(w, **opt)
+def _run(w, impl=None, **opt):
+    out = pb.prefix_workload(w, **{**(impl or {}), **opt})
     torch.cuda.synchronize()
     st = pb.pa_get_device_status()
     assert st == 0, f"device status {st}"
@@ -48,24 +57,24 @@ def _run(w, **opt):
     ([0], [1]), ([0], [70]), ([16], [16]), ([17], [33]), ([100, 0, 31], [5, 64, 11]),
     ([511, 512, 513], [1, 2, 130]), ([2048], [200]),
 ])
-def test_small_gqa6_d256(dev, ctx, ql):
+def test_small_gqa6_d256(dev, impl, ctx, ql):
     w = W.make_prefix_workload("p", ctx, ql, num_blocks=sum((c + 15) // 16 for c in ctx) + 5, seed=sum(ctx) + sum(ql),
                                device=dev, tail_fill=float("nan"))
-    assert_parity(_run(w), _oracle(w), f"ctx={ctx} ql={ql}")
+    assert_parity(_run(w, impl), _oracle(w), f"ctx={ctx} ql={ql} {impl}")
 
 
 @pytest.mark.parametrize("H,Hkv,D", [(4, 4, 64), (8, 4, 128), (16, 2, 256), (12, 4, 64), (7, 1, 256), (5, 5, 128)])
-def test_group_sizes_and_head_dims(dev, H, Hkv, D):
+def test_group_sizes_and_head_dims(dev, impl, H, Hkv, D):
     w = W.make_prefix_workload("p", [300, 0, 45], [40, 17, 100], num_heads=H, num_kv_heads=Hkv, head_dim=D,
                                num_blocks=40, seed=H * D, device=dev, scale=1 / math.sqrt(D), tail_fill=float("inf"))
-    assert_parity(_run(w), _oracle(w), f"H={H} Hkv={Hkv} D={D}")
+    assert_parity(_run(w, impl), _oracle(w), f"H={H} Hkv={Hkv} D={D} {impl}")
 
 
-def test_single_new_token_matches_decode_over_the_extended_cache(dev):
+def test_single_new_token_matches_decode_over_the_extended_cache(dev, impl):
     # prefix attention of one new token == decode once that token is in the cache
     ctx = [40, 16, 1000]
     w = W.make_prefix_workload("p", ctx, [1, 1, 1], num_blocks=200, seed=3, device=dev)
-    pre = _run(w)
+    pre = _run(w, impl)
     k2, v2, bt2 = w.k_cache.clone(), w.v_cache.clone(), torch.cat(
         [w.block_tables, torch.full((3, 1), -1, dtype=torch.int32, device=dev)], 1)
     used = set(w.block_tables[w.block_tables >= 0].tolist())
@@ -83,9 +92,9 @@ def test_single_new_token_matches_decode_over_the_extended_cache(dev):
 
 
 @pytest.mark.parametrize("name", W.PREFIX_CONFIG_NAMES)
-def test_named_prefix_workload_sampled(dev, name):
+def test_named_prefix_workload_sampled(dev, impl, name):
     w = W.make_prefix_config(name, device=dev)
-    out = _run(w)
+    out = _run(w, impl)
     assert torch.isfinite(out).all()
     hq, hkn, hvn = host_bits(w.q), host_bits(w.k_new), host_bits(w.v_new)
     hk, hv = host_bits(w.k_cache), host_bits(w.v_cache)
@@ -105,9 +114,9 @@ def test_named_prefix_workload_sampled(dev, name):
     assert_parity(torch.stack(got), np.stack(ref), f"{name} sampled")
 
 
-def test_permuted_pool_is_bit_identical(dev):
+def test_permuted_pool_is_bit_identical(dev, impl):
     w = W.make_prefix_workload("p", [700, 33, 0], [50, 20, 9], num_blocks=120, seed=5, device=dev)
-    a = _run(w)
+    a = _run(w, impl)
     g = torch.Generator(device=dev).manual_seed(2)
     perm = torch.randperm(w.k_cache.shape[0], generator=g, device=dev)
     k2, v2 = torch.empty_like(w.k_cache), torch.empty_like(w.v_cache)
@@ -117,7 +126,7 @@ def test_permuted_pool_is_bit_identical(dev):
     w2 = W.PrefixWorkload(w.name, w.q, w.k_new, w.v_new, k2, v2, bt2, w.context_lens, w.query_start_loc,
                           w.context_lens_host, w.query_lens_host, w.num_heads, w.num_kv_heads, w.head_dim,
                           w.block_size, w.scale)
-    assert torch.equal(a, _run(w2))
+    assert torch.equal(a, _run(w2, impl))
 
 
 def test_bad_context_length_sets_status(dev):
@@ -128,9 +137,16 @@ def test_bad_context_length_sets_status(dev):
     assert pb.pa_get_device_status() & pb.PA_DEV_BAD_SEQ_LEN
 
 
-def test_forced_timeout_returns_status_and_context_survives(dev):
+def test_forced_timeout_returns_status_and_context_survives(dev, impl):
     w = W.make_prefix_workload("p", [300, 20], [40, 9], num_blocks=40, seed=7, device=dev)
     pb.pa_get_device_status()
-    pb.prefix_workload(w, flags=pb.PA_FLAG_FORCE_TIMEOUT)
+    pb.prefix_workload(w, flags=pb.PA_FLAG_FORCE_TIMEOUT | impl.get("flags", 0))
     assert pb.pa_get_device_status() & pb.PA_DEV_TIMEOUT
-    assert_parity(_run(w), _oracle(w), "after forced timeout")
+    assert_parity(_run(w, impl), _oracle(w), "after forced timeout")
+
+
+def test_both_kernels_agree(dev):
+    w = W.make_prefix_workload("p", [1000, 0, 77], [300, 129, 64], num_blocks=80, seed=8, device=dev)
+    a = _run(w, IMPLS["tcgen05"])
+    b = _run(w, IMPLS["warp_mma"])
+    assert (a.float() - b.float()).abs().max().item() < 2e-3
