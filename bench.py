@@ -160,7 +160,8 @@ def aggregate_gbs(bytes_per_step: int, steps: int, world: int, elapsed_max: floa
 
 def kernel_hash():
     h = hashlib.sha256()
-    for p in (KERNEL_SRC, os.path.join(ROOT, "paged_kv_cache_308_gb300", "csrc", "pa_internal.h")):
+    csrc = os.path.join(ROOT, "paged_kv_cache_308_gb300", "csrc")
+    for p in (KERNEL_SRC, os.path.join(csrc, "pa_device.cuh"), os.path.join(csrc, "pa_internal.h")):
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -396,6 +397,9 @@ def run_gpu(args):
                                 "l2": "larger than L2" if wc.kv_bytes > 129e6 else "fits in L2 (warm)"}
             del wc, oc
             torch.cuda.empty_cache()
+        # chunked prefill over the paged cache (both kernels), TFLOP/s
+        from paged_kv_cache_308_gb300 import prefix_bench
+        per_config["prefix"] = prefix_bench.measure(W.PREFIX_CONFIG_NAMES, list(prefix_bench.IMPLS), 20, 3, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

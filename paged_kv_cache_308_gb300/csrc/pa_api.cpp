@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "pa_internal.h"
+#include "pa_prefix.h"
 
 namespace {
 
@@ -228,7 +229,8 @@ int make_cache_map(CUtensorMap* map, const void* base, const pa_decode_args* a) 
 }
 
 // Diagnostic builds (-DPA_TRACE): device buffer for per-CTA timestamps of
-// the partition kernel, 5 x 8 bytes per CTA, set by pa_debug_set_trace.
+// the partition kernel (5 x 8 bytes per CTA) or of the tcgen05 prefix kernel
+// (kPrefixTraceIters x 16 x 8 bytes per CTA), set by pa_debug_set_trace.
 unsigned long long* g_trace = nullptr;
 
 int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_bytes, cudaStream_t stream,
@@ -311,6 +313,40 @@ int make_new_kv_map(CUtensorMap* map, const void* base, int num_tokens, int num_
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// Whole-block views for the tcgen05 prefix kernel's V copies: one box brings
+// a block's 16 rows x head_dim as [64-column chunk][16 rows][128 B] (each chunk
+// with the 128-byte swizzle), the layout its P.V MMA reads.  Cache: dims
+// (64 halves, rows, chunk), the chunk dimension stepping 128 B through a row.
+int make_cache_block_map(CUtensorMap* map, const void* base, long long num_blocks, int num_kv_heads, int head_dim) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PA_ERR_CUDA;
+    const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks) * num_kv_heads * pa::kBlockSize;
+    cuuint64_t dims[3] = {64, rows > 0 ? rows : 1, static_cast<cuuint64_t>(head_dim / 64)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2, 128};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(pa::kBlockSize), static_cast<cuuint32_t>(head_dim / 64)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// The same for the chunk's packed [token][kv head][head_dim] tensor: dims
+// (64 halves, kv head, token, chunk); tokens past the tensor read as zeros.
+int make_new_kv_block_map(CUtensorMap* map, const void* base, int num_tokens, int num_kv_heads, int head_dim) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PA_ERR_CUDA;
+    cuuint64_t dims[4] = {64, (cuuint64_t)num_kv_heads, (cuuint64_t)(num_tokens > 0 ? num_tokens : 1),
+                          (cuuint64_t)(head_dim / 64)};
+    cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_kv_heads * head_dim * 2, 128};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)pa::kBlockSize, (cuuint32_t)(head_dim / 64)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 int validate_prefix(const pa_prefix_args* a, const pa_decode_opts* o) {
     if (!a) return PA_ERR_INVALID_ARG;
     if (a->num_seqs < 0 || a->num_seqs > 65535 || a->num_tokens < 0) return PA_ERR_INVALID_ARG;
@@ -349,11 +385,21 @@ int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t st
     ca.num_kv_heads = a->num_kv_heads;
     ca.head_dim = a->head_dim;
     ca.block_size = a->block_size;
+    // tensor-core (tcgen05) kernel by default; the warp-level MMA kernel on request
+    const bool warp_mma = o && (o->flags & PA_FLAG_PREFIX_WARP_MMA);
+    // K cache, V cache, K new, V new; the tcgen05 kernel copies V a whole block per box
     CUtensorMap maps[4];
-    if ((rc = make_cache_map(&maps[0], a->k_cache, &ca)) || (rc = make_cache_map(&maps[1], a->v_cache, &ca)) ||
-        (rc = make_new_kv_map(&maps[2], a->k_new, a->num_tokens, a->num_kv_heads, a->head_dim)) ||
-        (rc = make_new_kv_map(&maps[3], a->v_new, a->num_tokens, a->num_kv_heads, a->head_dim)))
+    if ((rc = make_cache_map(&maps[0], a->k_cache, &ca)) ||
+        (rc = make_new_kv_map(&maps[2], a->k_new, a->num_tokens, a->num_kv_heads, a->head_dim)))
         return rc;
+    if (warp_mma) {
+        if ((rc = make_cache_map(&maps[1], a->v_cache, &ca)) ||
+            (rc = make_new_kv_map(&maps[3], a->v_new, a->num_tokens, a->num_kv_heads, a->head_dim)))
+            return rc;
+    } else if ((rc = make_cache_block_map(&maps[1], a->v_cache, ca.num_blocks, a->num_kv_heads, a->head_dim)) ||
+               (rc = make_new_kv_block_map(&maps[3], a->v_new, a->num_tokens, a->num_kv_heads, a->head_dim))) {
+        return rc;
+    }
     pa::PrefixParams prm;
     prm.out = static_cast<__half*>(a->out);
     prm.q = static_cast<const __half*>(a->q);
@@ -371,8 +417,9 @@ int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t st
     prm.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
     prm.wait_limit = (o && o->wait_limit) ? o->wait_limit : pa::kDefaultWaitLimit;
     prm.force_timeout = (o && (o->flags & PA_FLAG_FORCE_TIMEOUT)) ? 1 : 0;
-    // tensor-core (tcgen05) kernel by default; the warp-level MMA kernel on request
-    const bool warp_mma = o && (o->flags & PA_FLAG_PREFIX_WARP_MMA);
+    prm.status = pa::device_status_ptr();
+    if (!prm.status) return PA_ERR_CUDA;
+    prm.trace = g_trace;
     const int tile_tokens = (warp_mma ? 64 : 128) / prm.group;
     const dim3 grid((a->max_query_len + tile_tokens - 1) / tile_tokens, a->num_kv_heads, a->num_seqs);
     if (o && o->event_partition_begin &&

@@ -1,5 +1,6 @@
-// Internal interface between the C-ABI layer (pa_api.cpp) and the kernels
-// (pa_kernels.cu).  Not installed; the public interface is include/pa_decode.h.
+// Internal interface between the C-ABI layer (pa_api.cpp) and the decode
+// kernels (pa_kernels.cu).  Not installed; the public interface is
+// include/pa_decode.h.  The chunked-prefill kernels have their own (pa_prefix.h).
 #pragma once
 
 #include <cuda.h>          // CUtensorMap (header only; the driver is reached at run time)
@@ -45,30 +46,6 @@ struct ReduceParams {
     int partition_size, max_partitions;
 };
 
-struct PrefixParams {
-    __half* out;                    // [num_tokens][H][D]
-    const __half* q;                // [num_tokens][H][D]
-    const int32_t* block_tables;    // context blocks
-    const int32_t* context_lens;    // [B]
-    const int32_t* query_start_loc; // [B + 1]
-    long long num_blocks;
-    int num_heads, num_kv_heads, group;
-    int max_blocks_per_seq, max_context_len, max_query_len, num_tokens;
-    float scale_log2;
-    unsigned wait_limit;
-    int force_timeout;
-};
-
-// Chunked-prefill kernel: grid (query tiles, kv heads, sequences); maps are
-// {K cache, V cache (2-D, as for decode), K new, V new (3-D [token][kv head][dim])}.
-int prefix_smem_bytes(int head_dim);
-cudaError_t launch_prefix(int head_dim, const PrefixParams& prm, const CUtensorMap* maps, dim3 grid,
-                          cudaStream_t stream);
-// The tcgen05 version: 128-row tiles (floor(128 / G) tokens), same maps.
-int prefix_tc_smem_bytes(int head_dim);
-cudaError_t launch_prefix_tc(int head_dim, const PrefixParams& prm, const CUtensorMap* maps, dim3 grid,
-                             cudaStream_t stream);
-
 // Dynamic shared memory of a partition CTA of `warps` warps with `stages`
 // stages each (includes 1 KB of alignment slack for the 128-byte swizzle);
 // -1 for a shape that is not compiled.
@@ -85,5 +62,9 @@ cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3
 
 // Read and clear the status word of the current device (synchronises stream).
 cudaError_t read_and_clear_status(cudaStream_t stream, int* status);
+
+// Device address of that status word on the current device (null on error);
+// kernels of other translation units record their errors through it.
+unsigned int* device_status_ptr();
 
 }  // namespace pa

@@ -1,0 +1,40 @@
+// Internal interface between the C-ABI layer (pa_api.cpp) and the
+// chunked-prefill kernels (pa_prefix.cu).  Not installed.
+#pragma once
+
+#include "pa_internal.h"
+
+namespace pa {
+
+struct PrefixParams {
+    __half* out;                    // [num_tokens][H][D]
+    const __half* q;                // [num_tokens][H][D]
+    const int32_t* block_tables;    // context blocks
+    const int32_t* context_lens;    // [B]
+    const int32_t* query_start_loc; // [B + 1]
+    long long num_blocks;
+    int num_heads, num_kv_heads, group;
+    int max_blocks_per_seq, max_context_len, max_query_len, num_tokens;
+    float scale_log2;
+    unsigned wait_limit;
+    int force_timeout;
+    unsigned int* status;           // device status word (PA_DEV_* bits are OR-ed in)
+    // Diagnostic builds (-DPA_TRACE) only: the tcgen05 kernel records
+    // SM clock stamps of its pipeline events, kPrefixTraceIters x 16 per CTA.
+    unsigned long long* trace;
+};
+
+constexpr int kPrefixTraceIters = 256;
+
+// Chunked-prefill kernel: grid (query tiles, kv heads, sequences); maps are
+// {K cache, V cache (2-D, as for decode), K new, V new (3-D [token][kv head][dim])}.
+int prefix_smem_bytes(int head_dim);
+cudaError_t launch_prefix(int head_dim, const PrefixParams& prm, const CUtensorMap* maps, dim3 grid,
+                          cudaStream_t stream);
+// The tcgen05 version: 128-row tiles (floor(128 / G) tokens); its V maps are
+// whole-block views (3-D cache, 4-D chunk) whose box is one block.
+int prefix_tc_smem_bytes(int head_dim);
+cudaError_t launch_prefix_tc(int head_dim, const PrefixParams& prm, const CUtensorMap* maps, dim3 grid,
+                             cudaStream_t stream);
+
+}  // namespace pa

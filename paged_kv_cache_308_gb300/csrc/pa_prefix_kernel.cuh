@@ -1,6 +1,5 @@
 // Chunked-prefill ("prefix") attention over the paged cache, for GB300.
-// Included by pa_kernels.cu (same translation unit: it shares the device
-// helpers and the device status word).
+// Included by pa_prefix.cu.
 //
 // Sequence b has context_lens[b] tokens in the paged cache and brings a chunk
 // of q_len_b new tokens (rows query_start_loc[b] .. [b+1]-1 of q, k_new,
@@ -77,7 +76,7 @@ __global__ void __launch_bounds__(kPrefixWarps * 32, 1)
     const int qlen = q1 - q0;
     if (C < 0 || C > prm.max_context_len || C > prm.max_blocks_per_seq * kBlockSize || qlen < 0 ||
         qlen > prm.max_query_len || q0 < 0 || q1 > prm.num_tokens) {
-        if (tile == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(&g_status, PA_DEV_BAD_SEQ_LEN);
+        if (tile == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(prm.status, PA_DEV_BAD_SEQ_LEN);
         return;
     }
     const int t0 = tile * tile_tokens;  // first chunk token of this tile
@@ -116,7 +115,7 @@ __global__ void __launch_bounds__(kPrefixWarps * 32, 1)
                     tma_load_2d(vdst + ch * S::kBoxBytes, &tmap_vc, ch * 64, row, bar);
                 }
             } else {
-                atomicOr(&g_status, PA_DEV_BAD_BLOCK_ID);
+                atomicOr(prm.status, PA_DEV_BAD_BLOCK_ID);
                 mbar_arrive(bar);
             }
         } else {
@@ -275,7 +274,7 @@ __global__ void __launch_bounds__(kPrefixWarps * 32, 1)
 
     if (aborted) {
         if (lane == 0) {
-            atomicOr(&g_status, PA_DEV_TIMEOUT);
+            atomicOr(prm.status, PA_DEV_TIMEOUT);
             atomicExch(sm_abort, 1);
         }
         // drain the copies still in flight: the last one issued on each stage

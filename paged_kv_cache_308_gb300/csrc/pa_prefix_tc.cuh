@@ -1,37 +1,65 @@
 // Chunked-prefill attention on the 5th-generation tensor cores (tcgen05 +
-// TMEM), for GB300.  Included by pa_kernels.cu after pa_prefix_kernel.cuh.
+// TMEM), for GB300.  Included by pa_prefix.cu after pa_prefix_kernel.cuh.
 //
 // Same operation and inputs as pa_prefix_kernel (see pa_prefix_kernel.cuh).
 // Mapping:
 // * one CTA per (query tile, kv head, sequence); the tile is 128 rows of
-//   (new token, GQA head) pairs = floor(128 / G) tokens.  Warps 0-3 own one
-//   row per thread (= TMEM lane); warp 4 issues every copy and MMA; the two
-//   sides hand over only through mbarriers (scores done, P ready, P.V done);
+//   (new token, GQA head) pairs = floor(128 / G) tokens.  Three roles in
+//   separate warps, handing over only through mbarriers:
+//   - warps 0-3 (softmax): thread t owns row t (= TMEM lane t); it turns its
+//     score row into P (fp16) with the online-softmax update and rescales
+//     its O row in TMEM when its max moves;
+//   - warps 4-7 (loads): warp i copies block i of every K and V tile, in the
+//     order the MMAs consume them, each into a ring slot as soon as the MMA
+//     that read the slot's previous tile has completed; their lanes keep the
+//     block-table entries of the current and the next 32 blocks in registers;
+//   - warp 8 (MMA, one lane issues): S(j+1) = Q K(j+1)^T (M 128, N 64,
+//     K = head_dim) into one of two TMEM score buffers, then
+//     O += P(j) V(j) (M 128, N = head_dim, K 64) with P read from one of two
+//     TMEM P buffers; so S(j+1) runs on the tensor cores while the rows work
+//     on tile j;
 // * keys are walked in tiles of 64 (4 blocks of 16: paged context blocks
 //   through the block table, then the chunk's own blocks), K tiles in a
-//   3-slot ring and V tiles in a 2-slot ring, each block one 16-row TMA box
-//   per 64 head_dim columns with the 128-byte swizzle;
-// * the issuer runs S = Q K^T (M 128, N 64, K = head_dim) into one of two
-//   TMEM score buffers and O += P V (M 128, N = head_dim, K 64) with P read
-//   from one of two TMEM P buffers; every thread turns its score row into P (fp16) with
-//   the online-softmax update and rescales its O row in TMEM when its max
-//   moves; S(j+1) runs on the tensor cores while rows work on tile j;
-// * completion of MMAs and copies is tracked by mbarriers; every wait is
-//   bounded, a wait that gives up sets PA_DEV_TIMEOUT and the CTA drains its
-//   copies and MMAs, frees its TMEM and exits without writing.
+//   3-slot ring and V tiles in a 2-slot ring, all with the 128-byte swizzle:
+//   a K block as one 16-row box per 64 head_dim columns (the S operand needs
+//   the 64 keys of a tile contiguous per column chunk), a V block as a single
+//   box laid out [chunk][16 rows][128 B] (one P.V MMA per block reads it);
+// * every wait is bounded; a wait that gives up sets PA_DEV_TIMEOUT and an
+//   abort flag the other roles poll, and the CTA drains its copies and MMAs,
+//   frees its TMEM and exits without writing.
 
 constexpr int kTcRows = 128;   // MMA M: rows of (token, head)
 constexpr int kTcKeys = 64;    // keys per tile: MMA N of S, K of P.V
 constexpr int kTcKSlots = 3;
 constexpr int kTcVSlots = 2;
+constexpr int kTcSoftmaxWarps = kTcRows / 32;
+constexpr int kTcLoadWarps = kTcKeys / kBlockSize;   // one per block of a key tile
+constexpr int kTcLoadWarp0 = kTcSoftmaxWarps;
+constexpr int kTcMmaWarp = kTcLoadWarp0 + kTcLoadWarps;
+constexpr int kTcThreads = (kTcMmaWarp + 1) * 32;
+
+// mbarriers of one CTA, by index
+enum : int {
+    kTcBarKFull = 0,                          // K slot landed (one arrival per load warp + copy bytes)
+    kTcBarKEmpty = kTcBarKFull + kTcKSlots,   // K slot read by its S MMA (commit)
+    kTcBarVFull = kTcBarKEmpty + kTcKSlots,   // V slot landed (as K)
+    kTcBarVEmpty = kTcBarVFull + kTcVSlots,   // V slot read by its P.V MMA (commit)
+    kTcBarSDone = kTcBarVEmpty + kTcVSlots,   // score buffer b written (commit), 2
+    kTcBarPReady = kTcBarSDone + 2,           // P buffer b written by all 4 row warps, 2
+    kTcBarODone = kTcBarPReady + 2,           // a P.V completed (commit)
+    kTcBarMDone = kTcBarODone + 1,            // every MMA of the CTA completed (final commit)
+    kTcBars = kTcBarMDone + 1
+};
 
 template <int D>
 struct PrefixTcShape {
     static constexpr int kChunks = D / 64;
     static constexpr int kQBytes = kTcRows * D * 2;
     static constexpr int kTileBytes = kTcKeys * D * 2;          // K or V of one key tile
-    static constexpr int kChunkStride = kTcKeys * 128;          // one 64-column chunk of a tile
-    static constexpr int kSmemNeed = 1024 + kQBytes + (kTcKSlots + kTcVSlots) * kTileBytes + 128;
+    static constexpr int kChunkStride = kTcKeys * 128;          // one 64-column chunk of a K tile
+    static constexpr int kBlockBytes = kBlockSize * D * 2;      // one block of a V tile: [chunk][16][128 B]
+    static constexpr int kCtrlBytes = kTcBars * 8 + 16;         // barriers, TMEM address, abort flag
+    static constexpr int kSmemNeed = 1024 + kQBytes + (kTcKSlots + kTcVSlots) * kTileBytes + kCtrlBytes;
     // at most two CTAs per SM, so that their TMEM allocations always fit in
     // the SM's 512 columns (an allocation never has to wait for another CTA)
     static constexpr int kSmemBytes = kSmemNeed > 80 * 1024 ? kSmemNeed : 80 * 1024;
@@ -122,7 +150,61 @@ __device__ __forceinline__ float tc_ex2(float x) {  // the PTX ex2.approx instru
     return y;
 }
 
-constexpr int kTcThreads = kTcRows + 32;  // 4 softmax warps (one row each thread) + 1 issuer warp
+// Diagnostic builds (-DPA_TRACE): SM clock stamps of pipeline events per key
+// tile j, 16 slots: 0-3 and 12-13 by the MMA warp (loop top, S(j+1) issued,
+// P(j) ready, V(j) landed, K(j+1) landed, P.V(j) issued), 4 and 8-11 by the
+// load warp (V(j) issued, loop top, K(j+1) slot free, K(j+1) issued, V(j)
+// slot free), 5-6 by warp 0 (scores j in, P(j) out) and 7 by warp 3 (P(j) out).
+#ifdef PA_TRACE
+#define PA_TC_MARK(j, e)                                                                                          \
+    do {                                                                                                          \
+        if (prm.trace && (j) < kPrefixTraceIters) {                                                               \
+            const size_t cta_ = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;           \
+            prm.trace[(cta_ * kPrefixTraceIters + (j)) * 16 + (e)] = (unsigned long long)clock64();              \
+        }                                                                                                         \
+    } while (0)
+#else
+#define PA_TC_MARK(j, e) \
+    do {                 \
+    } while (0)
+#endif
+
+// Block-table entries of one copy stream, held by the 32 lanes of a warp:
+// lane l has the entry of block 32 g + l (g = the current group) and of
+// block 32 (g + 1) + l, loaded one group ahead so the lookup latency is hidden.
+struct TcBlockCursor {
+    int group = -1;
+    int cur = -1;
+    int nxt = -1;
+};
+
+// Bounded wait by every lane of a warp; true only if all lanes saw the phase.
+__device__ __forceinline__ bool tc_warp_wait(uint32_t bar, uint32_t parity, uint32_t limit,
+                                             const volatile int* abort_flag) {
+    const bool ok = tc_wait(bar, parity, limit, abort_flag);
+    return __all_sync(kFull, ok);
+}
+
+__device__ __forceinline__ void tc_tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                               uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
+
+// AND of `ok` over the load warps (named barrier 1); every thread of those
+// warps calls it at the same point, so they all take the same decision.
+__device__ __forceinline__ bool tc_load_warps_agree(bool ok) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.b32 pi, %1, 0;\n\tbar.red.and.pred po, 1, %2, pi;\n\t"
+        "selp.s32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(ok ? 1 : 0), "r"(kTcLoadWarps * 32)
+        : "memory");
+    return r != 0;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -139,9 +221,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* ks = qs + S::kQBytes;
     uint8_t* vs = ks + kTcKSlots * S::kTileBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(vs + kTcVSlots * S::kTileBytes);
-    // bars: kfull[3], vfull[2], sdone[2], odone, pready[2]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kTcBars);
     volatile int* sm_abort = reinterpret_cast<volatile int*>(tslot + 1);
+    const uint32_t bar0 = smem_addr(bars);
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
     const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -153,7 +236,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int qlen = q1 - q0;
     if (C < 0 || C > prm.max_context_len || C > prm.max_blocks_per_seq * kBlockSize || qlen < 0 ||
         qlen > prm.max_query_len || q0 < 0 || q1 > prm.num_tokens) {
-        if (tile == 0 && kvh == 0 && t == 0) atomicOr(&g_status, PA_DEV_BAD_SEQ_LEN);
+        if (tile == 0 && kvh == 0 && t == 0) atomicOr(prm.status, PA_DEV_BAD_SEQ_LEN);
         return;
     }
     const int t0 = tile * tile_tokens;
@@ -164,14 +247,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int ntiles = (nblocks + 3) / 4;
     const int32_t* bt = prm.block_tables + (size_t)b * prm.max_blocks_per_seq;
 
-    const uint32_t kfull0 = smem_addr(bars), vfull0 = kfull0 + 8 * kTcKSlots;
-    const uint32_t sdone0 = vfull0 + 8 * kTcVSlots, odone = sdone0 + 16, pready0 = odone + 8;
-    const bool issuer = warp == kTcRows / 32 && lane == 0;
-    if (issuer) {
+    if (t == 0) {
         *sm_abort = 0;
-        for (int i = 0; i < 8; ++i) mbar_init(kfull0 + 8 * i, 1);
-        mbar_init(pready0, kTcRows / 32);
-        mbar_init(pready0 + 8, kTcRows / 32);
+        for (int i = 0; i < kTcBars; ++i)
+            mbar_init(bar(i), (i == kTcBarPReady || i == kTcBarPReady + 1) ? kTcSoftmaxWarps
+                              : (i < kTcBarKEmpty || (i >= kTcBarVFull && i < kTcBarVEmpty)) ? kTcLoadWarps
+                                                                                           : 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -179,42 +260,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      "r"(S::kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-
-    // Copies of key tile j: block i of the tile is context block 4j + i when
-    // that is below nctx, else chunk block 4j + i - nctx (tokens past the
-    // packed tensor read as zeros).  K and V go to separate rings.
-    auto issue_tile = [&](int j, bool want_k) {
-        const uint32_t bar = want_k ? kfull0 + 8 * (j % kTcKSlots) : vfull0 + 8 * (j % kTcVSlots);
-        const uint32_t dst = smem_addr(want_k ? ks + (j % kTcKSlots) * S::kTileBytes : vs + (j % kTcVSlots) * S::kTileBytes);
-        mbar_arrive_expect_tx(bar, S::kTileBytes);
-        for (int i = 0; i < 4; ++i) {
-            const int blk = 4 * j + i;
-            int phys = -1;
-            if (blk < nctx) {
-                phys = __ldg(bt + blk);
-                if (phys < 0 || (long long)phys >= prm.num_blocks) {
-                    atomicOr(&g_status, PA_DEV_BAD_BLOCK_ID);
-                    phys = -2;  // read zeros instead (past the packed tokens)
-                }
-            }
-#pragma unroll
-            for (int ch = 0; ch < S::kChunks; ++ch) {
-                const uint32_t d = dst + ch * S::kChunkStride + i * (kBlockSize * 128);
-                if (phys >= 0)
-                    tma_load_2d(d, want_k ? &tmap_kc : &tmap_vc, ch * 64, (phys * prm.num_kv_heads + kvh) * kBlockSize,
-                                bar);
-                else {
-                    const int tok = phys == -2 ? prm.num_tokens : q0 + (blk - nctx) * kBlockSize;
-                    tma_load_3d(d, want_k ? &tmap_kn : &tmap_vn, ch * 64, kvh, tok, bar);
-                }
-            }
-        }
-    };
-
-    if (issuer) {
-        for (int j = 0; j < kTcKSlots && j < ntiles; ++j) issue_tile(j, true);
-        for (int j = 0; j < kTcVSlots && j < ntiles; ++j) issue_tile(j, false);
     }
 
     // Q tile: row r = (token t0 + r / G, head kvh * G + r % G), 64-column
@@ -227,10 +272,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             v = __ldg(reinterpret_cast<const uint4*>(prm.q + ((size_t)(q0 + t0 + ti) * H + kvh * G + h) * D) + u);
         *reinterpret_cast<uint4*>(qs + (u >> 3) * (kTcRows * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4)) = v;
     }
-    // V rows of cache slots past the context may hold anything; they are
-    // cleared (by the issuer, once their copy has landed) before P.V reads
-    // them: p is 0 there, but 0 * NaN is not.
-    const int partial_tile = C % kBlockSize != 0 ? (nctx - 1) / 4 : -1;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
@@ -241,16 +282,131 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tP0 = tS0 + 2 * kTcKeys;      // two P buffers of 32 columns (fp16 pairs)
     const unsigned limit = prm.force_timeout ? 0u : prm.wait_limit;
 
-    if (warp == kTcRows / 32) {
-        // ---------------- issuer warp: copies and MMAs (one lane) ----------------
+    if (warp >= kTcLoadWarp0 && warp < kTcMmaWarp) {
+        // ---------------- load warps: warp i copies block i of every key tile ----------------
+        // Copies go in the order the MMAs use them (S(0), S(1), P.V(0), S(2),
+        // P.V(1), ...: K(j+1) before V(j)).  A TMA instruction occupies its
+        // issuing thread for a fixed time whatever the box size, so four warps
+        // issue in parallel; they agree on every wait so that a tile is copied
+        // by all four or by none.
+        const int i = warp - kTcLoadWarp0;
+        TcBlockCursor kcur, vcur;
+        auto fetch = [&](int g) {
+            const int blk = 32 * g + lane;
+            return blk < nctx ? __ldg(bt + blk) : -1;
+        };
+        // physical block of block blk of the sequence (meaningful for blk < nctx); warp-collective
+        auto lookup = [&](TcBlockCursor& c, int blk) {
+            const int g = blk >> 5;
+            if (g != c.group) {
+                c.cur = g == c.group + 1 ? c.nxt : fetch(g);
+                c.nxt = fetch(g + 1);
+                c.group = g;
+            }
+            return __shfl_sync(kFull, c.cur, blk & 31);
+        };
+        // block blk of a tile: context block blk when below nctx (-2 for an
+        // invalid id: read zeros instead), else chunk block blk - nctx (-1)
+        auto checked = [&](int blk, int phys) {
+            if (blk >= nctx) return -1;
+            if (phys < 0 || (long long)phys >= prm.num_blocks) {
+                atomicOr(prm.status, PA_DEV_BAD_BLOCK_ID);
+                return -2;
+            }
+            return phys;
+        };
+        auto chunk_token = [&](int blk, int p) { return p == -2 ? prm.num_tokens : q0 + (blk - nctx) * kBlockSize; };
+        // K: head_dim/64 boxes of 16 rows x 64 columns, into rows 16 i.. of
+        // every 64-column chunk of the slot (the S MMA's operand layout)
+        auto issue_k = [&](int j) {
+            const int blk = 4 * j + i;
+            const int phys = lookup(kcur, blk);
+            if (lane == 0) {
+                const uint32_t full = bar(kTcBarKFull + j % kTcKSlots);
+                const uint32_t dst = smem_addr(ks + (j % kTcKSlots) * S::kTileBytes) + i * (kBlockSize * 128);
+                mbar_arrive_expect_tx(full, S::kBlockBytes);
+                const int p = checked(blk, phys);
+#pragma unroll
+                for (int ch = 0; ch < S::kChunks; ++ch) {
+                    if (p >= 0)
+                        tma_load_2d(dst + ch * S::kChunkStride, &tmap_kc, ch * 64,
+                                    (p * prm.num_kv_heads + kvh) * kBlockSize, full);
+                    else
+                        tma_load_3d(dst + ch * S::kChunkStride, &tmap_kn, ch * 64, kvh, chunk_token(blk, p), full);
+                }
+            }
+            __syncwarp();
+        };
+        // V: the whole block in one box, [chunk][16 rows][128 B], block i of the slot
+        auto issue_v = [&](int j) {
+            const int blk = 4 * j + i;
+            const int phys = lookup(vcur, blk);
+            if (lane == 0) {
+                const uint32_t full = bar(kTcBarVFull + j % kTcVSlots);
+                const uint32_t dst = smem_addr(vs + (j % kTcVSlots) * S::kTileBytes) + i * S::kBlockBytes;
+                mbar_arrive_expect_tx(full, S::kBlockBytes);
+                const int p = checked(blk, phys);
+                if (p >= 0)
+                    tma_load_3d(dst, &tmap_vc, 0, (p * prm.num_kv_heads + kvh) * kBlockSize, 0, full);
+                else
+                    tc_tma_load_4d(dst, &tmap_vn, 0, kvh, chunk_token(blk, p), 0, full);
+            }
+            __syncwarp();
+        };
+        kcur.nxt = vcur.nxt = fetch(0);
+        bool ok = true;
+        int k_issued = 0, v_issued = 0;
+        if (ntiles > 0) {
+            issue_k(0);
+            k_issued = 1;
+        }
+        for (int j = 0; j < ntiles; ++j) {
+            const int kj = j + 1;
+            if (lane == 0 && i == 0) PA_TC_MARK(j, 8);
+            if (kj < ntiles) {
+                // slot kj % 3 last held K(kj - 3): free once S(kj - 3) has completed
+                if (kj >= kTcKSlots &&
+                    !(ok = tc_load_warps_agree(tc_warp_wait(bar(kTcBarKEmpty + kj % kTcKSlots),
+                                                            (kj / kTcKSlots - 1) & 1, limit, sm_abort))))
+                    break;
+                if (lane == 0 && i == 0) PA_TC_MARK(j, 9);
+                issue_k(kj);
+                k_issued = kj + 1;
+            }
+            if (lane == 0 && i == 0) PA_TC_MARK(j, 10);
+            // slot j % 2 last held V(j - 2): free once P.V(j - 2) has completed
+            if (j >= kTcVSlots &&
+                !(ok = tc_load_warps_agree(tc_warp_wait(bar(kTcBarVEmpty + j % kTcVSlots), (j / kTcVSlots - 1) & 1,
+                                                        limit, sm_abort))))
+                break;
+            if (lane == 0 && i == 0) PA_TC_MARK(j, 11);
+            issue_v(j);
+            v_issued = j + 1;
+            if (lane == 0 && i == 0) PA_TC_MARK(j, 4);
+        }
         if (lane == 0) {
-            constexpr uint32_t idS = tc_idesc(kTcRows, kTcKeys, 0);
-            constexpr uint32_t idO = tc_idesc(kTcRows, D, 1);
-            const uint32_t qb = smem_addr(qs);
-            int k_issued = min(kTcKSlots, ntiles), v_issued = min(kTcVSlots, ntiles);
-            int s_issued = 0, pv_issued = 0;
-            bool ok = true;
-            auto issue_s = [&](int j) {  // S(j) = Q K(j)^T into score buffer j % 2
+            if (!ok && i == 0) {
+                *sm_abort = 1;
+                atomicOr(prm.status, PA_DEV_TIMEOUT);
+            }
+            // every copy issued lands before the CTA exits: all four warps
+            // issued the same tiles, and a slot holds at most one copy that
+            // nobody may have waited for (the latest one)
+            for (int x = max(0, k_issued - kTcKSlots); x < k_issued; ++x)
+                mbar_wait(bar(kTcBarKFull + x % kTcKSlots), (x / kTcKSlots) & 1, kDefaultWaitLimit);
+            for (int x = max(0, v_issued - kTcVSlots); x < v_issued; ++x)
+                mbar_wait(bar(kTcBarVFull + x % kTcVSlots), (x / kTcVSlots) & 1, kDefaultWaitLimit);
+        }
+        __syncwarp();
+    } else if (warp == kTcMmaWarp) {
+        // ---------------- MMA warp: lane 0 issues, every lane waits ----------------
+        constexpr uint32_t idS = tc_idesc(kTcRows, kTcKeys, 0);
+        constexpr uint32_t idO = tc_idesc(kTcRows, D, 1);
+        const uint32_t qb = smem_addr(qs);
+        const int partial_tile = C % kBlockSize != 0 ? (nctx - 1) / 4 : -1;
+        // S(j) = Q K(j)^T into score buffer j % 2; K slot j % 3 is free when it completes
+        auto issue_s = [&](int j) {
+            if (lane == 0) {
                 const uint32_t kb = smem_addr(ks + (j % kTcKSlots) * S::kTileBytes);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
@@ -259,74 +415,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_mma_ss(tS0 + (j & 1) * kTcKeys, tc_desc(qb + qo, 16, 1024), tc_desc(kb + ko, 16, 1024), idS,
                               k > 0);
                 }
-                tc_commit(sdone0 + 8 * (j & 1));
-            };
-            tc_fence_after();
-            ok = tc_wait(kfull0, 0, limit, sm_abort);
-            if (ok) {
-                issue_s(0);
-                s_issued = 1;
+                tc_commit(bar(kTcBarSDone + (j & 1)));
+                tc_commit(bar(kTcBarKEmpty + j % kTcKSlots));
             }
-            for (int j = 0; ok && j < ntiles; ++j) {
-                // S(j+1) right away: it overlaps the softmax of tile j (its score
-                // buffer was last read by the rows' softmax of tile j-1)
-                if (j + 1 < ntiles) {
-                    ok = tc_wait(kfull0 + 8 * ((j + 1) % kTcKSlots), ((j + 1) / kTcKSlots) & 1, limit, sm_abort);
-                    if (!ok) break;
-                    issue_s(j + 1);
-                    s_issued = j + 2;
-                }
-                // rows have written P(j) (and rescaled O if they had to)
-                ok = tc_wait(pready0 + 8 * (j & 1), (j >> 1) & 1, limit, sm_abort);
-                if (!ok) break;
+            __syncwarp();
+        };
+        bool ok = tc_warp_wait(bar(kTcBarKFull), 0, limit, sm_abort);
+        if (ok) {
+            tc_fence_after();
+            issue_s(0);
+        }
+        for (int j = 0; ok && j < ntiles; ++j) {
+            if (lane == 0) PA_TC_MARK(j, 0);
+            if (j + 1 < ntiles) {
+                // score buffer (j+1) % 2 last held S(j-1); the rows read it
+                // before P(j-1) was ready, which the previous step waited for
+                if (!(ok = tc_warp_wait(bar(kTcBarKFull + (j + 1) % kTcKSlots), ((j + 1) / kTcKSlots) & 1, limit,
+                                        sm_abort)))
+                    break;
+                if (lane == 0) PA_TC_MARK(j, 12);
                 tc_fence_after();
-                if (k_issued < ntiles && k_issued == j + kTcKSlots) {  // S(j) is done with K slot j % 3
-                    issue_tile(k_issued, true);
-                    ++k_issued;
+                issue_s(j + 1);
+            }
+            if (lane == 0) PA_TC_MARK(j, 1);
+            // rows have written P(j) (and rescaled O if they had to)
+            if (!(ok = tc_warp_wait(bar(kTcBarPReady + (j & 1)), (j >> 1) & 1, limit, sm_abort))) break;
+            if (lane == 0) PA_TC_MARK(j, 2);
+            if (!(ok = tc_warp_wait(bar(kTcBarVFull + j % kTcVSlots), (j / kTcVSlots) & 1, limit, sm_abort))) break;
+            if (lane == 0) PA_TC_MARK(j, 3);
+            uint8_t* vt = vs + (j % kTcVSlots) * S::kTileBytes;
+            if (j == partial_tile) {
+                // V rows of cache slots past the context may hold anything: p is
+                // 0 there, but 0 * NaN is not; clear them before P.V reads them
+                const int i = (nctx - 1) % 4, first = C % kBlockSize;
+                const int units = (kBlockSize - first) * S::kChunks * 8;
+                uint8_t* vb = vt + i * S::kBlockBytes;
+                for (int x = lane; x < units; x += 32) {
+                    const int r = first + x / (S::kChunks * 8), u = x % (S::kChunks * 8);
+                    *reinterpret_cast<uint4*>(vb + (u >> 3) * (kBlockSize * 128) + r * 128 + (u & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 }
-                if (j > 0) {  // P.V(j-1) done: its V slot takes tile j+1
-                    ok = tc_wait(odone, (j - 1) & 1, limit, sm_abort);
-                    if (!ok) break;
-                    if (v_issued < ntiles && v_issued == j + 1) {
-                        issue_tile(v_issued, false);
-                        ++v_issued;
-                    }
-                }
-                ok = tc_wait(vfull0 + 8 * (j % kTcVSlots), (j / kTcVSlots) & 1, limit, sm_abort);
-                if (!ok) break;
-                if (j == partial_tile) {
-                    uint8_t* vt = vs + (j % kTcVSlots) * S::kTileBytes;
-                    const int i = (nctx - 1) % 4, first = C % kBlockSize;
-                    for (int r = first; r < kBlockSize; ++r)
-                        for (int u = 0; u < S::kChunks * 8; ++u)
-                            *reinterpret_cast<uint4*>(vt + (u >> 3) * S::kChunkStride + (i * kBlockSize + r) * 128 +
-                                                      (u & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                }
-                // O += P(j) V(j), P in buffer j % 2
-                const uint32_t vb = smem_addr(vs + (j % kTcVSlots) * S::kTileBytes);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                // O += P(j) V(j), P in buffer j % 2, one MMA per block of 16 keys
+                // (V block: 64-column chunks 2 KB apart, 8-key groups 1 KB
+                // apart); V slot j % 2 is free when they complete
+                const uint32_t vb = smem_addr(vt);
 #pragma unroll
                 for (int k = 0; k < kTcKeys / 16; ++k)
-                    tc_mma_ts(tO, tP0 + (j & 1) * (kTcKeys / 2) + k * 8, tc_desc(vb + k * 2048, S::kChunkStride, 1024),
-                              idO, (j > 0 || k > 0));
-                tc_commit(odone);
-                pv_issued = j + 1;
+                    tc_mma_ts(tO, tP0 + (j & 1) * (kTcKeys / 2) + k * 8,
+                              tc_desc(vb + k * S::kBlockBytes, kBlockSize * 128, 1024), idO, (j > 0 || k > 0));
+                tc_commit(bar(kTcBarODone));
+                tc_commit(bar(kTcBarVEmpty + j % kTcVSlots));
+                PA_TC_MARK(j, 13);
             }
+            __syncwarp();
+        }
+        if (lane == 0) {
             if (!ok) {
                 *sm_abort = 1;
-                atomicOr(&g_status, PA_DEV_TIMEOUT);
-                // drain: copies issued and MMAs committed that nobody waited for
-                for (int j = max(0, k_issued - kTcKSlots); j < k_issued; ++j)
-                    mbar_wait(kfull0 + 8 * (j % kTcKSlots), (j / kTcKSlots) & 1, kDefaultWaitLimit);
-                for (int j = max(0, v_issued - kTcVSlots); j < v_issued; ++j)
-                    mbar_wait(vfull0 + 8 * (j % kTcVSlots), (j / kTcVSlots) & 1, kDefaultWaitLimit);
-                for (int j = max(0, s_issued - 2); j < s_issued; ++j)
-                    mbar_wait(sdone0 + 8 * (j & 1), (j >> 1) & 1, kDefaultWaitLimit);
-                for (int j = max(0, pv_issued - 2); j < pv_issued; ++j)
-                    mbar_wait(odone, j & 1, kDefaultWaitLimit);
+                atomicOr(prm.status, PA_DEV_TIMEOUT);
             }
+            // every MMA issued above has completed once this commit arrives
+            tc_commit(bar(kTcBarMDone));
+            mbar_wait(bar(kTcBarMDone), 0, kDefaultWaitLimit);
         }
-        __syncwarp();  // the issuer warp reaches the final barrier converged
+        __syncwarp();
     } else {
         // ---------------- softmax warps: thread t owns row t (TMEM lane t) ----------------
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -334,15 +491,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int my_tok = t0 + ti;  // chunk token index of the row
         const bool row_real = ti < tile_tokens && my_tok < qlen;
         const float sl2 = prm.scale_log2;
+        const uint32_t odone = bar(kTcBarODone);
         float m = -INFINITY, l = 0.f;  // reference max (scaled, log2 domain) and exp sum
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            ok = tc_wait(sdone0 + 8 * (j & 1), (j >> 1) & 1, limit, sm_abort);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
+            if (!(ok = tc_warp_wait(bar(kTcBarSDone + (j & 1)), (j >> 1) & 1, limit, sm_abort))) break;
             tc_fence_after();
+            if (t == 0) PA_TC_MARK(j, 5);
             uint32_t sv[2][32];
             const uint32_t tS = tS0 + (j & 1) * kTcKeys + lane_off;
             tc_ld32(tS, sv[0]);
@@ -391,16 +546,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 pk[c] = half2_bits(__floats2half2_rn(p0, p1));
             }
             l = l * alpha + (rs0 + rs1);
-            // P(j) to its own buffer; P.V(j-2), its last reader, completed
-            // before S(j) (committed after it) did
+            // P(j) to its own buffer; P.V(j-2), its last reader, was issued
+            // before S(j) and so completed before S(j) did
             tc_st32(tP0 + (j & 1) * (kTcKeys / 2) + lane_off, pk);
-            if (j > 0 && __any_sync(0xffffffffu, move)) {
-                // O is written by P.V(j-1): wait for it, then rescale this row
-                if (!tc_wait(odone, (j - 1) & 1, limit, sm_abort)) ok = false;
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
+            if (j > 0 && __any_sync(kFull, move)) {
+                // O is written by P.V(j-1): wait for it, then rescale this row.
+                // P.V(j-2) completed before S(j), so odone is at most one phase
+                // behind and the parity wait is unambiguous.
+                if (!(ok = tc_warp_wait(odone, (j - 1) & 1, limit, sm_abort))) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
@@ -413,16 +566,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(pready0 + 8 * (j & 1));
+            if (t == 0) PA_TC_MARK(j, 6);
+            if (t == 96) PA_TC_MARK(j, 7);
+            if (lane == 0) mbar_arrive(bar(kTcBarPReady + (j & 1)));
         }
         // odone completes once per P.V, in issue order.  S(ntiles-1) was issued
         // before P.V(ntiles-2), so that P.V may still run here; a parity wait
         // only tells phases apart within one of the current phase, so wait
         // for phase ntiles-2 before phase ntiles-1.
-        if (ok && ntiles >= 2) ok = tc_wait(odone, (ntiles - 2) & 1, limit, sm_abort);
-        if (ok) ok = tc_wait(odone, (ntiles - 1) & 1, limit, sm_abort);
-        if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) *sm_abort = 1;
+        if (ok && ntiles >= 2) ok = tc_warp_wait(odone, (ntiles - 2) & 1, limit, sm_abort);
+        if (ok) ok = tc_warp_wait(odone, (ntiles - 1) & 1, limit, sm_abort);
+        if (!ok) {
+            if (lane == 0) {
+                *sm_abort = 1;
+                atomicOr(prm.status, PA_DEV_TIMEOUT);
+            }
         } else {
             tc_fence_after();
             // O / l to fp16 for the rows that exist

@@ -1,0 +1,85 @@
+"""Time the chunked-prefill (prefix) attention kernels on the named workloads.
+
+For each workload and kernel, runs back-to-back pa_prefix_ex calls on one
+stream (after warm-up), times them with CUDA events and prints one JSON line:
+microseconds per call, useful TFLOP/s (score and P.V multiply-adds over the
+visible keys only, see workloads.PrefixWorkload.flops) and the fraction of
+the measured dense 16-bit tensor-core peak.
+
+    python -m paged_kv_cache_308_gb300.prefix_bench [--impl tcgen05|warp_mma|both] [--iters N] [workload ...]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+
+import torch
+
+from . import binding as pb
+from . import workloads as W
+
+IMPLS = {"tcgen05": 0, "warp_mma": pb.PA_FLAG_PREFIX_WARP_MMA}
+FALLBACK_TENSOR_TFLOPS = 1900.0
+
+
+def tensor_peak():
+    """Dense 16-bit tensor-core TFLOP/s: the measured burst figure when present."""
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_TENSOR_TFLOPS, "fallback"
+
+
+def time_prefix(w, flags: int, iters: int, warmup: int, stream=None) -> float:
+    """Mean seconds per pa_prefix_ex call over `iters` back-to-back calls."""
+    stream = stream or torch.cuda.current_stream()
+    out = torch.empty_like(w.q)
+    for _ in range(warmup):
+        pb.prefix_workload(w, out, stream=stream, flags=flags)
+    torch.cuda.synchronize()
+    if pb.pa_get_device_status() != 0:
+        raise RuntimeError("prefix kernel reported a device error")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        pb.prefix_workload(w, out, stream=stream, flags=flags)
+    e1.record(stream)
+    e1.synchronize()
+    if pb.pa_get_device_status() != 0:
+        raise RuntimeError("prefix kernel reported a device error")
+    return e0.elapsed_time(e1) / iters / 1e3
+
+
+def measure(names, impls, iters: int, warmup: int, device) -> list:
+    peak, kind = tensor_peak()
+    rows = []
+    for name in names:
+        w = W.make_prefix_config(name, device=device)
+        for impl in impls:
+            t = time_prefix(w, IMPLS[impl], iters, warmup)
+            tf = w.flops / t / 1e12
+            rows.append({"workload": name, "kernel": impl, "us_per_call": t * 1e6, "tflops": tf,
+                         "frac_of_tensor_peak": tf / peak, "peak_tflops": peak, "peak_kind": kind,
+                         "tokens": w.num_tokens, "flops_per_call": w.flops})
+        del w
+        torch.cuda.empty_cache()
+    return rows
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--impl", choices=["tcgen05", "warp_mma", "both"], default="both")
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("workloads", nargs="*", default=W.PREFIX_CONFIG_NAMES)
+    args = ap.parse_args()
+    impls = list(IMPLS) if args.impl == "both" else [args.impl]
+    for row in measure(args.workloads, impls, args.iters, args.warmup, torch.device("cuda:0")):
+        print(json.dumps(row), flush=True)
+
+
+if __name__ == "__main__":
+    main()
