@@ -9,15 +9,17 @@
 //   - warps 0-3 (softmax): thread t owns row t (= TMEM lane t); it turns its
 //     score row into P (fp16) with the online-softmax update and rescales
 //     its O row in TMEM when its max moves;
-//   - warps 4-7 (loads): warp i copies block i of every K and V tile, in the
-//     order the MMAs consume them, each into a ring slot as soon as the MMA
-//     that read the slot's previous tile has completed; their lanes keep the
+//   - warps 4-13 (loads): eight copy K (two per block of a tile), two copy V
+//     (two blocks each), each group into its ring slot as soon as the MMA that
+//     read the slot's previous tile has completed; their lanes keep the
 //     block-table entries of the current and the next 32 blocks in registers;
-//   - warp 8 (MMA, one lane issues): S(j+1) = Q K(j+1)^T (M 128, N 64,
-//     K = head_dim) into one of two TMEM score buffers, then
-//     O += P(j) V(j) (M 128, N = head_dim, K 64) with P read from one of two
-//     TMEM P buffers; so S(j+1) runs on the tensor cores while the rows work
-//     on tile j;
+//   - warps 14 and 15 (MMA, one lane each): warp 14 issues S(j) = Q K(j)^T
+//     (M 128, N 64, K = head_dim, Q read from TMEM so only K comes from
+//     shared memory) into the TMEM score buffer as soon as every row has
+//     read S(j-1) out of it, warp 15 O += P(j) V(j) (M 128, N = head_dim,
+//     K 64) with P read from one of two TMEM P buffers.  The tensor cores
+//     take few MMAs ahead of their issuer, so two issuing threads keep them
+//     busy while either waits; S(j+1) runs while the rows work on tile j;
 // * keys are walked in tiles of 64 (4 blocks of 16: paged context blocks
 //   through the block table, then the chunk's own blocks), K tiles in a
 //   3-slot ring and V tiles in a 2-slot ring, all with the 128-byte swizzle:
@@ -30,41 +32,55 @@
 
 constexpr int kTcRows = 128;   // MMA M: rows of (token, head)
 constexpr int kTcKeys = 64;    // keys per tile: MMA N of S, K of P.V
-constexpr int kTcKSlots = 3;
-constexpr int kTcVSlots = 2;
+constexpr int kTcMaxSlots = 4;  // K or V ring slots at most
 constexpr int kTcSoftmaxWarps = kTcRows / 32;
-constexpr int kTcLoadWarps = kTcKeys / kBlockSize;   // one per block of a key tile
+constexpr int kTcKLoadWarps = 2 * (kTcKeys / kBlockSize);  // two per K block of a key tile
+constexpr int kTcVLoadWarps = 2;                           // each copies every other V block
+constexpr int kTcLoadWarps = kTcKLoadWarps + kTcVLoadWarps;
 constexpr int kTcLoadWarp0 = kTcSoftmaxWarps;
-constexpr int kTcMmaWarp = kTcLoadWarp0 + kTcLoadWarps;
-constexpr int kTcThreads = (kTcMmaWarp + 1) * 32;
+constexpr int kTcSWarp = kTcLoadWarp0 + kTcLoadWarps;  // issues the S MMAs
+constexpr int kTcPVWarp = kTcSWarp + 1;                // issues the P.V MMAs
+constexpr int kTcThreads = (kTcPVWarp + 1) * 32;
+// registers per thread: the SM's 64 K registers over the CTA's threads, in
+// the allocation unit of 8
+constexpr int kTcMaxRegs = (65536 / kTcThreads) / 8 * 8;
 
 // mbarriers of one CTA, by index
 enum : int {
     kTcBarKFull = 0,                          // K slot landed (one arrival per load warp + copy bytes)
-    kTcBarKEmpty = kTcBarKFull + kTcKSlots,   // K slot read by its S MMA (commit)
-    kTcBarVFull = kTcBarKEmpty + kTcKSlots,   // V slot landed (as K)
-    kTcBarVEmpty = kTcBarVFull + kTcVSlots,   // V slot read by its P.V MMA (commit)
-    kTcBarSDone = kTcBarVEmpty + kTcVSlots,   // score buffer b written (commit), 2
-    kTcBarPReady = kTcBarSDone + 2,           // P buffer b written by all 4 row warps, 2
-    kTcBarODone = kTcBarPReady + 2,           // a P.V completed (commit)
-    kTcBarMDone = kTcBarODone + 1,            // every MMA of the CTA completed (final commit)
-    kTcBars = kTcBarMDone + 1
+    kTcBarKEmpty = kTcBarKFull + kTcMaxSlots,   // K slot read by its S MMA (commit)
+    kTcBarVFull = kTcBarKEmpty + kTcMaxSlots,   // V slot landed (as K)
+    kTcBarVEmpty = kTcBarVFull + kTcMaxSlots,   // V slot read by its P.V MMA (commit)
+    kTcBarSDone = kTcBarVEmpty + kTcMaxSlots,   // the score buffer holds S(j) (commit)
+    kTcBarSFree = kTcBarSDone + 1,            // every row warp has read S(j) into registers
+    kTcBarPReady = kTcBarSFree + 1,           // P buffer b written by all 4 row warps, 2
+    kTcBarPVDone = kTcBarPReady + 2,          // the P.V reading P buffer b completed (commit), 2
+    kTcBarQReady = kTcBarPVDone + 2,          // Q rows stored in TMEM by the 4 row warps
+    kTcBarSDrain = kTcBarQReady + 1,          // every S MMA completed (final commit)
+    kTcBarPVDrain = kTcBarSDrain + 1,         // every P.V MMA completed (final commit)
+    kTcBars = kTcBarPVDrain + 1
 };
 
 template <int D>
 struct PrefixTcShape {
     static constexpr int kChunks = D / 64;
-    static constexpr int kQBytes = kTcRows * D * 2;
     static constexpr int kTileBytes = kTcKeys * D * 2;          // K or V of one key tile
     static constexpr int kChunkStride = kTcKeys * 128;          // one 64-column chunk of a K tile
     static constexpr int kBlockBytes = kBlockSize * D * 2;      // one block of a V tile: [chunk][16][128 B]
     static constexpr int kCtrlBytes = kTcBars * 8 + 16;         // barriers, TMEM address, abort flag
-    static constexpr int kSmemNeed = 1024 + kQBytes + (kTcKSlots + kTcVSlots) * kTileBytes + kCtrlBytes;
+    // ring slots: 7 tiles of 32 KB fill the shared memory at head_dim 256
+    static constexpr int kKSlots = 4;
+    static constexpr int kVSlots = D == 256 ? 3 : 4;
+    static constexpr int kSmemNeed = 1024 + (kKSlots + kVSlots) * kTileBytes + kCtrlBytes;
     // at most two CTAs per SM, so that their TMEM allocations always fit in
     // the SM's 512 columns (an allocation never has to wait for another CTA)
     static constexpr int kSmemBytes = kSmemNeed > 80 * 1024 ? kSmemNeed : 80 * 1024;
-    // O (D columns), two score buffers (64 each), two P buffers (32 each)
-    static constexpr int kTmemCols = D + 2 * kTcKeys + kTcKeys <= 256 ? 256 : 512;
+    // O (D columns), Q (D / 2 columns of fp16 pairs), one score buffer (64),
+    // two P buffers (32 columns of fp16 pairs each)
+    static constexpr int kTmemUsed = D + D / 2 + 2 * kTcKeys;
+    static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+    static_assert(kTmemUsed <= 512, "tensor memory columns of one SM");
+    static_assert(kKSlots <= kTcMaxSlots && kVSlots <= kTcMaxSlots, "ring barriers");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
 };
 
@@ -154,7 +170,8 @@ __device__ __forceinline__ float tc_ex2(float x) {  // the PTX ex2.approx instru
 // tile j, 16 slots: 0-3 and 12-13 by the MMA warp (loop top, S(j+1) issued,
 // P(j) ready, V(j) landed, K(j+1) landed, P.V(j) issued), 4 and 8-11 by the
 // load warp (V(j) issued, loop top, K(j+1) slot free, K(j+1) issued, V(j)
-// slot free), 5-6 by warp 0 (scores j in, P(j) out) and 7 by warp 3 (P(j) out).
+// slot free), 5-6 by warp 0 (scores j in, P(j) out), 7 by warp 3 (P(j) out),
+// 14-15 by the S warp (K(j) landed, S(j-1) read by the rows).
 #ifdef PA_TRACE
 #define PA_TC_MARK(j, e)                                                                                          \
     do {                                                                                                          \
@@ -193,21 +210,22 @@ __device__ __forceinline__ void tc_tma_load_4d(uint32_t dst, const CUtensorMap* 
         : "memory");
 }
 
-// AND of `ok` over the load warps (named barrier 1); every thread of those
-// warps calls it at the same point, so they all take the same decision.
-__device__ __forceinline__ bool tc_load_warps_agree(bool ok) {
+// AND of `ok` over a group of warps (named barrier `id`, `threads` threads);
+// every thread of the group calls it at the same point, so they all take the
+// same decision.
+__device__ __forceinline__ bool tc_group_agree(bool ok, int id, int threads) {
     int r;
     asm volatile(
-        "{\n\t.reg .pred pi, po;\n\tsetp.ne.b32 pi, %1, 0;\n\tbar.red.and.pred po, 1, %2, pi;\n\t"
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.b32 pi, %1, 0;\n\tbar.red.and.pred po, %2, %3, pi;\n\t"
         "selp.s32 %0, 1, 0, po;\n\t}"
         : "=r"(r)
-        : "r"(ok ? 1 : 0), "r"(kTcLoadWarps * 32)
+        : "r"(ok ? 1 : 0), "r"(id), "r"(threads)
         : "memory");
     return r != 0;
 }
 
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __maxnreg__(kTcMaxRegs)
     pa_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_kc, const __grid_constant__ CUtensorMap tmap_vc,
                         const __grid_constant__ CUtensorMap tmap_kn, const __grid_constant__ CUtensorMap tmap_vn,
                         const PrefixParams prm) {
@@ -217,10 +235,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint8_t* qs = smem;
-    uint8_t* ks = qs + S::kQBytes;
-    uint8_t* vs = ks + kTcKSlots * S::kTileBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(vs + kTcVSlots * S::kTileBytes);
+    uint8_t* ks = smem;
+    uint8_t* vs = ks + S::kKSlots * S::kTileBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(vs + S::kVSlots * S::kTileBytes);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kTcBars);
     volatile int* sm_abort = reinterpret_cast<volatile int*>(tslot + 1);
     const uint32_t bar0 = smem_addr(bars);
@@ -249,10 +266,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (t == 0) {
         *sm_abort = 0;
-        for (int i = 0; i < kTcBars; ++i)
-            mbar_init(bar(i), (i == kTcBarPReady || i == kTcBarPReady + 1) ? kTcSoftmaxWarps
-                              : (i < kTcBarKEmpty || (i >= kTcBarVFull && i < kTcBarVEmpty)) ? kTcLoadWarps
-                                                                                           : 1);
+        for (int i = 0; i < kTcBars; ++i) {
+            const bool by_rows = i == kTcBarSFree || i == kTcBarPReady || i == kTcBarPReady + 1 || i == kTcBarQReady;
+            const bool by_k_loads = i < kTcBarKEmpty, by_v_loads = i >= kTcBarVFull && i < kTcBarVEmpty;
+            mbar_init(bar(i), by_rows ? kTcSoftmaxWarps : by_k_loads ? kTcKLoadWarps : by_v_loads ? kTcVLoadWarps : 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -262,48 +280,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 
-    // Q tile: row r = (token t0 + r / G, head kvh * G + r % G), 64-column
-    // chunks of 128 rows x 128 B with the 128-byte swizzle; missing rows are 0.
-    for (int idx = t; idx < kTcRows * (D / 8); idx += kTcThreads) {
-        const int r = idx / (D / 8), u = idx % (D / 8);
-        const int ti = r / G, h = r % G;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (ti < tile_tokens && t0 + ti < qlen)
-            v = __ldg(reinterpret_cast<const uint4*>(prm.q + ((size_t)(q0 + t0 + ti) * H + kvh * G + h) * D) + u);
-        *reinterpret_cast<uint4*>(qs + (u >> 3) * (kTcRows * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4)) = v;
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tO = tmem;                    // D columns
-    const uint32_t tS0 = tmem + D;               // two score buffers of 64 columns
-    const uint32_t tP0 = tS0 + 2 * kTcKeys;      // two P buffers of 32 columns (fp16 pairs)
+    const uint32_t tQ = tO + D;                  // D / 2 columns (fp16 pairs)
+    const uint32_t tS = tQ + D / 2;              // the score buffer, 64 columns
+    const uint32_t tP0 = tS + kTcKeys;           // two P buffers of 32 columns (fp16 pairs)
     const unsigned limit = prm.force_timeout ? 0u : prm.wait_limit;
 
-    if (warp >= kTcLoadWarp0 && warp < kTcMmaWarp) {
-        // ---------------- load warps: warp i copies block i of every key tile ----------------
-        // Copies go in the order the MMAs use them (S(0), S(1), P.V(0), S(2),
-        // P.V(1), ...: K(j+1) before V(j)).  A TMA instruction occupies its
-        // issuing thread for a fixed time whatever the box size, so four warps
-        // issue in parallel; they agree on every wait so that a tile is copied
-        // by all four or by none.
-        const int i = warp - kTcLoadWarp0;
-        TcBlockCursor kcur, vcur;
+    if (warp >= kTcLoadWarp0 && warp < kTcSWarp) {
+        // ---------------- load warps: K and V in two independent groups ----------------
+        // A TMA instruction occupies its issuing thread for a fixed time
+        // whatever the box size, so the copies are spread over many warps:
+        // K warp (i, h) copies half h of the 64-column chunks of block i of
+        // every K tile, V warp i the blocks i, i + 2 of every V tile (one box
+        // each).  Each group
+        // walks its own ring and agrees on every wait (one named barrier per
+        // group), so a tile is copied by all of a group or by none.
+        const int lw = warp - kTcLoadWarp0;
+        const bool is_k = lw < kTcKLoadWarps;
+        const int i = is_k ? (lw & 3) : lw - kTcKLoadWarps;  // (first) block of the tile
+        const int h = is_k ? (lw >> 2) : 0;
+        constexpr int kVBlocks = (kTcKeys / kBlockSize) / kTcVLoadWarps;  // V blocks per warp and tile
+        constexpr int kHalfChunks = (S::kChunks + 1) / 2;
+        const int ch0 = h * kHalfChunks, ch1 = min(S::kChunks, ch0 + kHalfChunks);
+        const int slots = is_k ? S::kKSlots : S::kVSlots;
+        const int full0 = is_k ? kTcBarKFull : kTcBarVFull, empty0 = is_k ? kTcBarKEmpty : kTcBarVEmpty;
+        const int group_bar = is_k ? 1 : 2, group_threads = (is_k ? kTcKLoadWarps : kTcVLoadWarps) * 32;
         auto fetch = [&](int g) {
             const int blk = 32 * g + lane;
             return blk < nctx ? __ldg(bt + blk) : -1;
         };
         // physical block of block blk of the sequence (meaningful for blk < nctx); warp-collective
-        auto lookup = [&](TcBlockCursor& c, int blk) {
+        TcBlockCursor cur;
+        auto lookup = [&](int blk) {
             const int g = blk >> 5;
-            if (g != c.group) {
-                c.cur = g == c.group + 1 ? c.nxt : fetch(g);
-                c.nxt = fetch(g + 1);
-                c.group = g;
+            if (g != cur.group) {
+                cur.cur = g == cur.group + 1 ? cur.nxt : fetch(g);
+                cur.nxt = fetch(g + 1);
+                cur.group = g;
             }
-            return __shfl_sync(kFull, c.cur, blk & 31);
+            return __shfl_sync(kFull, cur.cur, blk & 31);
         };
         // block blk of a tile: context block blk when below nctx (-2 for an
         // invalid id: read zeros instead), else chunk block blk - nctx (-1)
@@ -316,172 +335,172 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             return phys;
         };
         auto chunk_token = [&](int blk, int p) { return p == -2 ? prm.num_tokens : q0 + (blk - nctx) * kBlockSize; };
-        // K: head_dim/64 boxes of 16 rows x 64 columns, into rows 16 i.. of
-        // every 64-column chunk of the slot (the S MMA's operand layout)
-        auto issue_k = [&](int j) {
-            const int blk = 4 * j + i;
-            const int phys = lookup(kcur, blk);
-            if (lane == 0) {
-                const uint32_t full = bar(kTcBarKFull + j % kTcKSlots);
-                const uint32_t dst = smem_addr(ks + (j % kTcKSlots) * S::kTileBytes) + i * (kBlockSize * 128);
-                mbar_arrive_expect_tx(full, S::kBlockBytes);
-                const int p = checked(blk, phys);
+        auto issue = [&](int j) {
+            if (!is_k) {
+                // blocks i, i + kTcVLoadWarps, ... of the tile, each in one box
+                // laid out [chunk][16 rows][128 B]
+                int phys[kVBlocks];
 #pragma unroll
-                for (int ch = 0; ch < S::kChunks; ++ch) {
-                    if (p >= 0)
-                        tma_load_2d(dst + ch * S::kChunkStride, &tmap_kc, ch * 64,
-                                    (p * prm.num_kv_heads + kvh) * kBlockSize, full);
+                for (int x = 0; x < kVBlocks; ++x) phys[x] = lookup(4 * j + i + x * kTcVLoadWarps);
+                if (lane == 0) {
+                    const uint32_t full = bar(full0 + j % slots);
+                    mbar_arrive_expect_tx(full, kVBlocks * S::kBlockBytes);
+#pragma unroll
+                    for (int x = 0; x < kVBlocks; ++x) {
+                        const int bi = i + x * kTcVLoadWarps, blk = 4 * j + bi;
+                        const int p = checked(blk, phys[x]);
+                        const uint32_t dst = smem_addr(vs + (j % S::kVSlots) * S::kTileBytes) + bi * S::kBlockBytes;
+                        if (p >= 0)
+                            tma_load_3d(dst, &tmap_vc, 0, (p * prm.num_kv_heads + kvh) * kBlockSize, 0, full);
+                        else
+                            tc_tma_load_4d(dst, &tmap_vn, 0, kvh, chunk_token(blk, p), 0, full);
+                    }
+                }
+                __syncwarp();
+                return;
+            }
+            const int blk = 4 * j + i;
+            const int phys = lookup(blk);
+            if (lane == 0) {
+                const uint32_t full = bar(full0 + j % slots);
+                const int p = checked(blk, phys);
+                {
+                    // 16-row x 64-column boxes into rows 16 i.. of the slot's
+                    // column chunks (the S MMA's operand layout)
+                    const uint32_t dst = smem_addr(ks + (j % S::kKSlots) * S::kTileBytes) + i * (kBlockSize * 128);
+                    if (ch1 > ch0)
+                        mbar_arrive_expect_tx(full, (ch1 - ch0) * (kBlockSize * 128));
                     else
-                        tma_load_3d(dst + ch * S::kChunkStride, &tmap_kn, ch * 64, kvh, chunk_token(blk, p), full);
+                        mbar_arrive(full);
+                    for (int ch = ch0; ch < ch1; ++ch) {
+                        if (p >= 0)
+                            tma_load_2d(dst + ch * S::kChunkStride, &tmap_kc, ch * 64,
+                                        (p * prm.num_kv_heads + kvh) * kBlockSize, full);
+                        else
+                            tma_load_3d(dst + ch * S::kChunkStride, &tmap_kn, ch * 64, kvh, chunk_token(blk, p), full);
+                    }
                 }
             }
             __syncwarp();
         };
-        // V: the whole block in one box, [chunk][16 rows][128 B], block i of the slot
-        auto issue_v = [&](int j) {
-            const int blk = 4 * j + i;
-            const int phys = lookup(vcur, blk);
-            if (lane == 0) {
-                const uint32_t full = bar(kTcBarVFull + j % kTcVSlots);
-                const uint32_t dst = smem_addr(vs + (j % kTcVSlots) * S::kTileBytes) + i * S::kBlockBytes;
-                mbar_arrive_expect_tx(full, S::kBlockBytes);
-                const int p = checked(blk, phys);
-                if (p >= 0)
-                    tma_load_3d(dst, &tmap_vc, 0, (p * prm.num_kv_heads + kvh) * kBlockSize, 0, full);
-                else
-                    tc_tma_load_4d(dst, &tmap_vn, 0, kvh, chunk_token(blk, p), 0, full);
-            }
-            __syncwarp();
-        };
-        kcur.nxt = vcur.nxt = fetch(0);
+        cur.nxt = fetch(0);
         bool ok = true;
-        int k_issued = 0, v_issued = 0;
-        if (ntiles > 0) {
-            issue_k(0);
-            k_issued = 1;
-        }
+        int issued = 0;
         for (int j = 0; j < ntiles; ++j) {
-            const int kj = j + 1;
-            if (lane == 0 && i == 0) PA_TC_MARK(j, 8);
-            if (kj < ntiles) {
-                // slot kj % 3 last held K(kj - 3): free once S(kj - 3) has completed
-                if (kj >= kTcKSlots &&
-                    !(ok = tc_load_warps_agree(tc_warp_wait(bar(kTcBarKEmpty + kj % kTcKSlots),
-                                                            (kj / kTcKSlots - 1) & 1, limit, sm_abort))))
-                    break;
-                if (lane == 0 && i == 0) PA_TC_MARK(j, 9);
-                issue_k(kj);
-                k_issued = kj + 1;
-            }
-            if (lane == 0 && i == 0) PA_TC_MARK(j, 10);
-            // slot j % 2 last held V(j - 2): free once P.V(j - 2) has completed
-            if (j >= kTcVSlots &&
-                !(ok = tc_load_warps_agree(tc_warp_wait(bar(kTcBarVEmpty + j % kTcVSlots), (j / kTcVSlots - 1) & 1,
-                                                        limit, sm_abort))))
+            // slot j % slots last held tile j - slots: free once the MMA that
+            // read it has completed
+            if (j >= slots &&
+                !(ok = tc_group_agree(tc_warp_wait(bar(empty0 + j % slots), (j / slots - 1) & 1, limit, sm_abort),
+                                      group_bar, group_threads)))
                 break;
-            if (lane == 0 && i == 0) PA_TC_MARK(j, 11);
-            issue_v(j);
-            v_issued = j + 1;
-            if (lane == 0 && i == 0) PA_TC_MARK(j, 4);
+            if (lane == 0 && lw == 0) PA_TC_MARK(j, 9);
+            if (lane == 0 && lw == kTcKLoadWarps) PA_TC_MARK(j, 11);
+            issue(j);
+            issued = j + 1;
+            if (lane == 0 && lw == 0) PA_TC_MARK(j, 10);
+            if (lane == 0 && lw == kTcKLoadWarps) PA_TC_MARK(j, 4);
         }
         if (lane == 0) {
-            if (!ok && i == 0) {
+            if (!ok && (lw == 0 || lw == kTcKLoadWarps)) {
                 *sm_abort = 1;
                 atomicOr(prm.status, PA_DEV_TIMEOUT);
             }
-            // every copy issued lands before the CTA exits: all four warps
+            // every copy issued lands before the CTA exits: the whole group
             // issued the same tiles, and a slot holds at most one copy that
             // nobody may have waited for (the latest one)
-            for (int x = max(0, k_issued - kTcKSlots); x < k_issued; ++x)
-                mbar_wait(bar(kTcBarKFull + x % kTcKSlots), (x / kTcKSlots) & 1, kDefaultWaitLimit);
-            for (int x = max(0, v_issued - kTcVSlots); x < v_issued; ++x)
-                mbar_wait(bar(kTcBarVFull + x % kTcVSlots), (x / kTcVSlots) & 1, kDefaultWaitLimit);
+            for (int x = max(0, issued - slots); x < issued; ++x)
+                mbar_wait(bar(full0 + x % slots), (x / slots) & 1, kDefaultWaitLimit);
         }
         __syncwarp();
-    } else if (warp == kTcMmaWarp) {
-        // ---------------- MMA warp: lane 0 issues, every lane waits ----------------
-        constexpr uint32_t idS = tc_idesc(kTcRows, kTcKeys, 0);
-        constexpr uint32_t idO = tc_idesc(kTcRows, D, 1);
-        const uint32_t qb = smem_addr(qs);
+    } else if (warp == kTcSWarp || warp == kTcPVWarp) {
+        // ---------------- MMA warps: lane 0 issues, every lane waits ----------------
+        // S and P.V come from two threads so that while one waits for its
+        // next inputs the other's MMAs keep the tensor cores busy (each
+        // thread's own MMAs run in issue order; the two streams only meet
+        // through the barriers below).
         const int partial_tile = C % kBlockSize != 0 ? (nctx - 1) / 4 : -1;
-        // S(j) = Q K(j)^T into score buffer j % 2; K slot j % 3 is free when it completes
-        auto issue_s = [&](int j) {
-            if (lane == 0) {
-                const uint32_t kb = smem_addr(ks + (j % kTcKSlots) * S::kTileBytes);
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t qo = (k >> 2) * (kTcRows * 128) + (k & 3) * 32;
-                    const uint32_t ko = (k >> 2) * S::kChunkStride + (k & 3) * 32;
-                    tc_mma_ss(tS0 + (j & 1) * kTcKeys, tc_desc(qb + qo, 16, 1024), tc_desc(kb + ko, 16, 1024), idS,
-                              k > 0);
-                }
-                tc_commit(bar(kTcBarSDone + (j & 1)));
-                tc_commit(bar(kTcBarKEmpty + j % kTcKSlots));
-            }
-            __syncwarp();
-        };
-        bool ok = tc_warp_wait(bar(kTcBarKFull), 0, limit, sm_abort);
-        if (ok) {
-            tc_fence_after();
-            issue_s(0);
-        }
-        for (int j = 0; ok && j < ntiles; ++j) {
-            if (lane == 0) PA_TC_MARK(j, 0);
-            if (j + 1 < ntiles) {
-                // score buffer (j+1) % 2 last held S(j-1); the rows read it
-                // before P(j-1) was ready, which the previous step waited for
-                if (!(ok = tc_warp_wait(bar(kTcBarKFull + (j + 1) % kTcKSlots), ((j + 1) / kTcKSlots) & 1, limit,
-                                        sm_abort)))
+        bool ok = true;
+        if (warp == kTcSWarp) {
+            constexpr uint32_t idS = tc_idesc(kTcRows, kTcKeys, 0);
+            const uint64_t kdesc0 = tc_desc(smem_addr(ks), 16, 1024);
+            ok = tc_warp_wait(bar(kTcBarQReady), 0, limit, sm_abort);
+            for (int j = 0; ok && j < ntiles; ++j) {
+                if (lane == 0) PA_TC_MARK(j, 0);
+                // K(j) landed; every row has read S(j-1) out of the score buffer
+                if (!(ok = tc_warp_wait(bar(kTcBarKFull + j % S::kKSlots), (j / S::kKSlots) & 1, limit, sm_abort)))
                     break;
-                if (lane == 0) PA_TC_MARK(j, 12);
+                if (lane == 0) PA_TC_MARK(j, 14);
+                if (j >= 1 && !(ok = tc_warp_wait(bar(kTcBarSFree), (j - 1) & 1, limit, sm_abort))) break;
+                if (lane == 0) PA_TC_MARK(j, 15);
                 tc_fence_after();
-                issue_s(j + 1);
-            }
-            if (lane == 0) PA_TC_MARK(j, 1);
-            // rows have written P(j) (and rescaled O if they had to)
-            if (!(ok = tc_warp_wait(bar(kTcBarPReady + (j & 1)), (j >> 1) & 1, limit, sm_abort))) break;
-            if (lane == 0) PA_TC_MARK(j, 2);
-            if (!(ok = tc_warp_wait(bar(kTcBarVFull + j % kTcVSlots), (j / kTcVSlots) & 1, limit, sm_abort))) break;
-            if (lane == 0) PA_TC_MARK(j, 3);
-            uint8_t* vt = vs + (j % kTcVSlots) * S::kTileBytes;
-            if (j == partial_tile) {
-                // V rows of cache slots past the context may hold anything: p is
-                // 0 there, but 0 * NaN is not; clear them before P.V reads them
-                const int i = (nctx - 1) % 4, first = C % kBlockSize;
-                const int units = (kBlockSize - first) * S::kChunks * 8;
-                uint8_t* vb = vt + i * S::kBlockBytes;
-                for (int x = lane; x < units; x += 32) {
-                    const int r = first + x / (S::kChunks * 8), u = x % (S::kChunks * 8);
-                    *reinterpret_cast<uint4*>(vb + (u >> 3) * (kBlockSize * 128) + r * 128 + (u & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
+                if (lane == 0) {
+                    // S(j) = Q K(j)^T into the score buffer, Q (A) from TMEM 8
+                    // columns per 16 head_dim elements; a descriptor's low field is
+                    // the start address / 16, so stepping through a buffer adds
+                    // offset / 16
+                    const uint64_t kd = kdesc0 + (uint64_t)((j % S::kKSlots) * (S::kTileBytes >> 4));
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k)
+                        tc_mma_ts(tS, tQ + k * 8, kd + (uint64_t)(((k >> 2) * S::kChunkStride + (k & 3) * 32) >> 4), idS,
+                                  k > 0);
+                    tc_commit(bar(kTcBarSDone));
+                    tc_commit(bar(kTcBarKEmpty + j % S::kKSlots));
+                    PA_TC_MARK(j, 1);
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
             }
-            tc_fence_after();
-            if (lane == 0) {
-                // O += P(j) V(j), P in buffer j % 2, one MMA per block of 16 keys
-                // (V block: 64-column chunks 2 KB apart, 8-key groups 1 KB
-                // apart); V slot j % 2 is free when they complete
-                const uint32_t vb = smem_addr(vt);
+        } else {
+            constexpr uint32_t idO = tc_idesc(kTcRows, D, 1);
+            const uint64_t vdesc0 = tc_desc(smem_addr(vs), kBlockSize * 128, 1024);
+            for (int j = 0; j < ntiles; ++j) {
+                if (lane == 0) PA_TC_MARK(j, 12);
+                // rows have written P(j) (and rescaled O if they had to); V(j) landed
+                if (!(ok = tc_warp_wait(bar(kTcBarPReady + (j & 1)), (j >> 1) & 1, limit, sm_abort))) break;
+                if (lane == 0) PA_TC_MARK(j, 2);
+                if (!(ok = tc_warp_wait(bar(kTcBarVFull + j % S::kVSlots), (j / S::kVSlots) & 1, limit, sm_abort))) break;
+                if (lane == 0) PA_TC_MARK(j, 3);
+                uint8_t* vt = vs + (j % S::kVSlots) * S::kTileBytes;
+                if (j == partial_tile) {
+                    // V rows of cache slots past the context may hold anything: p is
+                    // 0 there, but 0 * NaN is not; clear them before P.V reads them
+                    const int i = (nctx - 1) % 4, first = C % kBlockSize;
+                    const int units = (kBlockSize - first) * S::kChunks * 8;
+                    uint8_t* vb = vt + i * S::kBlockBytes;
+                    for (int x = lane; x < units; x += 32) {
+                        const int r = first + x / (S::kChunks * 8), u = x % (S::kChunks * 8);
+                        *reinterpret_cast<uint4*>(vb + (u >> 3) * (kBlockSize * 128) + r * 128 + (u & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    // O += P(j) V(j), P in buffer j % 2, one MMA per block of 16
+                    // keys (V block: 64-column chunks 2 KB apart, 8-key groups
+                    // 1 KB apart); P buffer j % 2 and V slot j % kVSlots are free
+                    // when they complete
+                    const uint64_t vd = vdesc0 + (uint64_t)((j % S::kVSlots) * (S::kTileBytes >> 4));
+                    const uint32_t a = tP0 + (j & 1) * (kTcKeys / 2);
 #pragma unroll
-                for (int k = 0; k < kTcKeys / 16; ++k)
-                    tc_mma_ts(tO, tP0 + (j & 1) * (kTcKeys / 2) + k * 8,
-                              tc_desc(vb + k * S::kBlockBytes, kBlockSize * 128, 1024), idO, (j > 0 || k > 0));
-                tc_commit(bar(kTcBarODone));
-                tc_commit(bar(kTcBarVEmpty + j % kTcVSlots));
-                PA_TC_MARK(j, 13);
+                    for (int k = 0; k < kTcKeys / 16; ++k)
+                        tc_mma_ts(tO, a + k * 8, vd + (uint64_t)((k * S::kBlockBytes) >> 4), idO, (j > 0 || k > 0));
+                    tc_commit(bar(kTcBarPVDone + (j & 1)));
+                    tc_commit(bar(kTcBarVEmpty + j % S::kVSlots));
+                    PA_TC_MARK(j, 13);
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
         if (lane == 0) {
             if (!ok) {
                 *sm_abort = 1;
                 atomicOr(prm.status, PA_DEV_TIMEOUT);
             }
-            // every MMA issued above has completed once this commit arrives
-            tc_commit(bar(kTcBarMDone));
-            mbar_wait(bar(kTcBarMDone), 0, kDefaultWaitLimit);
+            // every MMA this thread issued has completed once this commit arrives
+            const uint32_t drain = bar(warp == kTcSWarp ? kTcBarSDrain : kTcBarPVDrain);
+            tc_commit(drain);
+            mbar_wait(drain, 0, kDefaultWaitLimit);
         }
         __syncwarp();
     } else {
@@ -491,17 +510,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int my_tok = t0 + ti;  // chunk token index of the row
         const bool row_real = ti < tile_tokens && my_tok < qlen;
         const float sl2 = prm.scale_log2;
-        const uint32_t odone = bar(kTcBarODone);
+        // Q row (token my_tok, head kvh * G + t % G) into TMEM columns tQ..,
+        // two halves per column; rows that do not exist hold zeros
+        {
+            const uint4* qrow = reinterpret_cast<const uint4*>(prm.q + ((size_t)(q0 + my_tok) * H + kvh * G + t % G) * D);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D / 2; c0 += 32) {
+                uint32_t v[32];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint4 x = row_real ? __ldg(qrow + c0 / 4 + u) : make_uint4(0u, 0u, 0u, 0u);
+                    v[4 * u] = x.x;
+                    v[4 * u + 1] = x.y;
+                    v[4 * u + 2] = x.z;
+                    v[4 * u + 3] = x.w;
+                }
+                tc_st32(tQ + lane_off + c0, v);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kTcBarQReady));
+        }
         float m = -INFINITY, l = 0.f;  // reference max (scaled, log2 domain) and exp sum
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            if (!(ok = tc_warp_wait(bar(kTcBarSDone + (j & 1)), (j >> 1) & 1, limit, sm_abort))) break;
+            if (!(ok = tc_warp_wait(bar(kTcBarSDone), j & 1, limit, sm_abort))) break;
             tc_fence_after();
             if (t == 0) PA_TC_MARK(j, 5);
             uint32_t sv[2][32];
-            const uint32_t tS = tS0 + (j & 1) * kTcKeys + lane_off;
-            tc_ld32(tS, sv[0]);
-            tc_ld32(tS + 32, sv[1]);
+            tc_ld32(tS + lane_off, sv[0]);
+            tc_ld32(tS + lane_off + 32, sv[1]);
+            // S(j) is in registers: the score buffer may take S(j+1)
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kTcBarSFree));
             // visibility: every key of a tile made only of full context blocks
             // is visible; otherwise mask per key
             const bool full_ctx = 4 * j + 3 < nctx - (C % kBlockSize != 0 ? 1 : 0);
@@ -546,14 +588,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 pk[c] = half2_bits(__floats2half2_rn(p0, p1));
             }
             l = l * alpha + (rs0 + rs1);
-            // P(j) to its own buffer; P.V(j-2), its last reader, was issued
-            // before S(j) and so completed before S(j) did
+            // P(j) to its own buffer once P.V(j-2), its last reader, has
+            // completed (this warp waited for P.V(j-4) two tiles ago, so the
+            // parity wait is unambiguous)
+            if (j >= 2 && !(ok = tc_warp_wait(bar(kTcBarPVDone + (j & 1)), ((j - 2) >> 1) & 1, limit, sm_abort)))
+                break;
+            tc_fence_after();
             tc_st32(tP0 + (j & 1) * (kTcKeys / 2) + lane_off, pk);
             if (j > 0 && __any_sync(kFull, move)) {
-                // O is written by P.V(j-1): wait for it, then rescale this row.
-                // P.V(j-2) completed before S(j), so odone is at most one phase
-                // behind and the parity wait is unambiguous.
-                if (!(ok = tc_warp_wait(odone, (j - 1) & 1, limit, sm_abort))) break;
+                // O is written by P.V(j-1): wait for it, then rescale this row
+                // (P.V(j-3) was waited for one tile ago)
+                if (!(ok = tc_warp_wait(bar(kTcBarPVDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, limit, sm_abort)))
+                    break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
@@ -570,12 +616,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (t == 96) PA_TC_MARK(j, 7);
             if (lane == 0) mbar_arrive(bar(kTcBarPReady + (j & 1)));
         }
-        // odone completes once per P.V, in issue order.  S(ntiles-1) was issued
-        // before P.V(ntiles-2), so that P.V may still run here; a parity wait
-        // only tells phases apart within one of the current phase, so wait
-        // for phase ntiles-2 before phase ntiles-1.
-        if (ok && ntiles >= 2) ok = tc_warp_wait(odone, (ntiles - 2) & 1, limit, sm_abort);
-        if (ok) ok = tc_warp_wait(odone, (ntiles - 1) & 1, limit, sm_abort);
+        // the last two P.Vs (one per P buffer) complete before O is read
+        if (ok && ntiles >= 2)
+            ok = tc_warp_wait(bar(kTcBarPVDone + ((ntiles - 2) & 1)), ((ntiles - 2) >> 1) & 1, limit, sm_abort);
+        if (ok) ok = tc_warp_wait(bar(kTcBarPVDone + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, limit, sm_abort);
         if (!ok) {
             if (lane == 0) {
                 *sm_abort = 1;
