@@ -81,9 +81,14 @@ enum {
 
 /* Execution modes. */
 enum {
-    PA_MODE_AUTO = 0,   /* library picks SINGLE or SPLIT from the sizes (see pa_decode_plan) */
+    PA_MODE_AUTO = 0,   /* library picks SINGLE, SPLIT or FUSED from the sizes (see pa_decode_plan) */
     PA_MODE_SINGLE = 1, /* one CTA per (kv head, sequence) covers the whole sequence; no reduce */
-    PA_MODE_SPLIT = 2   /* partitions of partition_size tokens + log-sum-exp reduce */
+    PA_MODE_SPLIT = 2,  /* partitions of partition_size tokens + log-sum-exp reduce kernel */
+    PA_MODE_FUSED = 3   /* partitions as SPLIT, one launch: the last CTA of each (sequence, kv head)
+                           to finish (an atomic ticket; nobody waits) merges the partials in
+                           partition order.  The workspace also holds one ticket per
+                           (sequence, kv head) that must be zero before the first call on it;
+                           every call leaves the tickets zero, also after a device error */
 };
 
 /* Option flags. */
@@ -127,14 +132,14 @@ typedef struct {
 
 /* What a call will launch (filled by pa_decode_plan; host-only, no CUDA calls). */
 typedef struct {
-    int mode;              /* PA_MODE_SINGLE or PA_MODE_SPLIT */
+    int mode;              /* PA_MODE_SINGLE, PA_MODE_SPLIT or PA_MODE_FUSED */
     int partition_size;    /* tokens per CTA (SINGLE: max_seq_len rounded up to block_size) */
     int grid_x, grid_y, grid_z;          /* partition kernel: partitions, kv heads, sequences */
     int threads;           /* threads per partition CTA */
     int smem_bytes;        /* dynamic shared memory per partition CTA */
     int launch_reduce;     /* 1 if the reduce kernel runs */
     int reduce_grid_x, reduce_grid_y, reduce_grid_z; /* heads, sequences, head_dim/32 */
-    size_t workspace_bytes; /* caller workspace pa_decode_ex needs (0 when no reduce) */
+    size_t workspace_bytes; /* caller workspace pa_decode_ex needs (0 when there are no partials) */
     int stages;            /* shared-memory stages per warp of the partition CTA */
 } pa_decode_plan_t;
 
@@ -162,7 +167,8 @@ int pa_decode_ex(const pa_decode_args* args, const pa_decode_opts* opts, void* w
 int pa_decode_plan(const pa_decode_args* args, const pa_decode_opts* opts, int num_sms,
                    pa_decode_plan_t* plan);
 
-/* Workspace bytes of a SPLIT call with these sizes (an upper bound for AUTO). */
+/* Workspace bytes of a SPLIT call with these sizes.  FUSED needs 256-byte-aligned
+ * num_seqs * num_kv_heads * 4 bytes more; pa_decode_plan gives every mode's exact figure. */
 size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim,
                                 int partition_size);
 

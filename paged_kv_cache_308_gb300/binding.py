@@ -33,7 +33,8 @@ PA_DEV_TIMEOUT = 4
 PA_MODE_AUTO = 0
 PA_MODE_SINGLE = 1
 PA_MODE_SPLIT = 2
-MODES = {"auto": PA_MODE_AUTO, "single": PA_MODE_SINGLE, "split": PA_MODE_SPLIT}
+PA_MODE_FUSED = 3
+MODES = {"auto": PA_MODE_AUTO, "single": PA_MODE_SINGLE, "split": PA_MODE_SPLIT, "fused": PA_MODE_FUSED}
 
 PA_FLAG_FORCE_TIMEOUT = 1
 PA_FLAG_PREFIX_WARP_MMA = 2
@@ -218,9 +219,10 @@ def pa_decode_ex(out, q, k_cache, v_cache, block_tables, seq_lens, num_heads, nu
 
 
 def alloc_workspace(plan: dict, device) -> Optional[torch.Tensor]:
-    """A device buffer of plan['workspace_bytes'] (256-byte aligned by the caching allocator)."""
+    """A zeroed device buffer of plan['workspace_bytes'] (256-byte aligned by the
+    caching allocator); zero because the fused combine's tickets start at zero."""
     n = int(plan["workspace_bytes"])
-    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+    return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
 
 
 def pa_decode_workspace_size(num_seqs, max_seq_len, num_heads, head_dim, partition_size=0) -> int:

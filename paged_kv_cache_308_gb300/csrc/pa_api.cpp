@@ -34,6 +34,14 @@ size_t split_workspace_bytes(long long num_seqs, long long num_heads, long long 
     return align_up(rows * 4, kWsAlign) * 2 + align_up(rows * head_dim * 4, kWsAlign);
 }
 
+// The fused combine also keeps one ticket per (sequence, kv head) after the partials.
+size_t fused_workspace_bytes(long long num_seqs, long long num_heads, long long num_kv_heads,
+                             long long max_partitions, long long head_dim) {
+    if (max_partitions <= 1) return 0;
+    return split_workspace_bytes(num_seqs, num_heads, max_partitions, head_dim) +
+           align_up(static_cast<size_t>(num_seqs) * num_kv_heads * 4, kWsAlign);
+}
+
 // SM count of the current device, cached per device.
 int query_sm_count(int* num_sms) {
     static int cached[kMaxDevices];
@@ -66,7 +74,7 @@ int validate(const pa_decode_args* a, const pa_decode_opts* o) {
     if (a->num_heads % a->num_kv_heads) return PA_ERR_INVALID_ARG;
     if (!isfinite(a->scale)) return PA_ERR_INVALID_ARG;
     if (a->max_seq_len < 0 || a->max_blocks_per_seq < 0 || a->num_blocks < 0) return PA_ERR_INVALID_ARG;
-    if (o && (o->mode < PA_MODE_AUTO || o->mode > PA_MODE_SPLIT)) return PA_ERR_INVALID_ARG;
+    if (o && (o->mode < PA_MODE_AUTO || o->mode > PA_MODE_FUSED)) return PA_ERR_INVALID_ARG;
     if (o && o->partition_size < 0) return PA_ERR_INVALID_ARG;
     if (o && o->partition_size % a->block_size) return PA_ERR_INVALID_ARG;
     if (o && (o->warps < 0 || o->stages < 0)) return PA_ERR_INVALID_ARG;
@@ -156,7 +164,15 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     if (num_sms <= 0 && query_sm_count(&num_sms) != PA_OK) num_sms = 1;
     memset(plan, 0, sizeof(*plan));
     const int bs = a->block_size;
-    const int part = (o && o->partition_size > 0) ? o->partition_size : kDefaultPartition;
+    int part = (o && o->partition_size > 0) ? o->partition_size : kDefaultPartition;
+    if (!(o && o->partition_size > 0) && a->max_seq_len > kDefaultPartition) {
+        // Short work: when partitions of the default size would give fewer CTAs
+        // than SMs, halve them so that twice as many SMs stream the cache
+        // (b1_l2048: 13.7 -> 10.5 us; smaller partitions cost more in the reduce).
+        const long long ctas = (long long)((a->max_seq_len + kDefaultPartition - 1) / kDefaultPartition) *
+                               a->num_kv_heads * a->num_seqs;
+        if (ctas < num_sms) part = kDefaultPartition / 2;
+    }
     const int split_parts = (a->max_seq_len + part - 1) / part;
     int mode = o ? o->mode : PA_MODE_AUTO;
     if (mode == PA_MODE_AUTO) {
@@ -182,6 +198,9 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     plan->stages = stages;
     plan->smem_bytes = pa::partition_smem_bytes(a->head_dim, warps, stages);
     plan->launch_reduce = (mode == PA_MODE_SPLIT && plan->grid_x > 1) ? 1 : 0;
+    if (mode == PA_MODE_FUSED)
+        plan->workspace_bytes =
+            fused_workspace_bytes(a->num_seqs, a->num_heads, a->num_kv_heads, plan->grid_x, a->head_dim);
     if (plan->launch_reduce) {
         plan->reduce_grid_x = a->num_heads;
         plan->reduce_grid_y = a->num_seqs;
@@ -252,9 +271,14 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.q = static_cast<const __half*>(a->q);
     prm.block_tables = a->block_tables;
     prm.seq_lens = a->seq_lens;
-    prm.max_logits = plan.launch_reduce ? reinterpret_cast<float*>(w) : nullptr;
-    prm.exp_sums = plan.launch_reduce ? reinterpret_cast<float*>(w + align_up(rows * 4, kWsAlign)) : nullptr;
-    prm.tmp_out = plan.launch_reduce ? reinterpret_cast<float*>(w + 2 * align_up(rows * 4, kWsAlign)) : nullptr;
+    const bool fused = plan.mode == PA_MODE_FUSED && plan.grid_x > 1;
+    const bool partials = plan.launch_reduce || fused;
+    prm.max_logits = partials ? reinterpret_cast<float*>(w) : nullptr;
+    prm.exp_sums = partials ? reinterpret_cast<float*>(w + align_up(rows * 4, kWsAlign)) : nullptr;
+    prm.tmp_out = partials ? reinterpret_cast<float*>(w + 2 * align_up(rows * 4, kWsAlign)) : nullptr;
+    prm.tickets = fused ? reinterpret_cast<unsigned int*>(
+                              w + split_workspace_bytes(a->num_seqs, a->num_heads, plan.grid_x, a->head_dim))
+                        : nullptr;
     prm.num_blocks = a->num_blocks;
     prm.num_heads = a->num_heads;
     prm.num_kv_heads = a->num_kv_heads;
@@ -458,6 +482,12 @@ int ensure_workspace(size_t need, void** out) {
             cudaGetLastError();
             g_ws[dev] = nullptr;
             return PA_ERR_OOM;
+        }
+        // the fused combine's tickets must start at zero (every call leaves them so)
+        if (cudaMemset(g_ws[dev], 0, grow) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+            cudaFree(g_ws[dev]);
+            g_ws[dev] = nullptr;
+            return PA_ERR_CUDA;
         }
         g_ws_bytes[dev] = grow;
     }

@@ -34,6 +34,9 @@ struct PartitionParams {
     // Diagnostic builds (-DPA_TRACE) only: per-CTA records of
     // {sm id, entry, first block ready, main loop done, exit} in globaltimer ns.
     unsigned long long* trace;
+    // Fused combine: one ticket per (sequence, kv head), zero before the call
+    // and left zero after it; null when a separate reduce kernel merges.
+    unsigned int* tickets;
 };
 
 struct ReduceParams {

@@ -64,6 +64,66 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 }  // namespace
 
+// Single-launch merge of the partials (fused combine), run by every thread of
+// a partition CTA after warp 0 wrote its partial.  The CTA publishes the
+// partial (fence), takes a ticket for its (sequence, kv head); the CTA that
+// draws the last ticket merges the n partials of the G heads in partition
+// order -- the log-sum-exp fold of the reduce kernel, so the result does not
+// depend on which CTA finished last -- and resets the ticket for the next
+// call.  No CTA ever waits for another.  Four partitions' loads are in
+// flight per thread at a time.
+template <int D, int NW>
+__device__ __forceinline__ void fused_combine(const PartitionParams& prm, int b, int kvh, int n, int* s_last) {
+    __threadfence();
+    __syncthreads();
+    unsigned int* tk = prm.tickets + (size_t)b * prm.num_kv_heads + kvh;
+    if (threadIdx.x == 0) *s_last = atomicAdd(tk, 1u) == (unsigned)(n - 1);
+    __syncthreads();
+    if (!*s_last) return;
+    __threadfence();  // the other partials were published before their tickets
+    if (threadIdx.x == 0) atomicExch(tk, 0u);
+    const int G = prm.group;
+    const size_t head0 = (size_t)b * prm.num_heads + (size_t)kvh * G;
+    for (int task = threadIdx.x; task < G * (D / 4); task += NW * 32) {
+        const int hh = task / (D / 4), col = task % (D / 4);
+        const size_t row = (head0 + hh) * prm.max_partitions;
+        const float* ml = prm.max_logits + row;
+        const float* el = prm.exp_sums + row;
+        const float4* tp = reinterpret_cast<const float4*>(prm.tmp_out + row * D) + col;
+        float m = -INFINITY, wsum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto fold = [&](float mp, float lp, float4 t) {
+            const float mn = fmaxf(m, mp);
+            const float alpha = exp2f(m - mn);  // 0 on the first partition (m = -inf)
+            const float beta = lp * exp2f(mp - mn);
+            wsum = wsum * alpha + beta;
+            acc.x = acc.x * alpha + beta * t.x;
+            acc.y = acc.y * alpha + beta * t.y;
+            acc.z = acc.z * alpha + beta * t.z;
+            acc.w = acc.w * alpha + beta * t.w;
+            m = mn;
+        };
+        int p = 0;
+        for (; p + 4 <= n; p += 4) {
+            float mp[4], lp[4];
+            float4 t[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                mp[u] = __ldcg(ml + p + u);
+                lp[u] = __ldcg(el + p + u);
+                t[u] = __ldcg(tp + (size_t)(p + u) * (D / 4));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) fold(mp[u], lp[u], t[u]);
+        }
+        for (; p < n; ++p) fold(__ldcg(ml + p), __ldcg(el + p), __ldcg(tp + (size_t)p * (D / 4)));
+        const float inv = 1.f / wsum;
+        __half2* o = reinterpret_cast<__half2*>(prm.out + (head0 + hh) * D + 4 * col);
+        o[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+        o[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+    }
+}
+
 template <int D, int NW, int NS>
 struct PartitionShape {
     static constexpr int kSteps = D / 16;                      // k-steps of QK, m-tiles of PV
@@ -314,7 +374,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
     __syncthreads();  // all stages consumed; the stage area is reused below
     PA_TRACE_MARK(3);
-    if (*sm_abort) return;
+    if (*sm_abort) {
+        // A fused combine counts every partition's ticket, so an aborted CTA
+        // still takes its own; the last one resets the count (the output is
+        // not written and the status word already reports the failure).
+        if (prm.tickets && n_part > 1 && threadIdx.x == 0) {
+            unsigned int* tk = prm.tickets + (size_t)b * prm.num_kv_heads + kvh;
+            if (atomicAdd(tk, 1u) == (unsigned)(n_part - 1)) atomicExch(tk, 0u);
+        }
+        return;
+    }
 
     // Merge the NW partial states of this CTA by the same max/rescale
     // rule: warps 1.. leave theirs in shared memory, warp 0 folds them into its
@@ -338,8 +407,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
         }
     }
     __syncthreads();
-    if (warp != 0) return;
-
+    const bool fused = prm.tickets && n_part > 1;
+    if (warp != 0 && !fused) return;
+    if (warp == 0) {
     // Per-head factors for heads 2c and 2c + 1: M = max over warps,
     // f_w = 2^(m_w - M) / L with L = sum_w 2^(m_w - M) l_w (warps without
     // blocks have m_w = -inf and contribute nothing).
@@ -414,6 +484,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
             prm.exp_sums[pi1] = L1;
         }
     }
+    }
+    if (fused) fused_combine<D, NW>(prm, b, kvh, n_part, sm_abort + 1);  // a spare word of the control area
     PA_TRACE_MARK(4);
 }
 

@@ -39,7 +39,8 @@ def run(w, **opt):
 
 SMALL_LENS = [[1], [15], [16], [17], [511], [512], [513], [1, 16, 17, 511, 512, 513, 1029], [2048, 3, 700]]
 MODES = [dict(), dict(mode="single"), dict(mode="split", partition_size=16), dict(mode="split", partition_size=64),
-         dict(mode="split", partition_size=512), dict(mode="split", partition_size=1024)]
+         dict(mode="split", partition_size=512), dict(mode="split", partition_size=1024),
+         dict(mode="fused", partition_size=16), dict(mode="fused", partition_size=512)]
 
 
 @pytest.mark.parametrize("lens", SMALL_LENS, ids=lambda x: "L" + "-".join(map(str, x)))
@@ -53,12 +54,12 @@ def test_small_gqa6_d256(dev, lens, opt):
 
 @pytest.mark.parametrize("H,Hkv,D", [(4, 4, 64), (8, 4, 128), (16, 2, 256), (12, 4, 64), (12, 2, 128),
                                      (16, 4, 256), (5, 5, 128), (7, 1, 256)])
-@pytest.mark.parametrize("mode", ["single", "split"])
+@pytest.mark.parametrize("mode", ["single", "split", "fused"])
 def test_group_sizes_and_head_dims(dev, H, Hkv, D, mode):
     lens = [1, 37, 700, 1500, 16 * 33]
     w = W.make_workload("shape", lens, num_heads=H, num_kv_heads=Hkv, head_dim=D, num_blocks=300, seed=H * D,
                         device=dev, scale=1 / math.sqrt(D), tail_fill=float("inf"))
-    out = run(w, mode=mode, partition_size=256 if mode == "split" else 0)
+    out = run(w, mode=mode, partition_size=0 if mode == "single" else 256)
     assert_parity(out, oracle_ref(w), f"H={H} Hkv={Hkv} D={D} {mode}")
 
 
@@ -68,8 +69,11 @@ def test_group_sizes_and_head_dims(dev, H, Hkv, D, mode):
     ("b8_u8192", dict(mode="single")),
     ("b8_u8192", dict(mode="split")),
     ("b8_u8192", dict()),
+    ("b8_u8192", dict(mode="fused")),
+    ("b1_l2048", dict(mode="fused", partition_size=128)),
     ("b4_l32768_peaked", dict()),
     ("b1_l102400", dict()),
+    ("b1_l102400", dict(mode="fused")),
 ])
 def test_named_workload_full(dev, name, opt):
     w = W.make_config(name, device=dev)
@@ -219,8 +223,8 @@ def test_bad_seq_len_sets_device_status(dev):
 def test_forced_timeout_returns_status_and_context_survives(dev):
     w = W.make_workload("timeout", [3000, 64], num_blocks=200, seed=13, device=dev)
     pb.pa_get_device_status()
-    for mode in ("single", "split"):
-        pb.decode_workload(w, mode=mode, partition_size=512 if mode == "split" else 0,
+    for mode in ("single", "split", "fused"):
+        pb.decode_workload(w, mode=mode, partition_size=0 if mode == "single" else 512,
                            flags=pb.PA_FLAG_FORCE_TIMEOUT)
         assert pb.pa_get_device_status() & pb.PA_DEV_TIMEOUT
     # the context is still healthy: a normal call afterwards is correct
@@ -248,3 +252,70 @@ def test_every_cta_shape(dev, warps, stages, mode):
     # the result does not depend on the CTA shape beyond rounding order
     ref = run(w, mode=mode, partition_size=256 if mode == "split" else 0, warps=2, stages=2)
     assert (out.float() - ref.float()).abs().max().item() < 2e-3
+
+
+def _fused_call(w, out, ws, stream=None, **extra):
+    pb.pa_decode_ex(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
+                    w.head_dim, w.block_size, w.scale, stream, max_seq_len=w.max_seq_len, mode="fused",
+                    partition_size=128, workspace=ws, **extra)
+
+
+def _tickets(w, ws, plan_split_bytes):
+    return ws[plan_split_bytes:plan_split_bytes + 4 * len(w.seq_lens_host) * w.num_kv_heads]
+
+
+def test_fused_combine_is_deterministic_and_leaves_tickets_zero(dev):
+    w = W.make_workload("fused", [3000, 17, 1029, 513, 128, 1], num_blocks=400, seed=15, device=dev,
+                        tail_fill=float("nan"))
+    out = torch.empty_like(w.q)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len,
+                             mode="fused", partition_size=128)
+    split = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                              w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len,
+                              mode="split", partition_size=128)
+    assert plan["launch_reduce"] == 0 and plan["workspace_bytes"] > split["workspace_bytes"]
+    ws = pb.alloc_workspace(plan, dev)
+    outs = []
+    for _ in range(4):
+        _fused_call(w, out, ws)
+        torch.cuda.synchronize()
+        assert pb.pa_get_device_status() == 0
+        assert torch.count_nonzero(_tickets(w, ws, split["workspace_bytes"])) == 0
+        outs.append(out.clone())
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    assert_parity(outs[0], oracle_ref(w), "fused")
+    # the same merge order as the separate reduce up to rounding
+    ref = run(w, mode="split", partition_size=128)
+    assert (outs[0].float() - ref.float()).abs().max().item() < 2e-3
+
+
+def test_fused_combine_after_forced_timeout_and_in_a_graph(dev):
+    w = W.make_workload("fusedg", [4000, 100, 2500], num_blocks=500, seed=16, device=dev)
+    out = torch.empty_like(w.q)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len,
+                             mode="fused", partition_size=128)
+    ws = pb.alloc_workspace(plan, dev)
+    pb.pa_get_device_status()
+    _fused_call(w, out, ws, flags=pb.PA_FLAG_FORCE_TIMEOUT)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() & pb.PA_DEV_TIMEOUT
+    # the tickets stayed consistent: the next call on the same workspace is right
+    _fused_call(w, out, ws)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    eager = out.clone()
+    assert_parity(eager, oracle_ref(w), "fused after timeout")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _fused_call(w, out, ws, stream=torch.cuda.current_stream())
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    assert torch.equal(out, eager)

@@ -75,6 +75,36 @@ def test_plan_modes():
     assert rc == 0
 
 
+def test_plan_halves_the_partition_when_the_grid_is_smaller_than_the_gpu():
+    o = pb.pa_decode_opts(0, 0, 0, 0, None, None)
+    pl = pb.pa_decode_plan_t()
+    # one 2048-token sequence: 4 partitions x 4 kv heads = 16 CTAs < 152 SMs
+    assert pb.lib.pa_decode_plan(ctypes.byref(args(max_seq_len=2048, num_blocks=128)), ctypes.byref(o), 152,
+                                 ctypes.byref(pl)) == 0
+    assert pl.partition_size == 256 and pl.grid_x == 8
+    # 64 of them give 1024 CTAs at the default size, which stays
+    a = args(num_seqs=64, max_seq_len=2048, num_blocks=64 * 128)
+    assert pb.lib.pa_decode_plan(ctypes.byref(a), ctypes.byref(o), 152, ctypes.byref(pl)) == 0
+    assert pl.partition_size == 512
+    # an explicit partition size is kept
+    o2 = pb.pa_decode_opts(0, 1024, 0, 0, None, None)
+    assert pb.lib.pa_decode_plan(ctypes.byref(args(max_seq_len=2048, num_blocks=128)), ctypes.byref(o2), 152,
+                                 ctypes.byref(pl)) == 0
+    assert pl.partition_size == 1024
+
+
+def test_plan_fused_mode_keeps_partials_and_tickets_and_launches_once():
+    a = args(max_seq_len=102400)
+    rc, fused = plan(a, mode=pb.PA_MODE_FUSED)
+    _, split = plan(a, mode=pb.PA_MODE_SPLIT)
+    assert rc == 0 and fused["mode"] == pb.PA_MODE_FUSED and fused["launch_reduce"] == 0
+    assert fused["grid_x"] == split["grid_x"] == 200 and fused["partition_size"] == 512
+    # the split partials plus one 4-byte ticket per (sequence, kv head), 256-byte aligned
+    assert fused["workspace_bytes"] == split["workspace_bytes"] + 256
+    rc, one = plan(args(max_seq_len=512, num_blocks=128), mode=pb.PA_MODE_FUSED)
+    assert rc == 0 and one["grid_x"] == 1 and one["workspace_bytes"] == 0   # one partition: written directly
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), pb.PA_ERR_INVALID_ARG),
     (dict(out=FAKE + 2), pb.PA_ERR_INVALID_ARG),
