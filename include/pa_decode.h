@@ -84,11 +84,18 @@ enum {
     PA_MODE_AUTO = 0,   /* library picks SINGLE, SPLIT or FUSED from the sizes (see pa_decode_plan) */
     PA_MODE_SINGLE = 1, /* one CTA per (kv head, sequence) covers the whole sequence; no reduce */
     PA_MODE_SPLIT = 2,  /* partitions of partition_size tokens + log-sum-exp reduce kernel */
-    PA_MODE_FUSED = 3   /* partitions as SPLIT, one launch: the last CTA of each (sequence, kv head)
+    PA_MODE_FUSED = 3,  /* partitions as SPLIT, one launch: the last CTA of each (sequence, kv head)
                            to finish (an atomic ticket; nobody waits) merges the partials in
                            partition order.  The workspace also holds one ticket per
                            (sequence, kv head) that must be zero before the first call on it;
                            every call leaves the tickets zero, also after a device error */
+    PA_MODE_PERSISTENT = 4 /* a fixed grid of (SMs x CTAs per SM) walks a work list that a small
+                              kernel builds on the device (a prefix sum of (partition, kv head)
+                              items per sequence); each sequence gets its own partition size, the
+                              fewest partitions of at most partition_size tokens evened out to
+                              whole blocks; then the log-sum-exp reduce.  The host never reads
+                              the lengths, so the call is graph-safe.  The workspace also holds
+                              the work list (num_seqs + 1 ints) */
 };
 
 /* Option flags. */
@@ -132,15 +139,17 @@ typedef struct {
 
 /* What a call will launch (filled by pa_decode_plan; host-only, no CUDA calls). */
 typedef struct {
-    int mode;              /* PA_MODE_SINGLE, PA_MODE_SPLIT or PA_MODE_FUSED */
+    int mode;              /* PA_MODE_SINGLE, PA_MODE_SPLIT, PA_MODE_FUSED or PA_MODE_PERSISTENT */
     int partition_size;    /* tokens per CTA (SINGLE: max_seq_len rounded up to block_size) */
-    int grid_x, grid_y, grid_z;          /* partition kernel: partitions, kv heads, sequences */
+    int grid_x, grid_y, grid_z;          /* partition kernel: partitions, kv heads, sequences
+                                            (PERSISTENT: the fixed grid, 1, 1) */
     int threads;           /* threads per partition CTA */
     int smem_bytes;        /* dynamic shared memory per partition CTA */
     int launch_reduce;     /* 1 if the reduce kernel runs */
     int reduce_grid_x, reduce_grid_y, reduce_grid_z; /* heads, sequences, head_dim/32 */
     size_t workspace_bytes; /* caller workspace pa_decode_ex needs (0 when there are no partials) */
     int stages;            /* shared-memory stages per warp of the partition CTA */
+    int max_partitions;    /* partials kept per (sequence, head) in the workspace */
 } pa_decode_plan_t;
 
 /* Decode attention with a library-owned workspace.

@@ -34,7 +34,9 @@ PA_MODE_AUTO = 0
 PA_MODE_SINGLE = 1
 PA_MODE_SPLIT = 2
 PA_MODE_FUSED = 3
-MODES = {"auto": PA_MODE_AUTO, "single": PA_MODE_SINGLE, "split": PA_MODE_SPLIT, "fused": PA_MODE_FUSED}
+PA_MODE_PERSISTENT = 4
+MODES = {"auto": PA_MODE_AUTO, "single": PA_MODE_SINGLE, "split": PA_MODE_SPLIT, "fused": PA_MODE_FUSED,
+         "persistent": PA_MODE_PERSISTENT}
 
 PA_FLAG_FORCE_TIMEOUT = 1
 PA_FLAG_PREFIX_WARP_MMA = 2
@@ -64,7 +66,7 @@ class pa_decode_plan_t(ctypes.Structure):
         ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int), ("threads", ctypes.c_int),
         ("smem_bytes", ctypes.c_int), ("launch_reduce", ctypes.c_int), ("reduce_grid_x", ctypes.c_int),
         ("reduce_grid_y", ctypes.c_int), ("reduce_grid_z", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
-        ("stages", ctypes.c_int),
+        ("stages", ctypes.c_int), ("max_partitions", ctypes.c_int),
     ]
 
     def as_dict(self):

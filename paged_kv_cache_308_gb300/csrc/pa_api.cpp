@@ -74,13 +74,18 @@ int validate(const pa_decode_args* a, const pa_decode_opts* o) {
     if (a->num_heads % a->num_kv_heads) return PA_ERR_INVALID_ARG;
     if (!isfinite(a->scale)) return PA_ERR_INVALID_ARG;
     if (a->max_seq_len < 0 || a->max_blocks_per_seq < 0 || a->num_blocks < 0) return PA_ERR_INVALID_ARG;
-    if (o && (o->mode < PA_MODE_AUTO || o->mode > PA_MODE_FUSED)) return PA_ERR_INVALID_ARG;
+    if (o && (o->mode < PA_MODE_AUTO || o->mode > PA_MODE_PERSISTENT)) return PA_ERR_INVALID_ARG;
     if (o && o->partition_size < 0) return PA_ERR_INVALID_ARG;
     if (o && o->partition_size % a->block_size) return PA_ERR_INVALID_ARG;
     if (o && (o->warps < 0 || o->stages < 0)) return PA_ERR_INVALID_ARG;
-    // every head_dim is compiled with the same set of CTA shapes
-    if (o && (o->warps || o->stages) && pa::partition_smem_bytes(256, o->warps, o->stages) < 0)
+    // every head_dim is compiled with the same set of CTA shapes; the
+    // persistent kernel with one warp and 2 or 3 stages
+    if (o && o->mode == PA_MODE_PERSISTENT) {
+        if ((o->warps && o->warps != 1) || (o->stages && pa::persistent_smem_bytes(256, o->stages) < 0))
+            return PA_ERR_UNSUPPORTED;
+    } else if (o && (o->warps || o->stages) && pa::partition_smem_bytes(256, o->warps, o->stages) < 0) {
         return PA_ERR_UNSUPPORTED;
+    }
     if (a->head_dim != 64 && a->head_dim != 128 && a->head_dim != 256) return PA_ERR_UNSUPPORTED;
     if (a->block_size != pa::kBlockSize) return PA_ERR_UNSUPPORTED;
     if (a->num_heads / a->num_kv_heads > pa::kMaxGroup) return PA_ERR_UNSUPPORTED;
@@ -190,14 +195,33 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         plan->partition_size = part;
         plan->grid_x = split_parts > 0 ? split_parts : 1;
     }
+    plan->max_partitions = plan->grid_x;
     plan->grid_y = a->num_kv_heads;
     plan->grid_z = a->num_seqs;
     int warps = o ? o->warps : 0, stages = o ? o->stages : 0;
-    if (!warps) choose_shape(a, plan, num_sms, &warps, &stages);
+    if (mode == PA_MODE_PERSISTENT) {
+        // one warp per CTA, the finest unit of work: 6 CTAs per SM at
+        // head_dim 256 with 2 stages
+        warps = 1;
+        if (!stages) stages = 2;
+    } else if (!warps) {
+        choose_shape(a, plan, num_sms, &warps, &stages);
+    }
     plan->threads = warps * 32;
     plan->stages = stages;
-    plan->smem_bytes = pa::partition_smem_bytes(a->head_dim, warps, stages);
-    plan->launch_reduce = (mode == PA_MODE_SPLIT && plan->grid_x > 1) ? 1 : 0;
+    plan->smem_bytes = mode == PA_MODE_PERSISTENT ? pa::persistent_smem_bytes(a->head_dim, stages)
+                                                  : pa::partition_smem_bytes(a->head_dim, warps, stages);
+    if (mode == PA_MODE_PERSISTENT) {
+        // a fixed grid of every CTA the SMs hold at once
+        long long per_sm = kSmemPerSm / (plan->smem_bytes + 1024);
+        if (per_sm > 2048 / plan->threads) per_sm = 2048 / plan->threads;
+        if (per_sm > 32) per_sm = 32;
+        if (per_sm < 1) per_sm = 1;
+        plan->grid_x = (int)(per_sm * num_sms);
+        plan->grid_y = plan->grid_z = 1;
+    }
+    plan->launch_reduce =
+        ((mode == PA_MODE_SPLIT || mode == PA_MODE_PERSISTENT) && plan->max_partitions > 1) ? 1 : 0;
     if (mode == PA_MODE_FUSED)
         plan->workspace_bytes =
             fused_workspace_bytes(a->num_seqs, a->num_heads, a->num_kv_heads, plan->grid_x, a->head_dim);
@@ -205,8 +229,11 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         plan->reduce_grid_x = a->num_heads;
         plan->reduce_grid_y = a->num_seqs;
         plan->reduce_grid_z = a->head_dim / reduce_slice(a->head_dim, (long long)a->num_seqs * a->num_heads, num_sms);
-        plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->grid_x, a->head_dim);
+        plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim);
     }
+    if (mode == PA_MODE_PERSISTENT)  // + the work list
+        plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim) +
+                                align_up(static_cast<size_t>(a->num_seqs + 1) * 4, kWsAlign);
     return PA_OK;
 }
 
@@ -247,6 +274,8 @@ int make_cache_map(CUtensorMap* map, const void* base, const pa_decode_args* a) 
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+int make_cache_block_map(CUtensorMap* map, const void* base, long long num_blocks, int num_kv_heads, int head_dim);
+
 // Diagnostic builds (-DPA_TRACE): device buffer for per-CTA timestamps of
 // the partition kernel (5 x 8 bytes per CTA) or of the tcgen05 prefix kernel
 // (kPrefixTraceIters x 16 x 8 bytes per CTA), set by pa_debug_set_trace.
@@ -259,12 +288,12 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
         return PA_ERR_WORKSPACE;
 
     CUtensorMap tk, tv;
-    int rc = make_cache_map(&tk, a->k_cache, a);
+    int rc = make_cache_block_map(&tk, a->k_cache, a->num_blocks, a->num_kv_heads, a->head_dim);
     if (rc) return rc;
-    rc = make_cache_map(&tv, a->v_cache, a);
+    rc = make_cache_block_map(&tv, a->v_cache, a->num_blocks, a->num_kv_heads, a->head_dim);
     if (rc) return rc;
 
-    const size_t rows = static_cast<size_t>(a->num_seqs) * a->num_heads * plan.grid_x;
+    const size_t rows = static_cast<size_t>(a->num_seqs) * a->num_heads * plan.max_partitions;
     uint8_t* w = static_cast<uint8_t*>(ws);
     pa::PartitionParams prm;
     prm.out = static_cast<__half*>(a->out);
@@ -272,13 +301,15 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.block_tables = a->block_tables;
     prm.seq_lens = a->seq_lens;
     const bool fused = plan.mode == PA_MODE_FUSED && plan.grid_x > 1;
+    const bool persistent = plan.mode == PA_MODE_PERSISTENT;
     const bool partials = plan.launch_reduce || fused;
+    const size_t partial_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan.max_partitions, a->head_dim);
     prm.max_logits = partials ? reinterpret_cast<float*>(w) : nullptr;
     prm.exp_sums = partials ? reinterpret_cast<float*>(w + align_up(rows * 4, kWsAlign)) : nullptr;
     prm.tmp_out = partials ? reinterpret_cast<float*>(w + 2 * align_up(rows * 4, kWsAlign)) : nullptr;
-    prm.tickets = fused ? reinterpret_cast<unsigned int*>(
-                              w + split_workspace_bytes(a->num_seqs, a->num_heads, plan.grid_x, a->head_dim))
-                        : nullptr;
+    prm.tickets = fused ? reinterpret_cast<unsigned int*>(w + partial_bytes) : nullptr;
+    prm.work_offsets = persistent ? reinterpret_cast<const int*>(w + partial_bytes) : nullptr;
+    prm.num_seqs = a->num_seqs;
     prm.num_blocks = a->num_blocks;
     prm.num_heads = a->num_heads;
     prm.num_kv_heads = a->num_kv_heads;
@@ -286,19 +317,31 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.max_blocks_per_seq = a->max_blocks_per_seq;
     prm.max_seq_len = a->max_seq_len;
     prm.partition_size = plan.partition_size;
-    prm.max_partitions = plan.grid_x;
+    prm.max_partitions = plan.max_partitions;
     prm.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
     prm.wait_limit = (o && o->wait_limit) ? o->wait_limit : pa::kDefaultWaitLimit;
     prm.force_timeout = (o && (o->flags & PA_FLAG_FORCE_TIMEOUT)) ? 1 : 0;
     prm.trace = g_trace;
 
+    if (persistent) {
+        pa::ScanParams sp;
+        sp.seq_lens = a->seq_lens;
+        sp.work_offsets = reinterpret_cast<int*>(w + partial_bytes);
+        sp.num_seqs = a->num_seqs;
+        sp.max_seq_len = a->max_seq_len;
+        sp.max_blocks_per_seq = a->max_blocks_per_seq;
+        sp.partition_size = plan.partition_size;
+        sp.num_kv_heads = a->num_kv_heads;
+        if (pa::launch_work_scan(sp, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
     if (o && o->event_partition_begin &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_begin), stream) != cudaSuccess)
         return PA_ERR_CUDA;
-    if (pa::launch_partition(a->head_dim, plan.threads / 32, plan.stages, prm, tk, tv,
-                             dim3(plan.grid_x, plan.grid_y, plan.grid_z), stream) !=
-        cudaSuccess)
-        return PA_ERR_CUDA;
+    const cudaError_t le =
+        persistent ? pa::launch_partition_persistent(a->head_dim, plan.stages, prm, tk, tv, plan.grid_x, stream)
+                   : pa::launch_partition(a->head_dim, plan.threads / 32, plan.stages, prm, tk, tv,
+                                          dim3(plan.grid_x, plan.grid_y, plan.grid_z), stream);
+    if (le != cudaSuccess) return PA_ERR_CUDA;
     if (o && o->event_partition_end &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_end), stream) != cudaSuccess)
         return PA_ERR_CUDA;
@@ -313,7 +356,8 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
         rp.max_blocks_per_seq = a->max_blocks_per_seq;
         rp.max_seq_len = a->max_seq_len;
         rp.partition_size = plan.partition_size;
-        rp.max_partitions = plan.grid_x;
+        rp.max_partitions = plan.max_partitions;
+        rp.balanced = persistent ? 1 : 0;
         if (pa::launch_reduce(a->head_dim, a->head_dim / plan.reduce_grid_z, rp,
                               dim3(plan.reduce_grid_x, plan.reduce_grid_y, plan.reduce_grid_z), stream) != cudaSuccess)
             return PA_ERR_CUDA;
@@ -337,10 +381,13 @@ int make_new_kv_map(CUtensorMap* map, const void* base, int num_tokens, int num_
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
-// Whole-block views for the tcgen05 prefix kernel's V copies: one box brings
-// a block's 16 rows x head_dim as [64-column chunk][16 rows][128 B] (each chunk
-// with the 128-byte swizzle), the layout its P.V MMA reads.  Cache: dims
-// (64 halves, rows, chunk), the chunk dimension stepping 128 B through a row.
+// Whole-block views: one box brings a block's 16 rows x head_dim as
+// [64-column chunk][16 rows][128 B] (each chunk with the 128-byte swizzle),
+// the stage layout of the decode kernels and of the tcgen05 prefix kernel's
+// P.V operand.  A TMA instruction holds its issuing thread for a fixed time
+// whatever the box size, so one box per tile instead of one per 64-column
+// chunk cuts that time by D / 64.  Cache: dims (64 halves, rows, chunk), the
+// chunk dimension stepping 128 B through a row.
 int make_cache_block_map(CUtensorMap* map, const void* base, long long num_blocks, int num_kv_heads, int head_dim) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PA_ERR_CUDA;

@@ -16,6 +16,27 @@ constexpr int kReduceThreads = 256;
 constexpr int kReduceMinSlice = 32;  // narrowest head_dim slice of a reduce CTA
 constexpr unsigned kDefaultWaitLimit = 1u << 20;
 
+// Partition size of a sequence of L tokens in the persistent schedule: the
+// fewest partitions of at most `pmax` tokens, evened out and rounded up to
+// whole blocks (so every partition is non-empty).  Host and device use the
+// same rule; the partition count is (L + size - 1) / size.
+__host__ __device__ inline int balanced_partition(int L, int pmax) {
+    if (L <= 0) return pmax;
+    const int n = (L + pmax - 1) / pmax;
+    const int even = (L + n - 1) / n;
+    return ((even + kBlockSize - 1) / kBlockSize) * kBlockSize;
+}
+
+// Work items of one sequence in the persistent schedule: an invalid length
+// gets one (to report it), an empty sequence one per kv head (to zero its
+// output), otherwise one per (partition, kv head).
+__host__ __device__ inline int work_items(int L, int max_seq_len, int max_blocks_per_seq, int pmax, int num_kv_heads) {
+    if (L < 0 || L > max_seq_len || L > max_blocks_per_seq * kBlockSize) return 1;
+    if (L == 0) return num_kv_heads;
+    const int part = balanced_partition(L, pmax);
+    return ((L + part - 1) / part) * num_kv_heads;
+}
+
 struct PartitionParams {
     __half* out;
     const __half* q;
@@ -37,6 +58,10 @@ struct PartitionParams {
     // Fused combine: one ticket per (sequence, kv head), zero before the call
     // and left zero after it; null when a separate reduce kernel merges.
     unsigned int* tickets;
+    // Persistent schedule: exclusive prefix sums of work_items over the
+    // sequences (num_seqs + 1 entries); null for one CTA per grid cell.
+    const int* work_offsets;
+    int num_seqs;
 };
 
 struct ReduceParams {
@@ -47,6 +72,13 @@ struct ReduceParams {
     const int32_t* seq_lens;
     int num_heads, max_blocks_per_seq, max_seq_len;
     int partition_size, max_partitions;
+    int balanced;  // per-sequence partition sizes of the persistent schedule
+};
+
+struct ScanParams {
+    const int32_t* seq_lens;
+    int* work_offsets;  // [num_seqs + 1]
+    int num_seqs, max_seq_len, max_blocks_per_seq, partition_size, num_kv_heads;
 };
 
 // Dynamic shared memory of a partition CTA of `warps` warps with `stages`
@@ -62,6 +94,16 @@ cudaError_t launch_partition(int head_dim, int warps, int stages, const Partitio
 // dependency before it reads any memory.  `width` is the head_dim slice of a
 // reduce CTA (32, 64, 128 or 256, at most head_dim).
 cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3 grid, cudaStream_t stream);
+
+// The persistent schedule's work list: one CTA scans the sequences' item counts.
+cudaError_t launch_work_scan(const ScanParams& prm, cudaStream_t stream);
+
+// Persistent schedule: `grid` one-warp CTAs walk the work list in
+// prm.work_offsets (stages 2 or 3); persistent_smem_bytes is the dynamic
+// shared memory of one such CTA (-1 for a shape that is not compiled).
+int persistent_smem_bytes(int head_dim, int stages);
+cudaError_t launch_partition_persistent(int head_dim, int stages, const PartitionParams& prm, const CUtensorMap& tk,
+                                        const CUtensorMap& tv, int grid, cudaStream_t stream);
 
 // Read and clear the status word of the current device (synchronises stream).
 cudaError_t read_and_clear_status(cudaStream_t stream, int* status);

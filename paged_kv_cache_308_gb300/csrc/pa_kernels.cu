@@ -6,14 +6,18 @@
 //   all query heads of the GQA group.  It writes the compound partial
 //   (max score, exp sum, normalised weighted V) of the "docs" commit page, or
 //   the final output when the sequence has a single partition.
+// pa_partition_persistent_kernel -- the same partition work over a fixed grid
+//   of one-warp CTAs that walk a device-built work list (PA_MODE_PERSISTENT).
 // pa_reduce_kernel -- Phase 2 of the same page: merges the partials of each
 //   (sequence, head) with a log-sum-exp reduce.
 //
 // Hardware mapping (written for sm_103a, not translated from the pages' Triton):
 // * Cache layout [block][kv_head][16 tokens][D]: one (block, kv head) is 16
-//   rows of D halves.  A 2-D tensor map views a cache as rows x D; each block
-//   arrives as D/64 TMA boxes of 16 rows x 64 halves (128 B) with the 128-byte
-//   swizzle, so the ldmatrix reads below hit 8 distinct bank groups.
+//   rows of D halves.  A 3-D tensor map views a cache as (64-half column,
+//   row, 64-column chunk); each K or V tile of a block arrives as ONE TMA box
+//   laid out [chunk][16 rows][128 B] with the 128-byte swizzle, so the
+//   ldmatrix reads below hit 8 distinct bank groups (a TMA instruction holds
+//   its issuing thread for a fixed time, so one box per tile, not per chunk).
 // * Each of the NW warps of a CTA owns NS shared-memory stages (K and V of one
 //   block each), an mbarrier per stage, and a private online-softmax state;
 //   blocks of the partition are dealt round-robin to the warps.  Several CTA
@@ -140,6 +144,90 @@ struct PartitionShape {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
 };
 
+// One 16-token block of a warp's online softmax, in the swapped MMA form:
+// S^T = K . Q^T, the running-max update with rescale alpha = 2^(m_old - m_new),
+// P^T by movmatrix, then O^T += V^T . P^T.  `kst`/`vst` are the block's K and
+// V stages (shared-memory addresses, 64-column boxes with the 128-byte
+// swizzle), `vgen` the V stage as a generic pointer: rows from `nvalid` on are
+// cleared there before P.V reads them.  Lane (g, c) holds heads 2c, 2c + 1.
+template <int D>
+__device__ __forceinline__ void warp_block_update(const uint32_t (&qb)[D / 16][2], float (&o)[D / 16][4], float& m0,
+                                                  float& m1, float& l0, float& l1, uint32_t kst, uint32_t vst,
+                                                  uint8_t* vgen, int nvalid, float sl2) {
+    constexpr int kSteps = D / 16, kChunks = D / 64, kBoxBytes = kBlockSize * 128;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;
+    const int mi = lane >> 3, r8 = lane & 7;
+    const int rq = r8 + ((mi & 1) << 3);   // ldmatrix row (token) for K . Q^T
+    const int rv = r8 + ((mi >> 1) << 3);  // ldmatrix row (token) for V^T . P^T
+
+    // S^T = K . Q^T  (two accumulators for instruction-level parallelism)
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < kSteps; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(a, kst + (ks >> 2) * kBoxBytes + swz(rq, ((ks & 3) << 1) + (mi >> 1)));
+        if (ks & 1)
+            mma_16816(sb, a, qb[ks][0], qb[ks][1]);
+        else
+            mma_16816(sa, a, qb[ks][0], qb[ks][1]);
+    }
+    // lane holds tokens g (s0, s1) and g + 8 (s2, s3) of heads 2c, 2c + 1
+    float s0 = (sa[0] + sb[0]) * sl2, s1 = (sa[1] + sb[1]) * sl2;
+    float s2 = (sa[2] + sb[2]) * sl2, s3 = (sa[3] + sb[3]) * sl2;
+    if (g >= nvalid) s0 = s1 = -INFINITY;  // tokens past the end are excluded
+    if (g + 8 >= nvalid) s2 = s3 = -INFINITY;
+
+    float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+    }
+    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    const __half2 p01 = __floats2half2_rn(exp2f(s0 - mn0), exp2f(s1 - mn1));
+    const __half2 p23 = __floats2half2_rn(exp2f(s2 - mn0), exp2f(s3 - mn1));
+    // the exp sums use the rounded probabilities that enter P.V
+    const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
+    l0 = l0 * al0 + (f01.x + f23.x);
+    l1 = l1 * al1 + (f01.y + f23.y);
+    if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < kSteps; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+    }
+    const uint32_t pb0 = movmatrix_trans(half2_bits(p01));  // P^T rows: heads; cols: tokens 0..7
+    const uint32_t pb1 = movmatrix_trans(half2_bits(p23));  // tokens 8..15
+
+    if (nvalid < kBlockSize) {
+        // Slots past the end may hold anything (even NaN); 0 * NaN would
+        // poison P.V, so clear those V rows before the MMA reads them.
+        const int units = (kBlockSize - nvalid) * kChunks * 8;
+        for (int u = lane; u < units; u += 32) {
+            const int r = nvalid + u / (kChunks * 8), rem = u % (kChunks * 8);
+            *reinterpret_cast<uint4*>(vgen + (rem >> 3) * kBoxBytes + r * 128 + (rem & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+    }
+
+    // O^T += V^T . P^T
+#pragma unroll
+    for (int mt = 0; mt < kSteps; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_trans(a, vst + (mt >> 2) * kBoxBytes + swz(rv, ((mt & 3) << 1) + (mi & 1)));
+        mma_16816(o[mt], a, pb0, pb1);
+    }
+}
+
 template <int D, int NW, int NS>
 __global__ void __launch_bounds__(NW * 32, 1)
     pa_partition_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -233,11 +321,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 mbar_arrive_expect_tx(bar, S::kStageBytes);
                 const int row = (phys * prm.num_kv_heads + kvh) * kBlockSize;
                 const uint32_t kdst = stage0 + s * S::kStageBytes, vdst = kdst + S::kTileBytes;
-#pragma unroll
-                for (int ch = 0; ch < S::kChunks; ++ch) {
-                    tma_load_2d(kdst + ch * S::kBoxBytes, &tmap_k, ch * 64, row, bar);
-                    tma_load_2d(vdst + ch * S::kBoxBytes, &tmap_v, ch * 64, row, bar);
-                }
+                // one box per tile: all D / 64 column chunks of the 16 rows
+                tma_load_3d(kdst, &tmap_k, 0, row, 0, bar);
+                tma_load_3d(vdst, &tmap_v, 0, row, 0, bar);
             } else {
                 atomicOr(&g_status, PA_DEV_BAD_BLOCK_ID);
                 mbar_arrive(bar);  // complete the phase so the wait below stays in step
@@ -267,9 +353,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
     float l0 = 0.f, l1 = 0.f;              // this lane's share of the exp sums
 
     const float sl2 = prm.scale_log2;
-    const int mi = lane >> 3, r8 = lane & 7;
-    const int rq = r8 + ((mi & 1) << 3);  // ldmatrix row (token) for K . Q^T
-    const int rv = r8 + ((mi >> 1) << 3);  // ldmatrix row (token) for V^T . P^T
     int i = 0;
     bool timed_out = false;
     for (; i < nmine; ++i) {
@@ -282,75 +365,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
         if (i == 0) PA_TRACE_MARK(2);
         if ((valid_bits >> s) & 1u) {
             const int tok0 = (blk0 + warp + i * NW) * kBlockSize;
-            const int nvalid = min(kBlockSize, L - tok0);
-            const uint32_t kst = stage0 + s * S::kStageBytes, vst = kst + S::kTileBytes;
-
-            // S^T = K . Q^T  (two accumulators for instruction-level parallelism)
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < S::kSteps; ++ks) {
-                uint32_t a[4];
-                ldsm_x4(a, kst + (ks >> 2) * S::kBoxBytes + swz(rq, ((ks & 3) << 1) + (mi >> 1)));
-                if (ks & 1)
-                    mma_16816(sb, a, qb[ks][0], qb[ks][1]);
-                else
-                    mma_16816(sa, a, qb[ks][0], qb[ks][1]);
-            }
-            // lane holds tokens g (s0, s1) and g + 8 (s2, s3) of heads 2c, 2c + 1
-            float s0 = (sa[0] + sb[0]) * sl2, s1 = (sa[1] + sb[1]) * sl2;
-            float s2 = (sa[2] + sb[2]) * sl2, s3 = (sa[3] + sb[3]) * sl2;
-            if (g >= nvalid) s0 = s1 = -INFINITY;      // tokens past the end are excluded
-            if (g + 8 >= nvalid) s2 = s3 = -INFINITY;
-
-            float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
-                bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
-            }
-            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-            const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            const __half2 p01 = __floats2half2_rn(exp2f(s0 - mn0), exp2f(s1 - mn1));
-            const __half2 p23 = __floats2half2_rn(exp2f(s2 - mn0), exp2f(s3 - mn1));
-            // the exp sums use the rounded probabilities that enter P.V
-            const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
-            l0 = l0 * al0 + (f01.x + f23.x);
-            l1 = l1 * al1 + (f01.y + f23.y);
-            if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-                for (int mt = 0; mt < S::kSteps; ++mt) {
-                    o[mt][0] *= al0;
-                    o[mt][1] *= al1;
-                    o[mt][2] *= al0;
-                    o[mt][3] *= al1;
-                }
-            }
-            const uint32_t pb0 = movmatrix_trans(half2_bits(p01));  // P^T rows: heads; cols: tokens 0..7
-            const uint32_t pb1 = movmatrix_trans(half2_bits(p23));  // tokens 8..15
-
-            if (nvalid < kBlockSize) {
-                // Slots past the end may hold anything (even NaN); 0 * NaN would
-                // poison P.V, so clear those V rows before the MMA reads them.
-                uint8_t* vgen = smem + (vst - smem_addr(smem));
-                const int units = (kBlockSize - nvalid) * S::kChunks * 8;
-                for (int u = lane; u < units; u += 32) {
-                    const int r = nvalid + u / (S::kChunks * 8), rem = u % (S::kChunks * 8);
-                    *reinterpret_cast<uint4*>(vgen + (rem >> 3) * S::kBoxBytes + r * 128 + (rem & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-            }
-
-            // O^T += V^T . P^T
-#pragma unroll
-            for (int mt = 0; mt < S::kSteps; ++mt) {
-                uint32_t a[4];
-                ldsm_x4_trans(a, vst + (mt >> 2) * S::kBoxBytes + swz(rv, ((mt & 3) << 1) + (mi & 1)));
-                mma_16816(o[mt], a, pb0, pb1);
-            }
+            const uint32_t kst = stage0 + s * S::kStageBytes;
+            warp_block_update<D>(qb, o, m0, m1, l0, l1, kst, kst + S::kTileBytes,
+                                 smem + (kst + S::kTileBytes - smem_addr(smem)), min(kBlockSize, L - tok0), sl2);
         }
         __syncwarp();
         if (i + NS < nmine) issue(i + NS);
@@ -489,6 +506,231 @@ __global__ void __launch_bounds__(NW * 32, 1)
     PA_TRACE_MARK(4);
 }
 
+// ---------------------------------------------------------------------------
+// Persistent schedule (PA_MODE_PERSISTENT).  pa_work_scan_kernel writes, per
+// sequence, the exclusive prefix sum of its work items (work_items: one per
+// (partition, kv head), one per kv head for an empty sequence, one for an
+// invalid length).  A fixed grid of one-warp CTAs walks that list, CTA x
+// taking items x, x + grid, x + 2 grid, ...; sequence b of L tokens is cut
+// into partitions of balanced_partition(L, P) tokens, the fewest of at most P
+// evened out to whole blocks, so that no item is much shorter than the rest.
+//
+// The warp's K/V blocks form ONE stream across all of its items: stream
+// position g goes to stage g % NS and completes phase g / NS of that stage's
+// mbarrier, and the copies run NS positions ahead of the math, into the next
+// item when the current one ends.  The mbarriers are initialised once per CTA
+// and never again, and an item boundary is, for the stages and barriers, just
+// the next position of the ring -- the same protocol as inside one partition.
+// ---------------------------------------------------------------------------
+
+// Work item i of the persistent schedule.  nblk = the blocks it streams:
+// 0 for an invalid length, an empty sequence, or (never, with a work list
+// built from the same lengths) a partition past the end.
+struct PersistentItem {
+    int b, p, kvh, L, part, nblk;
+    bool bad;
+};
+
+__device__ __forceinline__ PersistentItem persistent_item(const PartitionParams& prm, int i) {
+    int lo = 0, hi = prm.num_seqs;  // offsets[lo] <= i < offsets[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(prm.work_offsets + mid) <= i)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    PersistentItem it;
+    const int r = i - __ldg(prm.work_offsets + lo);
+    it.b = lo;
+    it.p = r / prm.num_kv_heads;
+    it.kvh = r % prm.num_kv_heads;
+    it.L = __ldg(prm.seq_lens + lo);
+    it.bad = it.L < 0 || it.L > prm.max_seq_len || it.L > prm.max_blocks_per_seq * kBlockSize;
+    it.part = balanced_partition(it.L, prm.partition_size);
+    it.nblk = 0;
+    if (!it.bad && it.L > 0) {
+        const int bpp = it.part / kBlockSize;
+        it.nblk = max(0, min(bpp, (it.L + kBlockSize - 1) / kBlockSize - it.p * bpp));
+    }
+    return it;
+}
+
+template <int D, int NS>
+__global__ void __launch_bounds__(32, 1)
+    pa_partition_persistent_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                   const __grid_constant__ CUtensorMap tmap_v, const PartitionParams prm) {
+    using S = PartitionShape<D, 1, NS>;
+    // the work list is written by the preceding (scan) grid
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t stage0 = smem_addr(smem);
+    const uint32_t bar0 = stage0 + S::kStageArea;
+    const int lane = threadIdx.x & 31;
+    const int G = prm.group, H = prm.num_heads;
+    const int total = __ldg(prm.work_offsets + prm.num_seqs);
+
+    if (lane == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+
+    // ---- copy side: walks the same items in the same order as the math ----
+    int is_i = (int)blockIdx.x - (int)gridDim.x;  // item being copied
+    int is_j = 0, is_nblk = 0, is_kvh = 0, is_ids = -1;
+    const int32_t* is_bt = prm.block_tables;
+    bool is_done = false;
+    uint32_t issued = 0;      // stream positions issued so far
+    uint32_t valid_bits = 0;  // stage s holds a block with a legal id
+    auto issue_next = [&]() {
+        while (!is_done && is_j >= is_nblk) {  // warp-uniform: next item with blocks
+            is_i += (int)gridDim.x;
+            if (is_i >= total) {
+                is_done = true;
+                break;
+            }
+            const PersistentItem it = persistent_item(prm, is_i);
+            is_nblk = it.nblk;
+            is_kvh = it.kvh;
+            is_j = 0;
+            is_bt = prm.block_tables + (size_t)it.b * prm.max_blocks_per_seq + it.p * (it.part / kBlockSize);
+        }
+        if (is_done) return;
+        // block ids 32 at a time, only below the sequence's last block
+        if ((is_j & 31) == 0) is_ids = is_j + lane < is_nblk ? __ldg(is_bt + is_j + lane) : -1;
+        const int phys = __shfl_sync(kFull, is_ids, is_j & 31);
+        const int s = (int)(issued % NS);
+        const uint32_t bar = bar0 + 8 * s;
+        const bool ok = phys >= 0 && (long long)phys < prm.num_blocks;
+        valid_bits = ok ? (valid_bits | (1u << s)) : (valid_bits & ~(1u << s));
+        if (lane == 0) {
+            if (ok) {
+                mbar_arrive_expect_tx(bar, S::kStageBytes);
+                const int row = (phys * prm.num_kv_heads + is_kvh) * kBlockSize;
+                const uint32_t kdst = stage0 + s * S::kStageBytes, vdst = kdst + S::kTileBytes;
+                // one box per tile: all D / 64 column chunks of the 16 rows
+                tma_load_3d(kdst, &tmap_k, 0, row, 0, bar);
+                tma_load_3d(vdst, &tmap_v, 0, row, 0, bar);
+            } else {
+                atomicOr(&g_status, PA_DEV_BAD_BLOCK_ID);
+                mbar_arrive(bar);  // complete the phase so the math stays in step
+            }
+        }
+        ++is_j;
+        ++issued;
+    };
+    for (int k = 0; k < NS; ++k) issue_next();
+
+    // ---- math side ----
+    const int g = lane >> 2, c = lane & 3;  // MMA fragment row group / column pair
+    const float sl2 = prm.scale_log2;
+    uint32_t pos = 0;  // stream position of the next block
+    for (int i = blockIdx.x; i < total; i += gridDim.x) {
+        const PersistentItem it = persistent_item(prm, i);
+        if (it.bad) {
+            if (lane == 0) atomicOr(&g_status, PA_DEV_BAD_SEQ_LEN);
+            continue;
+        }
+        if (it.L == 0) {  // empty sequence: its G heads of this kv head are zero
+            for (int x = lane; x < G * D; x += 32)
+                prm.out[((size_t)it.b * H + it.kvh * G) * D + x] = __float2half_rn(0.f);
+            continue;
+        }
+        if (it.nblk == 0) continue;
+        const int n_part = (it.L + it.part - 1) / it.part;
+        const int blk0 = it.p * (it.part / kBlockSize);
+
+        uint32_t qb[S::kSteps][2];
+        {
+            const int hq = g < G ? g : 0;  // lanes of padding heads load nothing
+            const uint32_t* qrow =
+                reinterpret_cast<const uint32_t*>(prm.q + ((size_t)it.b * H + it.kvh * G + hq) * D);
+#pragma unroll
+            for (int ks = 0; ks < S::kSteps; ++ks) {
+                qb[ks][0] = g < G ? __ldg(qrow + 8 * ks + c) : 0u;
+                qb[ks][1] = g < G ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
+            }
+        }
+        float o[S::kSteps][4];
+#pragma unroll
+        for (int k = 0; k < S::kSteps; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+        for (int j = 0; j < it.nblk; ++j, ++pos) {
+            const int s = (int)(pos % NS);
+            if (prm.force_timeout || !mbar_wait(bar0 + 8 * s, (pos / NS) & 1, prm.wait_limit)) {
+                // drain the copies in flight, report, and stop this CTA
+                for (uint32_t k = pos; k < issued; ++k)
+                    mbar_wait(bar0 + 8 * (k % NS), (k / NS) & 1, kDefaultWaitLimit);
+                if (lane == 0) atomicOr(&g_status, PA_DEV_TIMEOUT);
+                return;
+            }
+            if ((valid_bits >> s) & 1u) {
+                const uint32_t kst = stage0 + s * S::kStageBytes;
+                warp_block_update<D>(qb, o, m0, m1, l0, l1, kst, kst + S::kTileBytes,
+                                     smem + s * S::kStageBytes + S::kTileBytes,
+                                     min(kBlockSize, it.L - (blk0 + j) * kBlockSize), sl2);
+            }
+            __syncwarp();
+            issue_next();  // the stage just read takes position pos + NS
+        }
+
+        // exp sums: add the shares of the 8 lanes holding the same heads
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(kFull, l0, off);
+            l1 += __shfl_xor_sync(kFull, l1, off);
+        }
+        // normalised partial (or final output): o / l; a partition whose
+        // blocks all had illegal ids (m = -inf) was reported above
+        const float w0 = m0 == -INFINITY ? 0.f : 1.f, w1 = m1 == -INFINITY ? 0.f : 1.f;
+        const float L0 = w0 * l0, L1 = w1 * l1;
+        const float f0 = w0 * (1.f / L0), f1 = w1 * (1.f / L1);
+        const bool has0 = 2 * c < G, has1 = 2 * c + 1 < G;  // padding heads are not written
+        const size_t head0 = (size_t)it.b * H + it.kvh * G + 2 * c;
+        const bool direct = n_part == 1;
+        const size_t pi0 = head0 * prm.max_partitions + it.p, pi1 = pi0 + prm.max_partitions;
+#pragma unroll
+        for (int mt = 0; mt < S::kSteps; ++mt) {
+            const int d = 16 * mt + g;
+            const float v00 = f0 * o[mt][0], v10 = f1 * o[mt][1], v08 = f0 * o[mt][2], v18 = f1 * o[mt][3];
+            if (direct) {
+                if (has0) {
+                    prm.out[head0 * D + d] = __float2half_rn(v00);
+                    prm.out[head0 * D + d + 8] = __float2half_rn(v08);
+                }
+                if (has1) {
+                    prm.out[(head0 + 1) * D + d] = __float2half_rn(v10);
+                    prm.out[(head0 + 1) * D + d + 8] = __float2half_rn(v18);
+                }
+            } else {
+                if (has0) {
+                    prm.tmp_out[pi0 * D + d] = v00;
+                    prm.tmp_out[pi0 * D + d + 8] = v08;
+                }
+                if (has1) {
+                    prm.tmp_out[pi1 * D + d] = v10;
+                    prm.tmp_out[pi1 * D + d + 8] = v18;
+                }
+            }
+        }
+        if (!direct && g == 0) {
+            if (has0) {
+                prm.max_logits[pi0] = m0;
+                prm.exp_sums[pi0] = L0;
+            }
+            if (has1) {
+                prm.max_logits[pi1] = m1;
+                prm.exp_sums[pi1] = L1;
+            }
+        }
+    }
+}
+
 // Phase 2: merge the partials of each (sequence, head).  With M = max_p m_p,
 // out = sum_p w_p acc_p / sum_p w_p and w_p = l_p 2^(m_p - M): the
 // log-sum-exp merge.  One CTA per (head, sequence, W-wide slice of head_dim);
@@ -510,7 +752,8 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
     const int L = prm.seq_lens[b];
     // single-partition, empty and invalid sequences were finished by the partition kernel
     if (L <= prm.partition_size || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) return;
-    const int n = (L + prm.partition_size - 1) / prm.partition_size;
+    const int part = prm.balanced ? balanced_partition(L, prm.partition_size) : prm.partition_size;
+    const int n = (L + part - 1) / part;
     const size_t base = ((size_t)b * prm.num_heads + h) * prm.max_partitions;
     const float* ml = prm.max_logits + base;
     const float* el = prm.exp_sums + base;
@@ -653,6 +896,108 @@ cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3
         case 256: return launch_reduce_d<256>(width, prm, grid, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// The persistent kernel is compiled for one warp and 2 or 3 stages.
+int persistent_smem_bytes(int head_dim, int stages) {
+    if (stages != 2 && stages != 3) return -1;
+    switch (head_dim) {
+        case 64: return stages == 2 ? PartitionShape<64, 1, 2>::kSmemBytes : PartitionShape<64, 1, 3>::kSmemBytes;
+        case 128: return stages == 2 ? PartitionShape<128, 1, 2>::kSmemBytes : PartitionShape<128, 1, 3>::kSmemBytes;
+        case 256: return stages == 2 ? PartitionShape<256, 1, 2>::kSmemBytes : PartitionShape<256, 1, 3>::kSmemBytes;
+        default: return -1;
+    }
+}
+
+namespace {
+template <int D, int NS>
+cudaError_t launch_persistent_t(const PartitionParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                                cudaStream_t stream) {
+    const int smem = PartitionShape<D, 1, NS>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(pa_partition_persistent_kernel<D, NS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, pa_partition_persistent_kernel<D, NS>, tk, tv, prm);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_partition_persistent(int head_dim, int stages, const PartitionParams& prm, const CUtensorMap& tk,
+                                        const CUtensorMap& tv, int grid, cudaStream_t stream) {
+    if (!prm.work_offsets || grid <= 0 || (stages != 2 && stages != 3)) return cudaErrorInvalidValue;
+    switch (head_dim) {
+        case 64: return stages == 2 ? launch_persistent_t<64, 2>(prm, tk, tv, grid, stream)
+                                    : launch_persistent_t<64, 3>(prm, tk, tv, grid, stream);
+        case 128: return stages == 2 ? launch_persistent_t<128, 2>(prm, tk, tv, grid, stream)
+                                     : launch_persistent_t<128, 3>(prm, tk, tv, grid, stream);
+        case 256: return stages == 2 ? launch_persistent_t<256, 2>(prm, tk, tv, grid, stream)
+                                     : launch_persistent_t<256, 3>(prm, tk, tv, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// Exclusive prefix sums of the per-sequence work items (one CTA of 1024
+// threads; each thread sums a contiguous run of sequences, then the runs are
+// scanned across the block).
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads) pa_work_scan_kernel(const ScanParams prm) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ int warp_sums[kScanThreads / 32];
+    const int per = (prm.num_seqs + kScanThreads - 1) / kScanThreads;
+    const int b0 = threadIdx.x * per, b1 = min(prm.num_seqs, b0 + per);
+    int local = 0;
+    for (int b = b0; b < b1; ++b)
+        local += work_items(__ldg(prm.seq_lens + b), prm.max_seq_len, prm.max_blocks_per_seq, prm.partition_size,
+                            prm.num_kv_heads);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(kFull, w, off);
+            if (lane >= off) w += v;
+        }
+        warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);  // exclusive start of this thread's run
+    for (int b = b0; b < b1; ++b) {
+        prm.work_offsets[b] = run;
+        run += work_items(__ldg(prm.seq_lens + b), prm.max_seq_len, prm.max_blocks_per_seq, prm.partition_size,
+                          prm.num_kv_heads);
+    }
+    if (threadIdx.x == kScanThreads - 1) prm.work_offsets[prm.num_seqs] = warp_sums[kScanThreads / 32 - 1];
+}
+
+cudaError_t launch_work_scan(const ScanParams& prm, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kScanThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, pa_work_scan_kernel, prm);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 unsigned int* device_status_ptr() {

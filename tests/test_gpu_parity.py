@@ -40,7 +40,8 @@ def run(w, **opt):
 SMALL_LENS = [[1], [15], [16], [17], [511], [512], [513], [1, 16, 17, 511, 512, 513, 1029], [2048, 3, 700]]
 MODES = [dict(), dict(mode="single"), dict(mode="split", partition_size=16), dict(mode="split", partition_size=64),
          dict(mode="split", partition_size=512), dict(mode="split", partition_size=1024),
-         dict(mode="fused", partition_size=16), dict(mode="fused", partition_size=512)]
+         dict(mode="fused", partition_size=16), dict(mode="fused", partition_size=512),
+         dict(mode="persistent"), dict(mode="persistent", partition_size=64)]
 
 
 @pytest.mark.parametrize("lens", SMALL_LENS, ids=lambda x: "L" + "-".join(map(str, x)))
@@ -54,7 +55,7 @@ def test_small_gqa6_d256(dev, lens, opt):
 
 @pytest.mark.parametrize("H,Hkv,D", [(4, 4, 64), (8, 4, 128), (16, 2, 256), (12, 4, 64), (12, 2, 128),
                                      (16, 4, 256), (5, 5, 128), (7, 1, 256)])
-@pytest.mark.parametrize("mode", ["single", "split", "fused"])
+@pytest.mark.parametrize("mode", ["single", "split", "fused", "persistent"])
 def test_group_sizes_and_head_dims(dev, H, Hkv, D, mode):
     lens = [1, 37, 700, 1500, 16 * 33]
     w = W.make_workload("shape", lens, num_heads=H, num_kv_heads=Hkv, head_dim=D, num_blocks=300, seed=H * D,
@@ -74,6 +75,9 @@ def test_group_sizes_and_head_dims(dev, H, Hkv, D, mode):
     ("b4_l32768_peaked", dict()),
     ("b1_l102400", dict()),
     ("b1_l102400", dict(mode="fused")),
+    ("b8_u8192", dict(mode="persistent")),
+    ("b4_l32768_peaked", dict(mode="persistent")),
+    ("b1_l102400", dict(mode="persistent")),
 ])
 def test_named_workload_full(dev, name, opt):
     w = W.make_config(name, device=dev)
@@ -84,9 +88,10 @@ def test_named_workload_full(dev, name, opt):
     print(name, opt, r)
 
 
-def test_mixed_batch_sampled(dev):
+@pytest.mark.parametrize("opt", [dict(), dict(mode="persistent")], ids=["default", "persistent"])
+def test_mixed_batch_sampled(dev, opt):
     w = W.make_config("b64_loguniform", device=dev)
-    out = pb.decode_workload(w)
+    out = pb.decode_workload(w, **opt)
     torch.cuda.synchronize()
     assert pb.pa_get_device_status() == 0
     lens = np.array(w.seq_lens_host)
@@ -120,7 +125,7 @@ def _permuted_pool(w, seed):
 
 
 @pytest.mark.parametrize("opt", [dict(mode="single"), dict(mode="split", partition_size=512),
-                                 dict(mode="split", partition_size=48)])
+                                 dict(mode="split", partition_size=48), dict(mode="persistent")])
 def test_permuted_block_table_is_bit_identical(dev, opt):
     w = W.make_workload("perm", [3000, 517, 8000, 1], num_blocks=900, seed=5, device=dev)
     a = run(w, **opt)
@@ -223,7 +228,7 @@ def test_bad_seq_len_sets_device_status(dev):
 def test_forced_timeout_returns_status_and_context_survives(dev):
     w = W.make_workload("timeout", [3000, 64], num_blocks=200, seed=13, device=dev)
     pb.pa_get_device_status()
-    for mode in ("single", "split", "fused"):
+    for mode in ("single", "split", "fused", "persistent"):
         pb.decode_workload(w, mode=mode, partition_size=0 if mode == "single" else 512,
                            flags=pb.PA_FLAG_FORCE_TIMEOUT)
         assert pb.pa_get_device_status() & pb.PA_DEV_TIMEOUT
@@ -319,3 +324,60 @@ def test_fused_combine_after_forced_timeout_and_in_a_graph(dev):
     torch.cuda.synchronize()
     assert pb.pa_get_device_status() == 0
     assert torch.equal(out, eager)
+
+
+def test_persistent_schedule_empty_bad_and_graph(dev):
+    # empty sequences are zero, single-partition ones are written directly, the rest merged
+    w = W.make_workload("pers", [0, 700, 16, 5000, 0, 513, 1], num_blocks=500, seed=17, device=dev,
+                        tail_fill=float("nan"))
+    out = run(w, mode="persistent")
+    assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[4]) == 0
+    assert_parity(out, oracle_ref(w), "persistent ragged")
+    assert torch.equal(out, run(w, mode="persistent"))  # repeat: bit-identical
+    # a length beyond the host bound is reported, as in the grid schedule
+    bad = W.make_workload("persbad", [100, 40], num_blocks=20, seed=18, device=dev, extra_table_cols=4)
+    pb.pa_get_device_status()
+    o2 = torch.empty_like(bad.q)
+    bad.seq_lens[1] = 101
+    pb.pa_decode_ex(o2, bad.q, bad.k_cache, bad.v_cache, bad.block_tables, bad.seq_lens, bad.num_heads,
+                    bad.num_kv_heads, bad.head_dim, bad.block_size, bad.scale, max_seq_len=100, mode="persistent",
+                    workspace=pb.alloc_workspace(pb.pa_decode_plan(
+                        o2, bad.q, bad.k_cache, bad.v_cache, bad.block_tables, bad.seq_lens, bad.num_heads,
+                        bad.num_kv_heads, bad.head_dim, bad.block_size, bad.scale, max_seq_len=100,
+                        mode="persistent"), dev))
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() & pb.PA_DEV_BAD_SEQ_LEN
+    # captured once, replayed with new lengths: the work list is rebuilt on the device
+    kw = dict(max_seq_len=w.max_seq_len, mode="persistent")
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, **kw)
+    ws = pb.alloc_workspace(plan, dev)
+    args = (out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads, w.head_dim,
+            w.block_size, w.scale)
+    pb.pa_decode_ex(*args, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pb.pa_decode_ex(*args, torch.cuda.current_stream(), workspace=ws, **kw)
+    new_lens = [0, 690, 16, 4000, 0, 500, 1]  # within each sequence's blocks
+    w.seq_lens.copy_(torch.tensor(new_lens, dtype=torch.int32, device=dev))
+    w.seq_lens_host[:] = new_lens
+    g.replay()
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    assert_parity(out, oracle_ref(w), "persistent graph replay with new lengths")
+
+
+@pytest.mark.parametrize("stages", [2, 3])
+@pytest.mark.parametrize("P", [16, 64, 512])
+def test_persistent_many_items_per_cta(dev, stages, P):
+    # small partitions give many more work items than resident CTAs, so each
+    # CTA streams its blocks across many items and sequences through one ring
+    lens = [1, 17, 513, 3000, 100, 0, 2049, 16, 4000, 777] * 3
+    w = W.make_workload("pmany", lens, num_blocks=2100, seed=40 + stages, device=dev, tail_fill=float("nan"))
+    out = run(w, mode="persistent", partition_size=P, stages=stages)
+    assert_parity(out, oracle_ref(w), f"persistent P={P} stages={stages}")
+    assert torch.count_nonzero(out[5]) == 0
+    # the stage count changes nothing but the copy depth: same rounding order
+    assert torch.equal(out, run(w, mode="persistent", partition_size=P, stages=5 - stages))

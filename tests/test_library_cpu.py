@@ -93,6 +93,17 @@ def test_plan_halves_the_partition_when_the_grid_is_smaller_than_the_gpu():
     assert pl.partition_size == 1024
 
 
+def test_plan_persistent_mode_has_a_fixed_grid_and_a_work_list():
+    a = args(num_seqs=64, max_seq_len=65536, num_blocks=64 * 4096)
+    rc, pl = plan(a, mode=pb.PA_MODE_PERSISTENT)
+    _, split = plan(a, mode=pb.PA_MODE_SPLIT)
+    assert rc == 0 and pl["mode"] == pb.PA_MODE_PERSISTENT
+    assert pl["threads"] == 32 and pl["stages"] == 2 and pl["grid_y"] == pl["grid_z"] == 1
+    assert pl["grid_x"] == SMS * 6                      # every CTA the SMs hold at once (6 per SM)
+    assert pl["max_partitions"] == split["grid_x"] == 128 and pl["launch_reduce"] == 1
+    assert pl["workspace_bytes"] == split["workspace_bytes"] + 512   # + 65 ints of work list, 256-aligned
+
+
 def test_plan_fused_mode_keeps_partials_and_tickets_and_launches_once():
     a = args(max_seq_len=102400)
     rc, fused = plan(a, mode=pb.PA_MODE_FUSED)
