@@ -128,7 +128,10 @@ typedef struct {
 /* Tuning and debug options; an all-zero struct means "defaults". */
 typedef struct {
     int mode;                    /* PA_MODE_* */
-    int partition_size;          /* tokens per partition in SPLIT mode, multiple of block_size; 0 = 512 */
+    int partition_size;          /* tokens per partition in SPLIT mode, multiple of block_size; 0 = chosen
+                                    by the planner: 512 (256 when that gives fewer CTAs than SMs; for
+                                    one long sequence, as many partitions per kv head as SMs allow,
+                                    one wave of one 4-warp CTA per SM, when that exceeds 2048 tokens) */
     int flags;                   /* PA_FLAG_* */
     unsigned int wait_limit;     /* polls before a copy wait gives up; 0 = library default (2^20) */
     void* event_partition_begin; /* optional cudaEvent_t recorded on `stream` right before ... */
@@ -176,8 +179,10 @@ int pa_decode_ex(const pa_decode_args* args, const pa_decode_opts* opts, void* w
 int pa_decode_plan(const pa_decode_args* args, const pa_decode_opts* opts, int num_sms,
                    pa_decode_plan_t* plan);
 
-/* Workspace bytes of a SPLIT call with these sizes.  FUSED needs 256-byte-aligned
- * num_seqs * num_kv_heads * 4 bytes more; pa_decode_plan gives every mode's exact figure. */
+/* Workspace bytes of a SPLIT call with these sizes; partition_size 0 gives an upper
+ * bound for the automatic partition size.  FUSED needs 256-byte-aligned
+ * num_seqs * num_kv_heads * 4 bytes more, PERSISTENT 256-byte-aligned (num_seqs + 1) * 4;
+ * pa_decode_plan gives every mode's exact figure. */
 size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim,
                                 int partition_size);
 

@@ -21,6 +21,7 @@
 namespace {
 
 constexpr int kDefaultPartition = 512;
+constexpr int kOneWaveMinPartition = 2048;  // see make_plan
 constexpr int kMaxDevices = 64;
 constexpr size_t kWsAlign = 256;
 
@@ -178,6 +179,25 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
                                a->num_kv_heads * a->num_seqs;
         if (ctas < num_sms) part = kDefaultPartition / 2;
     }
+    // One long sequence: its grid is known exactly, so it runs as ONE wave of
+    // one 4-warp CTA per SM (partitions x kv heads = SMs).  Fewer, longer CTAs
+    // pay a CTA's start-up and merge once per SM and leave fewer partials
+    // (GB300, 4 kv heads, head_dim 256, against 512-token partitions: 102400
+    // tokens 70.5 -> 68.9 us, 262144: 174.4 -> 161.6, 524288: 343.9 -> 305.0;
+    // below ~2048 tokens per partition the two are within a few per cent).
+    bool one_wave = false;
+    const int req_mode = o ? o->mode : PA_MODE_AUTO;
+    if (!(o && o->partition_size > 0) && !(o && (o->warps || o->stages)) && a->num_seqs == 1 &&
+        (req_mode == PA_MODE_AUTO || req_mode == PA_MODE_SPLIT)) {
+        const int per_head = num_sms / a->num_kv_heads;  // partitions of the sequence
+        if (per_head >= 2) {
+            const long long p1 = ((a->max_seq_len + per_head - 1) / per_head + bs - 1) / bs * bs;
+            if (p1 >= kOneWaveMinPartition) {
+                part = static_cast<int>(p1);
+                one_wave = true;
+            }
+        }
+    }
     const int split_parts = (a->max_seq_len + part - 1) / part;
     int mode = o ? o->mode : PA_MODE_AUTO;
     if (mode == PA_MODE_AUTO) {
@@ -204,6 +224,9 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         // head_dim 256 with 2 stages
         warps = 1;
         if (!stages) stages = 2;
+    } else if (one_wave) {
+        warps = 4;
+        stages = 2;
     } else if (!warps) {
         choose_shape(a, plan, num_sms, &warps, &stages);
     }
@@ -621,7 +644,8 @@ int pa_prefix(void* out, const void* q, const void* k_new, const void* v_new, co
 
 size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim, int partition_size) {
     if (num_seqs <= 0 || max_seq_len <= 0 || num_heads <= 0 || head_dim <= 0) return 0;
-    const int part = partition_size > 0 ? partition_size : kDefaultPartition;
+    // 0: the smallest partition the automatic choice takes (the most partials)
+    const int part = partition_size > 0 ? partition_size : kDefaultPartition / 2;
     return split_workspace_bytes(num_seqs, num_heads, (max_seq_len + part - 1) / part, head_dim);
 }
 

@@ -50,15 +50,31 @@ def ws_bytes(B, H, parts, D):
     return 2 * a(B * H * parts * 4) + a(B * H * parts * D * 4)
 
 
-def test_plan_long_context_splits_into_512_token_partitions():
+def test_plan_long_context_runs_one_wave_of_one_cta_per_sm():
+    # one 102400-token sequence: 152 SMs / 4 kv heads = 38 partitions of
+    # ceil(102400 / 38) = 2695 -> 2704 tokens, one 4-warp CTA per SM
     rc, pl = plan(args())
     assert rc == pb.PA_OK
-    assert pl["mode"] == pb.PA_MODE_SPLIT and pl["partition_size"] == 512
-    assert (pl["grid_x"], pl["grid_y"], pl["grid_z"]) == (200, 4, 1)      # 800 CTAs on kv heads
+    assert pl["mode"] == pb.PA_MODE_SPLIT and pl["partition_size"] == 2704
+    assert (pl["grid_x"], pl["grid_y"], pl["grid_z"]) == (38, 4, 1)
+    assert pl["threads"] == 128 and pl["stages"] == 2
+    assert pl["grid_x"] * pl["grid_y"] <= SMS
     assert pl["launch_reduce"] == 1
-    assert (pl["reduce_grid_x"], pl["reduce_grid_y"], pl["reduce_grid_z"]) == (24, 1, 8)
-    assert pl["workspace_bytes"] == ws_bytes(1, 24, 200, 256)
-    assert pl["workspace_bytes"] == pb.pa_decode_workspace_size(1, 102400, 24, 256, 512)
+    assert pl["workspace_bytes"] == ws_bytes(1, 24, 38, 256)
+    assert pl["workspace_bytes"] <= pb.pa_decode_workspace_size(1, 102400, 24, 256, 0)
+    # below 2048 tokens per partition, and for batches, the 512-token default stays
+    rc, short = plan(args(max_seq_len=65536, num_blocks=4096))
+    assert rc == 0 and short["partition_size"] == 512 and short["grid_x"] == 128
+    rc, batch = plan(args(num_seqs=2, num_blocks=12800))
+    assert rc == 0 and batch["partition_size"] == 512 and batch["grid_x"] == 200
+    # an explicit partition size or mode keeps the old plan
+    rc, fixed = plan(args(), partition_size=512)
+    assert rc == 0 and (fixed["grid_x"], fixed["grid_y"]) == (200, 4)
+    assert (fixed["reduce_grid_x"], fixed["reduce_grid_y"], fixed["reduce_grid_z"]) == (24, 1, 8)
+    assert fixed["workspace_bytes"] == ws_bytes(1, 24, 200, 256)
+    assert fixed["workspace_bytes"] == pb.pa_decode_workspace_size(1, 102400, 24, 256, 512)
+    rc, fused = plan(args(), mode=pb.PA_MODE_FUSED)
+    assert rc == 0 and fused["partition_size"] == 512
 
 
 def test_plan_modes():
@@ -107,7 +123,7 @@ def test_plan_persistent_mode_has_a_fixed_grid_and_a_work_list():
 def test_plan_fused_mode_keeps_partials_and_tickets_and_launches_once():
     a = args(max_seq_len=102400)
     rc, fused = plan(a, mode=pb.PA_MODE_FUSED)
-    _, split = plan(a, mode=pb.PA_MODE_SPLIT)
+    _, split = plan(a, mode=pb.PA_MODE_SPLIT, partition_size=512)
     assert rc == 0 and fused["mode"] == pb.PA_MODE_FUSED and fused["launch_reduce"] == 0
     assert fused["grid_x"] == split["grid_x"] == 200 and fused["partition_size"] == 512
     # the split partials plus one 4-byte ticket per (sequence, kv head), 256-byte aligned
@@ -204,5 +220,6 @@ def test_cta_shape_option():
     (64, 65536, (1, 2)),     # many waves: the finest slots
 ])
 def test_cta_shape_follows_the_wave_model(B, L, shape):
-    rc, pl = plan(args(num_seqs=B, max_seq_len=L, num_blocks=B * L // 16))
+    # at the 512-token partitions the model was fitted for
+    rc, pl = plan(args(num_seqs=B, max_seq_len=L, num_blocks=B * L // 16), partition_size=512 if L > 2048 else 0)
     assert rc == 0 and (pl["threads"] // 32, pl["stages"]) == shape
