@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kDefaultPartition = 512;
 constexpr int kOneWaveMinPartition = 2048;  // see make_plan
+constexpr int kPersistentWarps = 1, kPersistentStages = 2;  // PA_MODE_PERSISTENT CTA shape
 constexpr int kMaxDevices = 64;
 constexpr size_t kWsAlign = 256;
 
@@ -82,7 +83,9 @@ int validate(const pa_decode_args* a, const pa_decode_opts* o) {
     // every head_dim is compiled with the same set of CTA shapes; the
     // persistent kernel with one warp and 2 or 3 stages
     if (o && o->mode == PA_MODE_PERSISTENT) {
-        if ((o->warps && o->warps != 1) || (o->stages && pa::persistent_smem_bytes(256, o->stages) < 0))
+        if ((o->warps || o->stages) &&
+            pa::persistent_smem_bytes(256, o->warps ? o->warps : kPersistentWarps,
+                                      o->stages ? o->stages : kPersistentStages) < 0)
             return PA_ERR_UNSUPPORTED;
     } else if (o && (o->warps || o->stages) && pa::partition_smem_bytes(256, o->warps, o->stages) < 0) {
         return PA_ERR_UNSUPPORTED;
@@ -220,10 +223,8 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     plan->grid_z = a->num_seqs;
     int warps = o ? o->warps : 0, stages = o ? o->stages : 0;
     if (mode == PA_MODE_PERSISTENT) {
-        // one warp per CTA, the finest unit of work: 6 CTAs per SM at
-        // head_dim 256 with 2 stages
-        warps = 1;
-        if (!stages) stages = 2;
+        if (!warps) warps = kPersistentWarps;
+        if (!stages) stages = kPersistentStages;
     } else if (one_wave) {
         warps = 4;
         stages = 2;
@@ -232,7 +233,8 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     }
     plan->threads = warps * 32;
     plan->stages = stages;
-    plan->smem_bytes = mode == PA_MODE_PERSISTENT ? pa::persistent_smem_bytes(a->head_dim, stages)
+    plan->smem_bytes = mode == PA_MODE_PERSISTENT ? pa::persistent_smem_bytes(a->head_dim, warps, stages) +
+                                                        pa::persistent_seq_cache_bytes(a->num_seqs)
                                                   : pa::partition_smem_bytes(a->head_dim, warps, stages);
     if (mode == PA_MODE_PERSISTENT) {
         // a fixed grid of every CTA the SMs hold at once
@@ -254,9 +256,9 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         plan->reduce_grid_z = a->head_dim / reduce_slice(a->head_dim, (long long)a->num_seqs * a->num_heads, num_sms);
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim);
     }
-    if (mode == PA_MODE_PERSISTENT)  // + the work list
+    if (mode == PA_MODE_PERSISTENT)  // + the work list and the item counter
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim) +
-                                align_up(static_cast<size_t>(a->num_seqs + 1) * 4, kWsAlign);
+                                align_up(static_cast<size_t>(a->num_seqs + 2) * 4, kWsAlign);
     return PA_OK;
 }
 
@@ -332,6 +334,7 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.tmp_out = partials ? reinterpret_cast<float*>(w + 2 * align_up(rows * 4, kWsAlign)) : nullptr;
     prm.tickets = fused ? reinterpret_cast<unsigned int*>(w + partial_bytes) : nullptr;
     prm.work_offsets = persistent ? reinterpret_cast<const int*>(w + partial_bytes) : nullptr;
+    prm.work_counter = persistent ? reinterpret_cast<int*>(w + partial_bytes) + a->num_seqs + 1 : nullptr;
     prm.num_seqs = a->num_seqs;
     prm.num_blocks = a->num_blocks;
     prm.num_heads = a->num_heads;
@@ -355,13 +358,16 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
         sp.max_blocks_per_seq = a->max_blocks_per_seq;
         sp.partition_size = plan.partition_size;
         sp.num_kv_heads = a->num_kv_heads;
+        sp.work_counter = reinterpret_cast<int*>(w + partial_bytes) + a->num_seqs + 1;
+        sp.first_dynamic = plan.grid_x;
         if (pa::launch_work_scan(sp, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
     if (o && o->event_partition_begin &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_begin), stream) != cudaSuccess)
         return PA_ERR_CUDA;
     const cudaError_t le =
-        persistent ? pa::launch_partition_persistent(a->head_dim, plan.stages, prm, tk, tv, plan.grid_x, stream)
+        persistent ? pa::launch_partition_persistent(a->head_dim, plan.threads / 32, plan.stages, prm, tk, tv,
+                                                     plan.grid_x, stream)
                    : pa::launch_partition(a->head_dim, plan.threads / 32, plan.stages, prm, tk, tv,
                                           dim3(plan.grid_x, plan.grid_y, plan.grid_z), stream);
     if (le != cudaSuccess) return PA_ERR_CUDA;

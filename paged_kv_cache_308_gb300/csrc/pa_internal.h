@@ -37,6 +37,13 @@ __host__ __device__ inline int work_items(int L, int max_seq_len, int max_blocks
     return ((L + part - 1) / part) * num_kv_heads;
 }
 
+// Batches of at most this many sequences keep the persistent schedule's work
+// list and lengths in each CTA's shared memory (these extra bytes).
+constexpr int kPersistentSeqCache = 256;
+inline int persistent_seq_cache_bytes(int num_seqs) {
+    return num_seqs <= kPersistentSeqCache ? ((2 * num_seqs + 1) * 4 + 15) / 16 * 16 : 0;
+}
+
 struct PartitionParams {
     __half* out;
     const __half* q;
@@ -59,8 +66,10 @@ struct PartitionParams {
     // and left zero after it; null when a separate reduce kernel merges.
     unsigned int* tickets;
     // Persistent schedule: exclusive prefix sums of work_items over the
-    // sequences (num_seqs + 1 entries); null for one CTA per grid cell.
+    // sequences (num_seqs + 1 entries) and the next item to hand out; null
+    // for one CTA per grid cell.
     const int* work_offsets;
+    int* work_counter;
     int num_seqs;
 };
 
@@ -78,7 +87,8 @@ struct ReduceParams {
 struct ScanParams {
     const int32_t* seq_lens;
     int* work_offsets;  // [num_seqs + 1]
-    int num_seqs, max_seq_len, max_blocks_per_seq, partition_size, num_kv_heads;
+    int* work_counter;  // set to first_dynamic (the persistent grid size)
+    int num_seqs, max_seq_len, max_blocks_per_seq, partition_size, num_kv_heads, first_dynamic;
 };
 
 // Dynamic shared memory of a partition CTA of `warps` warps with `stages`
@@ -98,12 +108,13 @@ cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3
 // The persistent schedule's work list: one CTA scans the sequences' item counts.
 cudaError_t launch_work_scan(const ScanParams& prm, cudaStream_t stream);
 
-// Persistent schedule: `grid` one-warp CTAs walk the work list in
-// prm.work_offsets (stages 2 or 3); persistent_smem_bytes is the dynamic
-// shared memory of one such CTA (-1 for a shape that is not compiled).
-int persistent_smem_bytes(int head_dim, int stages);
-cudaError_t launch_partition_persistent(int head_dim, int stages, const PartitionParams& prm, const CUtensorMap& tk,
-                                        const CUtensorMap& tv, int grid, cudaStream_t stream);
+// Persistent schedule: `grid` CTAs of `warps` warps take the items of the
+// work list in prm.work_offsets from prm.work_counter; persistent_smem_bytes
+// is the dynamic shared memory of one such CTA (-1 for a shape that is not
+// compiled).
+int persistent_smem_bytes(int head_dim, int warps, int stages);
+cudaError_t launch_partition_persistent(int head_dim, int warps, int stages, const PartitionParams& prm,
+                                        const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t stream);
 
 // Read and clear the status word of the current device (synchronises stream).
 cudaError_t read_and_clear_status(cudaStream_t stream, int* status);

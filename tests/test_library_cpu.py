@@ -117,7 +117,17 @@ def test_plan_persistent_mode_has_a_fixed_grid_and_a_work_list():
     assert pl["threads"] == 32 and pl["stages"] == 2 and pl["grid_y"] == pl["grid_z"] == 1
     assert pl["grid_x"] == SMS * 6                      # every CTA the SMs hold at once (6 per SM)
     assert pl["max_partitions"] == split["grid_x"] == 128 and pl["launch_reduce"] == 1
-    assert pl["workspace_bytes"] == split["workspace_bytes"] + 512   # + 65 ints of work list, 256-aligned
+    # + 65 ints of work list and the item counter, 256-aligned
+    assert pl["workspace_bytes"] == split["workspace_bytes"] + 512
+    for w, s, per_sm in ((4, 2, 1), (2, 2, 2)):
+        o = pb.make_opts(mode="persistent", warps=w, stages=s)
+        p2 = pb.pa_decode_plan_t()
+        assert pb.lib.pa_decode_plan(ctypes.byref(a), ctypes.byref(o), SMS, ctypes.byref(p2)) == 0
+        assert (p2.threads, p2.stages, p2.grid_x) == (32 * w, s, SMS * per_sm)
+    for w, s in ((3, 2), (4, 3)):
+        o = pb.make_opts(mode="persistent", warps=w, stages=s)
+        assert pb.lib.pa_decode_plan(ctypes.byref(a), ctypes.byref(o), SMS,
+                                     ctypes.byref(pb.pa_decode_plan_t())) == pb.PA_ERR_UNSUPPORTED
 
 
 def test_plan_fused_mode_keeps_partials_and_tickets_and_launches_once():
