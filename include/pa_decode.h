@@ -89,13 +89,14 @@ enum {
                            partition order.  The workspace also holds one ticket per
                            (sequence, kv head) that must be zero before the first call on it;
                            every call leaves the tickets zero, also after a device error */
-    PA_MODE_PERSISTENT = 4 /* a fixed grid of (SMs x CTAs per SM) walks a work list that a small
-                              kernel builds on the device (a prefix sum of (partition, kv head)
-                              items per sequence); each sequence gets its own partition size, the
-                              fewest partitions of at most partition_size tokens evened out to
-                              whole blocks; then the log-sum-exp reduce.  The host never reads
-                              the lengths, so the call is graph-safe.  The workspace also holds
-                              the work list (num_seqs + 1 ints) */
+    PA_MODE_PERSISTENT = 4 /* a fixed grid of (SMs x CTAs per SM) takes the items of a work list
+                              that a small kernel builds on the device (a prefix sum of
+                              (partition, kv head) items per sequence) from a device counter;
+                              each sequence gets its own partition size, the fewest partitions of
+                              at most partition_size tokens evened out to whole blocks; then the
+                              log-sum-exp reduce.  The host never reads the lengths, so the call
+                              is graph-safe.  The workspace also holds the work list and the
+                              counter (num_seqs + 2 ints, rewritten by every call) */
 };
 
 /* Option flags. */
@@ -137,7 +138,8 @@ typedef struct {
     void* event_partition_begin; /* optional cudaEvent_t recorded on `stream` right before ... */
     void* event_partition_end;   /* ... and right after the partition kernel (timing only) */
     int warps;                   /* partition CTA shape: warps per CTA and shared-memory stages per */
-    int stages;                  /* warp; 0/0 = library choice; compiled: 2x2, 1x2, 1x3, 4x2 */
+    int stages;                  /* warp; 0/0 = library choice; compiled: 2x2, 1x2, 1x3, 4x2
+                                    (PERSISTENT: 1x2, 2x2, 4x2; default 1x2) */
 } pa_decode_opts;
 
 /* What a call will launch (filled by pa_decode_plan; host-only, no CUDA calls). */
