@@ -5,7 +5,8 @@ A step is one decode call over the whole batch: the partition kernel and the
 log-sum-exp reduce, through the library's C ABI, with q, the K/V pool, the
 block tables and the sequence lengths already resident in HBM.  The default
 workload is the 100K-token long-context decode: batch 1, seq_len 102400
-(200 partitions of 512), 24 query / 4 kv heads, head_dim 256, block_size 16,
+(the library's plan: one wave of 38 partitions x 4 kv heads), 24 query /
+4 kv heads, head_dim 256, block_size 16,
 fp16 N(0,1) data, scale 1/16; its 419 MB of K/V exceed the 129 MB L2, so
 back-to-back steps read from HBM.
 
@@ -46,10 +47,10 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic_partition_b1_l102400.j
 KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_308_gb300", "csrc", "pa_kernels.cu")
 
 WORKLOAD_TEXT = {
-    "b1_l2048": "batch 1, seq_len 2048, heads 24/4, head_dim 256, block_size 16, partition 512",
+    "b1_l2048": "batch 1, seq_len 2048, heads 24/4, head_dim 256, block_size 16",
     "b8_u8192": "batch 8, seq_lens uniform [1, 8192], heads 24/4, head_dim 256, block_size 16, pool 8192 blocks",
-    "b4_l32768_peaked": "batch 4, seq_len 32768, 1% of keys x8, heads 24/4, head_dim 256, block_size 16, partition 512",
-    "b1_l102400": "batch 1, seq_len 102400 (200 partitions of 512), heads 24/4, head_dim 256, block_size 16",
+    "b4_l32768_peaked": "batch 4, seq_len 32768, 1% of keys x8, heads 24/4, head_dim 256, block_size 16",
+    "b1_l102400": "batch 1, seq_len 102400, heads 24/4, head_dim 256, block_size 16",
     "b64_loguniform": "batch 64, seq_lens log-uniform [16, 65536], heads 24/4, head_dim 256, block_size 16, "
                       "pool 98304 blocks",
 }
@@ -345,7 +346,7 @@ def run_gpu(args):
     part_s = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
     achieved = kv / part_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(args.workload), "kernel": "pa_partition_kernel<256>",
+                "traffic": profiled_traffic(args.workload), "kernel": f"pa_partition_kernel<{w.head_dim}, {plan['threads'] // 32}, {plan['stages']}>",
                 "algorithmic_bytes_per_launch": kv, "launch_us": part_s * 1e6,
                 "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)"}
 
