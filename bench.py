@@ -162,7 +162,8 @@ def aggregate_gbs(bytes_per_step: int, steps: int, world: int, elapsed_max: floa
 def kernel_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_308_gb300", "csrc")
-    for p in (KERNEL_SRC, os.path.join(csrc, "pa_device.cuh"), os.path.join(csrc, "pa_internal.h")):
+    for p in (KERNEL_SRC, os.path.join(csrc, "pa_partition_block.cuh"), os.path.join(csrc, "pa_device.cuh"),
+              os.path.join(csrc, "pa_internal.h")):
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

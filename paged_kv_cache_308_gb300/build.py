@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpa_decode.so")
-SOURCES = ["pa_kernels.cu", "pa_prefix.cu", "pa_api.cpp", "pa_noalloc.cu"]
+SOURCES = ["pa_kernels.cu", "pa_persistent.cu", "pa_prefix.cu", "pa_api.cpp", "pa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -336,6 +336,8 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.work_offsets = persistent ? reinterpret_cast<const int*>(w + partial_bytes) : nullptr;
     prm.work_counter = persistent ? reinterpret_cast<int*>(w + partial_bytes) + a->num_seqs + 1 : nullptr;
     prm.num_seqs = a->num_seqs;
+    prm.status = persistent ? pa::device_status_ptr() : nullptr;
+    if (persistent && !prm.status) return PA_ERR_CUDA;
     prm.num_blocks = a->num_blocks;
     prm.num_heads = a->num_heads;
     prm.num_kv_heads = a->num_kv_heads;

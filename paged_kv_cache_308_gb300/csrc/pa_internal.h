@@ -71,6 +71,9 @@ struct PartitionParams {
     const int* work_offsets;
     int* work_counter;
     int num_seqs;
+    // Device status word (PA_DEV_* bits) for kernels compiled outside
+    // pa_kernels.cu, where the word itself is defined.
+    unsigned int* status;
 };
 
 struct ReduceParams {
