@@ -7,7 +7,9 @@ exit): start-up, streaming and epilogue times, CTAs per SM, and how many CTAs
 are resident / streaming over the launch.  The default library is rebuilt
 afterwards.
 
-    python -m paged_kv_cache_308_gb300.timeline b1_l102400:512 [name:partition ...]
+    python -m paged_kv_cache_308_gb300.timeline b1_l102400:512 [name:partition[:warps:stages] ...]
+
+A partition of 0 takes the library's own plan.
 """
 from __future__ import annotations
 
@@ -19,11 +21,11 @@ import numpy as np
 import torch
 
 
-def _analyse(pb, W, name: str, partition: int, out=print):
+def _analyse(pb, W, name: str, partition: int, warps: int = 0, stages: int = 0, out=print):
     dev = torch.device("cuda:0")
     w = W.make_config(name, device=dev)
     res = torch.empty_like(w.q)
-    opt = dict(mode="split", partition_size=partition)
+    opt = dict(mode="split", partition_size=partition, warps=warps, stages=stages) if partition else dict()
     plan = pb.pa_decode_plan(res, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
                              w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len, **opt)
     ncta = plan["grid_x"] * plan["grid_y"] * plan["grid_z"]
@@ -41,7 +43,7 @@ def _analyse(pb, W, name: str, partition: int, out=print):
     sm, t0 = t[:, 0], t[:, 1].min()
     e, f, l, x = [(t[:, k] - t0) / 1e3 for k in (1, 2, 3, 4)]
     q = lambda a: np.percentile(a, [0, 10, 50, 90, 100]).round(2).tolist()
-    out(f"== {name} P={partition}, CTA {plan['threads'] // 32} warp(s) x {plan['stages']} stages: "
+    out(f"== {name} P={plan['partition_size']}, CTA {plan['threads'] // 32} warp(s) x {plan['stages']} stages: "
         f"{len(t)} working CTAs of {ncta}; span {x.max():.2f} us = {w.kv_bytes / x.max() / 1e3:.0f} GB/s in-kernel")
     out(f"  start-up (entry -> first block)  us, pct 0/10/50/90/100: {q(f - e)}")
     out(f"  streaming (first block -> loop end): {q(l - f)}")
@@ -63,8 +65,9 @@ def main(argv):
         from . import binding as pb
         from . import workloads as W
         for spec in (argv or ["b1_l102400:512"]):
-            name, partition = spec.split(":")
-            _analyse(pb, W, name, int(partition))
+            name, *rest = spec.split(":")
+            nums = [int(v) for v in rest] + [0] * (3 - len(rest))
+            _analyse(pb, W, name, *nums[:3])
     finally:
         build.build(force=True)
 
