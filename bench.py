@@ -206,9 +206,60 @@ def cpu_baseline(w, budget_s: float):
         if el >= budget_s or (calls >= 1 and el * (calls + 1) / calls > 3 * budget_s):
             break
     gbs = w.kv_bytes * calls / el / 1e9
+    # the same oracle on one thread, over one call
+    t1 = time.perf_counter()
+    oracle.paged_decode(q, k, v, bt, sl, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, w.scale, threads=1)
+    el1 = time.perf_counter() - t1
     return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{calls} whole decode call(s) of {w.name} ({w.total_tokens} tokens, {w.num_heads} heads), "
-                      f"{el:.1f} s, float64, OpenMP over (seq, head) pairs"}, calls / el
+                      f"{el:.1f} s, float64, OpenMP over (seq, head) pairs",
+            "value_1_thread": w.kv_bytes / el1 / 1e9}, calls / el
+
+
+def flushed_latency_us(fn, stream, dev, n=50):
+    """Median device time of `n` single calls, each after a write of twice
+    the L2 size on the same stream, so every call starts from a cold L2."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size or (129 << 20)
+    scratch = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for e0, e1 in evs:
+        scratch.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    del scratch
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+
+
+def graph_calls_per_s(pb, w, dev, per_graph=20, replays=25):
+    """Calls/s with the calls captured once in a CUDA graph and replayed
+    (caller workspace, no allocation in the captured region)."""
+    out = torch.empty_like(w.q)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len)
+    ws = pb.alloc_workspace(plan, dev)
+
+    def call(s):
+        pb.pa_decode_ex(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
+                        w.head_dim, w.block_size, w.scale, s, max_seq_len=w.max_seq_len, workspace=ws)
+
+    call(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            call(torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(replays):
+        g.replay()
+    e1.record(s)
+    e1.synchronize()
+    return per_graph * replays / (e0.elapsed_time(e1) / 1e3)
 
 
 def time_steps(fn, steps, stream):
@@ -424,6 +475,10 @@ def run_gpu(args):
            "ms_per_step": e2e_el / e2e_steps * 1e3,
            "pipelining": "step i's copies overlap step i-1's call (2 buffer sets, separate copy streams)"}
 
+    # single-call latency from a cold L2 (median of 50) and CUDA-graph-replayed calls/s
+    lat_flushed = flushed_latency_us(step, stream, dev)
+    graph_cps = graph_calls_per_s(pb, w, dev)
+
     per_config = None
     if args.all_configs and rank == 0:
         per_config = {}
@@ -444,7 +499,9 @@ def run_gpu(args):
                                 "GB_per_s": wc.kv_bytes * n / el / 1e9,
                                 "pct_of_hbm_peak": 100 * wc.kv_bytes * n / el / 1e9 / peak,
                                 "calls_per_s": n / el, "tokens_per_s": wc.num_seqs * n / el,
-                                "l2": "larger than L2" if wc.kv_bytes > 129e6 else "fits in L2 (warm)"}
+                                "l2": "larger than L2" if wc.kv_bytes > 129e6 else "fits in L2 (warm)",
+                                "latency_us_l2_flushed": flushed_latency_us(fn, stream, dev),
+                                "graph_calls_per_s": graph_calls_per_s(pb, wc, dev)}
             del wc, oc
             torch.cuda.empty_cache()
         # chunked prefill over the paged cache (both kernels), TFLOP/s
@@ -473,6 +530,8 @@ def run_gpu(args):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "latency_us_l2_flushed": lat_flushed,
+            "graph_calls_per_s": graph_cps,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
