@@ -548,16 +548,23 @@ __global__ void __maxnreg__(kTcMaxRegs)
             // is visible; otherwise mask per key
             const bool full_ctx = 4 * j + 3 < nctx - (C % kBlockSize != 0 ? 1 : 0);
             if (!full_ctx) {
+                // visible slots of each 16-key block of the tile for this row:
+                // a context block shows its keys below C, a chunk block the
+                // chunk tokens up to the row's own; then one compare per key
+                // against its (compile-time) slot
+                int nvis[4];
+#pragma unroll
+                for (int qb = 0; qb < 4; ++qb) {
+                    const int blk = 4 * j + qb;
+                    const int n = blk < nctx ? C - blk * kBlockSize : my_tok + 1 - (blk - nctx) * kBlockSize;
+                    nvis[qb] = min(max(n, 0), kBlockSize);
+                }
+                const uint32_t hidden = __float_as_uint(sl2 >= 0.f ? -INFINITY : INFINITY);
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int col = h2 * 32 + c;
-                        const int blk = 4 * j + (col >> 4), slot = col & 15;
-                        const bool vis = blk < nctx ? blk * kBlockSize + slot < C
-                                                    : ((blk - nctx) * kBlockSize + slot <= my_tok);
-                        if (!vis) sv[h2][c] = __float_as_uint(sl2 >= 0.f ? -INFINITY : INFINITY);
-                    }
+                    for (int c = 0; c < 32; ++c)
+                        if (((h2 * 32 + c) & 15) >= nvis[(h2 * 32 + c) >> 4]) sv[h2][c] = hidden;
             }
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
