@@ -139,6 +139,20 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         : "memory");
 }
 
+// Two such loads (64 columns, e.g. two 32-column chunks) in flight under one
+// wait::ld.
+__device__ __forceinline__ void tc_ld32x2(uint32_t taddr0, uint32_t (&v)[32], uint32_t taddr1, uint32_t (&w)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : PA_TC_REGS32(v), PA_TC_REGS32(w)
+        : "r"(taddr0), "r"(taddr1)
+        : "memory");
+}
+
 // The matching store, also waited for in the same statement: tcgen05.st reads
 // its source registers until tcgen05.wait::st, so they must not be reused
 // before it.
@@ -513,19 +527,25 @@ __global__ void __maxnreg__(kTcMaxRegs)
         // Q row (token my_tok, head kvh * G + t % G) into TMEM columns tQ..,
         // two halves per column; rows that do not exist hold zeros
         {
+            // two 32-column chunks (16 loads) in flight per round: the row
+            // arrives in D / 128 round trips instead of D / 64
             const uint4* qrow = reinterpret_cast<const uint4*>(prm.q + ((size_t)(q0 + my_tok) * H + kvh * G + t % G) * D);
+            constexpr int kPer = D / 2 >= 64 ? 2 : 1;  // chunks per round
 #pragma unroll 1
-            for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                uint32_t v[32];
+            for (int c0 = 0; c0 < D / 2; c0 += 32 * kPer) {
+                uint32_t v[kPer][32];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint4 x = row_real ? __ldg(qrow + c0 / 4 + u) : make_uint4(0u, 0u, 0u, 0u);
-                    v[4 * u] = x.x;
-                    v[4 * u + 1] = x.y;
-                    v[4 * u + 2] = x.z;
-                    v[4 * u + 3] = x.w;
-                }
-                tc_st32(tQ + lane_off + c0, v);
+                for (int h = 0; h < kPer; ++h)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint4 x = row_real ? __ldg(qrow + (c0 + 32 * h) / 4 + u) : make_uint4(0u, 0u, 0u, 0u);
+                        v[h][4 * u] = x.x;
+                        v[h][4 * u + 1] = x.y;
+                        v[h][4 * u + 2] = x.z;
+                        v[h][4 * u + 3] = x.w;
+                    }
+#pragma unroll
+                for (int h = 0; h < kPer; ++h) tc_st32(tQ + lane_off + c0 + 32 * h, v[h]);
             }
             tc_fence_before();
             __syncwarp();
@@ -538,8 +558,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
             tc_fence_after();
             if (t == 0) PA_TC_MARK(j, 5);
             uint32_t sv[2][32];
-            tc_ld32(tS + lane_off, sv[0]);
-            tc_ld32(tS + lane_off + 32, sv[1]);
+            tc_ld32x2(tS + lane_off, sv[0], tS + lane_off + 32, sv[1]);
             // S(j) is in registers: the score buffer may take S(j+1)
             tc_fence_before();
             __syncwarp();
@@ -637,21 +656,24 @@ __global__ void __maxnreg__(kTcMaxRegs)
             // O / l to fp16 for the rows that exist
             const float inv = 1.f / l;
             __half* orow = prm.out + ((size_t)(q0 + my_tok) * H + kvh * G + (t % G)) * D;
+            // two 32-column chunks per wait::ld
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t ov[32];
-                tc_ld32(tO + lane_off + c0, ov);
+            for (int c0 = 0; c0 < D; c0 += 64) {
+                uint32_t ov[2][32];
+                tc_ld32x2(tO + lane_off + c0, ov[0], tO + lane_off + c0 + 32, ov[1]);
                 if (row_real) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 8) {
-                        uint4 w;
-                        uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+                    for (int h = 0; h < 2; ++h)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            wp[e] = half2_bits(__floats2half2_rn(__uint_as_float(ov[c + 2 * e]) * inv,
-                                                                 __uint_as_float(ov[c + 2 * e + 1]) * inv));
-                        *reinterpret_cast<uint4*>(orow + c0 + c) = w;
-                    }
+                        for (int c = 0; c < 32; c += 8) {
+                            uint4 w;
+                            uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                wp[e] = half2_bits(__floats2half2_rn(__uint_as_float(ov[h][c + 2 * e]) * inv,
+                                                                     __uint_as_float(ov[h][c + 2 * e + 1]) * inv));
+                            *reinterpret_cast<uint4*>(orow + c0 + 32 * h + c) = w;
+                        }
                 }
             }
         }
