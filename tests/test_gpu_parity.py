@@ -371,14 +371,16 @@ def test_persistent_schedule_empty_bad_and_graph(dev):
 
 @pytest.mark.parametrize("warps", [1, 2, 4])
 @pytest.mark.parametrize("P", [16, 64, 512])
-def test_persistent_many_items_per_cta(dev, warps, P):
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_persistent_many_items_per_cta(dev, warps, P, D):
     # small partitions give many more work items than resident CTAs, so each
     # CTA draws many items from the counter and its warps stream their blocks
     # across items and sequences through one ring each
     lens = [1, 17, 513, 3000, 100, 0, 2049, 16, 4000, 777] * 3
-    w = W.make_workload("pmany", lens, num_blocks=2100, seed=40 + warps, device=dev, tail_fill=float("nan"))
+    w = W.make_workload("pmany", lens, num_blocks=2100, seed=40 + warps, device=dev, tail_fill=float("nan"),
+                        head_dim=D, num_heads=24 if D == 256 else 16, num_kv_heads=4)
     out = run(w, mode="persistent", partition_size=P, warps=warps, stages=2)
-    assert_parity(out, oracle_ref(w), f"persistent P={P} warps={warps}")
+    assert_parity(out, oracle_ref(w), f"persistent P={P} warps={warps} D={D}")
     assert torch.count_nonzero(out[5]) == 0
     # which CTA draws which item changes from call to call; the bits do not
     assert torch.equal(out, run(w, mode="persistent", partition_size=P, warps=warps, stages=2))
