@@ -303,75 +303,23 @@ __global__ void __launch_bounds__(NW * 32, 1)
         return;
     }
 
-    // Merge the NW partial states of this CTA by the same max/rescale
-    // rule: warps 1.. leave theirs in shared memory, warp 0 folds them into its
-    // own MMA fragments with per-head factors and stores straight from registers.
-    float* red = reinterpret_cast<float*>(smem);  // [NW - 1][kMaxGroup][kRedStride]
-    if (warp > 0) {
-        float* rw = red + (warp - 1) * kMaxGroup * S::kRedStride;
-#pragma unroll
-        for (int mt = 0; mt < S::kSteps; ++mt) {
-            const int d = 16 * mt + g;
-            rw[(2 * c) * S::kRedStride + d] = o[mt][0];
-            rw[(2 * c + 1) * S::kRedStride + d] = o[mt][1];
-            rw[(2 * c) * S::kRedStride + d + 8] = o[mt][2];
-            rw[(2 * c + 1) * S::kRedStride + d + 8] = o[mt][3];
-        }
-        if (g == 0) {
-            sm_m[warp * kMaxGroup + 2 * c] = m0;
-            sm_m[warp * kMaxGroup + 2 * c + 1] = m1;
-            sm_l[warp * kMaxGroup + 2 * c] = l0;
-            sm_l[warp * kMaxGroup + 2 * c + 1] = l1;
-        }
-    }
-    __syncthreads();
     const bool fused = prm.tickets && n_part > 1;
-    if (warp != 0 && !fused) return;
-    if (warp == 0) {
-    // Per-head factors for heads 2c and 2c + 1: M = max over warps,
-    // f_w = 2^(m_w - M) / L with L = sum_w 2^(m_w - M) l_w (warps without
-    // blocks have m_w = -inf and contribute nothing).
-    float M0 = m0, M1 = m1;
-#pragma unroll
-    for (int w = 1; w < NW; ++w) {
-        M0 = fmaxf(M0, sm_m[w * kMaxGroup + 2 * c]);
-        M1 = fmaxf(M1, sm_m[w * kMaxGroup + 2 * c + 1]);
-    }
-    float f0[NW], f1[NW];
-    f0[0] = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
-    f1[0] = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
-    float L0 = f0[0] * l0, L1 = f1[0] * l1;
-#pragma unroll
-    for (int w = 1; w < NW; ++w) {
-        const float mw0 = sm_m[w * kMaxGroup + 2 * c], mw1 = sm_m[w * kMaxGroup + 2 * c + 1];
-        f0[w] = mw0 == -INFINITY ? 0.f : exp2f(mw0 - M0);
-        f1[w] = mw1 == -INFINITY ? 0.f : exp2f(mw1 - M1);
-        L0 += f0[w] * sm_l[w * kMaxGroup + 2 * c];
-        L1 += f1[w] * sm_l[w * kMaxGroup + 2 * c + 1];
-    }
-    const float inv0 = 1.f / L0, inv1 = 1.f / L1;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-        f0[w] *= inv0;
-        f1[w] *= inv1;
-    }
+    const bool direct = n_part == 1;
+    if constexpr (NW == 1) {
+    // One warp: the output is its own state, o / l, stored from the MMA
+    // fragments (lane (g, c) holds heads 2c, 2c + 1).  A partition whose
+    // blocks all had illegal ids (m = -inf) was reported above.
+    const float w0 = m0 == -INFINITY ? 0.f : 1.f, w1 = m1 == -INFINITY ? 0.f : 1.f;
+    const float L0 = w0 * l0, L1 = w1 * l1;
+    const float f0 = w0 * (1.f / L0), f1 = w1 * (1.f / L1);
     const bool has0 = 2 * c < G, has1 = 2 * c + 1 < G;  // padding heads are not written
     const size_t head0 = (size_t)b * H + kvh * G + 2 * c;
-    const bool direct = n_part == 1;
     const size_t pi0 = head0 * prm.max_partitions + p, pi1 = pi0 + prm.max_partitions;
 #pragma unroll
     for (int mt = 0; mt < S::kSteps; ++mt) {
         const int d = 16 * mt + g;
-        float v00 = f0[0] * o[mt][0], v10 = f1[0] * o[mt][1];  // (head 2c, d), (head 2c+1, d)
-        float v08 = f0[0] * o[mt][2], v18 = f1[0] * o[mt][3];  // ... at d + 8
-#pragma unroll
-        for (int w = 1; w < NW; ++w) {
-            const float* rw = red + (w - 1) * kMaxGroup * S::kRedStride;
-            v00 += f0[w] * rw[(2 * c) * S::kRedStride + d];
-            v10 += f1[w] * rw[(2 * c + 1) * S::kRedStride + d];
-            v08 += f0[w] * rw[(2 * c) * S::kRedStride + d + 8];
-            v18 += f1[w] * rw[(2 * c + 1) * S::kRedStride + d + 8];
-        }
+        const float v00 = f0 * o[mt][0], v10 = f1 * o[mt][1];  // (head 2c, d), (head 2c+1, d)
+        const float v08 = f0 * o[mt][2], v18 = f1 * o[mt][3];  // ... at d + 8
         if (direct) {
             if (has0) {
                 prm.out[head0 * D + d] = __float2half_rn(v00);
@@ -394,12 +342,82 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
     if (!direct && g == 0) {
         if (has0) {
-            prm.max_logits[pi0] = M0;
+            prm.max_logits[pi0] = m0;
             prm.exp_sums[pi0] = L0;
         }
         if (has1) {
-            prm.max_logits[pi1] = M1;
+            prm.max_logits[pi1] = m1;
             prm.exp_sums[pi1] = L1;
+        }
+    }
+    } else {
+    // Merge the NW partial states of this CTA by the same max/rescale rule.
+    // Every warp leaves (m, l, O) in shared memory; then warp w merges dims
+    // [w D/NW, (w+1) D/NW) of every head: lane (h, q) = (lane / 4, lane % 4)
+    // takes head h and the dim pairs 2q, 2q + 1 of each 8-dim group, so a
+    // head's stores are contiguous.  The sums run in warp order, as in the
+    // one-warp form, so the bits do not depend on which warp merges.
+    float* red = reinterpret_cast<float*>(smem);  // [NW][kMaxGroup][kRedStride]
+    {
+        float* rw = red + warp * kMaxGroup * S::kRedStride;
+#pragma unroll
+        for (int mt = 0; mt < S::kSteps; ++mt) {
+            const int d = 16 * mt + g;
+            rw[(2 * c) * S::kRedStride + d] = o[mt][0];
+            rw[(2 * c + 1) * S::kRedStride + d] = o[mt][1];
+            rw[(2 * c) * S::kRedStride + d + 8] = o[mt][2];
+            rw[(2 * c + 1) * S::kRedStride + d + 8] = o[mt][3];
+        }
+        if (g == 0) {
+            sm_m[warp * kMaxGroup + 2 * c] = m0;
+            sm_m[warp * kMaxGroup + 2 * c + 1] = m1;
+            sm_l[warp * kMaxGroup + 2 * c] = l0;
+            sm_l[warp * kMaxGroup + 2 * c + 1] = l1;
+        }
+    }
+    __syncthreads();
+    constexpr int kSlice = D / NW;  // dims merged by one warp
+    static_assert(kSlice % 8 == 0, "a warp merges whole 8-dim groups");
+    const int h = lane >> 2, qd = lane & 3;
+    if (h < G) {  // padding heads are not written
+        // M = max over warps, f_w = 2^(m_w - M) / L, L = sum_w 2^(m_w - M) l_w
+        // (warps without blocks have m_w = -inf and contribute nothing)
+        float Mh = sm_m[h];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) Mh = fmaxf(Mh, sm_m[w * kMaxGroup + h]);
+        float f[NW];
+        f[0] = sm_m[h] == -INFINITY ? 0.f : exp2f(sm_m[h] - Mh);
+        float Lh = f[0] * sm_l[h];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) {
+            const float mw = sm_m[w * kMaxGroup + h];
+            f[w] = mw == -INFINITY ? 0.f : exp2f(mw - Mh);
+            Lh += f[w] * sm_l[w * kMaxGroup + h];
+        }
+        const float inv = 1.f / Lh;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) f[w] *= inv;
+        const size_t head = (size_t)b * H + kvh * G + h;
+        const size_t pi = head * prm.max_partitions + p;
+#pragma unroll
+        for (int k = 0; k < kSlice / 8; ++k) {
+            const int d = warp * kSlice + 8 * k + 2 * qd;
+            const float* r0 = red + h * S::kRedStride + d;
+            float v0 = f[0] * r0[0], v1 = f[0] * r0[1];
+#pragma unroll
+            for (int w = 1; w < NW; ++w) {
+                const float* rw = red + (w * kMaxGroup + h) * S::kRedStride + d;
+                v0 += f[w] * rw[0];
+                v1 += f[w] * rw[1];
+            }
+            if (direct)
+                *reinterpret_cast<__half2*>(prm.out + head * D + d) = __floats2half2_rn(v0, v1);
+            else
+                *reinterpret_cast<float2*>(prm.tmp_out + pi * D + d) = make_float2(v0, v1);
+        }
+        if (!direct && warp == 0 && qd == 0) {
+            prm.max_logits[pi] = Mh;
+            prm.exp_sums[pi] = Lh;
         }
     }
     }
