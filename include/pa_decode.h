@@ -90,13 +90,14 @@ enum {
                            (sequence, kv head) that must be zero before the first call on it;
                            every call leaves the tickets zero, also after a device error */
     PA_MODE_PERSISTENT = 4 /* a fixed grid of (SMs x CTAs per SM) takes the items of a work list
-                              that a small kernel builds on the device (a prefix sum of
-                              (partition, kv head) items per sequence) from a device counter;
-                              each sequence gets its own partition size, the fewest partitions of
+                              that a small kernel builds on the device from a device counter,
+                              longest partitions first.  Each sequence gets its own partition size:
+                              with partition_size 0 the grid's partitions are apportioned over the
+                              batch by length (one wave when it fits), else the fewest partitions of
                               at most partition_size tokens evened out to whole blocks; then the
-                              log-sum-exp reduce.  The host never reads the lengths, so the call
-                              is graph-safe.  The workspace also holds the work list and the
-                              counter (num_seqs + 2 ints, rewritten by every call) */
+                              log-sum-exp reduce.  The host never reads the lengths, so the call is
+                              graph-safe.  The workspace also holds the work list, the counter,
+                              the order and the sizes (rewritten by every call) */
 };
 
 /* Option flags. */
@@ -139,13 +140,15 @@ typedef struct {
     void* event_partition_end;   /* ... and right after the partition kernel (timing only) */
     int warps;                   /* partition CTA shape: warps per CTA and shared-memory stages per */
     int stages;                  /* warp; 0/0 = library choice; compiled: 2x2, 1x2, 1x3, 4x2
-                                    (PERSISTENT: 1x2, 2x2, 4x2; default 1x2) */
+                                    (PERSISTENT: 1x2, 2x2, 4x2; default 4x2, or 1x2 with a
+                                    partition_size) */
 } pa_decode_opts;
 
 /* What a call will launch (filled by pa_decode_plan; host-only, no CUDA calls). */
 typedef struct {
     int mode;              /* PA_MODE_SINGLE, PA_MODE_SPLIT, PA_MODE_FUSED or PA_MODE_PERSISTENT */
-    int partition_size;    /* tokens per CTA (SINGLE: max_seq_len rounded up to block_size) */
+    int partition_size;    /* tokens per CTA (SINGLE: max_seq_len rounded up to block_size;
+                              PERSISTENT: 0 = apportioned per sequence on the device) */
     int grid_x, grid_y, grid_z;          /* partition kernel: partitions, kv heads, sequences
                                             (PERSISTENT: the fixed grid, 1, 1) */
     int threads;           /* threads per partition CTA */

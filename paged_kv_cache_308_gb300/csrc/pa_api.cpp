@@ -22,7 +22,9 @@ namespace {
 
 constexpr int kDefaultPartition = 512;
 constexpr int kOneWaveMinPartition = 2048;  // see make_plan
-constexpr int kPersistentWarps = 1, kPersistentStages = 2;  // PA_MODE_PERSISTENT CTA shape
+// PA_MODE_PERSISTENT CTA shapes: 4 x 2 when the scan apportions the partitions
+// (about one item per CTA), 1 x 2 for a caller's partition size (many items)
+constexpr int kPersistentWarps = 4, kPersistentWarpsFixedSize = 1, kPersistentStages = 2;
 constexpr int kMaxDevices = 64;
 constexpr size_t kWsAlign = 256;
 
@@ -222,8 +224,9 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     plan->grid_y = a->num_kv_heads;
     plan->grid_z = a->num_seqs;
     int warps = o ? o->warps : 0, stages = o ? o->stages : 0;
+    const bool apportion = mode == PA_MODE_PERSISTENT && !(o && o->partition_size > 0);
     if (mode == PA_MODE_PERSISTENT) {
-        if (!warps) warps = kPersistentWarps;
+        if (!warps) warps = apportion ? kPersistentWarps : kPersistentWarpsFixedSize;
         if (!stages) stages = kPersistentStages;
     } else if (one_wave) {
         warps = 4;
@@ -244,6 +247,14 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         if (per_sm < 1) per_sm = 1;
         plan->grid_x = (int)(per_sm * num_sms);
         plan->grid_y = plan->grid_z = 1;
+        if (apportion) {
+            // partitions per kv head shared out over the batch: about one wave
+            plan->partition_size = 0;
+            plan->max_partitions = plan->grid_x / a->num_kv_heads > 1 ? plan->grid_x / a->num_kv_heads : 1;
+        }
+        // the work list holds at most num_seqs * (max_partitions + 1) * num_kv_heads items
+        if ((long long)a->num_seqs * (plan->max_partitions + 1) * a->num_kv_heads >= (1ll << 31))
+            return PA_ERR_UNSUPPORTED;
     }
     plan->launch_reduce =
         ((mode == PA_MODE_SPLIT || mode == PA_MODE_PERSISTENT) && plan->max_partitions > 1) ? 1 : 0;
@@ -256,9 +267,10 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         plan->reduce_grid_z = a->head_dim / reduce_slice(a->head_dim, (long long)a->num_seqs * a->num_heads, num_sms);
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim);
     }
-    if (mode == PA_MODE_PERSISTENT)  // + the work list and the item counter
+    if (mode == PA_MODE_PERSISTENT)  // + the work list and item counter, the order, the partition sizes
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim) +
-                                align_up(static_cast<size_t>(a->num_seqs + 2) * 4, kWsAlign);
+                                align_up(static_cast<size_t>(a->num_seqs + 2) * 4, kWsAlign) +
+                                2 * align_up(static_cast<size_t>(a->num_seqs) * 4, kWsAlign);
     return PA_OK;
 }
 
@@ -333,8 +345,16 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.exp_sums = partials ? reinterpret_cast<float*>(w + align_up(rows * 4, kWsAlign)) : nullptr;
     prm.tmp_out = partials ? reinterpret_cast<float*>(w + 2 * align_up(rows * 4, kWsAlign)) : nullptr;
     prm.tickets = fused ? reinterpret_cast<unsigned int*>(w + partial_bytes) : nullptr;
-    prm.work_offsets = persistent ? reinterpret_cast<const int*>(w + partial_bytes) : nullptr;
-    prm.work_counter = persistent ? reinterpret_cast<int*>(w + partial_bytes) + a->num_seqs + 1 : nullptr;
+    // persistent schedule tables after the partials: work list + counter, order, partition sizes
+    int* list = persistent ? reinterpret_cast<int*>(w + partial_bytes) : nullptr;
+    int* order = persistent ? reinterpret_cast<int*>(w + partial_bytes +
+                                                     align_up(static_cast<size_t>(a->num_seqs + 2) * 4, kWsAlign))
+                            : nullptr;
+    int* parts = persistent ? order + align_up(static_cast<size_t>(a->num_seqs) * 4, kWsAlign) / 4 : nullptr;
+    prm.work_offsets = list;
+    prm.work_counter = persistent ? list + a->num_seqs + 1 : nullptr;
+    prm.seq_order = order;
+    prm.part_sizes = parts;
     prm.num_seqs = a->num_seqs;
     prm.status = persistent ? pa::device_status_ptr() : nullptr;
     if (persistent && !prm.status) return PA_ERR_CUDA;
@@ -354,14 +374,17 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     if (persistent) {
         pa::ScanParams sp;
         sp.seq_lens = a->seq_lens;
-        sp.work_offsets = reinterpret_cast<int*>(w + partial_bytes);
+        sp.work_offsets = list;
+        sp.seq_order = order;
+        sp.part_sizes = parts;
+        sp.work_counter = list + a->num_seqs + 1;
         sp.num_seqs = a->num_seqs;
         sp.max_seq_len = a->max_seq_len;
         sp.max_blocks_per_seq = a->max_blocks_per_seq;
-        sp.partition_size = plan.partition_size;
         sp.num_kv_heads = a->num_kv_heads;
-        sp.work_counter = reinterpret_cast<int*>(w + partial_bytes) + a->num_seqs + 1;
         sp.first_dynamic = plan.grid_x;
+        sp.partition_size = plan.partition_size;  // 0: apportion max_partitions per kv head
+        sp.slots = plan.max_partitions;
         if (pa::launch_work_scan(sp, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
     if (o && o->event_partition_begin &&
@@ -388,7 +411,7 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
         rp.max_seq_len = a->max_seq_len;
         rp.partition_size = plan.partition_size;
         rp.max_partitions = plan.max_partitions;
-        rp.balanced = persistent ? 1 : 0;
+        rp.part_sizes = parts;
         if (pa::launch_reduce(a->head_dim, a->head_dim / plan.reduce_grid_z, rp,
                               dim3(plan.reduce_grid_x, plan.reduce_grid_y, plan.reduce_grid_z), stream) != cudaSuccess)
             return PA_ERR_CUDA;

@@ -16,10 +16,10 @@ constexpr int kReduceThreads = 256;
 constexpr int kReduceMinSlice = 32;  // narrowest head_dim slice of a reduce CTA
 constexpr unsigned kDefaultWaitLimit = 1u << 20;
 
-// Partition size of a sequence of L tokens in the persistent schedule: the
-// fewest partitions of at most `pmax` tokens, evened out and rounded up to
-// whole blocks (so every partition is non-empty).  Host and device use the
-// same rule; the partition count is (L + size - 1) / size.
+// Partition size of a sequence of L tokens in the persistent schedule with a
+// given partition size `pmax`: the fewest partitions of at most pmax tokens,
+// evened out and rounded up to whole blocks (so every partition is
+// non-empty).  The partition count is (L + size - 1) / size.
 __host__ __device__ inline int balanced_partition(int L, int pmax) {
     if (L <= 0) return pmax;
     const int n = (L + pmax - 1) / pmax;
@@ -27,21 +27,29 @@ __host__ __device__ inline int balanced_partition(int L, int pmax) {
     return ((even + kBlockSize - 1) / kBlockSize) * kBlockSize;
 }
 
-// Work items of one sequence in the persistent schedule: an invalid length
-// gets one (to report it), an empty sequence one per kv head (to zero its
-// output), otherwise one per (partition, kv head).
-__host__ __device__ inline int work_items(int L, int max_seq_len, int max_blocks_per_seq, int pmax, int num_kv_heads) {
-    if (L < 0 || L > max_seq_len || L > max_blocks_per_seq * kBlockSize) return 1;
-    if (L == 0) return num_kv_heads;
-    const int part = balanced_partition(L, pmax);
-    return ((L + part - 1) / part) * num_kv_heads;
+// Partition size of a sequence of L tokens when the persistent schedule
+// apportions `slots` partitions per kv head over a batch whose valid lengths
+// sum to T: n = slots * L / T partitions, rounded down when the batch's
+// rounded-down counts (each at least one) fit in the slots -- one wave of the
+// grid -- and rounded up otherwise (many short sequences: no item longer
+// than the average work of a CTA); at least one, at most slots and at most
+// one per block.  The partition count is (L + size - 1) / size <= slots.
+__host__ __device__ inline int apportioned_partition(int L, long long T, int slots, bool round_up) {
+    long long n = 1;
+    if (T > 0) n = round_up ? ((long long)slots * L + T - 1) / T : ((long long)slots * L) / T;
+    const long long max_n = slots < (L + kBlockSize - 1) / kBlockSize ? slots : (L + kBlockSize - 1) / kBlockSize;
+    if (n > max_n) n = max_n;
+    if (n < 1) n = 1;
+    const int even = (int)((L + n - 1) / n);
+    return ((even + kBlockSize - 1) / kBlockSize) * kBlockSize;
 }
 
 // Batches of at most this many sequences keep the persistent schedule's work
-// list and lengths in each CTA's shared memory (these extra bytes).
+// list, order, lengths and partition sizes in each CTA's shared memory (these
+// extra bytes).
 constexpr int kPersistentSeqCache = 256;
 inline int persistent_seq_cache_bytes(int num_seqs) {
-    return num_seqs <= kPersistentSeqCache ? ((2 * num_seqs + 1) * 4 + 15) / 16 * 16 : 0;
+    return num_seqs <= kPersistentSeqCache ? ((4 * num_seqs + 1) * 4 + 15) / 16 * 16 : 0;
 }
 
 struct PartitionParams {
@@ -65,10 +73,13 @@ struct PartitionParams {
     // Fused combine: one ticket per (sequence, kv head), zero before the call
     // and left zero after it; null when a separate reduce kernel merges.
     unsigned int* tickets;
-    // Persistent schedule: exclusive prefix sums of work_items over the
-    // sequences (num_seqs + 1 entries) and the next item to hand out; null
-    // for one CTA per grid cell.
+    // Persistent schedule: the sequences in schedule order (seq_order), the
+    // exclusive prefix sums of their work items in that order (num_seqs + 1
+    // entries), each sequence's partition size, and the next item to hand
+    // out; null for one CTA per grid cell.
     const int* work_offsets;
+    const int* seq_order;
+    const int* part_sizes;
     int* work_counter;
     int num_seqs;
     // Device status word (PA_DEV_* bits) for kernels compiled outside
@@ -84,14 +95,18 @@ struct ReduceParams {
     const int32_t* seq_lens;
     int num_heads, max_blocks_per_seq, max_seq_len;
     int partition_size, max_partitions;
-    int balanced;  // per-sequence partition sizes of the persistent schedule
+    const int* part_sizes;  // per-sequence partition sizes (persistent schedule), else null
 };
 
 struct ScanParams {
     const int32_t* seq_lens;
-    int* work_offsets;  // [num_seqs + 1]
+    int* work_offsets;  // [num_seqs + 1], over the schedule order
+    int* seq_order;     // [num_seqs]: schedule position -> sequence
+    int* part_sizes;    // [num_seqs]: partition size of each sequence
     int* work_counter;  // set to first_dynamic (the persistent grid size)
-    int num_seqs, max_seq_len, max_blocks_per_seq, partition_size, num_kv_heads, first_dynamic;
+    int num_seqs, max_seq_len, max_blocks_per_seq, num_kv_heads, first_dynamic;
+    int partition_size;  // > 0: balanced_partition with this size
+    int slots;           // else apportioned_partition with this many partitions per kv head
 };
 
 // Dynamic shared memory of a partition CTA of `warps` warps with `stages`
@@ -108,7 +123,8 @@ cudaError_t launch_partition(int head_dim, int warps, int stages, const Partitio
 // reduce CTA (32, 64, 128 or 256, at most head_dim).
 cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3 grid, cudaStream_t stream);
 
-// The persistent schedule's work list: one CTA scans the sequences' item counts.
+// The persistent schedule's work list: one CTA sizes the partitions, orders the
+// sequences longest partition first and sums their item counts.
 cudaError_t launch_work_scan(const ScanParams& prm, cudaStream_t stream);
 
 // Persistent schedule: `grid` CTAs of `warps` warps take the items of the

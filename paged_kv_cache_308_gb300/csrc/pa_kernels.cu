@@ -445,9 +445,10 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
     const int h = blockIdx.x, b = blockIdx.y, slice = blockIdx.z;
     const int L = prm.seq_lens[b];
     // single-partition, empty and invalid sequences were finished by the partition kernel
-    if (L <= prm.partition_size || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) return;
-    const int part = prm.balanced ? balanced_partition(L, prm.partition_size) : prm.partition_size;
+    if (L <= 0 || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) return;
+    const int part = prm.part_sizes ? prm.part_sizes[b] : prm.partition_size;
     const int n = (L + part - 1) / part;
+    if (n <= 1) return;
     const size_t base = ((size_t)b * prm.num_heads + h) * prm.max_partitions;
     const float* ml = prm.max_logits + base;
     const float* el = prm.exp_sums + base;

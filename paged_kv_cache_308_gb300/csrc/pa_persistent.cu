@@ -13,16 +13,18 @@
 namespace pa {
 
 // ---------------------------------------------------------------------------
-// Persistent schedule (PA_MODE_PERSISTENT).  pa_work_scan_kernel writes, per
-// sequence, the exclusive prefix sum of its work items (work_items: one per
-// (partition, kv head), one per kv head for an empty sequence, one for an
-// invalid length) and resets the item counter.  A fixed grid of NW-warp CTAs
-// (every CTA the SMs hold at once) takes items from that counter: CTA x
-// starts with item x and then draws the next index with atomicAdd, so the
-// last items end within about one item of each other whatever the length
-// mix.  Sequence b of L tokens is cut into partitions of
-// balanced_partition(L, P) tokens, the fewest of at most P evened out to
-// whole blocks.
+// Persistent schedule (PA_MODE_PERSISTENT).  pa_work_scan_kernel sizes each
+// sequence's partitions, orders the sequences longest partition first and
+// writes the exclusive prefix sums of their work items in that order (one
+// item per (partition, kv head), one per kv head for an empty sequence, one
+// for an invalid length), then resets the item counter.  Without a caller's
+// partition size, the partitions are apportioned: a batch whose lengths sum
+// to T gives sequence b floor(slots * L_b / T) partitions (at least one),
+// slots = grid / kv heads, so the items fill about one wave of the grid.
+// A fixed grid of NW-warp CTAs (every CTA the SMs hold at once) takes items
+// from that counter: CTA x starts with item x and then draws the next index
+// with atomicAdd, so the last items -- the shortest, by the order -- end
+// within about one item of each other.
 //
 // Inside a CTA, warp w takes blocks w, w + NW, ... of every item, and its
 // blocks form ONE stream across the CTA's items: stream position g uses the
@@ -46,26 +48,33 @@ struct PersistentItem {
     bool bad;
 };
 
-// `offs` and `lens` are the work list and the lengths, in shared memory when
-// the CTA cached them (persistent_seq_cache_bytes), else in global memory.
-__device__ __forceinline__ PersistentItem persistent_item(const PartitionParams& prm, const int* offs,
-                                                          const int* lens, int i) {
+// The schedule's tables (work list over the schedule order, the order, the
+// lengths and the partition sizes), in shared memory when the CTA cached them
+// (persistent_seq_cache_bytes), else in global memory.
+struct ScheduleTables {
+    const int* offs;
+    const int* order;
+    const int* lens;
+    const int* parts;
+};
+
+__device__ __forceinline__ PersistentItem persistent_item(const PartitionParams& prm, const ScheduleTables& tb, int i) {
     int lo = 0, hi = prm.num_seqs;  // offs[lo] <= i < offs[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (offs[mid] <= i)
+        if (tb.offs[mid] <= i)
             lo = mid;
         else
             hi = mid;
     }
     PersistentItem it;
-    const int r = i - offs[lo];
-    it.b = lo;
+    const int r = i - tb.offs[lo];
+    it.b = tb.order[lo];
     it.p = r / prm.num_kv_heads;
     it.kvh = r % prm.num_kv_heads;
-    it.L = lens[lo];
+    it.L = tb.lens[it.b];
     it.bad = it.L < 0 || it.L > prm.max_seq_len || it.L > prm.max_blocks_per_seq * kBlockSize;
-    it.part = balanced_partition(it.L, prm.partition_size);
+    it.part = tb.parts[it.b];
     it.nblk = 0;
     if (!it.bad && it.L > 0) {
         const int bpp = it.part / kBlockSize;
@@ -119,15 +128,18 @@ __global__ void __launch_bounds__(NW * 32, 1)
     // Items are located by binary search over the work list, on the copy
     // side and again at the start of each item's math: from shared memory
     // when the batch is small enough to cache.
-    const int* offs = prm.work_offsets;
-    const int* lens = prm.seq_lens;
+    ScheduleTables tb{prm.work_offsets, prm.seq_order, prm.seq_lens, prm.part_sizes};
     if (prm.num_seqs <= kPersistentSeqCache) {
+        const int B = prm.num_seqs;
         int* so = reinterpret_cast<int*>(smem + Q::kSmemBytes - 1024);
-        int* sl = so + prm.num_seqs + 1;
-        for (int x = threadIdx.x; x <= prm.num_seqs; x += blockDim.x) so[x] = __ldg(prm.work_offsets + x);
-        for (int x = threadIdx.x; x < prm.num_seqs; x += blockDim.x) sl[x] = __ldg(prm.seq_lens + x);
-        offs = so;
-        lens = sl;
+        int *sr = so + B + 1, *sl = sr + B, *sp = sl + B;
+        for (int x = threadIdx.x; x <= B; x += blockDim.x) so[x] = __ldg(prm.work_offsets + x);
+        for (int x = threadIdx.x; x < B; x += blockDim.x) {
+            sr[x] = __ldg(prm.seq_order + x);
+            sl[x] = __ldg(prm.seq_lens + x);
+            sp[x] = __ldg(prm.part_sizes + x);
+        }
+        tb = ScheduleTables{so, sr, sl, sp};
     }
     const int total = __ldg(prm.work_offsets + prm.num_seqs);
 
@@ -161,7 +173,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
             if (is_k > known) return;
             const int I = items[is_k & 3];
             if (I >= total) return;
-            const PersistentItem it = persistent_item(prm, offs, lens, I);
+            const PersistentItem it = persistent_item(prm, tb, I);
             is_nblk = it.nblk;
             is_kvh = it.kvh;
             is_j = warp;
@@ -204,7 +216,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     for (int k = 0;; ++k) {
         const int I = items[k & 3];
         if (I >= total) break;  // the same for every warp
-        const PersistentItem it = persistent_item(prm, offs, lens, I);
+        const PersistentItem it = persistent_item(prm, tb, I);
         // thread 0 draws the index of item k + 2 now; it is published at this item's barrier
         int drawn = total;
         if (threadIdx.x == 0 && items[(k + 1) & 3] < total) drawn = atomicAdd(prm.work_counter, 1);
@@ -423,7 +435,8 @@ cudaError_t launch_persistent_t(const PartitionParams& prm, const CUtensorMap& t
 
 cudaError_t launch_partition_persistent(int head_dim, int warps, int stages, const PartitionParams& prm,
                                         const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t stream) {
-    if (!prm.work_offsets || !prm.work_counter || grid <= 0) return cudaErrorInvalidValue;
+    if (!prm.work_offsets || !prm.work_counter || !prm.seq_order || !prm.part_sizes || grid <= 0)
+        return cudaErrorInvalidValue;
 #define PA_PLAUNCH_CASE(W_, S_)                                                              \
     if (warps == W_ && stages == S_) {                                                      \
         switch (head_dim) {                                                                 \
@@ -438,26 +451,37 @@ cudaError_t launch_partition_persistent(int head_dim, int warps, int stages, con
     return cudaErrorInvalidValue;
 }
 
-// Exclusive prefix sums of the per-sequence work items (one CTA of 1024
-// threads; each thread sums a contiguous run of sequences, then the runs are
-// scanned across the block).
+// The work list of the persistent schedule, built by one CTA of 1024 threads
+// (thread x handles a contiguous run of sequences):
+//  1. T = the sum of the valid lengths, and whether the rounded-down
+//     apportioned counts fit one wave (block reductions);
+//  2. each sequence's partition size (apportioned_partition over T, or
+//     balanced_partition with the caller's size) and item count: one per
+//     (partition, kv head), one per kv head for an empty sequence (its output
+//     is zeroed), one for an invalid length (it is reported);
+//  3. the schedule order: a counting sort of the sequences by partition
+//     length in blocks, longest first (empty and invalid ones last), so the
+//     items handed out last are the shortest; the order within a length is
+//     whatever the atomics give, which changes only which CTA takes an item,
+//     never a result;
+//  4. the exclusive prefix sums of the item counts in that order, and the item
+//     counter reset to the grid size.
 constexpr int kScanThreads = 1024;
-__global__ void __launch_bounds__(kScanThreads) pa_work_scan_kernel(const ScanParams prm) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;");
-    __shared__ int warp_sums[kScanThreads / 32];
-    const int per = (prm.num_seqs + kScanThreads - 1) / kScanThreads;
-    const int b0 = threadIdx.x * per, b1 = min(prm.num_seqs, b0 + per);
-    int local = 0;
-    for (int b = b0; b < b1; ++b)
-        local += work_items(__ldg(prm.seq_lens + b), prm.max_seq_len, prm.max_blocks_per_seq, prm.partition_size,
-                            prm.num_kv_heads);
+constexpr int kOrderKeys = 1024;  // partition lengths in blocks, the longest clamped
+static_assert(kOrderKeys == kScanThreads, "one key per thread in the key scan");
+
+__device__ __forceinline__ bool scan_valid(const ScanParams& prm, int L) {
+    return L >= 0 && L <= prm.max_seq_len && L <= prm.max_blocks_per_seq * kBlockSize;
+}
+
+// Block-wide exclusive scan of one int per thread (kScanThreads threads).
+__device__ __forceinline__ int scan_block_exclusive(int v, int* warp_sums, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = local;
+    int incl = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(kFull, incl, off);
-        if (lane >= off) incl += v;
+        const int u = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += u;
     }
     if (lane == 31) warp_sums[warp] = incl;
     __syncthreads();
@@ -465,20 +489,103 @@ __global__ void __launch_bounds__(kScanThreads) pa_work_scan_kernel(const ScanPa
         int w = warp_sums[lane];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(kFull, w, off);
-            if (lane >= off) w += v;
+            const int u = __shfl_up_sync(kFull, w, off);
+            if (lane >= off) w += u;
         }
         warp_sums[lane] = w;  // inclusive over warps
     }
     __syncthreads();
-    int run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);  // exclusive start of this thread's run
+    const int excl = incl - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    if (total) *total = warp_sums[kScanThreads / 32 - 1];
+    __syncthreads();  // warp_sums may be reused by the caller
+    return excl;
+}
+
+__global__ void __launch_bounds__(kScanThreads) pa_work_scan_kernel(const ScanParams prm) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ int cursor[kOrderKeys];  // per key: count, then next rank
+    __shared__ int warp_sums[kScanThreads / 32];
+    __shared__ unsigned long long s_total, s_floor_parts;
+    const int B = prm.num_seqs;
+    const int per = (B + kScanThreads - 1) / kScanThreads;
+    const int b0 = threadIdx.x * per, b1 = min(B, b0 + per);
+    for (int x = threadIdx.x; x < kOrderKeys; x += kScanThreads) cursor[x] = 0;
+    if (threadIdx.x == 0) s_total = s_floor_parts = 0;
+    __syncthreads();
+
+    // 1. the sum of the valid lengths
+    unsigned long long mine = 0;
     for (int b = b0; b < b1; ++b) {
-        prm.work_offsets[b] = run;
-        run += work_items(__ldg(prm.seq_lens + b), prm.max_seq_len, prm.max_blocks_per_seq, prm.partition_size,
-                          prm.num_kv_heads);
+        const int L = __ldg(prm.seq_lens + b);
+        if (scan_valid(prm, L)) mine += (unsigned long long)L;
     }
-    if (threadIdx.x == kScanThreads - 1) {
-        prm.work_offsets[prm.num_seqs] = warp_sums[kScanThreads / 32 - 1];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(kFull, mine, off);
+    if ((threadIdx.x & 31) == 0 && mine) atomicAdd(&s_total, mine);
+    __syncthreads();
+    const long long T = (long long)s_total;
+    // the rounded-down partition counts (at least one each): do they fit one wave?
+    bool round_up = false;
+    if (prm.partition_size <= 0) {
+        unsigned long long fl = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int L = __ldg(prm.seq_lens + b);
+            if (scan_valid(prm, L) && L > 0) {
+                const int part = apportioned_partition(L, T, prm.slots, false);
+                fl += (unsigned long long)((L + part - 1) / part);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) fl += __shfl_xor_sync(kFull, fl, off);
+        if ((threadIdx.x & 31) == 0 && fl) atomicAdd(&s_floor_parts, fl);
+        __syncthreads();
+        round_up = s_floor_parts > (unsigned long long)prm.slots;
+    }
+
+    // 2. partition sizes, item counts, sort keys (bucket 0 = the longest)
+    auto key_of = [&](int L, int part) {
+        if (!scan_valid(prm, L) || L == 0) return kOrderKeys - 1;
+        return kOrderKeys - 1 - min(part / kBlockSize, kOrderKeys - 1);
+    };
+    for (int b = b0; b < b1; ++b) {
+        const int L = __ldg(prm.seq_lens + b);
+        int part = kBlockSize;
+        if (scan_valid(prm, L) && L > 0)
+            part = prm.partition_size > 0 ? balanced_partition(L, prm.partition_size)
+                                          : apportioned_partition(L, T, prm.slots, round_up);
+        prm.part_sizes[b] = part;
+        atomicAdd(&cursor[key_of(L, part)], 1);
+    }
+    __syncthreads();
+
+    // 3. the first rank of each key, then every sequence's rank
+    const int first = scan_block_exclusive(cursor[threadIdx.x], warp_sums, nullptr);
+    cursor[threadIdx.x] = first;
+    __syncthreads();
+    for (int b = b0; b < b1; ++b) {
+        const int L = __ldg(prm.seq_lens + b);
+        const int part = prm.part_sizes[b];
+        const int rank = atomicAdd(&cursor[key_of(L, part)], 1);
+        int items = 1;  // an invalid length: one item reports it
+        if (scan_valid(prm, L)) items = L == 0 ? prm.num_kv_heads : ((L + part - 1) / part) * prm.num_kv_heads;
+        prm.seq_order[rank] = b;
+        prm.work_offsets[rank] = items;  // turned into prefix sums below
+    }
+    __syncthreads();  // the block's global writes are visible to all its threads
+
+    // 4. exclusive prefix sums over the schedule order, in place
+    int local = 0;
+    for (int r = b0; r < b1; ++r) local += prm.work_offsets[r];
+    int total = 0;
+    int run = scan_block_exclusive(local, warp_sums, &total);
+    for (int r = b0; r < b1; ++r) {
+        const int it = prm.work_offsets[r];
+        prm.work_offsets[r] = run;
+        run += it;
+    }
+    if (threadIdx.x == 0) {
+        prm.work_offsets[B] = total;
         *prm.work_counter = prm.first_dynamic;  // items below it are taken by CTA index
     }
 }

@@ -114,12 +114,18 @@ def test_plan_persistent_mode_has_a_fixed_grid_and_a_work_list():
     rc, pl = plan(a, mode=pb.PA_MODE_PERSISTENT)
     _, split = plan(a, mode=pb.PA_MODE_SPLIT)
     assert rc == 0 and pl["mode"] == pb.PA_MODE_PERSISTENT
-    assert pl["threads"] == 32 and pl["stages"] == 2 and pl["grid_y"] == pl["grid_z"] == 1
-    assert pl["grid_x"] == SMS * 6                      # every CTA the SMs hold at once (6 per SM)
-    assert pl["max_partitions"] == split["grid_x"] == 128 and pl["launch_reduce"] == 1
-    # + 65 ints of work list and the item counter, 256-aligned
-    assert pl["workspace_bytes"] == split["workspace_bytes"] + 512
-    for w, s, per_sm in ((4, 2, 1), (2, 2, 2)):
+    # apportioned partitions: 4-warp CTAs, one per SM; at most SMs / kv heads partitions per sequence
+    assert pl["threads"] == 128 and pl["stages"] == 2 and pl["grid_y"] == pl["grid_z"] == 1
+    assert pl["grid_x"] == SMS and pl["partition_size"] == 0
+    assert pl["max_partitions"] == SMS // 4 == 38 and pl["launch_reduce"] == 1
+    # + the work list with the item counter (66 ints), the order and the partition sizes (64 ints each)
+    assert pl["workspace_bytes"] == ws_bytes(64, 24, 38, 256) + 512 + 256 + 256
+    # a caller's partition size: that size per sequence, balanced, on one-warp CTAs (6 per SM)
+    rc, fixed = plan(a, mode=pb.PA_MODE_PERSISTENT, partition_size=512)
+    assert rc == 0 and fixed["threads"] == 32 and fixed["grid_x"] == SMS * 6 and fixed["partition_size"] == 512
+    assert fixed["max_partitions"] == split["grid_x"] == 128
+    assert fixed["workspace_bytes"] == split["workspace_bytes"] + 512 + 256 + 256
+    for w, s, per_sm in ((1, 2, 6), (2, 2, 2)):
         o = pb.make_opts(mode="persistent", warps=w, stages=s)
         p2 = pb.pa_decode_plan_t()
         assert pb.lib.pa_decode_plan(ctypes.byref(a), ctypes.byref(o), SMS, ctypes.byref(p2)) == 0
