@@ -186,8 +186,8 @@ int pa_decode_plan(const pa_decode_args* args, const pa_decode_opts* opts, int n
 
 /* Workspace bytes of a SPLIT call with these sizes; partition_size 0 gives an upper
  * bound for the automatic partition size.  FUSED needs 256-byte-aligned
- * num_seqs * num_kv_heads * 4 bytes more, PERSISTENT 256-byte-aligned (num_seqs + 1) * 4;
- * pa_decode_plan gives every mode's exact figure. */
+ * num_seqs * num_kv_heads * 4 bytes more; PERSISTENT has its own partition count and
+ * tables (work list, order, sizes).  pa_decode_plan gives every mode's exact figure. */
 size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim,
                                 int partition_size);
 
