@@ -265,8 +265,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
             l0 += __shfl_xor_sync(kFull, l0, off);
             l1 += __shfl_xor_sync(kFull, l1, off);
         }
-        const int merger = k % NW, buf = k & 1;
-        if (warp != merger && warp < it.nblk) {
+        const int buf = k & 1;
+        if (NW > 1 && warp < it.nblk) {  // warps with blocks leave (m, l, O) in merge area buf
             float* rw = red + (buf * NW + warp) * kMaxGroup * S::kRedStride;
 #pragma unroll
             for (int mt = 0; mt < S::kSteps; ++mt) {
@@ -288,104 +288,120 @@ __global__ void __launch_bounds__(NW * 32, 1)
         if (*sm_abort) break;  // the same for every warp
         // top the copies up to NS ahead: item k + 2 is known now
         for (int x = 0; x < NS && issued - pos < (uint32_t)NS; ++x) issue_next(k + 2);
-        if (warp != merger) continue;
 
-        // ---- merger warp: item k's output ----
+        // ---- item k's output ----
         if (it.bad) {
-            if (lane == 0) atomicOr(prm.status, PA_DEV_BAD_SEQ_LEN);
+            if (warp == 0 && lane == 0) atomicOr(prm.status, PA_DEV_BAD_SEQ_LEN);
             continue;
         }
         if (it.L == 0) {  // empty sequence: its G heads of this kv head are zero
-            for (int x = lane; x < G * D; x += 32)
+            for (int x = threadIdx.x; x < G * D; x += NW * 32)
                 prm.out[((size_t)it.b * H + it.kvh * G) * D + x] = __float2half_rn(0.f);
             continue;
         }
         if (it.nblk == 0) continue;
-        // warps w < nw streamed blocks; the merger's own state is in registers,
-        // the others' in merge area `buf`.  M = max m_w, f_w = 2^(m_w - M) / L
-        // with L = sum_w 2^(m_w - M) l_w, summed in warp order.
-        const int nw = min(NW, it.nblk);
-        const float* sm = st_m + buf * NW * kMaxGroup;
-        const float* sl = st_l + buf * NW * kMaxGroup;
-        float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            if (w >= nw) continue;
-            M0 = fmaxf(M0, w == merger ? m0 : sm[w * kMaxGroup + 2 * c]);
-            M1 = fmaxf(M1, w == merger ? m1 : sm[w * kMaxGroup + 2 * c + 1]);
-        }
-        float f0[NW], f1[NW];
-        float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            f0[w] = f1[w] = 0.f;
-            if (w >= nw) continue;
-            const float mw0 = w == merger ? m0 : sm[w * kMaxGroup + 2 * c];
-            const float mw1 = w == merger ? m1 : sm[w * kMaxGroup + 2 * c + 1];
-            f0[w] = mw0 == -INFINITY ? 0.f : exp2f(mw0 - M0);
-            f1[w] = mw1 == -INFINITY ? 0.f : exp2f(mw1 - M1);
-            L0 += f0[w] * (w == merger ? l0 : sl[w * kMaxGroup + 2 * c]);
-            L1 += f1[w] * (w == merger ? l1 : sl[w * kMaxGroup + 2 * c + 1]);
-        }
-        const float inv0 = 1.f / L0, inv1 = 1.f / L1;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            f0[w] *= inv0;
-            f1[w] *= inv1;
-        }
         const int n_part = (it.L + it.part - 1) / it.part;
-        const bool has0 = 2 * c < G, has1 = 2 * c + 1 < G;  // padding heads are not written
-        const size_t head0 = (size_t)it.b * H + it.kvh * G + 2 * c;
         const bool direct = n_part == 1;
-        const size_t pi0 = head0 * prm.max_partitions + it.p, pi1 = pi0 + prm.max_partitions;
+        if constexpr (NW == 1) {
+            // one warp: o / l straight from the MMA fragments (lane (g, c)
+            // holds heads 2c, 2c + 1); a partition whose blocks all had
+            // illegal ids (m = -inf) was reported when they were copied
+            const float w0 = m0 == -INFINITY ? 0.f : 1.f, w1 = m1 == -INFINITY ? 0.f : 1.f;
+            const float L0 = w0 * l0, L1 = w1 * l1;
+            const float f0 = w0 * (1.f / L0), f1 = w1 * (1.f / L1);
+            const bool has0 = 2 * c < G, has1 = 2 * c + 1 < G;  // padding heads are not written
+            const size_t head0 = (size_t)it.b * H + it.kvh * G + 2 * c;
+            const size_t pi0 = head0 * prm.max_partitions + it.p, pi1 = pi0 + prm.max_partitions;
 #pragma unroll
-        for (int mt = 0; mt < S::kSteps; ++mt) {
-            const int d = 16 * mt + g;
-            float v00 = 0.f, v10 = 0.f, v08 = 0.f, v18 = 0.f;  // (head 2c, d), (2c+1, d), then d + 8
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                if (w >= nw) continue;
-                if (w == merger) {
-                    v00 += f0[w] * o[mt][0];
-                    v10 += f1[w] * o[mt][1];
-                    v08 += f0[w] * o[mt][2];
-                    v18 += f1[w] * o[mt][3];
+            for (int mt = 0; mt < S::kSteps; ++mt) {
+                const int d = 16 * mt + g;
+                const float v00 = f0 * o[mt][0], v10 = f1 * o[mt][1], v08 = f0 * o[mt][2], v18 = f1 * o[mt][3];
+                if (direct) {
+                    if (has0) {
+                        prm.out[head0 * D + d] = __float2half_rn(v00);
+                        prm.out[head0 * D + d + 8] = __float2half_rn(v08);
+                    }
+                    if (has1) {
+                        prm.out[(head0 + 1) * D + d] = __float2half_rn(v10);
+                        prm.out[(head0 + 1) * D + d + 8] = __float2half_rn(v18);
+                    }
                 } else {
-                    const float* rw = red + (buf * NW + w) * kMaxGroup * S::kRedStride;
-                    v00 += f0[w] * rw[(2 * c) * S::kRedStride + d];
-                    v10 += f1[w] * rw[(2 * c + 1) * S::kRedStride + d];
-                    v08 += f0[w] * rw[(2 * c) * S::kRedStride + d + 8];
-                    v18 += f1[w] * rw[(2 * c + 1) * S::kRedStride + d + 8];
+                    if (has0) {
+                        prm.tmp_out[pi0 * D + d] = v00;
+                        prm.tmp_out[pi0 * D + d + 8] = v08;
+                    }
+                    if (has1) {
+                        prm.tmp_out[pi1 * D + d] = v10;
+                        prm.tmp_out[pi1 * D + d + 8] = v18;
+                    }
                 }
             }
-            if (direct) {
+            if (!direct && g == 0) {
                 if (has0) {
-                    prm.out[head0 * D + d] = __float2half_rn(v00);
-                    prm.out[head0 * D + d + 8] = __float2half_rn(v08);
+                    prm.max_logits[pi0] = m0;
+                    prm.exp_sums[pi0] = L0;
                 }
                 if (has1) {
-                    prm.out[(head0 + 1) * D + d] = __float2half_rn(v10);
-                    prm.out[(head0 + 1) * D + d + 8] = __float2half_rn(v18);
-                }
-            } else {
-                if (has0) {
-                    prm.tmp_out[pi0 * D + d] = v00;
-                    prm.tmp_out[pi0 * D + d + 8] = v08;
-                }
-                if (has1) {
-                    prm.tmp_out[pi1 * D + d] = v10;
-                    prm.tmp_out[pi1 * D + d + 8] = v18;
+                    prm.max_logits[pi1] = m1;
+                    prm.exp_sums[pi1] = L1;
                 }
             }
-        }
-        if (!direct && g == 0) {
-            if (has0) {
-                prm.max_logits[pi0] = M0;
-                prm.exp_sums[pi0] = L0;
-            }
-            if (has1) {
-                prm.max_logits[pi1] = M1;
-                prm.exp_sums[pi1] = L1;
+        } else {
+            // every warp merges dims [w D/NW, (w+1) D/NW) of every head from
+            // merge area buf (lane (h, q): head h, dim pairs 2q, 2q + 1 of each
+            // 8-dim group), summing in warp order over the nw warps that had
+            // blocks: M = max m_w, f_w = 2^(m_w - M) / L, L = sum_w 2^(m_w - M) l_w
+            constexpr int kSlice = D / NW;
+            static_assert(kSlice % 8 == 0, "a warp merges whole 8-dim groups");
+            const int nw = min(NW, it.nblk);
+            const float* sm = st_m + buf * NW * kMaxGroup;
+            const float* sl = st_l + buf * NW * kMaxGroup;
+            const float* rb = red + buf * NW * kMaxGroup * S::kRedStride;
+            const int h = lane >> 2, qd = lane & 3;
+            if (h < G) {  // padding heads are not written
+                float Mh = sm[h];
+#pragma unroll
+                for (int w = 1; w < NW; ++w)
+                    if (w < nw) Mh = fmaxf(Mh, sm[w * kMaxGroup + h]);
+                float f[NW];
+                f[0] = sm[h] == -INFINITY ? 0.f : exp2f(sm[h] - Mh);
+                float Lh = f[0] * sl[h];
+#pragma unroll
+                for (int w = 1; w < NW; ++w) {
+                    f[w] = 0.f;
+                    if (w < nw) {
+                        const float mw = sm[w * kMaxGroup + h];
+                        f[w] = mw == -INFINITY ? 0.f : exp2f(mw - Mh);
+                        Lh += f[w] * sl[w * kMaxGroup + h];
+                    }
+                }
+                const float inv = 1.f / Lh;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) f[w] *= inv;
+                const size_t head = (size_t)it.b * H + it.kvh * G + h;
+                const size_t pi = head * prm.max_partitions + it.p;
+#pragma unroll
+                for (int kk = 0; kk < kSlice / 8; ++kk) {
+                    const int d = warp * kSlice + 8 * kk + 2 * qd;
+                    const float* r0 = rb + h * S::kRedStride + d;
+                    float v0 = f[0] * r0[0], v1 = f[0] * r0[1];
+#pragma unroll
+                    for (int w = 1; w < NW; ++w) {
+                        if (w < nw) {
+                            const float* rw = rb + (w * kMaxGroup + h) * S::kRedStride + d;
+                            v0 += f[w] * rw[0];
+                            v1 += f[w] * rw[1];
+                        }
+                    }
+                    if (direct)
+                        *reinterpret_cast<__half2*>(prm.out + head * D + d) = __floats2half2_rn(v0, v1);
+                    else
+                        *reinterpret_cast<float2*>(prm.tmp_out + pi * D + d) = make_float2(v0, v1);
+                }
+                if (!direct && warp == 0 && qd == 0) {
+                    prm.max_logits[pi] = Mh;
+                    prm.exp_sums[pi] = Lh;
+                }
             }
         }
     }
