@@ -165,6 +165,19 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32])
         : "memory");
 }
 
+// Two such stores (two 32-column chunks) under one wait::st.
+__device__ __forceinline__ void tc_st32x2(uint32_t taddr0, const uint32_t (&v)[32], uint32_t taddr1,
+                                          const uint32_t (&w)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};\n\t"
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%1], {%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+        "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr0),
+        "r"(taddr1), PA_TC_IN32(v), PA_TC_IN32(w)
+        : "memory");
+}
+
 // Bounded wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, uint32_t limit, const volatile int* abort_flag) {
     for (uint32_t n = 0; n < limit; ++n) {
@@ -544,8 +557,10 @@ __global__ void __maxnreg__(kTcMaxRegs)
                         v[h][4 * u + 2] = x.z;
                         v[h][4 * u + 3] = x.w;
                     }
-#pragma unroll
-                for (int h = 0; h < kPer; ++h) tc_st32(tQ + lane_off + c0 + 32 * h, v[h]);
+                if constexpr (kPer == 2)
+                    tc_st32x2(tQ + lane_off + c0, v[0], tQ + lane_off + c0 + 32, v[1]);
+                else
+                    tc_st32(tQ + lane_off + c0, v[0]);
             }
             tc_fence_before();
             __syncwarp();
