@@ -291,6 +291,18 @@ __global__ void __maxnreg__(kTcMaxRegs)
     const int ntiles = (nblocks + 3) / 4;
     const int32_t* bt = prm.block_tables + (size_t)b * prm.max_blocks_per_seq;
 
+    // The row threads read their Q rows into registers after the setup
+    // below; start those rows on their way to L2 now, so the setup hides
+    // part of the first read's latency.
+    if (t < kTcRows) {
+        const int pti = t / G, ptok = t0 + pti;
+        if (pti < tile_tokens && ptok < qlen) {
+            const char* row = reinterpret_cast<const char*>(prm.q + ((size_t)(q0 + ptok) * H + kvh * G + t % G) * D);
+#pragma unroll
+            for (int x = 0; x < D * 2; x += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + x));
+        }
+    }
+
     if (t == 0) {
         *sm_abort = 0;
         for (int i = 0; i < kTcBars; ++i) {
