@@ -20,7 +20,9 @@ struct PrefixParams {
     int force_timeout;
     unsigned int* status;           // device status word (PA_DEV_* bits are OR-ed in)
     // Diagnostic builds (-DPA_TRACE) only: the tcgen05 kernel records
-    // SM clock stamps of its pipeline events, kPrefixTraceIters x 16 per CTA.
+    // SM clock stamps of its pipeline events, kPrefixTraceIters x 16 per CTA
+    // (the last of the kPrefixTraceIters records holds the CTA's phases in
+    // global-timer ns).
     unsigned long long* trace;
 };
 

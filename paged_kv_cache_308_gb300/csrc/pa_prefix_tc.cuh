@@ -202,14 +202,34 @@ __device__ __forceinline__ float tc_ex2(float x) {  // the PTX ex2.approx instru
 #ifdef PA_TRACE
 #define PA_TC_MARK(j, e)                                                                                          \
     do {                                                                                                          \
-        if (prm.trace && (j) < kPrefixTraceIters) {                                                               \
+        if (prm.trace && (j) < kPrefixTraceIters - 1) {                                                           \
             const size_t cta_ = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;           \
             prm.trace[(cta_ * kPrefixTraceIters + (j)) * 16 + (e)] = (unsigned long long)clock64();              \
         }                                                                                                         \
     } while (0)
+// Per-CTA phases in global-timer ns, in the last record of the CTA: 0 entry,
+// 1 setup done, 2 Q in tensor memory (row thread 0), 3 tile loop done, 4 O
+// stored, 5 every role done, 7 the SM id.
+#define PA_TC_PHASE(e)                                                                                            \
+    do {                                                                                                          \
+        if (prm.trace && threadIdx.x == 0) {                                                                      \
+            const size_t cta_ = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;           \
+            unsigned long long g_;                                                                                \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g_));                                               \
+            prm.trace[(cta_ * kPrefixTraceIters + kPrefixTraceIters - 1) * 16 + (e)] = (e) == 7 ? smid_of() : g_; \
+        }                                                                                                         \
+    } while (0)
+__device__ __forceinline__ unsigned long long smid_of() {
+    unsigned s;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+    return s;
+}
 #else
 #define PA_TC_MARK(j, e) \
     do {                 \
+    } while (0)
+#define PA_TC_PHASE(e) \
+    do {               \
     } while (0)
 #endif
 
@@ -272,6 +292,8 @@ __global__ void __maxnreg__(kTcMaxRegs)
 
     const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    PA_TC_PHASE(0);
+    PA_TC_PHASE(7);
     const int G = prm.group, H = prm.num_heads;
     const int tile_tokens = kTcRows / G;
 
@@ -322,6 +344,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    PA_TC_PHASE(1);
     const uint32_t tmem = *tslot;
     const uint32_t tO = tmem;                    // D columns
     const uint32_t tQ = tO + D;                  // D / 2 columns (fp16 pairs)
@@ -578,6 +601,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kTcBarQReady));
         }
+        PA_TC_PHASE(2);
         float m = -INFINITY, l = 0.f;  // reference max (scaled, log2 domain) and exp sum
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
@@ -669,6 +693,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
             if (t == 96) PA_TC_MARK(j, 7);
             if (lane == 0) mbar_arrive(bar(kTcBarPReady + (j & 1)));
         }
+        PA_TC_PHASE(3);
         // the last two P.Vs (one per P buffer) complete before O is read
         if (ok && ntiles >= 2)
             ok = tc_warp_wait(bar(kTcBarPVDone + ((ntiles - 2) & 1)), ((ntiles - 2) >> 1) & 1, limit, sm_abort);
@@ -705,8 +730,10 @@ __global__ void __maxnreg__(kTcMaxRegs)
             }
         }
     }
+    PA_TC_PHASE(4);
     tc_fence_before();
     __syncthreads();  // every role done: no copy or MMA in flight past this point
+    PA_TC_PHASE(5);
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(S::kTmemCols));
 }
 
