@@ -103,6 +103,24 @@ struct PersistentShape {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
 };
 
+// Diagnostic builds (-DPA_TRACE): per-CTA records in the decode timeline's
+// format {sm id, entry, first block ready, first item done, exit}
+// (global-timer ns).
+#ifdef PA_TRACE
+#define PA_PT_MARK(slot)                                                      \
+    do {                                                                      \
+        if (prm.trace && threadIdx.x == 0) {                                  \
+            unsigned long long g_;                                            \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g_));           \
+            prm.trace[(size_t)blockIdx.x * 5 + (slot)] = g_;                  \
+        }                                                                     \
+    } while (0)
+#else
+#define PA_PT_MARK(slot) \
+    do {                 \
+    } while (0)
+#endif
+
 template <int D, int NW, int NS>
 __global__ void __launch_bounds__(NW * 32, 1)
     pa_partition_persistent_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -112,6 +130,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
     // the work list and the item counter are written by the preceding (scan) grid
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+#ifdef PA_TRACE
+    if (prm.trace && threadIdx.x == 0) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        prm.trace[(size_t)blockIdx.x * 5] = smid;
+    }
+#endif
+    PA_PT_MARK(1);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -249,6 +275,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                     }
                     break;
                 }
+                if (k == 0 && j == warp) PA_PT_MARK(2);
                 if ((valid_bits >> s) & 1u) {
                     const uint32_t kst = stage0 + s * S::kStageBytes;
                     warp_block_update<D>(qb, o, m0, m1, l0, l1, kst, kst + S::kTileBytes,
@@ -283,6 +310,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 st_l[(buf * NW + warp) * kMaxGroup + 2 * c + 1] = l1;
             }
         }
+        if (k == 0) PA_PT_MARK(3);
         if (threadIdx.x == 0) items[(k + 2) & 3] = drawn;
         __syncthreads();
         if (*sm_abort) break;  // the same for every warp
@@ -407,6 +435,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
     // copies issued ahead of an abort complete before the CTA exits
     for (uint32_t x = pos; x < issued; ++x) mbar_wait(bar0 + 8 * (x % NS), (x / NS) & 1, kDefaultWaitLimit);
+    PA_PT_MARK(4);
 }
 
 // The persistent kernel's CTA shapes (warps, stages per warp).

@@ -9,7 +9,9 @@ afterwards.
 
     python -m paged_kv_cache_308_gb300.timeline b1_l102400:512 [name:partition[:warps:stages] ...]
 
-A partition of 0 takes the library's own plan.
+A partition of 0 takes the library's own plan; `name:persistent` runs the
+persistent schedule with its default plan (its "main loop done" is the end of
+the CTA's first item).
 """
 from __future__ import annotations
 
@@ -21,11 +23,13 @@ import numpy as np
 import torch
 
 
-def _analyse(pb, W, name: str, partition: int, warps: int = 0, stages: int = 0, out=print):
+def _analyse(pb, W, name: str, partition: int, warps: int = 0, stages: int = 0, out=print, persistent=False):
     dev = torch.device("cuda:0")
     w = W.make_config(name, device=dev)
     res = torch.empty_like(w.q)
     opt = dict(mode="split", partition_size=partition, warps=warps, stages=stages) if partition else dict()
+    if persistent:
+        opt = dict(mode="persistent")
     plan = pb.pa_decode_plan(res, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
                              w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len, **opt)
     ncta = plan["grid_x"] * plan["grid_y"] * plan["grid_z"]
@@ -39,7 +43,7 @@ def _analyse(pb, W, name: str, partition: int, warps: int = 0, stages: int = 0, 
     torch.cuda.synchronize()
     pb.lib.pa_debug_set_trace(None)
     t = buf.view(ncta, 5).cpu().numpy()
-    t = t[t[:, 4] > 0]
+    t = t[(t[:, 4] > 0) & (t[:, 2] > 0)]
     sm, t0 = t[:, 0], t[:, 1].min()
     e, f, l, x = [(t[:, k] - t0) / 1e3 for k in (1, 2, 3, 4)]
     q = lambda a: np.percentile(a, [0, 10, 50, 90, 100]).round(2).tolist()
@@ -66,6 +70,9 @@ def main(argv):
         from . import workloads as W
         for spec in (argv or ["b1_l102400:512"]):
             name, *rest = spec.split(":")
+            if rest == ["persistent"]:
+                _analyse(pb, W, name, 0, persistent=True)
+                continue
             nums = [int(v) for v in rest] + [0] * (3 - len(rest))
             _analyse(pb, W, name, *nums[:3])
     finally:
