@@ -334,12 +334,15 @@ def time_e2e(pb, w, stream, dev, steps, nbuf=2):
     end.record(stream)
     end.synchronize()
     torch.cuda.synchronize()
-    # the pipelined calls give the same bits as a plain call on the resident inputs
+    # the pipelined calls agree with a plain call on the resident inputs (to
+    # the rounding of the partial sums: a pooled plan's partials cover
+    # timing-dependent blocks)
     ref = torch.empty_like(w.q)
     pb.pa_decode(ref, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
                  w.head_dim, w.block_size, w.scale, stream, max_seq_len=w.max_seq_len)
     torch.cuda.synchronize()
-    if not torch.equal(h_out[(count[0] - 1) % nbuf], ref.cpu()):
+    got, want = h_out[(count[0] - 1) % nbuf].float(), ref.cpu().float()
+    if not bool(((got - want).abs() <= 2e-3 + 1e-2 * want.abs()).all()):
         raise RuntimeError("pipelined end-to-end output differs from the direct call")
     return (start.elapsed_time(end) / 1e3, steps, h_in.numel(), h_out[0].numel() * 2)
 

@@ -104,8 +104,23 @@ enum {
 enum {
     PA_FLAG_FORCE_TIMEOUT = 1,   /* test hook: every copy wait gives up before its first poll; the
                                     kernel then drains its copies, sets PA_DEV_TIMEOUT and returns */
-    PA_FLAG_PREFIX_WARP_MMA = 2  /* pa_prefix_ex: use the warp-level MMA kernel instead of the
+    PA_FLAG_PREFIX_WARP_MMA = 2, /* pa_prefix_ex: use the warp-level MMA kernel instead of the
                                     tcgen05 (tensor-memory) one */
+    PA_FLAG_POOLED = 4,          /* SPLIT: the partition CTAs of a (sequence, kv head) share its
+                                    blocks in chunks of max(2, stages) blocks: each warp takes three
+                                    chunks round-robin, then claims the next from a device counter,
+                                    so CTAs on faster SMs take more and all finish together.  Same
+                                    partials and reduce as SPLIT, but which blocks a partial covers
+                                    depends on timing, so results may differ between calls in the
+                                    last bits.  Applies when the plan is SPLIT with partition_size
+                                    >= warps * 16 * max(2, stages) tokens (plan.pooled).  The
+                                    workspace also holds one 8-byte counter per (sequence, kv head)
+                                    after the partials; any initial value is safe (a counter the
+                                    reduce kernel has not armed keeps the round-robin).  The
+                                    planner's one-wave plan for one long sequence is pooled
+                                    without this flag */
+    PA_FLAG_DETERMINISTIC = 8    /* never pool (not even the one-wave plan): each partial covers
+                                    fixed blocks, so repeated calls give identical bits */
 };
 
 /* All inputs of one decode call (device pointers; see the layouts above). */
@@ -133,7 +148,8 @@ typedef struct {
     int partition_size;          /* tokens per partition in SPLIT mode, multiple of block_size; 0 = chosen
                                     by the planner: 512 (256 when that gives fewer CTAs than SMs; for
                                     one long sequence, as many partitions per kv head as SMs allow,
-                                    one wave of one 4-warp CTA per SM, when that exceeds 2048 tokens) */
+                                    one wave of one 4-warp CTA per SM, when that exceeds 2048 tokens;
+                                    that plan is pooled, see PA_FLAG_POOLED) */
     int flags;                   /* PA_FLAG_* */
     unsigned int wait_limit;     /* polls before a copy wait gives up; 0 = library default (2^20) */
     void* event_partition_begin; /* optional cudaEvent_t recorded on `stream` right before ... */
@@ -158,6 +174,7 @@ typedef struct {
     size_t workspace_bytes; /* caller workspace pa_decode_ex needs (0 when there are no partials) */
     int stages;            /* shared-memory stages per warp of the partition CTA */
     int max_partitions;    /* partials kept per (sequence, head) in the workspace */
+    int pooled;            /* 1 if the partition CTAs claim chunks of blocks (PA_FLAG_POOLED) */
 } pa_decode_plan_t;
 
 /* Decode attention with a library-owned workspace.

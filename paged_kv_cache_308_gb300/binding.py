@@ -40,6 +40,8 @@ MODES = {"auto": PA_MODE_AUTO, "single": PA_MODE_SINGLE, "split": PA_MODE_SPLIT,
 
 PA_FLAG_FORCE_TIMEOUT = 1
 PA_FLAG_PREFIX_WARP_MMA = 2
+PA_FLAG_POOLED = 4
+PA_FLAG_DETERMINISTIC = 8
 
 
 class pa_decode_args(ctypes.Structure):
@@ -66,7 +68,7 @@ class pa_decode_plan_t(ctypes.Structure):
         ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int), ("threads", ctypes.c_int),
         ("smem_bytes", ctypes.c_int), ("launch_reduce", ctypes.c_int), ("reduce_grid_x", ctypes.c_int),
         ("reduce_grid_y", ctypes.c_int), ("reduce_grid_z", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
-        ("stages", ctypes.c_int), ("max_partitions", ctypes.c_int),
+        ("stages", ctypes.c_int), ("max_partitions", ctypes.c_int), ("pooled", ctypes.c_int),
     ]
 
     def as_dict(self):
@@ -252,14 +254,17 @@ def pa_version() -> int:
     return lib.pa_version()
 
 
-def decode_workload(w, out: Optional[torch.Tensor] = None, stream=None, **opt) -> torch.Tensor:
-    """Run one decode call on a workloads.Workload (tensors already on the GPU)."""
+def decode_workload(w, out: Optional[torch.Tensor] = None, stream=None, workspace: Optional[torch.Tensor] = None,
+                    **opt) -> torch.Tensor:
+    """Run one decode call on a workloads.Workload (tensors already on the GPU).
+    With options, `workspace` (kept across calls, e.g. for the pooled split's
+    claim counters) replaces a fresh zeroed buffer."""
     if out is None:
         out = torch.empty_like(w.q)
     if opt:
         plan = pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
                               w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len, **opt)
-        ws = alloc_workspace(plan, w.q.device)
+        ws = workspace if workspace is not None else alloc_workspace(plan, w.q.device)
         if ws is not None and stream is not None:
             ws.record_stream(stream)  # keep the buffer alive until that stream's work is done
         pa_decode_ex(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,

@@ -258,6 +258,16 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     }
     plan->launch_reduce =
         ((mode == PA_MODE_SPLIT || mode == PA_MODE_PERSISTENT) && plan->max_partitions > 1) ? 1 : 0;
+    // Pooled: on request, and by default for the one-wave plan, where every
+    // CTA is resident from the start and the SMs' unequal shares of HBM
+    // bandwidth would otherwise set the finish (GB300, 102400 tokens: 66.8 ->
+    // 65.4 us per call; 262144: 158.5 -> 156.0).  Plans of several waves stay
+    // fixed: a later wave's CTAs would find only their first chunks left.
+    const int flags = o ? o->flags : 0;
+    const bool want_pool =
+        (flags & PA_FLAG_POOLED) || (one_wave && !(flags & PA_FLAG_DETERMINISTIC));
+    plan->pooled = want_pool && !(flags & PA_FLAG_DETERMINISTIC) && mode == PA_MODE_SPLIT && plan->launch_reduce &&
+                   plan->partition_size >= pa::pool_min_partition(warps, stages);
     if (mode == PA_MODE_FUSED)
         plan->workspace_bytes =
             fused_workspace_bytes(a->num_seqs, a->num_heads, a->num_kv_heads, plan->grid_x, a->head_dim);
@@ -267,6 +277,8 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         plan->reduce_grid_z = a->head_dim / reduce_slice(a->head_dim, (long long)a->num_seqs * a->num_heads, num_sms);
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim);
     }
+    if (plan->pooled)  // + the claim counters
+        plan->workspace_bytes += align_up(static_cast<size_t>(a->num_seqs) * a->num_kv_heads * 8, kWsAlign);
     if (mode == PA_MODE_PERSISTENT)  // + the work list and item counter, the order, the partition sizes
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim) +
                                 align_up(static_cast<size_t>(a->num_seqs + 2) * 4, kWsAlign) +
@@ -345,6 +357,7 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.exp_sums = partials ? reinterpret_cast<float*>(w + align_up(rows * 4, kWsAlign)) : nullptr;
     prm.tmp_out = partials ? reinterpret_cast<float*>(w + 2 * align_up(rows * 4, kWsAlign)) : nullptr;
     prm.tickets = fused ? reinterpret_cast<unsigned int*>(w + partial_bytes) : nullptr;
+    prm.claims = plan.pooled ? reinterpret_cast<unsigned long long*>(w + partial_bytes) : nullptr;
     // persistent schedule tables after the partials: work list + counter, order, partition sizes
     int* list = persistent ? reinterpret_cast<int*>(w + partial_bytes) : nullptr;
     int* order = persistent ? reinterpret_cast<int*>(w + partial_bytes +
@@ -412,6 +425,8 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
         rp.partition_size = plan.partition_size;
         rp.max_partitions = plan.max_partitions;
         rp.part_sizes = parts;
+        rp.claims = prm.claims;
+        rp.group = prm.group;
         if (pa::launch_reduce(a->head_dim, a->head_dim / plan.reduce_grid_z, rp,
                               dim3(plan.reduce_grid_x, plan.reduce_grid_y, plan.reduce_grid_z), stream) != cudaSuccess)
             return PA_ERR_CUDA;

@@ -44,6 +44,20 @@ __host__ __device__ inline int apportioned_partition(int L, long long T, int slo
     return ((even + kBlockSize - 1) / kBlockSize) * kBlockSize;
 }
 
+// Pooled split (PA_FLAG_POOLED): the blocks of a (sequence, kv head) are
+// dealt to the warps of its partition CTAs in chunks of pool_chunk(stages)
+// blocks (at least the copy depth, so the copies run at most one chunk
+// ahead); each warp takes three chunks round-robin and claims the rest from
+// a 64-bit counter whose high word must read kClaimTag (the reduce kernel
+// writes kClaimTag << 32 after every call).  Any other value -- a workspace
+// never used by a pooled call -- keeps every warp on the round-robin, which
+// needs no counter.  Every CTA has a chunk when the partition size is at
+// least warps * chunk * kBlockSize tokens.
+constexpr int kPoolChunk = 2;
+constexpr unsigned kClaimTag = 0x5a17c0deu;
+__host__ __device__ constexpr int pool_chunk(int stages) { return stages > kPoolChunk ? stages : kPoolChunk; }
+inline int pool_min_partition(int warps, int stages) { return warps * pool_chunk(stages) * kBlockSize; }
+
 // Batches of at most this many sequences keep the persistent schedule's work
 // list, order, lengths and partition sizes in each CTA's shared memory (these
 // extra bytes).
@@ -85,6 +99,9 @@ struct PartitionParams {
     // Device status word (PA_DEV_* bits) for kernels compiled outside
     // pa_kernels.cu, where the word itself is defined.
     unsigned int* status;
+    // Pooled split: one claim counter per (sequence, kv head); null for the
+    // fixed assignment of blocks to partitions.
+    unsigned long long* claims;
 };
 
 struct ReduceParams {
@@ -96,6 +113,10 @@ struct ReduceParams {
     int num_heads, max_blocks_per_seq, max_seq_len;
     int partition_size, max_partitions;
     const int* part_sizes;  // per-sequence partition sizes (persistent schedule), else null
+    // Pooled split: the claim counters to re-arm (kClaimTag << 32), one per
+    // (sequence, kv head); null otherwise.
+    unsigned long long* claims;
+    int group;  // query heads per kv head
 };
 
 struct ScanParams {
@@ -114,6 +135,7 @@ struct ScanParams {
 // -1 for a shape that is not compiled.
 int partition_smem_bytes(int head_dim, int warps, int stages);
 
+// prm.claims selects the pooled form of the kernel.
 cudaError_t launch_partition(int head_dim, int warps, int stages, const PartitionParams& prm,
                              const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, dim3 grid, cudaStream_t stream);
 

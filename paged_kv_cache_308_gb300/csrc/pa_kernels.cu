@@ -129,14 +129,44 @@ __device__ __forceinline__ void fused_combine(const PartitionParams& prm, int b,
     }
 }
 
-template <int D, int NW, int NS>
+// Pooled == false: CTA p takes the blocks of partition p, dealt round-robin
+// to its warps.  Pooled == true: the CTAs of a (sequence, kv head) share the
+// sequence's blocks in chunks of kPoolChunk; each warp starts with chunk
+// p * NW + w and claims further chunks from a device counter, so a warp on a
+// faster SM takes more of them and the CTAs finish together.  Every CTA still
+// leaves one partial (its warps' merged state); which chunks a partial covers
+// then depends on timing, so its rounding can differ from call to call.
+template <int D, int NW, int NS, bool Pooled>
 __global__ void __launch_bounds__(NW * 32, 1)
     pa_partition_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         const PartitionParams prm) {
     using S = PartitionShape<D, NW, NS>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStageArea);
+    float* sm_m = reinterpret_cast<float*>(bars + NW * NS);
+    float* sm_l = sm_m + NW * kMaxGroup;
+    int* sm_abort = reinterpret_cast<int*>(sm_l + NW * kMaxGroup);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t stage0 = smem_addr(smem) + warp * NS * S::kStageBytes;
+    const uint32_t bar0 = smem_addr(bars) + warp * NS * 8;
+
     // Launched as a programmatic dependent of whatever precedes it on the
-    // stream: the CTAs may become resident early, but nothing is read before
-    // the preceding grid has completed and its writes are visible.
+    // stream: the CTAs may become resident early.  What reads nothing that
+    // grid writes -- the copy barriers and the tensor maps' descriptors --
+    // is set up before the wait; nothing else is read before the preceding
+    // grid has completed and its writes are visible.
+    if (threadIdx.x == 0) {
+        *sm_abort = 0;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+    }
+    if (lane == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // Let the dependent reduce launch its CTAs as soon as SMs free up; it
     // still waits for this grid's completion before touching the partials.
@@ -151,16 +181,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     PA_TRACE_MARK(1);
 #endif
 
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_addr(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStageArea);
-    float* sm_m = reinterpret_cast<float*>(bars + NW * NS);
-    float* sm_l = sm_m + NW * kMaxGroup;
-    int* sm_abort = reinterpret_cast<int*>(sm_l + NW * kMaxGroup);
-
     const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = prm.group, H = prm.num_heads;
     const int blocks_per_part = prm.partition_size / kBlockSize;
     const int blk0 = p * blocks_per_part;
@@ -171,7 +192,17 @@ __global__ void __launch_bounds__(NW * 32, 1)
     // The first batch is read before the sequence length is known, bounded by
     // the block-table row, so the two loads overlap.
     const int jmax = max(0, min(blocks_per_part, prm.max_blocks_per_seq - blk0));
-    int ids_copy = (warp + lane * NW) < jmax ? __ldg(bt + warp + lane * NW) : -1;
+    constexpr int C = pool_chunk(NS);  // blocks per chunk of the pooled form
+    int ids_copy;
+    if constexpr (Pooled) {
+        // lane k < C: block k of the warp's first chunk
+        const int j = (p * NW + warp) * C + lane;
+        ids_copy = (lane < C && j < prm.max_blocks_per_seq)
+                       ? __ldg(prm.block_tables + (size_t)b * prm.max_blocks_per_seq + j)
+                       : -1;
+    } else {
+        ids_copy = (warp + lane * NW) < jmax ? __ldg(bt + warp + lane * NW) : -1;
+    }
     const int L = __ldg(prm.seq_lens + b);
     int batch_copy = 0;
     auto block_id = [&](int& ids, int& batch, int it) {
@@ -197,22 +228,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (p >= n_part) return;
     const int nblk = min(blocks_per_part, (L + kBlockSize - 1) / kBlockSize - blk0);
 
-    const uint32_t stage0 = smem_addr(smem) + warp * NS * S::kStageBytes;
-    const uint32_t bar0 = smem_addr(bars) + warp * NS * 8;
-    if (threadIdx.x == 0) *sm_abort = 0;
-    if (lane == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-
     // Blocks j = warp, warp + NW, ... of the partition belong to this warp.
     const int nmine = warp < nblk ? (nblk - warp + NW - 1) / NW : 0;
     uint32_t valid_bits = 0;  // stage s holds a block with a legal id
 
-    // Stage the K and V of iteration `it` into stage it % NS.
-    auto issue = [&](int it) {
-        const int phys = block_id(ids_copy, batch_copy, it);
+    // Stage the K and V of block `phys` (the warp's iteration `it`) into stage it % NS.
+    auto stage_block = [&](int it, int phys) {
         const int s = it % NS;
         const uint32_t bar = bar0 + 8 * s;
         const bool ok = phys >= 0 && (long long)phys < prm.num_blocks;
@@ -231,7 +252,34 @@ __global__ void __launch_bounds__(NW * 32, 1)
             }
         }
     };
-    for (int it = 0; it < NS && it < nmine; ++it) issue(it);
+    auto issue = [&](int it) { stage_block(it, block_id(ids_copy, batch_copy, it)); };
+
+    // Pooled: chunk q holds blocks [q C, (q + 1) C) of the sequence.  The
+    // nw = n_part * NW warps of the sequence's CTAs take chunks round-robin
+    // (warp v: v, v + nw, v + 2 nw, ...) up to chunk 3 nw; then a warp's k-th
+    // chunk (k >= 3) is 3 nw + the count its claim returned, or, if the
+    // counter was not armed, the round-robin one.  The first three need no
+    // counter, so the claims of a whole wave of warps do not queue at start.
+    const int nblk_seq = (L + kBlockSize - 1) / kBlockSize;
+    const int nchunks = (nblk_seq + C - 1) / C;
+    const int nw = n_part * NW;
+    unsigned long long* const ctr = Pooled ? prm.claims + (size_t)b * prm.num_kv_heads + kvh : nullptr;
+    auto chunk_len = [&](int q) { return q < nchunks ? min(C, nblk_seq - q * C) : 0; };
+    auto chunk_ids = [&](int q, int len) {
+        return lane < len ? __ldg(prm.block_tables + (size_t)b * prm.max_blocks_per_seq + (size_t)q * C + lane) : -1;
+    };
+    int q_cur = p * NW + warp, len_cur = 0, issued = 0;
+    int q_nxt = 0, len_nxt = 0, ids_nxt = -1;
+    if constexpr (Pooled) {
+        static_assert(NS <= C, "copies run at most one chunk ahead");
+        len_cur = chunk_len(q_cur);
+        q_nxt = q_cur + nw;
+        len_nxt = chunk_len(q_nxt);
+        ids_nxt = chunk_ids(q_nxt, len_nxt);
+        for (; issued < NS && issued < len_cur; ++issued) stage_block(issued, __shfl_sync(kFull, ids_copy, issued));
+    } else {
+        for (int it = 0; it < NS && it < nmine; ++it) issue(it);
+    }
 
     const int g = lane >> 2, c = lane & 3;  // MMA fragment row group / column pair
 
@@ -256,6 +304,62 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const float sl2 = prm.scale_log2;
     int i = 0;
     bool timed_out = false;
+    if constexpr (Pooled) {
+        // At the start of chunk k the warp holds chunks k and k + 1 (ids
+        // loaded a chunk ago), resolves chunk k + 2 from the claim it made at
+        // the start of chunk k - 1, loads its ids and claims again; neither
+        // latency stalls the copies, which run NS <= C blocks ahead.
+        int mode = 0;  // 0: no claim resolved yet, 1: counter armed, 2: round-robin
+        bool claimed = false;
+        unsigned long long raw = 0;  // lane 0: counter value returned by the last claim
+        int q_nn = 0, len_nn = 0, ids_nn = -1;
+        for (;; ++i) {
+            const int r = i % C;
+            if (r == 0) {
+                if (i > 0) {
+                    q_cur = q_nxt, len_cur = len_nxt, ids_copy = ids_nxt;
+                    q_nxt = q_nn, len_nxt = len_nn, ids_nxt = ids_nn;
+                }
+                if (len_cur == 0) break;
+                if (i == 0 || mode == 2) {
+                    q_nn = q_nxt + nw;
+                } else if (claimed) {
+                    const unsigned long long got = __shfl_sync(kFull, raw, 0);
+                    if (mode == 0) mode = (unsigned)(got >> 32) == kClaimTag ? 1 : 2;
+                    const unsigned cnt = (unsigned)got;  // claims before this one
+                    q_nn = mode == 2 ? q_nxt + nw : cnt < (unsigned)nchunks ? 3 * nw + (int)cnt : nchunks;
+                } else {
+                    q_nn = nchunks;  // the previous chunk resolved was past the end
+                }
+                len_nn = chunk_len(q_nn);
+                ids_nn = chunk_ids(q_nn, len_nn);
+                claimed = mode != 2 && len_nn > 0;
+                if (claimed && lane == 0) raw = atomicAdd(ctr, 1ull);
+            }
+            if (r >= len_cur) break;
+            const int s = i % NS;
+            const uint32_t bar = bar0 + 8 * s;
+            if (prm.force_timeout || !mbar_wait(bar, (i / NS) & 1, prm.wait_limit)) {
+                timed_out = true;
+                break;
+            }
+            if (i == 0) PA_TRACE_MARK(2);
+            if ((valid_bits >> s) & 1u) {
+                const int tok0 = (q_cur * C + r) * kBlockSize;
+                const uint32_t kst = stage0 + s * S::kStageBytes;
+                warp_block_update<D>(qb, o, m0, m1, l0, l1, kst, kst + S::kTileBytes,
+                                     smem + (kst + S::kTileBytes - smem_addr(smem)), min(kBlockSize, L - tok0),
+                                     sl2);
+            }
+            __syncwarp();
+            const int rn = r + NS;  // chunk-relative block of iteration i + NS
+            if (rn < C) {
+                if (rn < len_cur) stage_block(issued++, __shfl_sync(kFull, ids_copy, rn));
+            } else if (rn - C < len_nxt) {
+                stage_block(issued++, __shfl_sync(kFull, ids_nxt, rn - C));
+            }
+        }
+    } else {
     for (; i < nmine; ++i) {
         const int s = i % NS;
         const uint32_t bar = bar0 + 8 * s;
@@ -273,11 +377,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
         __syncwarp();
         if (i + NS < nmine) issue(i + NS);
     }
+    issued = min(nmine, i + NS);
+    }
 
     if (timed_out) {
         // Drain this warp's copies still in flight before the CTA may exit.
-        for (int k = i; k < nmine && k < i + NS; ++k)
-            mbar_wait(bar0 + 8 * (k % NS), (k / NS) & 1, kDefaultWaitLimit);
+        for (int k = i; k < issued; ++k) mbar_wait(bar0 + 8 * (k % NS), (k / NS) & 1, kDefaultWaitLimit);
         if (lane == 0) {
             atomicOr(&g_status, PA_DEV_TIMEOUT);
             atomicExch(sm_abort, 1);
@@ -443,28 +548,40 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int h = blockIdx.x, b = blockIdx.y, slice = blockIdx.z;
-    const int L = prm.seq_lens[b];
-    // single-partition, empty and invalid sequences were finished by the partition kernel
-    if (L <= 0 || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) return;
-    const int part = prm.part_sizes ? prm.part_sizes[b] : prm.partition_size;
-    const int n = (L + part - 1) / part;
-    if (n <= 1) return;
+    // re-arm the pooled split's claim counter of (b, kv head h / group): the
+    // partition grid that used it has completed
+    if (prm.claims && slice == 0 && h % prm.group == 0 && threadIdx.x == 0)
+        prm.claims[(size_t)b * (prm.num_heads / prm.group) + h / prm.group] = (unsigned long long)kClaimTag << 32;
     const size_t base = ((size_t)b * prm.num_heads + h) * prm.max_partitions;
     const float* ml = prm.max_logits + base;
     const float* el = prm.exp_sums + base;
+    const int col = threadIdx.x % kLanes, pg = threadIdx.x / kLanes;
+    const float4* tp = reinterpret_cast<const float4*>(prm.tmp_out + base * D + slice * W) + col;
+    // A thread's first partial is read together with the length, so the two
+    // latencies overlap: the row holds max_partitions entries, so the reads
+    // stay inside the workspace, and a value past the sequence's partitions
+    // is never used.
+    float mp0 = 0.f, lp0 = 0.f;
+    float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (pg < prm.max_partitions) {
+        mp0 = ml[pg];
+        lp0 = el[pg];
+        t0 = tp[(size_t)pg * (D / 4)];
+    }
+    const int L = prm.seq_lens[b];
+    const int part = prm.part_sizes ? prm.part_sizes[b] : prm.partition_size;
+    // single-partition, empty and invalid sequences were finished by the partition kernel
+    if (L <= 0 || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) return;
+    const int n = (L + part - 1) / part;
+    if (n <= 1) return;
 
     __shared__ float4 red_acc[kGroups][kLanes];
     __shared__ float red_m[kGroups];
     __shared__ float red_w[kGroups];
 
-    const int col = threadIdx.x % kLanes, pg = threadIdx.x / kLanes;
-    const float4* tp = reinterpret_cast<const float4*>(prm.tmp_out + base * D + slice * W) + col;
     float m = -INFINITY, wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int p = pg; p < n; p += kGroups) {
-        const float mp = ml[p], lp = el[p];
-        const float4 t = tp[(size_t)p * (D / 4)];
+    auto fold = [&](float mp, float lp, const float4& t) {
         const float mn = fmaxf(m, mp);
         const float alpha = exp2f(m - mn);  // 0 on the first partition (m = -inf)
         const float beta = lp * exp2f(mp - mn);
@@ -474,7 +591,10 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
         acc.z = acc.z * alpha + beta * t.z;
         acc.w = acc.w * alpha + beta * t.w;
         m = mn;
-    }
+    };
+    if (pg < n) fold(mp0, lp0, t0);
+#pragma unroll 4
+    for (int p = pg + kGroups; p < n; p += kGroups) fold(ml[p], el[p], tp[(size_t)p * (D / 4)]);
     red_acc[pg][col] = acc;
     if (col == 0) {
         red_m[pg] = m;
@@ -517,14 +637,18 @@ int partition_smem_bytes(int head_dim, int warps, int stages) {
 
 namespace {
 
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, bool Pooled>
 cudaError_t launch_partition_t(const PartitionParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                                cudaStream_t stream) {
     const int smem = PartitionShape<D, NW, NS>::kSmemBytes;
     // The attribute is per device; setting it on every call costs little and
     // keeps multi-device processes correct.
-    cudaError_t e =
-        cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS, Pooled>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // all of an SM's shared memory, so that the dependent reduce CTAs fit beside these
+    e = cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS, Pooled>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -534,13 +658,20 @@ cudaError_t launch_partition_t(const PartitionParams& prm, const CUtensorMap& tk
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, pa_partition_kernel<D, NW, NS>, tk, tv, prm);
+    e = cudaLaunchKernelEx(&cfg, pa_partition_kernel<D, NW, NS, Pooled>, tk, tv, prm);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <int D, int W>
 cudaError_t launch_reduce_t(const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
+    // The largest shared-memory carveout, as the partition kernel's needs: an
+    // SM runs CTAs of one carveout at a time, so with a smaller one the
+    // reduce CTAs could not become resident beside the partition CTAs that
+    // they wait on.
+    cudaError_t e = cudaFuncSetAttribute(pa_reduce_kernel<D, W>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kReduceThreads);
@@ -549,7 +680,7 @@ cudaError_t launch_reduce_t(const ReduceParams& prm, dim3 grid, cudaStream_t str
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, pa_reduce_kernel<D, W>, prm);
+    e = cudaLaunchKernelEx(&cfg, pa_reduce_kernel<D, W>, prm);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -570,14 +701,21 @@ cudaError_t launch_reduce_d(int width, const ReduceParams& prm, dim3 grid, cudaS
 
 cudaError_t launch_partition(int head_dim, int warps, int stages, const PartitionParams& prm, const CUtensorMap& tk,
                              const CUtensorMap& tv, dim3 grid, cudaStream_t stream) {
-#define PA_LAUNCH_CASE(W_, S_)                                                          \
-    if (warps == W_ && stages == S_) {                                                 \
-        switch (head_dim) {                                                            \
-            case 64: return launch_partition_t<64, W_, S_>(prm, tk, tv, grid, stream);   \
-            case 128: return launch_partition_t<128, W_, S_>(prm, tk, tv, grid, stream); \
-            case 256: return launch_partition_t<256, W_, S_>(prm, tk, tv, grid, stream); \
-            default: return cudaErrorInvalidValue;                                     \
-        }                                                                              \
+#define PA_LAUNCH_CASE(W_, S_)                                                                     \
+    if (warps == W_ && stages == S_) {                                                            \
+        const bool pooled = prm.claims != nullptr;                                                \
+        switch (head_dim) {                                                                       \
+            case 64:                                                                              \
+                return pooled ? launch_partition_t<64, W_, S_, true>(prm, tk, tv, grid, stream)   \
+                              : launch_partition_t<64, W_, S_, false>(prm, tk, tv, grid, stream); \
+            case 128:                                                                             \
+                return pooled ? launch_partition_t<128, W_, S_, true>(prm, tk, tv, grid, stream)  \
+                              : launch_partition_t<128, W_, S_, false>(prm, tk, tv, grid, stream); \
+            case 256:                                                                             \
+                return pooled ? launch_partition_t<256, W_, S_, true>(prm, tk, tv, grid, stream)  \
+                              : launch_partition_t<256, W_, S_, false>(prm, tk, tv, grid, stream); \
+            default: return cudaErrorInvalidValue;                                                \
+        }                                                                                         \
     }
     PA_FOR_EACH_SHAPE(PA_LAUNCH_CASE)
 #undef PA_LAUNCH_CASE

@@ -11,7 +11,7 @@ afterwards.
 
 A partition of 0 takes the library's own plan; `name:persistent` runs the
 persistent schedule with its default plan (its "main loop done" is the end of
-the CTA's first item).
+the CTA's first item); `name:pooled` the library's plan with PA_FLAG_POOLED.
 """
 from __future__ import annotations
 
@@ -23,23 +23,26 @@ import numpy as np
 import torch
 
 
-def _analyse(pb, W, name: str, partition: int, warps: int = 0, stages: int = 0, out=print, persistent=False):
+def _analyse(pb, W, name: str, partition: int, warps: int = 0, stages: int = 0, out=print, special=""):
     dev = torch.device("cuda:0")
     w = W.make_config(name, device=dev)
     res = torch.empty_like(w.q)
     opt = dict(mode="split", partition_size=partition, warps=warps, stages=stages) if partition else dict()
-    if persistent:
+    if special == "persistent":
         opt = dict(mode="persistent")
+    elif special == "pooled":
+        opt = dict(flags=pb.PA_FLAG_POOLED)
     plan = pb.pa_decode_plan(res, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
                              w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len, **opt)
     ncta = plan["grid_x"] * plan["grid_y"] * plan["grid_z"]
     buf = torch.zeros(ncta * 5, dtype=torch.int64, device=dev)
+    ws = pb.alloc_workspace(plan, dev) if opt else None  # kept: the pooled counters are armed by a call
     for _ in range(5):
-        pb.decode_workload(w, **opt)
+        pb.decode_workload(w, workspace=ws, **opt)
     torch.cuda.synchronize()
     pb.lib.pa_debug_set_trace.argtypes = [ctypes.c_void_p]
     pb.lib.pa_debug_set_trace(buf.data_ptr())
-    pb.decode_workload(w, **opt)
+    pb.decode_workload(w, workspace=ws, **opt)
     torch.cuda.synchronize()
     pb.lib.pa_debug_set_trace(None)
     t = buf.view(ncta, 5).cpu().numpy()
@@ -70,8 +73,8 @@ def main(argv):
         from . import workloads as W
         for spec in (argv or ["b1_l102400:512"]):
             name, *rest = spec.split(":")
-            if rest == ["persistent"]:
-                _analyse(pb, W, name, 0, persistent=True)
+            if rest in (["persistent"], ["pooled"]):
+                _analyse(pb, W, name, 0, special=rest[0])
                 continue
             nums = [int(v) for v in rest] + [0] * (3 - len(rest))
             _analyse(pb, W, name, *nums[:3])

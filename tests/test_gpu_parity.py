@@ -384,3 +384,103 @@ def test_persistent_many_items_per_cta(dev, warps, P, D):
     assert torch.count_nonzero(out[5]) == 0
     # which CTA draws which item changes from call to call; the bits do not
     assert torch.equal(out, run(w, mode="persistent", partition_size=P, warps=warps, stages=2))
+
+
+# ---- pooled split (PA_FLAG_POOLED): warps claim chunks of blocks from a counter ----
+
+CLAIM_ARMED = 0x5A17C0DE << 32  # the value the reduce kernel leaves in every claim counter
+
+
+def _claims(ws, plan, w):
+    """The (sequence, kv head) claim counters at the end of the workspace."""
+    n = w.block_tables.shape[0] * w.num_kv_heads
+    tail = (n * 8 + 255) // 256 * 256
+    return ws[plan["workspace_bytes"] - tail:].view(torch.int64)[:n]
+
+
+def _pooled_plan(w, **opt):
+    out = torch.empty_like(w.q)
+    return pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len,
+                             flags=pb.PA_FLAG_POOLED, **opt)
+
+
+@pytest.mark.parametrize("lens,opt", [
+    ([102400], dict()),                                              # the one-wave plan, 4 warps per CTA
+    ([1, 15, 16, 17, 63, 64, 65, 1029, 4097], dict(mode="split", partition_size=256)),
+    ([3000, 517, 8000, 1, 0], dict(mode="split", partition_size=512, warps=1, stages=3)),
+    ([3000, 517, 8000, 1, 0], dict(mode="split", partition_size=512, warps=2, stages=2)),
+    ([2048, 3, 700, 12000], dict(mode="split", partition_size=1024, warps=4, stages=2)),
+    ([5000] * 6, dict(mode="split", partition_size=256, warps=1, stages=2)),
+    ([1, 47, 48, 49, 700, 3001], dict(mode="split", partition_size=48, warps=1, stages=3)),
+    ([129, 128, 127, 4000, 9999], dict(mode="split", partition_size=128, warps=4, stages=2)),
+], ids=["b1_l102400", "ragged_P256", "P512_1x3", "P512_2x2", "P1024_4x2", "b6_P256_1x2", "P48_1x3", "P128_4x2"])
+def test_pooled_split_parity(dev, lens, opt):
+    w = W.make_workload("pooled", lens, num_blocks=sum((L + 15) // 16 for L in lens) + 11, seed=sum(lens) % 97,
+                        device=dev, tail_fill=float("nan"))
+    plan = _pooled_plan(w, **opt)
+    assert plan["pooled"] == 1
+    ws = pb.alloc_workspace(plan, dev)  # zero: the first call deals the chunks round-robin
+    ref = oracle_ref(w, THREADS)
+    for k in range(3):
+        out = run(w, workspace=ws, flags=pb.PA_FLAG_POOLED, **opt)
+        assert_parity(out, ref, f"pooled call {k} lens={lens} {opt}")
+        assert (_claims(ws, plan, w) == CLAIM_ARMED).all()
+        assert torch.count_nonzero(out[[i for i, L in enumerate(lens) if L == 0]]) == 0
+
+
+@pytest.mark.parametrize("name", ["b1_l102400", "b4_l32768_peaked", "b8_u8192"])
+def test_pooled_named_workload_full(dev, name):
+    w = W.make_config(name, device=dev)
+    plan = _pooled_plan(w)
+    ws = pb.alloc_workspace(plan, dev)
+    ref = oracle_ref(w, THREADS)
+    for k in range(2):
+        out = run(w, workspace=ws, flags=pb.PA_FLAG_POOLED)
+        print(name, "pooled" if k else "round-robin", assert_parity(out, ref, f"{name} pooled call {k}"))
+
+
+def test_pooled_garbage_workspace_timeout_and_graph(dev):
+    w = W.make_workload("poolg", [20000, 77, 9000], num_blocks=2000, seed=17, device=dev)
+    opt = dict(mode="split", partition_size=512, flags=pb.PA_FLAG_POOLED)
+    plan = _pooled_plan(w, mode="split", partition_size=512)
+    ref = oracle_ref(w)
+    # any bytes in a fresh workspace: the counters are not armed, the chunks go round-robin
+    ws = torch.randint(0, 256, (plan["workspace_bytes"],), dtype=torch.uint8, device=dev)
+    assert_parity(run(w, workspace=ws, **opt), ref, "pooled on a random workspace")
+    assert (_claims(ws, plan, w) == CLAIM_ARMED).all()
+    # a forced timeout is reported and leaves the counters armed for the next call
+    pb.pa_get_device_status()
+    pb.decode_workload(w, workspace=ws, mode="split", partition_size=512,
+                       flags=pb.PA_FLAG_POOLED | pb.PA_FLAG_FORCE_TIMEOUT)
+    assert pb.pa_get_device_status() & pb.PA_DEV_TIMEOUT
+    assert (_claims(ws, plan, w) == CLAIM_ARMED).all()
+    assert_parity(run(w, workspace=ws, **opt), ref, "pooled after a timeout")
+    # captured once, replayed: each replay claims from the counter its predecessor re-armed
+    out = torch.empty_like(w.q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pb.decode_workload(w, out=out, stream=torch.cuda.current_stream(), workspace=ws, **opt)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert pb.pa_get_device_status() == 0
+        assert_parity(out, ref, "pooled graph replay")
+
+
+def test_one_wave_plan_pools_by_default_and_deterministic_flag_fixes_the_bits(dev):
+    w = W.make_workload("onewave", [90000], num_blocks=90000 // 16 + 5, seed=23, device=dev)
+    assert _pooled_plan(w)["pooled"] == 1
+    ref = oracle_ref(w, THREADS)
+    fixed = [run(w, flags=pb.PA_FLAG_DETERMINISTIC) for _ in range(3)]
+    assert all(torch.equal(fixed[0], f) for f in fixed[1:])
+    assert_parity(fixed[0], ref, "one wave, deterministic")
+    ws = pb.alloc_workspace(_pooled_plan(w), dev)
+    for k in range(3):  # round-robin first, then claimed chunks
+        out = run(w, workspace=ws, mode="auto")
+        assert_parity(out, ref, f"one wave, pooled call {k}")
+        assert (out.float() - fixed[0].float()).abs().max().item() < 2e-3

@@ -60,7 +60,8 @@ def test_plan_long_context_runs_one_wave_of_one_cta_per_sm():
     assert pl["threads"] == 128 and pl["stages"] == 2
     assert pl["grid_x"] * pl["grid_y"] <= SMS
     assert pl["launch_reduce"] == 1
-    assert pl["workspace_bytes"] == ws_bytes(1, 24, 38, 256)
+    assert pl["pooled"] == 1  # + one 8-byte claim counter per kv head, in its own 256-byte slot
+    assert pl["workspace_bytes"] == ws_bytes(1, 24, 38, 256) + 256
     assert pl["workspace_bytes"] <= pb.pa_decode_workspace_size(1, 102400, 24, 256, 0)
     # below 2048 tokens per partition, and for batches, the 512-token default stays
     rc, short = plan(args(max_seq_len=65536, num_blocks=4096))
@@ -239,3 +240,35 @@ def test_cta_shape_follows_the_wave_model(B, L, shape):
     # at the 512-token partitions the model was fitted for
     rc, pl = plan(args(num_seqs=B, max_seq_len=L, num_blocks=B * L // 16), partition_size=512 if L > 2048 else 0)
     assert rc == 0 and (pl["threads"] // 32, pl["stages"]) == shape
+
+
+def _plan_opts(num_seqs, max_seq_len, mode=0, partition_size=0, flags=0, warps=0, stages=0):
+    o = pb.pa_decode_opts(mode, partition_size, flags, 0, None, None, warps, stages)
+    pl = pb.pa_decode_plan_t()
+    rc = pb.lib.pa_decode_plan(ctypes.byref(args(num_seqs=num_seqs, max_seq_len=max_seq_len,
+                                                 num_blocks=num_seqs * ((max_seq_len + 15) // 16))),
+                               ctypes.byref(o), SMS, ctypes.byref(pl))
+    assert rc == 0
+    return pl.as_dict()
+
+
+def test_pooled_plan_flags_and_workspace():
+    base = _plan_opts(1, 102400, flags=pb.PA_FLAG_DETERMINISTIC)
+    pooled = _plan_opts(1, 102400, flags=pb.PA_FLAG_POOLED)
+    assert base["pooled"] == 0 and pooled["pooled"] == 1
+    # the one-wave plan of one long sequence is pooled by default; DETERMINISTIC wins over POOLED
+    assert _plan_opts(1, 102400) == pooled
+    assert _plan_opts(1, 102400, flags=pb.PA_FLAG_POOLED | pb.PA_FLAG_DETERMINISTIC) == base
+    assert _plan_opts(4, 32768)["pooled"] == 0  # several waves: fixed
+    # same grid and partials as the fixed split, plus one 8-byte counter per (sequence, kv head)
+    for k in ("mode", "partition_size", "grid_x", "grid_y", "grid_z", "threads", "max_partitions"):
+        assert pooled[k] == base[k]
+    assert pooled["workspace_bytes"] == base["workspace_bytes"] + 256
+    # pooled only for SPLIT plans with at least one chunk (max(2, stages) blocks) per warp of every partition
+    assert _plan_opts(4, 4096, mode=2, partition_size=112, flags=pb.PA_FLAG_POOLED, warps=4, stages=2)["pooled"] == 0
+    assert _plan_opts(4, 4096, mode=2, partition_size=128, flags=pb.PA_FLAG_POOLED, warps=4, stages=2)["pooled"] == 1
+    assert _plan_opts(4, 4096, mode=2, partition_size=32, flags=pb.PA_FLAG_POOLED, warps=1, stages=3)["pooled"] == 0
+    assert _plan_opts(4, 4096, mode=2, partition_size=48, flags=pb.PA_FLAG_POOLED, warps=1, stages=3)["pooled"] == 1
+    assert _plan_opts(4, 500, flags=pb.PA_FLAG_POOLED)["pooled"] == 0  # one partition: no reduce
+    for mode in (1, 3, 4):
+        assert _plan_opts(4, 4096, mode=mode, flags=pb.PA_FLAG_POOLED)["pooled"] == 0
