@@ -8,6 +8,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace pa {
 
 constexpr int kBlockSize = 16;    // tokens per KV block (one MMA M-tile of tokens)
@@ -62,8 +64,24 @@ inline int pool_min_partition(int warps, int stages) { return warps * pool_chunk
 // list, order, lengths and partition sizes in each CTA's shared memory (these
 // extra bytes).
 constexpr int kPersistentSeqCache = 256;
-inline int persistent_seq_cache_bytes(int num_seqs) {
+constexpr int persistent_seq_cache_bytes(int num_seqs) {
     return num_seqs <= kPersistentSeqCache ? ((4 * num_seqs + 1) * 4 + 15) / 16 * 16 : 0;
+}
+
+// Runs `set` (a kernel's launch attributes, which are per device) the first
+// time it is reached on each device, tracked in that kernel's `done` word
+// (one bit per device; devices past 63 set it every time).  Each attribute
+// call costs driver time that a short decode call would notice.
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<unsigned long long>& done, F&& set) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = set();
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
 }
 
 struct PartitionParams {

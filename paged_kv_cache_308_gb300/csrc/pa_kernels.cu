@@ -641,14 +641,15 @@ template <int D, int NW, int NS, bool Pooled>
 cudaError_t launch_partition_t(const PartitionParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                                cudaStream_t stream) {
     const int smem = PartitionShape<D, NW, NS>::kSmemBytes;
-    // The attribute is per device; setting it on every call costs little and
-    // keeps multi-device processes correct.
-    cudaError_t e = cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS, Pooled>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    // all of an SM's shared memory, so that the dependent reduce CTAs fit beside these
-    e = cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS, Pooled>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
+    static std::atomic<unsigned long long> done{0};
+    cudaError_t e = once_per_device(done, [&] {
+        cudaError_t r = cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS, Pooled>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (r != cudaSuccess) return r;
+        // all of an SM's shared memory, so that the dependent reduce CTAs fit beside these
+        return cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS, Pooled>,
+                                    cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    });
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -669,8 +670,11 @@ cudaError_t launch_reduce_t(const ReduceParams& prm, dim3 grid, cudaStream_t str
     // SM runs CTAs of one carveout at a time, so with a smaller one the
     // reduce CTAs could not become resident beside the partition CTAs that
     // they wait on.
-    cudaError_t e = cudaFuncSetAttribute(pa_reduce_kernel<D, W>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         (int)cudaSharedmemCarveoutMaxShared);
+    static std::atomic<unsigned long long> done{0};
+    cudaError_t e = once_per_device(done, [] {
+        return cudaFuncSetAttribute(pa_reduce_kernel<D, W>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    (int)cudaSharedmemCarveoutMaxShared);
+    });
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;

@@ -127,18 +127,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
                                    const __grid_constant__ CUtensorMap tmap_v, const PartitionParams prm) {
     using S = PartitionShape<D, NW, NS>;
     using Q = PersistentShape<D, NW, NS>;
-    // the work list and the item counter are written by the preceding (scan) grid
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;");
-#ifdef PA_TRACE
-    if (prm.trace && threadIdx.x == 0) {
-        unsigned smid;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        prm.trace[(size_t)blockIdx.x * 5] = smid;
-    }
-#endif
-    PA_PT_MARK(1);
-
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     float* red = reinterpret_cast<float*>(smem + Q::kRedArea);    // [2][NW][8][kRedStride]
@@ -151,6 +139,29 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const int G = prm.group, H = prm.num_heads;
     const uint32_t stage0 = smem_addr(smem) + warp * NS * S::kStageBytes;
     const uint32_t bar0 = smem_addr(smem) + Q::kBarArea + warp * NS * 8;
+    // the copy barriers and the tensor maps' descriptors read nothing the
+    // preceding grids write: set up before the dependency wait
+    if (lane == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+    }
+
+    // the work list and the item counter are written by the preceding (scan) grid
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+#ifdef PA_TRACE
+    if (prm.trace && threadIdx.x == 0) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        prm.trace[(size_t)blockIdx.x * 5] = smid;
+    }
+#endif
+    PA_PT_MARK(1);
+
     // Items are located by binary search over the work list, on the copy
     // side and again at the start of each item's math: from shared memory
     // when the batch is small enough to cache.
@@ -169,10 +180,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
     const int total = __ldg(prm.work_offsets + prm.num_seqs);
 
-    if (lane == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
     if (threadIdx.x == 0) {
         items[0] = blockIdx.x;
         items[1] = (int)blockIdx.x < total ? atomicAdd(prm.work_counter, 1) : total;
@@ -461,8 +468,18 @@ template <int D, int NW, int NS>
 cudaError_t launch_persistent_t(const PartitionParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                                 cudaStream_t stream) {
     const int smem = PersistentShape<D, NW, NS>::kSmemBytes + persistent_seq_cache_bytes(prm.num_seqs);
-    cudaError_t e = cudaFuncSetAttribute(pa_partition_persistent_kernel<D, NW, NS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // the attribute allows the largest table cache, so it is set once per device
+    constexpr int kSmemMax = PersistentShape<D, NW, NS>::kSmemBytes + persistent_seq_cache_bytes(kPersistentSeqCache);
+    static_assert(kSmemMax <= 227 * 1024, "shared memory budget of one CTA with the table cache");
+    static std::atomic<unsigned long long> done{0};
+    cudaError_t e = once_per_device(done, [] {
+        cudaError_t r = cudaFuncSetAttribute(pa_partition_persistent_kernel<D, NW, NS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+        if (r != cudaSuccess) return r;
+        // all of an SM's shared memory, so that the dependent reduce CTAs fit beside these
+        return cudaFuncSetAttribute(pa_partition_persistent_kernel<D, NW, NS>,
+                                    cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    });
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

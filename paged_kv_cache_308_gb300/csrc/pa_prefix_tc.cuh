@@ -750,7 +750,10 @@ namespace {
 template <int D>
 cudaError_t launch_prefix_tc_t(const PrefixParams& prm, const CUtensorMap* maps, dim3 grid, cudaStream_t stream) {
     const int smem = PrefixTcShape<D>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(pa_prefix_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<unsigned long long> done{0};
+    cudaError_t e = once_per_device(done, [&] {
+        return cudaFuncSetAttribute(pa_prefix_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
