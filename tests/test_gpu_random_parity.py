@@ -53,3 +53,33 @@ def test_random_case(dev, i):
     for b, L in enumerate(c["lens"]):
         if L == 0:
             assert torch.count_nonzero(out[b]) == 0, f"case {i}: empty sequence {b} not zero"
+
+
+POOL_SHAPES = [(1, 2), (1, 3), (2, 2), (4, 2)]
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_pooled_case(dev, i):
+    # the pooled split on random shapes: the first call on a fresh workspace
+    # deals the chunks round-robin, the later ones claim them from the counter
+    c = draw_case(100 + i)
+    warps, stages = POOL_SHAPES[i % len(POOL_SHAPES)]
+    part = warps * 16 * max(2, stages) * random.Random(i).choice([1, 2, 3])
+    opt = dict(mode="split", partition_size=part, warps=warps, stages=stages, flags=pb.PA_FLAG_POOLED)
+    blocks = sum((L + 15) // 16 for L in c["lens"]) + 3
+    w = W.make_workload(f"randpool{i}", c["lens"], num_heads=c["num_heads"], num_kv_heads=c["num_kv_heads"],
+                        head_dim=c["head_dim"], num_blocks=blocks, seed=c["seed"], device=dev,
+                        tail_fill=float("nan"))
+    out = torch.empty_like(w.q)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len, **opt)
+    ws = pb.alloc_workspace(plan, dev)
+    ref = oracle_ref(w)
+    for k in range(2):
+        out = pb.decode_workload(w, workspace=ws, **opt)
+        torch.cuda.synchronize()
+        assert pb.pa_get_device_status() == 0
+        assert_parity(out, ref, f"pooled case {i} call {k}: {c} {opt} pooled={plan['pooled']}")
+        for b, L in enumerate(c["lens"]):
+            if L == 0:
+                assert torch.count_nonzero(out[b]) == 0, f"pooled case {i}: empty sequence {b} not zero"
