@@ -92,9 +92,11 @@ enum {
     PA_MODE_PERSISTENT = 4 /* a fixed grid of (SMs x CTAs per SM) takes the items of a work list
                               that a small kernel builds on the device from a device counter,
                               longest partitions first.  Each sequence gets its own partition size:
-                              with partition_size 0 the grid's partitions are apportioned over the
-                              batch by length (one wave when it fits), else the fewest partitions of
-                              at most partition_size tokens evened out to whole blocks; then the
+                              with partition_size 0 the grid's partitions per kv head are
+                              apportioned over the batch with the smallest cap on a partition's
+                              blocks that lets them fit (one wave when the sequences are fewer than
+                              those partitions), else the fewest partitions of at most
+                              partition_size tokens; either way evened out to whole blocks; then the
                               log-sum-exp reduce.  The host never reads the lengths, so the call is
                               graph-safe.  The workspace also holds the work list, the counter,
                               the order and the sizes (rewritten by every call) */

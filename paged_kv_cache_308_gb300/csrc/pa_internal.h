@@ -29,23 +29,6 @@ __host__ __device__ inline int balanced_partition(int L, int pmax) {
     return ((even + kBlockSize - 1) / kBlockSize) * kBlockSize;
 }
 
-// Partition size of a sequence of L tokens when the persistent schedule
-// apportions `slots` partitions per kv head over a batch whose valid lengths
-// sum to T: n = slots * L / T partitions, rounded down when the batch's
-// rounded-down counts (each at least one) fit in the slots -- one wave of the
-// grid -- and rounded up otherwise (many short sequences: no item longer
-// than the average work of a CTA); at least one, at most slots and at most
-// one per block.  The partition count is (L + size - 1) / size <= slots.
-__host__ __device__ inline int apportioned_partition(int L, long long T, int slots, bool round_up) {
-    long long n = 1;
-    if (T > 0) n = round_up ? ((long long)slots * L + T - 1) / T : ((long long)slots * L) / T;
-    const long long max_n = slots < (L + kBlockSize - 1) / kBlockSize ? slots : (L + kBlockSize - 1) / kBlockSize;
-    if (n > max_n) n = max_n;
-    if (n < 1) n = 1;
-    const int even = (int)((L + n - 1) / n);
-    return ((even + kBlockSize - 1) / kBlockSize) * kBlockSize;
-}
-
 // Pooled split (PA_FLAG_POOLED): the blocks of a (sequence, kv head) are
 // dealt to the warps of its partition CTAs in chunks of pool_chunk(stages)
 // blocks (at least the copy depth, so the copies run at most one chunk
@@ -145,7 +128,7 @@ struct ScanParams {
     int* work_counter;  // set to first_dynamic (the persistent grid size)
     int num_seqs, max_seq_len, max_blocks_per_seq, num_kv_heads, first_dynamic;
     int partition_size;  // > 0: balanced_partition with this size
-    int slots;           // else apportioned_partition with this many partitions per kv head
+    int slots;           // else partitions per kv head to apportion (the cap that fits them)
 };
 
 // Dynamic shared memory of a partition CTA of `warps` warps with `stages`

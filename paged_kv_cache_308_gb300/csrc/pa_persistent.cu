@@ -18,9 +18,11 @@ namespace pa {
 // writes the exclusive prefix sums of their work items in that order (one
 // item per (partition, kv head), one per kv head for an empty sequence, one
 // for an invalid length), then resets the item counter.  Without a caller's
-// partition size, the partitions are apportioned: a batch whose lengths sum
-// to T gives sequence b floor(slots * L_b / T) partitions (at least one),
-// slots = grid / kv heads, so the items fill about one wave of the grid.
+// partition size, the partitions are apportioned: with slots = grid / kv
+// heads, the scan finds the smallest cap S (blocks per partition) for which
+// the batch's partitions -- ceil(blocks_b / S) per sequence -- fit the
+// slots, so the items fill one wave and the longest is as short as one wave
+// allows; with at least as many sequences as slots, S = total blocks / slots.
 // A fixed grid of NW-warp CTAs (every CTA the SMs hold at once) takes items
 // from that counter: CTA x starts with item x and then draws the next index
 // with atomicAdd, so the last items -- the shortest, by the order -- end
@@ -515,10 +517,11 @@ cudaError_t launch_partition_persistent(int head_dim, int warps, int stages, con
 
 // The work list of the persistent schedule, built by one CTA of 1024 threads
 // (thread x handles a contiguous run of sequences):
-//  1. T = the sum of the valid lengths, and whether the rounded-down
-//     apportioned counts fit one wave (block reductions);
-//  2. each sequence's partition size (apportioned_partition over T, or
-//     balanced_partition with the caller's size) and item count: one per
+//  1. T = the valid non-empty sequences' blocks and their count (block
+//     reductions), then the apportioning cap: each round the 32 warps count
+//     the partitions of 32 candidate caps at once;
+//  2. each sequence's partition size (balanced_partition with the cap, or
+//     with the caller's size) and item count: one per
 //     (partition, kv head), one per kv head for an empty sequence (its output
 //     is zeroed), one for an invalid length (it is reported);
 //  3. the schedule order: a counting sort of the sequences by partition
@@ -568,41 +571,84 @@ __global__ void __launch_bounds__(kScanThreads) pa_work_scan_kernel(const ScanPa
     asm volatile("griddepcontrol.launch_dependents;");
     __shared__ int cursor[kOrderKeys];  // per key: count, then next rank
     __shared__ int warp_sums[kScanThreads / 32];
-    __shared__ unsigned long long s_total, s_floor_parts;
+    __shared__ int s_nblk[kScanThreads];  // blocks of sequence b when B <= kScanThreads (0: empty or invalid)
+    __shared__ int s_fits[kScanThreads / 32];
+    __shared__ unsigned long long s_blocks;
+    __shared__ int s_count;
     const int B = prm.num_seqs;
     const int per = (B + kScanThreads - 1) / kScanThreads;
     const int b0 = threadIdx.x * per, b1 = min(B, b0 + per);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int x = threadIdx.x; x < kOrderKeys; x += kScanThreads) cursor[x] = 0;
-    if (threadIdx.x == 0) s_total = s_floor_parts = 0;
+    if (threadIdx.x == 0) {
+        s_blocks = 0;
+        s_count = 0;
+    }
     __syncthreads();
-
-    // 1. the sum of the valid lengths
-    unsigned long long mine = 0;
-    for (int b = b0; b < b1; ++b) {
+    auto blocks_at = [&](int b) {
         const int L = __ldg(prm.seq_lens + b);
-        if (scan_valid(prm, L)) mine += (unsigned long long)L;
+        return (scan_valid(prm, L) && L > 0) ? (L + kBlockSize - 1) / kBlockSize : 0;
+    };
+
+    // 1. the valid non-empty sequences' blocks and their count
+    unsigned long long mine = 0;
+    int cnt = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int nb = blocks_at(b);
+        if (B <= kScanThreads) s_nblk[b] = nb;
+        if (nb) {
+            mine += (unsigned long long)nb;
+            ++cnt;
+        }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(kFull, mine, off);
-    if ((threadIdx.x & 31) == 0 && mine) atomicAdd(&s_total, mine);
+    for (int off = 16; off > 0; off >>= 1) {
+        mine += __shfl_xor_sync(kFull, mine, off);
+        cnt += __shfl_xor_sync(kFull, cnt, off);
+    }
+    if (lane == 0 && cnt) {
+        atomicAdd(&s_blocks, mine);
+        atomicAdd(&s_count, cnt);
+    }
     __syncthreads();
-    const long long T = (long long)s_total;
-    // the rounded-down partition counts (at least one each): do they fit one wave?
-    bool round_up = false;
-    if (prm.partition_size <= 0) {
-        unsigned long long fl = 0;
-        for (int b = b0; b < b1; ++b) {
-            const int L = __ldg(prm.seq_lens + b);
-            if (scan_valid(prm, L) && L > 0) {
-                const int part = apportioned_partition(L, T, prm.slots, false);
-                fl += (unsigned long long)((L + part - 1) / part);
+    // The apportioning cap: the smallest S with sum_b ceil(blocks_b / S) <= slots
+    // (the count only falls as S grows).  lo = ceil(T / slots) is a lower
+    // bound; with fewer sequences than slots, hi = ceil(T / (slots - count))
+    // fits, since each ceiling adds less than one.  Each round the 32 warps
+    // count the partitions of 32 caps spread over [lo, hi] at once and keep
+    // the stretch below the smallest cap that fits: the range shrinks 32-fold
+    // a round, one or two rounds in practice.
+    long long cap = 1;
+    if (prm.partition_size <= 0 && s_count > 0) {
+        const long long Tb = (long long)s_blocks;
+        const int slots = prm.slots, nv = s_count;
+        long long lo = (Tb + slots - 1) / slots, hi = lo;
+        if (nv < slots) hi = (Tb + (slots - nv) - 1) / (slots - nv);
+        while (lo < hi) {  // lo and hi are the same on every thread
+            const long long c = lo + ((hi - lo) * warp) / 32;
+            unsigned long long parts = 0;
+            for (int b = lane; b < B; b += 32) {
+                const int nb = B <= kScanThreads ? s_nblk[b] : blocks_at(b);
+                parts += (unsigned long long)((nb + c - 1) / c);
             }
-        }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) fl += __shfl_xor_sync(kFull, fl, off);
-        if ((threadIdx.x & 31) == 0 && fl) atomicAdd(&s_floor_parts, fl);
-        __syncthreads();
-        round_up = s_floor_parts > (unsigned long long)prm.slots;
+            for (int off = 16; off > 0; off >>= 1) parts += __shfl_xor_sync(kFull, parts, off);
+            if (lane == 0) s_fits[warp] = parts <= (unsigned long long)slots;
+            __syncthreads();
+            int first = 32;  // the smallest candidate that fits
+            for (int w = 31; w >= 0; --w)
+                if (s_fits[w]) first = w;
+            const long long c_first = lo + ((hi - lo) * (first < 32 ? first : 31)) / 32;
+            const long long c_before = first > 0 ? lo + ((hi - lo) * (first - 1)) / 32 : lo - 1;
+            if (first == 32) {
+                lo = c_first + 1;
+            } else {
+                hi = c_first;
+                lo = c_before + 1;
+            }
+            __syncthreads();  // s_fits is written again next round
+        }
+        cap = lo;
     }
 
     // 2. partition sizes, item counts, sort keys (bucket 0 = the longest)
@@ -610,12 +656,11 @@ __global__ void __launch_bounds__(kScanThreads) pa_work_scan_kernel(const ScanPa
         if (!scan_valid(prm, L) || L == 0) return kOrderKeys - 1;
         return kOrderKeys - 1 - min(part / kBlockSize, kOrderKeys - 1);
     };
+    const int pmax = prm.partition_size > 0 ? prm.partition_size : (int)min(cap * kBlockSize, (long long)1 << 30);
     for (int b = b0; b < b1; ++b) {
         const int L = __ldg(prm.seq_lens + b);
         int part = kBlockSize;
-        if (scan_valid(prm, L) && L > 0)
-            part = prm.partition_size > 0 ? balanced_partition(L, prm.partition_size)
-                                          : apportioned_partition(L, T, prm.slots, round_up);
+        if (scan_valid(prm, L) && L > 0) part = balanced_partition(L, pmax);
         prm.part_sizes[b] = part;
         atomicAdd(&cursor[key_of(L, part)], 1);
     }
