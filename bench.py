@@ -472,7 +472,8 @@ def run_gpu(args):
     part_s = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
     achieved = kv / part_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(args.workload), "kernel": f"pa_partition_kernel<{w.head_dim}, {plan['threads'] // 32}, {plan['stages']}>",
+                "traffic": profiled_traffic(args.workload), "kernel": f"pa_partition_kernel<{w.head_dim}, {plan['threads'] // 32}, {plan['stages']}"
+                + (", pooled>" if plan["pooled"] else ">"),
                 "algorithmic_bytes_per_launch": kv, "launch_us": part_s * 1e6,
                 "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)"}
 
@@ -536,6 +537,7 @@ def run_gpu(args):
                        "kv_bytes_per_step": kv, "tokens_in_cache": w.total_tokens,
                        "mode": "split" if plan["launch_reduce"] else "single",
                        "partition_size": plan["partition_size"],
+                       "pooled": bool(plan["pooled"]),
                        "l2": f"inputs larger than L2 ({kv / 1e6:.0f} MB of K/V vs 129 MB L2), no flush",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_hbm_peak": 100 * per_gpu / peak,
