@@ -484,3 +484,28 @@ def test_one_wave_plan_pools_by_default_and_deterministic_flag_fixes_the_bits(de
         out = run(w, workspace=ws, mode="auto")
         assert_parity(out, ref, f"one wave, pooled call {k}")
         assert (out.float() - fixed[0].float()).abs().max().item() < 2e-3
+
+
+def test_pooled_bad_block_id_and_bad_length(dev):
+    # the kernel's own checks in the pooled form: an illegal block id is
+    # reported and skipped, an illegal length reported, and the claim
+    # counters stay armed for the next call
+    w = W.make_workload("poolbad", [5000, 3000], num_blocks=600, seed=19, device=dev)
+    opt = dict(mode="split", partition_size=512, flags=pb.PA_FLAG_POOLED)
+    plan = _pooled_plan(w, mode="split", partition_size=512)
+    ws = pb.alloc_workspace(plan, dev)
+    ref = oracle_ref(w)
+    assert_parity(run(w, workspace=ws, **opt), ref, "pooled before")
+    good = w.block_tables.clone()
+    pb.pa_get_device_status()
+    w.block_tables[0, 37] = w.num_blocks + 3
+    w.block_tables[1, 5] = -5
+    pb.decode_workload(w, workspace=ws, **opt)
+    assert pb.pa_get_device_status() & pb.PA_DEV_BAD_BLOCK_ID
+    assert (_claims(ws, plan, w) == CLAIM_ARMED).all()
+    w.block_tables.copy_(good)
+    w.seq_lens[1] = 5001  # above the max_seq_len hint
+    pb.decode_workload(w, workspace=ws, **opt)
+    assert pb.pa_get_device_status() & pb.PA_DEV_BAD_SEQ_LEN
+    w.seq_lens[1] = 3000
+    assert_parity(run(w, workspace=ws, **opt), ref, "pooled after the errors")
