@@ -417,7 +417,7 @@ def _pooled_plan(w, **opt):
 ], ids=["b1_l102400", "ragged_P256", "P512_1x3", "P512_2x2", "P1024_4x2", "b6_P256_1x2", "P48_1x3", "P128_4x2"])
 def test_pooled_split_parity(dev, lens, opt):
     w = W.make_workload("pooled", lens, num_blocks=sum((L + 15) // 16 for L in lens) + 11, seed=sum(lens) % 97,
-                        device=dev, tail_fill=float("nan"))
+                        device=dev, tail_fill=float("nan"), extra_table_cols=len(lens) % 3 * 5)
     plan = _pooled_plan(w, **opt)
     assert plan["pooled"] == 1
     ws = pb.alloc_workspace(plan, dev)  # zero: the first call deals the chunks round-robin
