@@ -272,3 +272,11 @@ def test_pooled_plan_flags_and_workspace():
     assert _plan_opts(4, 500, flags=pb.PA_FLAG_POOLED)["pooled"] == 0  # one partition: no reduce
     for mode in (1, 3, 4):
         assert _plan_opts(4, 4096, mode=mode, flags=pb.PA_FLAG_POOLED)["pooled"] == 0
+
+
+@pytest.mark.parametrize("B,L", [(1, 2048), (1, 30000), (1, 77824), (1, 102400), (1, 1 << 20), (8, 8192), (64, 65536)])
+def test_workspace_size_bounds_every_automatic_plan(B, L):
+    # pa_decode_workspace_size(..., 0) is documented as an upper bound for the
+    # automatic partition size, pooled counters included
+    pl = _plan_opts(B, L)
+    assert pb.pa_decode_workspace_size(B, L, 24, 256, 0) >= pl["workspace_bytes"]
