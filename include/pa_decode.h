@@ -204,9 +204,10 @@ int pa_decode_plan(const pa_decode_args* args, const pa_decode_opts* opts, int n
                    pa_decode_plan_t* plan);
 
 /* Workspace bytes of a SPLIT call with these sizes; partition_size 0 gives an upper
- * bound for the automatic partition size.  FUSED needs 256-byte-aligned
- * num_seqs * num_kv_heads * 4 bytes more; PERSISTENT has its own partition count and
- * tables (work list, order, sizes).  pa_decode_plan gives every mode's exact figure. */
+ * bound for the automatic partition size (its pooled claim counters included).  FUSED
+ * needs 256-byte-aligned num_seqs * num_kv_heads * 4 bytes more, a pooled SPLIT
+ * num_seqs * num_kv_heads * 8; PERSISTENT has its own partition count and tables (work
+ * list, order, sizes).  pa_decode_plan gives every mode's exact figure. */
 size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim,
                                 int partition_size);
 
