@@ -117,8 +117,10 @@ enum {
                                     last bits.  Applies when the plan is SPLIT with partition_size
                                     >= warps * 16 * max(2, stages) tokens (plan.pooled).  The
                                     workspace also holds one 8-byte counter per (sequence, kv head)
-                                    after the partials; any initial value is safe (a counter the
-                                    reduce kernel has not armed keeps the round-robin).  The
+                                    after the partials; it needs no initialisation: a counter whose
+                                    high word is not the tag the reduce kernel writes there keeps
+                                    the round-robin (values that other calls leave in a shared
+                                    workspace are floats, never that tag).  The
                                     planner's one-wave plan for one long sequence is pooled
                                     without this flag */
     PA_FLAG_DETERMINISTIC = 8    /* never pool (not even the one-wave plan): each partial covers
