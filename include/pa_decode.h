@@ -119,8 +119,9 @@ enum {
                                     workspace also holds one 8-byte counter per (sequence, kv head)
                                     after the partials; it needs no initialisation: a counter whose
                                     high word is not the tag the reduce kernel writes there keeps
-                                    the round-robin (values that other calls leave in a shared
-                                    workspace are floats, never that tag).  The
+                                    the round-robin (the partials, tickets and work lists that
+                                    other calls leave in a shared workspace never hold that tag).
+                                    The
                                     planner's one-wave plan for one long sequence is pooled
                                     without this flag */
     PA_FLAG_DETERMINISTIC = 8    /* never pool (not even the one-wave plan): each partial covers
