@@ -121,8 +121,7 @@ enum {
                                     high word is not the tag the reduce kernel writes there keeps
                                     the round-robin (the partials, tickets and work lists that
                                     other calls leave in a shared workspace never hold that tag).
-                                    The
-                                    planner's one-wave plan for one long sequence is pooled
+                                    The planner's one-wave plan for one long sequence is pooled
                                     without this flag */
     PA_FLAG_DETERMINISTIC = 8    /* never pool (not even the one-wave plan): each partial covers
                                     fixed blocks, so repeated calls give identical bits */
