@@ -280,3 +280,30 @@ def test_workspace_size_bounds_every_automatic_plan(B, L):
     # automatic partition size, pooled counters included
     pl = _plan_opts(B, L)
     assert pb.pa_decode_workspace_size(B, L, 24, 256, 0) >= pl["workspace_bytes"]
+
+
+def _plan_heads(num_kv_heads, max_seq_len, flags=0, num_heads=None):
+    H = num_heads or 6 * num_kv_heads
+    o = pb.pa_decode_opts(0, 0, flags, 0, None, None, 0, 0)
+    pl = pb.pa_decode_plan_t()
+    a = args(num_seqs=1, max_seq_len=max_seq_len, H=H, Hkv=num_kv_heads,
+             num_blocks=(max_seq_len + 15) // 16)
+    assert pb.lib.pa_decode_plan(ctypes.byref(a), ctypes.byref(o), SMS, ctypes.byref(pl)) == 0
+    return pl.as_dict()
+
+
+@pytest.mark.parametrize("hkv", [1, 2, 4, 8])
+@pytest.mark.parametrize("L", [102400, 262144, 1 << 20])
+def test_one_wave_pooled_plan_for_every_kv_head_count(hkv, L):
+    pl = _plan_heads(hkv, L)
+    per_head = SMS // hkv
+    if -(-L // per_head) < 2048:  # partitions shorter than 2048 tokens keep the 512-token plan
+        assert pl["partition_size"] == 512 and pl["pooled"] == 0
+        return
+    # one 4-warp CTA per SM at most, partitions of whole blocks covering the sequence, pooled
+    assert pl["threads"] == 128 and pl["stages"] == 2 and pl["pooled"] == 1
+    assert pl["grid_x"] * pl["grid_y"] <= SMS and pl["grid_y"] == hkv
+    assert pl["partition_size"] % 16 == 0 and pl["partition_size"] * pl["grid_x"] >= L
+    fixed = _plan_heads(hkv, L, flags=pb.PA_FLAG_DETERMINISTIC)
+    assert fixed["pooled"] == 0 and fixed["grid_x"] == pl["grid_x"] and fixed["partition_size"] == pl["partition_size"]
+    assert fixed["workspace_bytes"] + 256 == pl["workspace_bytes"]
