@@ -221,3 +221,43 @@ def test_lse_and_fold_agree_on_random_partials():
                                    rtol=1e-12, atol=1e-14)
     z = oracle.combine_lse(np.zeros(0), np.zeros(0), np.zeros((0, 4)))
     assert np.array_equal(z, np.zeros(4))
+
+
+@pytest.mark.parametrize("H,Hkv,D,bs,lens", [
+    (6, 2, 16, 4, [1, 9, 23]),      # more heads than sequences
+    (4, 4, 8, 2, [7, 2, 5, 11, 3]),  # more sequences than heads
+    (24, 4, 64, 16, [15, 40]),
+])
+def test_decode_one_row_by_row_against_dense_library_attention(H, Hkv, D, bs, lens):
+    # The single-(sequence, head) entry point, pinned independently of the
+    # batch routine: each (b, h) row against torch's dense attention on the
+    # dense K/V the paged pool was scattered from, and against the batch.
+    q, kc, vc, bt, sl, dk, dv = _dense_then_paged(lens, H, Hkv, D, bs, extra_blocks=2, seed=100 + H + D)
+    scale = 1.0 / math.sqrt(D)
+    G = H // Hkv
+    full = oracle.paged_decode(q, kc, vc, bt, sl, H, Hkv, D, bs, scale)
+    for b, L in enumerate(lens):
+        for h in range(H):
+            row = oracle.paged_decode_one(q, kc, vc, bt, sl, H, Hkv, D, bs, scale, b, h)
+            qq = torch.from_numpy(q[b, h].astype(np.float64)).view(1, 1, 1, D)
+            kk = torch.from_numpy(dk[b][h // G].astype(np.float64)).view(1, 1, L, D)
+            vv = torch.from_numpy(dv[b][h // G].astype(np.float64)).view(1, 1, L, D)
+            ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, scale=scale).view(D).numpy()
+            np.testing.assert_allclose(row, ref, rtol=1e-12, atol=1e-13)
+            assert np.array_equal(row, full[b, h])
+
+
+def test_decode_one_closed_forms_and_bounds():
+    q, kc, vc, bt, sl, dk, dv = _dense_then_paged([1, 30], 4, 2, 8, 4, 1, seed=101)
+    # one key: its value exactly; zero query: the mean of the values
+    for h in range(4):
+        assert np.array_equal(oracle.paged_decode_one(q, kc, vc, bt, sl, 4, 2, 8, 4, 0.5, 0, h),
+                              dv[0][h // 2, 0].astype(np.float64))
+    q0 = q.copy()
+    q0[1] = 0
+    for h in range(4):
+        np.testing.assert_allclose(oracle.paged_decode_one(q0, kc, vc, bt, sl, 4, 2, 8, 4, 0.5, 1, h),
+                                   dv[1][h // 2].astype(np.float64).mean(axis=0), rtol=1e-13, atol=1e-15)
+    for b, h in ((2, 0), (-1, 0), (0, 4), (0, -1)):
+        with pytest.raises(oracle.OracleError):
+            oracle.paged_decode_one(q, kc, vc, bt, sl, 4, 2, 8, 4, 0.5, b, h)
