@@ -63,7 +63,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.CONFIG_NAMES)
-    ap.add_argument("--all-configs", action="store_true", help="also time the other four workloads")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="longer per-workload timing (500 calls instead of 200); the other workloads are always timed")
+    ap.add_argument("--no-per-config", action="store_true", help="time the headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
     ap.add_argument("--seed", type=int, default=0)
@@ -347,6 +349,80 @@ def time_e2e(pb, w, stream, dev, steps, nbuf=2):
     return (start.elapsed_time(end) / 1e3, steps, h_in.numel(), h_out[0].numel() * 2)
 
 
+def measure_workload(pb, w, stream, dev, peak, n):
+    """Back-to-back, cold-L2 and graph-replayed figures of the library's own
+    plan (pa_decode, AUTO) on one workload."""
+    out = torch.empty_like(w.q)
+    fn = lambda: pb.pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                              w.num_kv_heads, w.head_dim, w.block_size, w.scale, stream, max_seq_len=w.max_seq_len)
+    for _ in range(20):
+        fn()
+    torch.cuda.synchronize()
+    el = time_steps(fn, n, stream)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len)
+    return {"kv_bytes": w.kv_bytes, "us_per_call": el / n * 1e6, "GB_per_s": w.kv_bytes * n / el / 1e9,
+            "pct_of_hbm_peak": 100 * w.kv_bytes * n / el / 1e9 / peak, "calls_per_s": n / el,
+            "tokens_per_s": w.num_seqs * n / el,
+            "plan": {"mode": "split" if plan["launch_reduce"] else "single", "partition_size": plan["partition_size"],
+                     "cta": f"{plan['threads'] // 32}x{plan['stages']}", "grid": [plan["grid_x"], plan["grid_y"],
+                                                                                   plan["grid_z"]],
+                     "pooled": bool(plan["pooled"])},
+            "l2": "larger than L2" if w.kv_bytes > 129e6 else "fits in L2 (warm)",
+            "latency_us_l2_flushed": flushed_latency_us(fn, stream, dev),
+            "graph_calls_per_s": graph_calls_per_s(pb, w, dev)}
+
+
+def measure_variant(pb, w, stream, dev, peak, n, **opt):
+    """Back-to-back figure of one explicitly requested plan (pa_decode_ex with a
+    caller workspace kept across calls)."""
+    out = torch.empty_like(w.q)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len, **opt)
+    ws = pb.alloc_workspace(plan, dev)
+    fn = lambda: pb.pa_decode_ex(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                                 w.num_kv_heads, w.head_dim, w.block_size, w.scale, stream,
+                                 max_seq_len=w.max_seq_len, workspace=ws, **opt)
+    for _ in range(20):
+        fn()
+    torch.cuda.synchronize()
+    el = time_steps(fn, n, stream)
+    return {"us_per_call": el / n * 1e6, "GB_per_s": w.kv_bytes * n / el / 1e9,
+            "pct_of_hbm_peak": 100 * w.kv_bytes * n / el / 1e9 / peak, "calls_per_s": n / el,
+            "partition_size": plan["partition_size"], "partitions": plan["max_partitions"],
+            "cta": f"{plan['threads'] // 32}x{plan['stages']}", "pooled": bool(plan["pooled"])}
+
+
+def measure_split_kv(pb, w, stream, dev, peak, n, sources=2, partition_size=512):
+    """Split-KV across devices, kernel side, emulated on this one GPU: the
+    partials of each source's range of partitions (one pa_decode_partials
+    call per source into its slot of the gathered buffer), then
+    pa_merge_partials.  No exchange between devices takes place."""
+    from paged_kv_cache_308_gb300 import split_kv
+    ranges = [split_kv.partition_range(r, sources, w.max_seq_len, partition_size) for r in range(sources)]
+    count = ranges[0][1]
+    gm, gl, gacc = split_kv.alloc_partials(w.num_seqs, w.num_heads, w.head_dim, count, dev, sources=sources)
+    out = torch.empty_like(w.q)
+
+    def fn():
+        for r, (b, c) in enumerate(ranges):
+            pb.pa_decode_partials(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                                  w.num_kv_heads, w.head_dim, w.block_size, w.scale, partition_size, b, c, gm[r],
+                                  gl[r], gacc[r], stream, max_seq_len=w.max_seq_len)
+        pb.pa_merge_partials(out, gm, gl, gacc, w.seq_lens, w.num_heads, w.head_dim, partition_size, sources, count,
+                             stream, max_seq_len=w.max_seq_len)
+
+    for _ in range(20):
+        fn()
+    torch.cuda.synchronize()
+    el = time_steps(fn, n, stream)
+    return {"us_per_call": el / n * 1e6, "GB_per_s": w.kv_bytes * n / el / 1e9,
+            "pct_of_hbm_peak": 100 * w.kv_bytes * n / el / 1e9 / peak, "sources": sources,
+            "partition_size": partition_size, "partitions_per_source": count,
+            "launches_per_call": sources + 1,
+            "note": "all sources on this one GPU, one after another; no exchange between devices"}
+
+
 def run_reference(args):
     """The float64 oracle on the host cores.  Each step is a bounded sample of
     the workload: every (sequence, head) pair over the first L' tokens of its
@@ -494,30 +570,30 @@ def run_gpu(args):
     lat_flushed = flushed_latency_us(step, stream, dev)
     graph_cps = graph_calls_per_s(pb, w, dev)
 
+    # the same workload under two other plans: the pages' 512-token partitions
+    # (fixed split), and the one-wave plan with fixed partitions (deterministic);
+    # and the split-KV-across-devices kernels with two sources on this GPU
+    n_var = 500 if args.all_configs else 200
+    variants = None
+    if rank == 0 and not args.no_per_config:
+        variants = {"split_p512": measure_variant(pb, w, stream, dev, peak, n_var, mode="split", partition_size=512),
+                    "auto_deterministic": measure_variant(pb, w, stream, dev, peak, n_var,
+                                                          flags=pb.PA_FLAG_DETERMINISTIC),
+                    "split_kv_2_sources_1gpu": measure_split_kv(pb, w, stream, dev, peak, n_var)}
+
     per_config = None
-    if args.all_configs and rank == 0:
+    if rank == 0 and not args.no_per_config:
         per_config = {}
         for name in W.CONFIG_NAMES:
             if name == args.workload:
                 continue
             wc = W.make_config(name, device=dev, seed=args.seed)
-            oc = torch.empty_like(wc.q)
-            fn = lambda: pb.pa_decode(oc, wc.q, wc.k_cache, wc.v_cache, wc.block_tables, wc.seq_lens,
-                                      wc.num_heads, wc.num_kv_heads, wc.head_dim, wc.block_size, wc.scale, stream,
-                                      max_seq_len=wc.max_seq_len)
-            for _ in range(20):
-                fn()
-            torch.cuda.synchronize()
-            n = 500
-            el = time_steps(fn, n, stream)
-            per_config[name] = {"kv_bytes": wc.kv_bytes, "us_per_call": el / n * 1e6,
-                                "GB_per_s": wc.kv_bytes * n / el / 1e9,
-                                "pct_of_hbm_peak": 100 * wc.kv_bytes * n / el / 1e9 / peak,
-                                "calls_per_s": n / el, "tokens_per_s": wc.num_seqs * n / el,
-                                "l2": "larger than L2" if wc.kv_bytes > 129e6 else "fits in L2 (warm)",
-                                "latency_us_l2_flushed": flushed_latency_us(fn, stream, dev),
-                                "graph_calls_per_s": graph_calls_per_s(pb, wc, dev)}
-            del wc, oc
+            per_config[name] = measure_workload(pb, wc, stream, dev, peak, n_var)
+            if name == "b8_u8192":  # both decode modes of this workload
+                per_config[name]["single"] = measure_variant(pb, wc, stream, dev, peak, n_var, mode="single")
+                per_config[name]["split_p512"] = measure_variant(pb, wc, stream, dev, peak, n_var, mode="split",
+                                                                 partition_size=512)
+            del wc
             torch.cuda.empty_cache()
         # chunked prefill over the paged cache (both kernels), TFLOP/s
         from paged_kv_cache_308_gb300 import prefix_bench
@@ -551,6 +627,8 @@ def run_gpu(args):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
+        if variants is not None:
+            line["variants"] = variants
         if per_config is not None:
             line["per_config"] = per_config
         print(json.dumps(line), flush=True)

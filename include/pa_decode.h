@@ -81,15 +81,22 @@ enum {
 
 /* Execution modes. */
 enum {
-    PA_MODE_AUTO = 0,   /* library picks SINGLE, SPLIT or FUSED from the sizes (see pa_decode_plan) */
+    PA_MODE_AUTO = 0,   /* library picks SINGLE or SPLIT from the sizes (see pa_decode_plan) */
     PA_MODE_SINGLE = 1, /* one CTA per (kv head, sequence) covers the whole sequence; no reduce */
     PA_MODE_SPLIT = 2,  /* partitions of partition_size tokens + log-sum-exp reduce kernel */
     PA_MODE_FUSED = 3,  /* partitions as SPLIT, one launch: the last CTA of each (sequence, kv head)
                            to finish (an atomic ticket; nobody waits) merges the partials in
-                           partition order.  The workspace also holds one ticket per
-                           (sequence, kv head) that must be zero before the first call on it;
-                           every call leaves the tickets zero, also after a device error */
-    PA_MODE_PERSISTENT = 4 /* a fixed grid of (SMs x CTAs per SM) takes the items of a work list
+                           partition order ("docs" commit page, the cross-partition level of the
+                           reduction hierarchy, here without any CTA waiting on another).  The
+                           workspace also holds one 4-byte ticket per (sequence, kv head), after
+                           the partials and a slot the size of the pooled claim counters, so a
+                           pooled call of the same shape on the same workspace leaves them
+                           alone.  The tickets must be zero before the first FUSED call on a
+                           workspace, and again after the workspace served a call of another
+                           shape or a PERSISTENT call (whose tables cover that slot): zero
+                           plan.workspace_bytes, e.g. with cudaMemsetAsync.  Every FUSED call
+                           leaves them zero, also after a device error */
+    PA_MODE_PERSISTENT = 4, /* a fixed grid of (SMs x CTAs per SM) takes the items of a work list
                               that a small kernel builds on the device from a device counter,
                               longest partitions first.  Each sequence gets its own partition size:
                               with partition_size 0 the grid's partitions per kv head are
@@ -100,6 +107,15 @@ enum {
                               log-sum-exp reduce.  The host never reads the lengths, so the call is
                               graph-safe.  The workspace also holds the work list, the counter,
                               the order and the sizes (rewritten by every call) */
+    PA_MODE_FLAT = 5    /* one wave of one CTA per SM, num_SMs / num_kv_heads CTAs per kv head:
+                           every CTA reads the lengths on the device and streams an equal share
+                           (to within one block) of the batch's concatenated blocks, one partial
+                           per sequence its share meets, then the log-sum-exp reduce; no ragged
+                           tail of short and long CTAs, whatever the lengths.  At most 256
+                           sequences (else PA_ERR_UNSUPPORTED).  The workspace also holds each
+                           sequence's partial count (rewritten by every call).  A refinement of
+                           the "docs" commit page's partitions: a partition is a CTA's share of
+                           one sequence, and the partials and their merge are unchanged */
 };
 
 /* Option flags. */
@@ -117,12 +133,16 @@ enum {
                                     last bits.  Applies when the plan is SPLIT with partition_size
                                     >= warps * 16 * max(2, stages) tokens (plan.pooled).  The
                                     workspace also holds one 8-byte counter per (sequence, kv head)
-                                    after the partials; it needs no initialisation: a counter whose
-                                    high word is not the tag the reduce kernel writes there keeps
-                                    the round-robin (the partials, tickets and work lists that
-                                    other calls leave in a shared workspace never hold that tag).
+                                    right after the partials; it needs no initialisation: a counter
+                                    whose high word is not the tag the reduce kernel writes there
+                                    keeps the round-robin, and the reduce leaves every counter
+                                    tagged with a zero count (a call whose reduce launch fails
+                                    resets them to zero instead).  Stale bytes left by other calls
+                                    are therefore tolerated: this library's partials (bounded by
+                                    the fp16 inputs), tickets and work lists never hold the tag.
                                     The planner's one-wave plan for one long sequence is pooled
-                                    without this flag */
+                                    without this flag.  Source of the split it refines: "docs"
+                                    commit page, GQA-aware grid and partition paragraphs */
     PA_FLAG_DETERMINISTIC = 8    /* never pool (not even the one-wave plan): each partial covers
                                     fixed blocks, so repeated calls give identical bits */
 };
@@ -182,6 +202,10 @@ typedef struct {
 } pa_decode_plan_t;
 
 /* Decode attention with a library-owned workspace.
+ * Sources: "docs" commit page (GQA-aware grid on kv heads, Phase 1 partition
+ * and Phase 2 reduce kernels, the compound partial); "paged_attention_v2_triton.py"
+ * commit page (the alpha/beta online-softmax update); "qwen3_6_scripts/paged_attn.py"
+ * commit page (decode dispatch by sequence length; the buffer-reuse paragraphs).
  * The workspace for the partials is cached per device and grown on demand
  * (allocate once, reuse across calls); growing it synchronises the device, so
  * the first call with a larger size must not be inside a stream capture, and
@@ -195,32 +219,57 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
 
 /* Decode attention with caller-owned workspace (device memory, 256-byte
  * aligned, at least plan.workspace_bytes; may be NULL when that is 0).
- * Allocates nothing, so it can be captured in a CUDA graph.  opts may be NULL. */
+ * Allocates nothing, so it can be captured in a CUDA graph.  opts may be NULL.
+ * Same operation and sources as pa_decode; the caller-owned buffer follows the
+ * buffer-reuse paragraphs of the "qwen3_6_scripts/paged_attn.py" commit page
+ * (allocate once outside the hot loop, pass it in).  The workspace's layout
+ * (partials, then the pooled counters, FUSED tickets or PERSISTENT tables) is
+ * the library's; its contents between calls are described under the modes and
+ * flags above.  Returns PA_ERR_WORKSPACE for a buffer that is too small or
+ * misaligned, before launching anything. */
 int pa_decode_ex(const pa_decode_args* args, const pa_decode_opts* opts, void* workspace,
                  size_t workspace_bytes, pa_stream_t stream);
 
 /* Validate the arguments and fill *plan with the launches a call would make.
  * num_sms > 0 is the SM count to plan for; 0 asks the current device.  Pure
- * host logic when num_sms > 0.  Returns the same codes a call would. */
+ * host logic when num_sms > 0.  Returns the same codes a call would.
+ * Source: the decode dispatch of the "qwen3_6_scripts/paged_attn.py" commit
+ * page (single-CTA kernel vs partitioned kernel by sequence length; the
+ * thresholds here are this library's, from GB300 measurements) and the grid
+ * arithmetic of the "docs" commit page's GQA-aware grid paragraph
+ * ((partitions, kv heads) programs per sequence). */
 int pa_decode_plan(const pa_decode_args* args, const pa_decode_opts* opts, int num_sms,
                    pa_decode_plan_t* plan);
 
-/* Workspace bytes of a SPLIT call with these sizes; partition_size 0 gives an upper
- * bound for the automatic partition size (its pooled claim counters included).  FUSED
- * needs 256-byte-aligned num_seqs * num_kv_heads * 4 bytes more, a pooled SPLIT
- * num_seqs * num_kv_heads * 8; PERSISTENT has its own partition count and tables (work
- * list, order, sizes).  pa_decode_plan gives every mode's exact figure. */
+/* Workspace bytes of a SPLIT call with these sizes: the compound partials of
+ * the "docs" commit page (max score, exp sum, weighted V per partition, fp32),
+ * sized once for reuse as the "qwen3_6_scripts/paged_attn.py" commit page's
+ * buffer-reuse paragraphs advise.  partition_size 0 gives an upper bound for the
+ * automatic partition size (its pooled claim counters included).  A pooled SPLIT
+ * needs 256-byte-aligned num_seqs * num_kv_heads * 8 bytes more; FUSED that much
+ * plus 256-byte-aligned num_seqs * num_kv_heads * 4; PERSISTENT has its own
+ * partition count and tables (work list, order, sizes).  pa_decode_plan gives
+ * every mode's exact figure.  Returns 0 for non-positive sizes. */
 size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim,
                                 int partition_size);
 
 /* Synchronise `stream`, then read and clear the current device's status word
- * into *status (PA_DEV_* bits).  Returns PA_OK or PA_ERR_CUDA. */
+ * into *status (PA_DEV_* bits).  Returns PA_OK, PA_ERR_INVALID_ARG (status
+ * NULL) or PA_ERR_CUDA.  Source: the "qwen3_6_scripts/paged_attn.py" commit
+ * page's account of a prefill kernel that hung the GPU for good and of the
+ * try/except fallbacks added around it; this library replaces both with
+ * bounded waits and this host-read status word (no fallback, no trap). */
 int pa_get_device_status(pa_stream_t stream, int* status);
 
-/* Static English text for a return code. */
+/* Static English text for a return code (never NULL; "unknown status" for a
+ * code not listed above).  Part of the same error reporting as
+ * pa_get_device_status; the pages print no counterpart. */
 const char* pa_status_string(int status);
 
-/* Free the library-owned workspaces of every device (synchronises them). */
+/* Free the library-owned workspaces of every device (synchronises them, then
+ * restores the current device).  The counterpart of the allocate-once cache of
+ * the "qwen3_6_scripts/paged_attn.py" commit page's buffer-reuse paragraphs: the
+ * next pa_decode allocates again.  Never frees caller memory. */
 void pa_release_workspace(void);
 
 /* Chunked-prefill ("prefix") attention over the paged cache.
@@ -296,13 +345,67 @@ int pa_prefix_ex(const pa_prefix_args* args, const pa_decode_opts* opts, pa_stre
  *    GPU (other streams, other host threads) race and give wrong outputs.
  *    Calls queued on a single stream are safe.
  *  - Nothing in the array has to start at zero: each call writes every partial
- *    it reads. */
+ *    it reads, and the pooled split's claim counters tolerate whatever an
+ *    earlier call of another shape left there (see PA_FLAG_POOLED). */
 int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
                       int max_blocks_per_seq, int max_seq_len, int64_t num_blocks, int num_heads,
                       int num_kv_heads, int head_dim, int block_size, float scale, pa_stream_t stream);
 
-/* Library version, major*10000 + minor*100 + patch. */
+/* Split-KV across devices, step 1 of 2 (no counterpart on the pages beyond
+ * their partitions: "docs" commit page, GQA-aware grid and partition
+ * paragraphs, and its compound partial).  Sequence b's tokens are cut into
+ * partitions of partition_size tokens (partition p holds tokens
+ * [p * partition_size, min((p + 1) * partition_size, seq_lens[b])));
+ * this call computes partitions partition_begin .. partition_begin +
+ * partition_count - 1 of every sequence and writes their partials:
+ *   max_logits  fp32 [num_seqs][num_heads][partition_count]: the partition's
+ *               largest score in base 2, m = log2(e) * max_t(scale * q . k_t)
+ *   exp_sums    fp32 [num_seqs][num_heads][partition_count]:
+ *               l = sum_t 2^(log2(e) * scale * q . k_t - m)
+ *   tmp_out     fp32 [num_seqs][num_heads][partition_count][head_dim]: the
+ *               partition's softmax-weighted V, normalised by l
+ * A partition past its sequence's end (or of an empty sequence) gets
+ * m = -inf, l = 0 and a zero row.  Each device of a split calls this with its
+ * own range over a pool that holds the blocks of that range (the block-table
+ * entries outside the range are never read), the devices exchange the arrays
+ * (an all-gather of local buffers), and pa_merge_partials finishes.
+ * args as for pa_decode_ex except that args->out is not used (may be NULL);
+ * partition_size a positive multiple of block_size; partition_begin >= 0,
+ * partition_count >= 1.  opts: mode AUTO or SPLIT, warps/stages, wait_limit,
+ * PA_FLAG_FORCE_TIMEOUT and the timing events apply; the partitions are fixed
+ * (never pooled).  tmp_out 16-byte aligned, the other two 4-byte aligned, all
+ * device memory owned by the caller.  Allocates nothing.  Device-detected
+ * problems set the status word as for pa_decode; the partials are then
+ * unspecified. */
+int pa_decode_partials(const pa_decode_args* args, const pa_decode_opts* opts, int partition_size,
+                       int partition_begin, int partition_count, float* max_logits, float* exp_sums,
+                       float* tmp_out, pa_stream_t stream);
+
+/* Split-KV across devices, step 2 of 2: the log-sum-exp merge of the
+ * partials that num_sources calls of pa_decode_partials produced, source r
+ * having computed partitions [r * partitions_per_source, (r + 1) *
+ * partitions_per_source) with the same partition_size.  The arrays hold the
+ * sources one after another, as an all-gather of their buffers along a new
+ * leading dimension gives them:
+ *   max_logits, exp_sums fp32 [num_sources][num_seqs][num_heads][partitions_per_source]
+ *   tmp_out              fp32 [num_sources][num_seqs][num_heads][partitions_per_source][head_dim]
+ * out fp16 [num_seqs][num_heads][head_dim] gets, per (sequence, head), the
+ * merge of its ceil(seq_lens[b] / partition_size) partials: M = max_p m_p,
+ * w_p = l_p 2^(m_p - M), out = sum_p w_p acc_p / sum_p w_p ("docs" commit
+ * page, Phase 2 reduce; the alpha/beta fold of the "paged_attention_v2_triton.py"
+ * commit page); zero for an empty sequence.  The sources must cover the
+ * longest sequence: num_sources * partitions_per_source >= ceil(max_seq_len /
+ * partition_size), else PA_ERR_INVALID_ARG.  seq_lens int32 [num_seqs], each in
+ * [0, max_seq_len] (a length outside sets PA_DEV_BAD_SEQ_LEN and leaves that
+ * output unwritten).  out and tmp_out 16-byte aligned, the rest 4-byte
+ * aligned; device memory owned by the caller; allocates nothing; asynchronous
+ * on stream.  head_dim in {64, 128, 256}. */
+int pa_merge_partials(void* out, const float* max_logits, const float* exp_sums, const float* tmp_out,
+                      const int32_t* seq_lens, int num_seqs, int num_heads, int head_dim, int max_seq_len,
+                      int partition_size, int num_sources, int partitions_per_source, pa_stream_t stream);
+
+/* Library version, major*10000 + minor*100 + patch.  No counterpart on the pages. */
 int pa_version(void);
 
 #ifdef __cplusplus

@@ -35,7 +35,8 @@ PA_MODE_SINGLE = 1
 PA_MODE_SPLIT = 2
 PA_MODE_FUSED = 3
 PA_MODE_PERSISTENT = 4
-MODES = {"auto": PA_MODE_AUTO, "single": PA_MODE_SINGLE, "split": PA_MODE_SPLIT, "fused": PA_MODE_FUSED,
+PA_MODE_FLAT = 5
+MODES = {"auto": PA_MODE_AUTO, "single": PA_MODE_SINGLE, "split": PA_MODE_SPLIT, "fused": PA_MODE_FUSED, "flat": PA_MODE_FLAT,
          "persistent": PA_MODE_PERSISTENT}
 
 PA_FLAG_FORCE_TIMEOUT = 1
@@ -121,6 +122,13 @@ def _load() -> ctypes.CDLL:
     lib.pa_prefix.argtypes = [vp] * 9 + [i32] * 5 + [i64, i32, i32, i32, i32, f32, vp]
     lib.pa_prefix_ex.restype = i32
     lib.pa_prefix_ex.argtypes = [ctypes.POINTER(pa_prefix_args), ctypes.POINTER(pa_decode_opts), vp]
+    lib.pa_decode_partials.restype = i32
+    lib.pa_decode_partials.argtypes = [ctypes.POINTER(pa_decode_args), ctypes.POINTER(pa_decode_opts), i32, i32, i32,
+                                       vp, vp, vp, vp]
+    lib.pa_merge_partials.restype = i32
+    lib.pa_merge_partials.argtypes = [vp, vp, vp, vp, vp] + [i32] * 7 + [vp]
+    lib.pa_decode_noalloc.restype = i32
+    lib.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, i32, i32, i32, f32, vp]
     return lib
 
 
@@ -279,12 +287,8 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, num_head
                       block_size, scale, stream=None, *, max_seq_len: int) -> None:
     """The no-allocation call: the partials live in the library's fixed device
     scratch (PA_NOALLOC_SCRATCH_BYTES); raises PaDecodeError on a non-zero code."""
-    fn = lib.pa_decode_noalloc
-    vp, i32 = ctypes.c_void_p, ctypes.c_int
-    fn.restype = i32
-    fn.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int64, i32, i32, i32, i32, ctypes.c_float, vp]
     _check_tensors(out, q, k_cache, v_cache, block_tables, seq_lens)
-    rc = fn(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+    rc = lib.pa_decode_noalloc(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
             seq_lens.data_ptr(), int(seq_lens.shape[0]), int(block_tables.shape[1]), int(max_seq_len),
             int(k_cache.shape[0]), int(num_heads), int(num_kv_heads), int(head_dim), int(block_size), float(scale),
             _stream_handle(stream))
@@ -330,3 +334,44 @@ def prefix_workload(w, out: Optional[torch.Tensor] = None, stream=None, **opt) -
               max_context_len=w.max_context_len, max_query_len=w.max_query_len, **opt)
     return out
 
+
+
+def _check_partials(max_logits, exp_sums, tmp_out):
+    for name, t in (("max_logits", max_logits), ("exp_sums", exp_sums), ("tmp_out", tmp_out)):
+        if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor")
+
+
+def pa_decode_partials(q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_kv_heads, head_dim, block_size,
+                       scale, partition_size: int, partition_begin: int, partition_count: int, max_logits,
+                       exp_sums, tmp_out, stream=None, *, max_seq_len: int, **opt) -> None:
+    """Partials of partitions [partition_begin, partition_begin + partition_count)
+    of every sequence (split-KV across devices, step 1): max_logits / exp_sums
+    float32 [B, H, count] (max in base 2), tmp_out float32 [B, H, count, D]."""
+    dummy = q  # `out` is not used by this call
+    _check_tensors(dummy, q, k_cache, v_cache, block_tables, seq_lens)
+    _check_partials(max_logits, exp_sums, tmp_out)
+    args = make_args(None, q, k_cache, v_cache, block_tables, seq_lens, num_heads, num_kv_heads, head_dim,
+                     block_size, scale, max_seq_len)
+    rc = lib.pa_decode_partials(ctypes.byref(args), ctypes.byref(make_opts(**opt)), int(partition_size),
+                                int(partition_begin), int(partition_count), max_logits.data_ptr(),
+                                exp_sums.data_ptr(), tmp_out.data_ptr(), _stream_handle(stream))
+    if rc != PA_OK:
+        raise PaDecodeError(rc, "pa_decode_partials")
+
+
+def pa_merge_partials(out, max_logits, exp_sums, tmp_out, seq_lens, num_heads, head_dim, partition_size: int,
+                      num_sources: int, partitions_per_source: int, stream=None, *, max_seq_len: int) -> None:
+    """Log-sum-exp merge of partials gathered from `num_sources` sources
+    (split-KV across devices, step 2): max_logits / exp_sums float32
+    [R, B, H, pps], tmp_out float32 [R, B, H, pps, D]; out fp16 [B, H, D]."""
+    _check_partials(max_logits, exp_sums, tmp_out)
+    for name, t, dt in (("out", out, torch.float16), ("seq_lens", seq_lens, torch.int32)):
+        if t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    rc = lib.pa_merge_partials(out.data_ptr(), max_logits.data_ptr(), exp_sums.data_ptr(), tmp_out.data_ptr(),
+                               seq_lens.data_ptr(), int(seq_lens.shape[0]), int(num_heads), int(head_dim),
+                               int(max_seq_len), int(partition_size), int(num_sources), int(partitions_per_source),
+                               _stream_handle(stream))
+    if rc != PA_OK:
+        raise PaDecodeError(rc, "pa_merge_partials")

@@ -38,12 +38,21 @@ size_t split_workspace_bytes(long long num_seqs, long long num_heads, long long 
     return align_up(rows * 4, kWsAlign) * 2 + align_up(rows * head_dim * 4, kWsAlign);
 }
 
-// The fused combine also keeps one ticket per (sequence, kv head) after the partials.
+// Bytes of the pooled split's claim counters, one u64 per (sequence, kv head);
+// they sit right after the partials.
+size_t claims_bytes(long long num_seqs, long long num_kv_heads) {
+    return align_up(static_cast<size_t>(num_seqs) * num_kv_heads * 8, kWsAlign);
+}
+
+// The fused combine also keeps one u32 ticket per (sequence, kv head).  The
+// tickets sit after a slot the size of the claim counters, so that a pooled
+// call of the same shape on the same workspace (which arms those counters)
+// never touches them.
 size_t fused_workspace_bytes(long long num_seqs, long long num_heads, long long num_kv_heads,
                              long long max_partitions, long long head_dim) {
     if (max_partitions <= 1) return 0;
     return split_workspace_bytes(num_seqs, num_heads, max_partitions, head_dim) +
-           align_up(static_cast<size_t>(num_seqs) * num_kv_heads * 4, kWsAlign);
+           claims_bytes(num_seqs, num_kv_heads) + align_up(static_cast<size_t>(num_seqs) * num_kv_heads * 4, kWsAlign);
 }
 
 // SM count of the current device, cached per device.
@@ -78,17 +87,19 @@ int validate(const pa_decode_args* a, const pa_decode_opts* o) {
     if (a->num_heads % a->num_kv_heads) return PA_ERR_INVALID_ARG;
     if (!isfinite(a->scale)) return PA_ERR_INVALID_ARG;
     if (a->max_seq_len < 0 || a->max_blocks_per_seq < 0 || a->num_blocks < 0) return PA_ERR_INVALID_ARG;
-    if (o && (o->mode < PA_MODE_AUTO || o->mode > PA_MODE_PERSISTENT)) return PA_ERR_INVALID_ARG;
+    if (o && (o->mode < PA_MODE_AUTO || o->mode > PA_MODE_FLAT)) return PA_ERR_INVALID_ARG;
     if (o && o->partition_size < 0) return PA_ERR_INVALID_ARG;
     if (o && o->partition_size % a->block_size) return PA_ERR_INVALID_ARG;
     if (o && (o->warps < 0 || o->stages < 0)) return PA_ERR_INVALID_ARG;
     // every head_dim is compiled with the same set of CTA shapes; the
     // persistent kernel with one warp and 2 or 3 stages
-    if (o && o->mode == PA_MODE_PERSISTENT) {
+    if (o && (o->mode == PA_MODE_PERSISTENT || o->mode == PA_MODE_FLAT)) {
         if ((o->warps || o->stages) &&
             pa::persistent_smem_bytes(256, o->warps ? o->warps : kPersistentWarps,
                                       o->stages ? o->stages : kPersistentStages) < 0)
             return PA_ERR_UNSUPPORTED;
+        // the flat split keeps the batch's lengths and prefix sums in each CTA
+        if (o->mode == PA_MODE_FLAT && a->num_seqs > pa::kPersistentSeqCache) return PA_ERR_UNSUPPORTED;
     } else if (o && (o->warps || o->stages) && pa::partition_smem_bytes(256, o->warps, o->stages) < 0) {
         return PA_ERR_UNSUPPORTED;
     }
@@ -225,8 +236,9 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     plan->grid_z = a->num_seqs;
     int warps = o ? o->warps : 0, stages = o ? o->stages : 0;
     const bool apportion = mode == PA_MODE_PERSISTENT && !(o && o->partition_size > 0);
-    if (mode == PA_MODE_PERSISTENT) {
-        if (!warps) warps = apportion ? kPersistentWarps : kPersistentWarpsFixedSize;
+    const bool flat = mode == PA_MODE_FLAT;
+    if (mode == PA_MODE_PERSISTENT || flat) {
+        if (!warps) warps = (apportion || flat) ? kPersistentWarps : kPersistentWarpsFixedSize;
         if (!stages) stages = kPersistentStages;
     } else if (one_wave) {
         warps = 4;
@@ -236,9 +248,18 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     }
     plan->threads = warps * 32;
     plan->stages = stages;
-    plan->smem_bytes = mode == PA_MODE_PERSISTENT ? pa::persistent_smem_bytes(a->head_dim, warps, stages) +
-                                                        pa::persistent_seq_cache_bytes(a->num_seqs)
-                                                  : pa::partition_smem_bytes(a->head_dim, warps, stages);
+    plan->smem_bytes = (mode == PA_MODE_PERSISTENT || flat) ? pa::persistent_smem_bytes(a->head_dim, warps, stages) +
+                                                                  pa::persistent_seq_cache_bytes(a->num_seqs)
+                                                            : pa::partition_smem_bytes(a->head_dim, warps, stages);
+    if (flat) {
+        // one CTA per SM: C CTAs per kv head, each streaming an equal share
+        // of the batch's blocks (the share is fixed on the device)
+        const int C = num_sms / a->num_kv_heads > 0 ? num_sms / a->num_kv_heads : 1;
+        plan->grid_x = C * a->num_kv_heads;
+        plan->grid_y = plan->grid_z = 1;
+        plan->partition_size = 0;
+        plan->max_partitions = C;
+    }
     if (mode == PA_MODE_PERSISTENT) {
         // a fixed grid of every CTA the SMs hold at once
         long long per_sm = kSmemPerSm / (plan->smem_bytes + 1024);
@@ -257,7 +278,7 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
             return PA_ERR_UNSUPPORTED;
     }
     plan->launch_reduce =
-        ((mode == PA_MODE_SPLIT || mode == PA_MODE_PERSISTENT) && plan->max_partitions > 1) ? 1 : 0;
+        ((mode == PA_MODE_SPLIT || mode == PA_MODE_PERSISTENT || flat) && plan->max_partitions > 1) ? 1 : 0;
     // Pooled: on request, and by default for the one-wave plan, where every
     // CTA is resident from the start and the SMs' unequal shares of HBM
     // bandwidth would otherwise set the finish (GB300, 102400 tokens: 66.8 ->
@@ -278,11 +299,14 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim);
     }
     if (plan->pooled)  // + the claim counters
-        plan->workspace_bytes += align_up(static_cast<size_t>(a->num_seqs) * a->num_kv_heads * 8, kWsAlign);
+        plan->workspace_bytes += claims_bytes(a->num_seqs, a->num_kv_heads);
     if (mode == PA_MODE_PERSISTENT)  // + the work list and item counter, the order, the partition sizes
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim) +
                                 align_up(static_cast<size_t>(a->num_seqs + 2) * 4, kWsAlign) +
                                 2 * align_up(static_cast<size_t>(a->num_seqs) * 4, kWsAlign);
+    if (flat)  // + each sequence's number of partials
+        plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim) +
+                                align_up(static_cast<size_t>(a->num_seqs) * 4, kWsAlign);
     return PA_OK;
 }
 
@@ -350,22 +374,28 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.block_tables = a->block_tables;
     prm.seq_lens = a->seq_lens;
     const bool fused = plan.mode == PA_MODE_FUSED && plan.grid_x > 1;
-    const bool persistent = plan.mode == PA_MODE_PERSISTENT;
+    const bool flat = plan.mode == PA_MODE_FLAT;
+    const bool persistent = plan.mode == PA_MODE_PERSISTENT || flat;
     const bool partials = plan.launch_reduce || fused;
     const size_t partial_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan.max_partitions, a->head_dim);
     prm.max_logits = partials ? reinterpret_cast<float*>(w) : nullptr;
     prm.exp_sums = partials ? reinterpret_cast<float*>(w + align_up(rows * 4, kWsAlign)) : nullptr;
     prm.tmp_out = partials ? reinterpret_cast<float*>(w + 2 * align_up(rows * 4, kWsAlign)) : nullptr;
-    prm.tickets = fused ? reinterpret_cast<unsigned int*>(w + partial_bytes) : nullptr;
+    prm.tickets = fused ? reinterpret_cast<unsigned int*>(w + partial_bytes + claims_bytes(a->num_seqs, a->num_kv_heads))
+                        : nullptr;
     prm.claims = plan.pooled ? reinterpret_cast<unsigned long long*>(w + partial_bytes) : nullptr;
     // persistent schedule tables after the partials: work list + counter, order, partition sizes
-    int* list = persistent ? reinterpret_cast<int*>(w + partial_bytes) : nullptr;
-    int* order = persistent ? reinterpret_cast<int*>(w + partial_bytes +
-                                                     align_up(static_cast<size_t>(a->num_seqs + 2) * 4, kWsAlign))
-                            : nullptr;
-    int* parts = persistent ? order + align_up(static_cast<size_t>(a->num_seqs) * 4, kWsAlign) / 4 : nullptr;
+    // (the flat split: each sequence's number of partials)
+    const bool listed = persistent && !flat;
+    int* list = listed ? reinterpret_cast<int*>(w + partial_bytes) : nullptr;
+    int* order = listed ? reinterpret_cast<int*>(w + partial_bytes +
+                                                 align_up(static_cast<size_t>(a->num_seqs + 2) * 4, kWsAlign))
+                        : nullptr;
+    int* parts = listed ? order + align_up(static_cast<size_t>(a->num_seqs) * 4, kWsAlign) / 4 : nullptr;
+    prm.flat = flat ? 1 : 0;
+    prm.part_counts = flat && plan.launch_reduce ? reinterpret_cast<int*>(w + partial_bytes) : nullptr;
     prm.work_offsets = list;
-    prm.work_counter = persistent ? list + a->num_seqs + 1 : nullptr;
+    prm.work_counter = listed ? list + a->num_seqs + 1 : nullptr;
     prm.seq_order = order;
     prm.part_sizes = parts;
     prm.num_seqs = a->num_seqs;
@@ -384,7 +414,7 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.force_timeout = (o && (o->flags & PA_FLAG_FORCE_TIMEOUT)) ? 1 : 0;
     prm.trace = g_trace;
 
-    if (persistent) {
+    if (listed) {
         pa::ScanParams sp;
         sp.seq_lens = a->seq_lens;
         sp.work_offsets = list;
@@ -425,13 +455,134 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
         rp.partition_size = plan.partition_size;
         rp.max_partitions = plan.max_partitions;
         rp.part_sizes = parts;
+        rp.part_counts = prm.part_counts;
         rp.claims = prm.claims;
         rp.group = prm.group;
         if (pa::launch_reduce(a->head_dim, a->head_dim / plan.reduce_grid_z, rp,
-                              dim3(plan.reduce_grid_x, plan.reduce_grid_y, plan.reduce_grid_z), stream) != cudaSuccess)
+                              dim3(plan.reduce_grid_x, plan.reduce_grid_y, plan.reduce_grid_z), stream) != cudaSuccess) {
+            // The partition grid may have consumed claims, and only the reduce
+            // re-arms the counters: disarm them, so the next pooled call on this
+            // workspace deals its chunks round-robin instead of skipping some.
+            if (prm.claims) pa::disarm_claims(prm.claims, static_cast<size_t>(a->num_seqs) * a->num_kv_heads, stream);
             return PA_ERR_CUDA;
+        }
     }
     return PA_OK;
+}
+
+// Partials of partitions [begin, begin + count) of every sequence, into the
+// caller's arrays (split-KV across devices: each device computes its own range
+// of partitions over its own part of the cache; pa_merge_partials merges them).
+int run_partials(const pa_decode_args* a, const pa_decode_opts* o, int partition_size, int begin, int count,
+                 float* max_logits, float* exp_sums, float* tmp_out, cudaStream_t stream) {
+    if (!a) return PA_ERR_INVALID_ARG;
+    if (partition_size <= 0 || begin < 0 || count <= 0) return PA_ERR_INVALID_ARG;
+    if ((long long)(begin + (long long)count) * partition_size >= (1ll << 31)) return PA_ERR_INVALID_ARG;
+    if (o && o->mode != PA_MODE_AUTO && o->mode != PA_MODE_SPLIT) return PA_ERR_INVALID_ARG;
+    pa_decode_args ca = *a;
+    ca.out = tmp_out;  // the output is never written; the partials take its place
+    pa_decode_opts co;
+    memset(&co, 0, sizeof(co));
+    if (o) co = *o;
+    co.mode = PA_MODE_SPLIT;
+    co.partition_size = partition_size;
+    co.flags = (co.flags & PA_FLAG_FORCE_TIMEOUT) | PA_FLAG_DETERMINISTIC;  // fixed partitions, never pooled
+    pa_decode_plan_t plan;
+    int rc = make_plan(&ca, &co, 0, &plan);
+    if (rc) return rc;
+    if (a->num_seqs == 0) return PA_OK;
+    if (!max_logits || !exp_sums || !tmp_out || !aligned(max_logits, 4) || !aligned(exp_sums, 4) ||
+        !aligned(tmp_out, 16))
+        return PA_ERR_INVALID_ARG;
+    plan.grid_x = count;
+    plan.max_partitions = count;
+    if (!co.warps && !co.stages) {
+        int num_sms = 0;
+        if (query_sm_count(&num_sms) != PA_OK) num_sms = 1;
+        int warps = 0, stages = 0;
+        choose_shape(&ca, &plan, num_sms, &warps, &stages);
+        plan.threads = warps * 32;
+        plan.stages = stages;
+    }
+
+    CUtensorMap tk, tv;
+    if ((rc = make_cache_block_map(&tk, a->k_cache, a->num_blocks, a->num_kv_heads, a->head_dim)) ||
+        (rc = make_cache_block_map(&tv, a->v_cache, a->num_blocks, a->num_kv_heads, a->head_dim)))
+        return rc;
+    pa::PartitionParams prm{};
+    prm.out = nullptr;
+    prm.q = static_cast<const __half*>(a->q);
+    prm.block_tables = a->block_tables;
+    prm.seq_lens = a->seq_lens;
+    prm.max_logits = max_logits;
+    prm.exp_sums = exp_sums;
+    prm.tmp_out = tmp_out;
+    prm.num_seqs = a->num_seqs;
+    prm.num_blocks = a->num_blocks;
+    prm.num_heads = a->num_heads;
+    prm.num_kv_heads = a->num_kv_heads;
+    prm.group = a->num_heads / a->num_kv_heads;
+    prm.max_blocks_per_seq = a->max_blocks_per_seq;
+    prm.max_seq_len = a->max_seq_len;
+    prm.partition_size = partition_size;
+    prm.max_partitions = count;
+    prm.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+    prm.wait_limit = co.wait_limit ? co.wait_limit : pa::kDefaultWaitLimit;
+    prm.force_timeout = (co.flags & PA_FLAG_FORCE_TIMEOUT) ? 1 : 0;
+    prm.trace = g_trace;
+    prm.part_begin = begin;
+    prm.partials_only = 1;
+    if (co.event_partition_begin &&
+        cudaEventRecord(static_cast<cudaEvent_t>(co.event_partition_begin), stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (pa::launch_partition(a->head_dim, plan.threads / 32, plan.stages, prm, tk, tv,
+                             dim3(plan.grid_x, plan.grid_y, plan.grid_z), stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (co.event_partition_end &&
+        cudaEventRecord(static_cast<cudaEvent_t>(co.event_partition_end), stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+// The log-sum-exp merge of partials gathered from num_sources sources, each
+// holding partitions_per_source consecutive partitions of every sequence.
+int run_merge(void* out, const float* max_logits, const float* exp_sums, const float* tmp_out,
+              const int32_t* seq_lens, int num_seqs, int num_heads, int head_dim, int max_seq_len, int partition_size,
+              int num_sources, int partitions_per_source, cudaStream_t stream) {
+    if (num_seqs < 0 || num_seqs > 65535 || num_heads <= 0 || max_seq_len < 0) return PA_ERR_INVALID_ARG;
+    if (partition_size <= 0 || partition_size % pa::kBlockSize || num_sources <= 0 || partitions_per_source <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    const long long slots = (long long)num_sources * partitions_per_source;
+    if (slots >= (1ll << 31)) return PA_ERR_INVALID_ARG;
+    // the sources must cover every partition of the longest sequence
+    if ((max_seq_len + (long long)partition_size - 1) / partition_size > slots) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !max_logits || !exp_sums || !tmp_out || !seq_lens || !aligned(out, 16) || !aligned(tmp_out, 16) ||
+        !aligned(max_logits, 4) || !aligned(exp_sums, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    int num_sms = 0;
+    if (query_sm_count(&num_sms) != PA_OK) num_sms = 1;
+    pa::ReduceParams rp{};
+    rp.out = static_cast<__half*>(out);
+    rp.max_logits = max_logits;
+    rp.exp_sums = exp_sums;
+    rp.tmp_out = tmp_out;
+    rp.seq_lens = seq_lens;
+    rp.num_heads = num_heads;
+    rp.max_seq_len = max_seq_len;
+    rp.max_blocks_per_seq = (max_seq_len + pa::kBlockSize - 1) / pa::kBlockSize;
+    rp.partition_size = partition_size;
+    rp.max_partitions = static_cast<int>(slots);
+    rp.part_sizes = nullptr;
+    rp.claims = nullptr;
+    rp.group = 1;
+    rp.src_parts = partitions_per_source;
+    rp.src_stride = (long long)num_seqs * num_heads * partitions_per_source;
+    const int width = reduce_slice(head_dim, (long long)num_seqs * num_heads, num_sms);
+    return pa::launch_reduce(head_dim, width, rp, dim3(num_heads, num_seqs, head_dim / width), stream) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 // New tokens' K or V viewed as a 3-D tensor [num_tokens][num_kv_heads][head_dim];
@@ -686,6 +837,19 @@ int pa_prefix(void* out, const void* q, const void* k_new, const void* v_new, co
     a.block_size = block_size;
     a.scale = scale;
     return run_prefix(&a, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_decode_partials(const pa_decode_args* args, const pa_decode_opts* opts, int partition_size, int partition_begin,
+                       int partition_count, float* max_logits, float* exp_sums, float* tmp_out, pa_stream_t stream) {
+    return run_partials(args, opts, partition_size, partition_begin, partition_count, max_logits, exp_sums, tmp_out,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_merge_partials(void* out, const float* max_logits, const float* exp_sums, const float* tmp_out,
+                      const int32_t* seq_lens, int num_seqs, int num_heads, int head_dim, int max_seq_len,
+                      int partition_size, int num_sources, int partitions_per_source, pa_stream_t stream) {
+    return run_merge(out, max_logits, exp_sums, tmp_out, seq_lens, num_seqs, num_heads, head_dim, max_seq_len,
+                     partition_size, num_sources, partitions_per_source, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim, int partition_size) {

@@ -103,6 +103,18 @@ struct PartitionParams {
     // Pooled split: one claim counter per (sequence, kv head); null for the
     // fixed assignment of blocks to partitions.
     unsigned long long* claims;
+    // Partials of a range of partitions (split-KV across devices): CTA x
+    // computes partition part_begin + x of its sequence and always writes a
+    // partial (slot x of max_partitions), never the output; a partition past
+    // the sequence's end gets the empty partial (m = -inf, l = 0, acc = 0).
+    int part_begin = 0;
+    int partials_only = 0;
+    // Flat one-wave split (persistent kernel without a work list; flat = 1):
+    // max_partitions is then the CTAs per kv head, and part_counts receives
+    // the number of partials of each sequence from the CTA that holds its
+    // first block (null when there is one CTA per kv head: no partials).
+    int flat = 0;
+    int* part_counts = nullptr;
 };
 
 struct ReduceParams {
@@ -118,6 +130,18 @@ struct ReduceParams {
     // (sequence, kv head); null otherwise.
     unsigned long long* claims;
     int group;  // query heads per kv head
+    // Merge of partials gathered from several sources (split-KV across
+    // devices): partition p of a sequence is slot p % src_parts of source
+    // p / src_parts, the sources src_stride rows apart; every sequence's
+    // output is written (one partial, or none for an empty sequence, too).
+    // src_parts = 0: the partials of one partition grid (max_partitions
+    // slots per (sequence, head)), and sequences with at most one partition
+    // are skipped.
+    int src_parts = 0;
+    long long src_stride = 0;
+    // Flat split: the number of partials of each sequence (else derived from
+    // the partition size)
+    const int* part_counts = nullptr;
 };
 
 struct ScanParams {
@@ -145,6 +169,11 @@ cudaError_t launch_partition(int head_dim, int warps, int stages, const Partitio
 // dependency before it reads any memory.  `width` is the head_dim slice of a
 // reduce CTA (32, 64, 128 or 256, at most head_dim).
 cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3 grid, cudaStream_t stream);
+
+// The disarmed state of the pooled split's claim counters (all zero, so the
+// next pooled call deals its chunks round-robin), for a call whose reduce
+// launch failed after its partition launch had consumed claims.
+cudaError_t disarm_claims(unsigned long long* claims, size_t count, cudaStream_t stream);
 
 // The persistent schedule's work list: one CTA sizes the partitions, orders the
 // sequences longest partition first and sums their item counts.

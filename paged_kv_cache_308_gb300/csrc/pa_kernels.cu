@@ -281,7 +281,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
     PA_TRACE_MARK(1);
 #endif
 
-    const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    // p: the partition of the sequence; slot: its partial's index in the
+    // workspace (they differ only for the partials of a partition range)
+    const int p = blockIdx.x + prm.part_begin, slot = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int G = prm.group, H = prm.num_heads;
     const int blocks_per_part = prm.partition_size / kBlockSize;
     const int blk0 = p * blocks_per_part;
@@ -315,17 +317,36 @@ __global__ void __launch_bounds__(NW * 32, 1)
     };
 
     if (L < 0 || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) {
-        if (p == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(&g_status, PA_DEV_BAD_SEQ_LEN);
+        if (slot == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(&g_status, PA_DEV_BAD_SEQ_LEN);
         return;
     }
+    // The empty partial of a partition past the sequence's end (partials of a
+    // range only): no tokens, so nothing it holds may weigh in a merge.
+    auto write_empty_partial = [&]() {
+        const size_t head0 = (size_t)b * H + (size_t)kvh * G;
+        for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+            const size_t pi = (head0 + i / D) * prm.max_partitions + slot;
+            prm.tmp_out[pi * D + i % D] = 0.f;
+            if (i % D == 0) {
+                prm.max_logits[pi] = -INFINITY;
+                prm.exp_sums[pi] = 0.f;
+            }
+        }
+    };
     if (L == 0) {  // empty sequence: the output is zero
-        if (p == 0)
+        if (prm.partials_only) {
+            write_empty_partial();
+        } else if (p == 0) {
             for (int i = threadIdx.x; i < G * D; i += blockDim.x)
                 prm.out[((size_t)b * H + kvh * G) * D + i] = __float2half_rn(0.f);
+        }
         return;
     }
     const int n_part = (L + prm.partition_size - 1) / prm.partition_size;
-    if (p >= n_part) return;
+    if (p >= n_part) {
+        if (prm.partials_only) write_empty_partial();
+        return;
+    }
     const int nblk = min(blocks_per_part, (L + kBlockSize - 1) / kBlockSize - blk0);
 
     // Blocks j = warp, warp + NW, ... of the partition belong to this warp.
@@ -509,7 +530,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
 
     const bool fused = prm.tickets && n_part > 1;
-    const bool direct = n_part == 1;
+    const bool direct = n_part == 1 && !prm.partials_only;
     if constexpr (NW == 1) {
     // One warp: the output is its own state, o / l, stored from the MMA
     // fragments (lane (g, c) holds heads 2c, 2c + 1).  A partition whose
@@ -519,7 +540,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const float f0 = w0 * (1.f / L0), f1 = w1 * (1.f / L1);
     const bool has0 = 2 * c < G, has1 = 2 * c + 1 < G;  // padding heads are not written
     const size_t head0 = (size_t)b * H + kvh * G + 2 * c;
-    const size_t pi0 = head0 * prm.max_partitions + p, pi1 = pi0 + prm.max_partitions;
+    const size_t pi0 = head0 * prm.max_partitions + slot, pi1 = pi0 + prm.max_partitions;
 #pragma unroll
     for (int mt = 0; mt < S::kSteps; ++mt) {
         const int d = 16 * mt + g;
@@ -603,7 +624,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
         for (int w = 0; w < NW; ++w) f[w] *= inv;
         const size_t head = (size_t)b * H + kvh * G + h;
-        const size_t pi = head * prm.max_partitions + p;
+        const size_t pi = head * prm.max_partitions + slot;
 #pragma unroll
         for (int k = 0; k < kSlice / 8; ++k) {
             const int d = warp * kSlice + 8 * k + 2 * qd;
@@ -641,7 +662,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
 // 2^(m_old - m_new), beta = l_p 2^(m_p - m_new)), so no separate pass for
 // the max is needed; the groups are then merged by the same rule in a fixed
 // order, which keeps results deterministic.
-template <int D, int W>
+// Merge: the partials were gathered from several sources (split-KV across
+// devices; see ReduceParams::src_parts), and every sequence's output is
+// written here, also for one partition or none.
+template <int D, int W, bool Merge>
 __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceParams prm) {
     constexpr int kLanes = W / 4;                    // float4 columns of a slice
     constexpr int kGroups = kReduceThreads / kLanes; // partition groups
@@ -653,11 +677,20 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
     // partition grid that used it has completed
     if (prm.claims && slice == 0 && h % prm.group == 0 && threadIdx.x == 0)
         prm.claims[(size_t)b * (prm.num_heads / prm.group) + h / prm.group] = (unsigned long long)kClaimTag << 32;
-    const size_t base = ((size_t)b * prm.num_heads + h) * prm.max_partitions;
+    const size_t base = ((size_t)b * prm.num_heads + h) * (Merge ? prm.src_parts : prm.max_partitions);
     const float* ml = prm.max_logits + base;
     const float* el = prm.exp_sums + base;
     const int col = threadIdx.x % kLanes, pg = threadIdx.x / kLanes;
     const float4* tp = reinterpret_cast<const float4*>(prm.tmp_out + base * D + slice * W) + col;
+    // offset of partition p from base: slot p % src_parts of source p / src_parts
+    auto at = [&](int p) -> size_t {
+        if constexpr (Merge) {
+            const int r = p / prm.src_parts;
+            return (size_t)r * prm.src_stride + (size_t)(p - r * prm.src_parts);
+        } else {
+            return (size_t)p;
+        }
+    };
     // A thread's first partial is read together with the length, so the two
     // latencies overlap: the row holds max_partitions entries, so the reads
     // stay inside the workspace, and a value past the sequence's partitions
@@ -665,16 +698,28 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
     float mp0 = 0.f, lp0 = 0.f;
     float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f);
     if (pg < prm.max_partitions) {
-        mp0 = ml[pg];
-        lp0 = el[pg];
-        t0 = tp[(size_t)pg * (D / 4)];
+        mp0 = ml[at(pg)];
+        lp0 = el[at(pg)];
+        t0 = tp[at(pg) * (D / 4)];
     }
     const int L = prm.seq_lens[b];
     const int part = prm.part_sizes ? prm.part_sizes[b] : prm.partition_size;
-    // single-partition, empty and invalid sequences were finished by the partition kernel
-    if (L <= 0 || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) return;
-    const int n = (L + part - 1) / part;
-    if (n <= 1) return;
+    if constexpr (Merge) {
+        if (L < 0 || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) {
+            if (h == 0 && slice == 0 && threadIdx.x == 0) atomicOr(&g_status, PA_DEV_BAD_SEQ_LEN);
+            return;
+        }
+        if (L == 0) {  // empty sequence: the output is zero
+            if (threadIdx.x < W)
+                prm.out[((size_t)b * prm.num_heads + h) * D + slice * W + threadIdx.x] = __float2half_rn(0.f);
+            return;
+        }
+    } else if (L <= 0 || L > prm.max_seq_len || L > prm.max_blocks_per_seq * kBlockSize) {
+        // single-partition, empty and invalid sequences were finished by the partition kernel
+        return;
+    }
+    const int n = prm.part_counts ? prm.part_counts[b] : (L + part - 1) / part;
+    if (!Merge && n <= 1) return;
 
     __shared__ float4 red_acc[kGroups][kLanes];
     __shared__ float red_m[kGroups];
@@ -695,7 +740,7 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
     };
     if (pg < n) fold(mp0, lp0, t0);
 #pragma unroll 4
-    for (int p = pg + kGroups; p < n; p += kGroups) fold(ml[p], el[p], tp[(size_t)p * (D / 4)]);
+    for (int p = pg + kGroups; p < n; p += kGroups) fold(ml[at(p)], el[at(p)], tp[at(p) * (D / 4)]);
     red_acc[pg][col] = acc;
     if (col == 0) {
         red_m[pg] = m;
@@ -765,7 +810,7 @@ cudaError_t launch_partition_t(const PartitionParams& prm, const CUtensorMap& tk
     return cudaGetLastError();
 }
 
-template <int D, int W>
+template <int D, int W, bool Merge>
 cudaError_t launch_reduce_t(const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
     // The largest shared-memory carveout, as the partition kernel's needs: an
     // SM runs CTAs of one carveout at a time, so with a smaller one the
@@ -773,7 +818,7 @@ cudaError_t launch_reduce_t(const ReduceParams& prm, dim3 grid, cudaStream_t str
     // they wait on.
     static std::atomic<unsigned long long> done{0};
     cudaError_t e = once_per_device(done, [] {
-        return cudaFuncSetAttribute(pa_reduce_kernel<D, W>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        return cudaFuncSetAttribute(pa_reduce_kernel<D, W, Merge>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                     (int)cudaSharedmemCarveoutMaxShared);
     });
     if (e != cudaSuccess) return e;
@@ -785,21 +830,27 @@ cudaError_t launch_reduce_t(const ReduceParams& prm, dim3 grid, cudaStream_t str
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, pa_reduce_kernel<D, W>, prm);
+    e = cudaLaunchKernelEx(&cfg, pa_reduce_kernel<D, W, Merge>, prm);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t launch_reduce_d(int width, const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
+template <int D, bool Merge>
+cudaError_t launch_reduce_m(int width, const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
     switch (width) {
-        case 32: return launch_reduce_t<D, 32>(prm, grid, stream);
-        case 64: return launch_reduce_t<D, 64>(prm, grid, stream);
-        case 128: if constexpr (D >= 128) return launch_reduce_t<D, 128>(prm, grid, stream); else break;
-        case 256: if constexpr (D >= 256) return launch_reduce_t<D, 256>(prm, grid, stream); else break;
+        case 32: return launch_reduce_t<D, 32, Merge>(prm, grid, stream);
+        case 64: return launch_reduce_t<D, 64, Merge>(prm, grid, stream);
+        case 128: if constexpr (D >= 128) return launch_reduce_t<D, 128, Merge>(prm, grid, stream); else break;
+        case 256: if constexpr (D >= 256) return launch_reduce_t<D, 256, Merge>(prm, grid, stream); else break;
         default: break;
     }
     return cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t launch_reduce_d(int width, const ReduceParams& prm, dim3 grid, cudaStream_t stream) {
+    return prm.src_parts > 0 ? launch_reduce_m<D, true>(width, prm, grid, stream)
+                             : launch_reduce_m<D, false>(width, prm, grid, stream);
 }
 
 }  // namespace
@@ -834,6 +885,10 @@ cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3
         case 256: return launch_reduce_d<256>(width, prm, grid, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t disarm_claims(unsigned long long* claims, size_t count, cudaStream_t stream) {
+    return cudaMemsetAsync(claims, 0, count * sizeof(unsigned long long), stream);
 }
 
 unsigned int* device_status_ptr() {

@@ -76,7 +76,9 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache, 
         rc = noalloc_scratch(&ws);
         if (rc) return rc;
     }
-    // Every partial the reduce reads is written earlier in the same call, so
-    // nothing in the scratch has to start at zero.
+    // Every partial the reduce reads is written earlier in the same call, and
+    // the pooled plan's claim counters treat anything but their own armed
+    // state (which the reduce leaves behind) as "not armed"; so nothing in the
+    // scratch has to start at zero, whatever shape the previous call had.
     return pa_decode_ex(&a, nullptr, ws, plan.workspace_bytes > 0 ? PA_NOALLOC_SCRATCH_BYTES : 0, stream);
 }

@@ -42,12 +42,15 @@ namespace pa {
 // others go on to item k + 1.
 // ---------------------------------------------------------------------------
 
-// Work item i of the persistent schedule.  nblk = the blocks it streams:
-// 0 for an invalid length, an empty sequence, or (never, with a work list
-// built from the same lengths) a partition past the end.
+// Work item i of the persistent schedule: blocks blk0 .. blk0 + nblk - 1 of
+// sequence b for kv head kvh.  nblk = 0 for an invalid length, an empty
+// sequence, or (never, with a work list built from the same lengths) a
+// partition past the end.  The item's partial goes to slot `slot` of its
+// (sequence, head) rows, or straight to the output when the sequence has no
+// other item (`direct`).
 struct PersistentItem {
-    int b, p, kvh, L, part, nblk;
-    bool bad;
+    int b, kvh, L, blk0, nblk, slot;
+    bool bad, direct;
 };
 
 // The schedule's tables (work list over the schedule order, the order, the
@@ -72,17 +75,42 @@ __device__ __forceinline__ PersistentItem persistent_item(const PartitionParams&
     PersistentItem it;
     const int r = i - tb.offs[lo];
     it.b = tb.order[lo];
-    it.p = r / prm.num_kv_heads;
+    const int p = r / prm.num_kv_heads;
     it.kvh = r % prm.num_kv_heads;
     it.L = tb.lens[it.b];
     it.bad = it.L < 0 || it.L > prm.max_seq_len || it.L > prm.max_blocks_per_seq * kBlockSize;
-    it.part = tb.parts[it.b];
+    const int part = tb.parts[it.b];
+    const int bpp = part / kBlockSize;
+    it.blk0 = p * bpp;
+    it.slot = p;
     it.nblk = 0;
+    it.direct = false;
     if (!it.bad && it.L > 0) {
-        const int bpp = it.part / kBlockSize;
-        it.nblk = max(0, min(bpp, (it.L + kBlockSize - 1) / kBlockSize - it.p * bpp));
+        it.nblk = max(0, min(bpp, (it.L + kBlockSize - 1) / kBlockSize - it.blk0));
+        it.direct = it.L <= part;  // one partition
     }
     return it;
+}
+
+// ---------------------------------------------------------------------------
+// Flat one-wave split (PA_MODE_FLAT): no work list.  Every CTA reads the
+// batch's lengths, and with nb_b = ceil(L_b / 16) blocks per valid sequence,
+// S_b their exclusive prefix sums and T = S_B, CTA c of the C CTAs of a kv
+// head (C' = min(C, T) of them busy) streams blocks [f(c), f(c + 1)) of the
+// batch's concatenated block list, f(c) = floor(c T / C').  Each sequence
+// that range meets is one item: its blocks j0 .. j1 - 1, with slot
+// c - c_first(b) of the sequence's partials, c_first(b) = the CTA whose range
+// holds the sequence's first block; a sequence met by one CTA only is written
+// straight to the output.  Every CTA streams T / C' blocks (+-1), whatever
+// the lengths, so the wave has no ragged tail of short and long CTAs.
+// ---------------------------------------------------------------------------
+
+// The flat split's CTA range start f(c) and the CTA holding block `pos`.
+__device__ __forceinline__ int flat_start(int c, int T, int C) { return (int)(((long long)c * T) / C); }
+__device__ __forceinline__ int flat_cta_of(int pos, int T, int C) {
+    int c = (int)(((long long)pos * C) / T);
+    while (c + 1 < C && flat_start(c + 1, T, C) <= pos) ++c;
+    return c;
 }
 
 // Shared memory of a persistent CTA: the NW x NS stages, then two merge areas
@@ -123,7 +151,7 @@ struct PersistentShape {
     } while (0)
 #endif
 
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, bool Flat>
 __global__ void __launch_bounds__(NW * 32, 1)
     pa_partition_persistent_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                    const __grid_constant__ CUtensorMap tmap_v, const PartitionParams prm) {
@@ -168,7 +196,93 @@ __global__ void __launch_bounds__(NW * 32, 1)
     // side and again at the start of each item's math: from shared memory
     // when the batch is small enough to cache.
     ScheduleTables tb{prm.work_offsets, prm.seq_order, prm.seq_lens, prm.part_sizes};
-    if (prm.num_seqs <= kPersistentSeqCache) {
+    // Flat split: this CTA's kv head, its place c among the C CTAs of that kv
+    // head, the busy CTAs Cb = min(C, T), its block range [f_lo, f_hi), and in
+    // shared memory the lengths, the block prefix sums and its items (the
+    // sequences its range meets)
+    int f_kvh = 0, f_c = 0, f_T = 0, f_Cb = 0, f_lo = 0, f_hi = 0;
+    const int* f_len = nullptr;
+    const int* f_S = nullptr;
+    const int* f_items = nullptr;
+    int total = 0;
+    if constexpr (Flat) {
+        const int B = prm.num_seqs;  // at most kPersistentSeqCache (the host checks)
+        int* sl = reinterpret_cast<int*>(smem + Q::kSmemBytes - 1024);
+        int* sS = sl + B;      // [B + 1]
+        int* sI = sS + B + 1;  // [B + 1]: the items, then their count
+        for (int x = threadIdx.x; x < B; x += blockDim.x) {
+            const int L = __ldg(prm.seq_lens + x);
+            sl[x] = L;
+            const bool ok = L > 0 && L <= prm.max_seq_len && L <= prm.max_blocks_per_seq * kBlockSize;
+            sS[x + 1] = ok ? (L + kBlockSize - 1) / kBlockSize : 0;
+        }
+        __syncthreads();
+        if (warp == 0) {  // inclusive scan of the block counts, 32 at a time
+            int run = 0;
+            if (lane == 0) sS[0] = 0;
+            for (int base = 0; base < B; base += 32) {
+                const int x = base + lane;
+                int v = x < B ? sS[x + 1] : 0;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int u = __shfl_up_sync(kFull, v, off);
+                    if (lane >= off) v += u;
+                }
+                if (x < B) sS[x + 1] = run + v;
+                run += __shfl_sync(kFull, v, 31);
+            }
+        }
+        __syncthreads();
+        const int C = prm.max_partitions;  // CTAs per kv head
+        f_kvh = (int)blockIdx.x % prm.num_kv_heads;
+        f_c = (int)blockIdx.x / prm.num_kv_heads;
+        f_T = sS[B];
+        f_Cb = min(C, f_T);
+        if (f_c < f_Cb) {
+            f_lo = flat_start(f_c, f_T, f_Cb);
+            f_hi = flat_start(f_c + 1, f_T, f_Cb);
+        }
+        if (threadIdx.x == 0) {
+            int n = 0;
+            if (f_c < f_Cb) {
+                int a = 0, z = B;  // the first sequence whose blocks end past f_lo
+                while (a < z) {
+                    const int mid = (a + z) >> 1;
+                    if (sS[mid + 1] > f_lo)
+                        z = mid;
+                    else
+                        a = mid + 1;
+                }
+                for (int b = a; b < B && sS[b] < f_hi; ++b) {
+                    if (sS[b + 1] == sS[b]) continue;  // no blocks
+                    sI[n++] = b;
+                    // the CTA with a sequence's first block records its partial count
+                    if (prm.part_counts && f_kvh == 0 && sS[b] >= f_lo)
+                        prm.part_counts[b] = flat_cta_of(sS[b + 1] - 1, f_T, f_Cb) - f_c + 1;
+                }
+            }
+            sI[B] = n;
+        }
+        // empty sequences: zero output (CTA b % C of each kv head); invalid
+        // lengths: reported once
+        for (int b = f_c; b < B; b += C) {
+            if (sl[b] == 0)
+                for (int x = threadIdx.x; x < G * D; x += blockDim.x)
+                    prm.out[((size_t)b * H + f_kvh * G) * D + x] = __float2half_rn(0.f);
+        }
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            for (int b = 0; b < B; ++b)
+                if (sl[b] < 0 || sl[b] > prm.max_seq_len || sl[b] > prm.max_blocks_per_seq * kBlockSize) {
+                    atomicOr(prm.status, PA_DEV_BAD_SEQ_LEN);
+                    break;
+                }
+        }
+        __syncthreads();
+        total = sI[B];
+        f_len = sl;
+        f_S = sS;
+        f_items = sI;
+    } else if (prm.num_seqs <= kPersistentSeqCache) {
         const int B = prm.num_seqs;
         int* so = reinterpret_cast<int*>(smem + Q::kSmemBytes - 1024);
         int *sr = so + B + 1, *sl = sr + B, *sp = sl + B;
@@ -180,11 +294,37 @@ __global__ void __launch_bounds__(NW * 32, 1)
         }
         tb = ScheduleTables{so, sr, sl, sp};
     }
-    const int total = __ldg(prm.work_offsets + prm.num_seqs);
+    if constexpr (!Flat) total = __ldg(prm.work_offsets + prm.num_seqs);
+
+    // Item I of this CTA's schedule (a work-list index, or for the flat split
+    // an index into this CTA's own items)
+    auto item_at = [&](int I) -> PersistentItem {
+        if constexpr (Flat) {
+            PersistentItem it;
+            it.b = f_items[I];
+            it.kvh = f_kvh;
+            it.L = f_len[it.b];
+            it.bad = false;
+            const int S0 = f_S[it.b], S1 = f_S[it.b + 1];
+            it.blk0 = max(f_lo, S0) - S0;
+            it.nblk = min(f_hi, S1) - S0 - it.blk0;
+            const int first = S0 >= f_lo ? f_c : flat_cta_of(S0, f_T, f_Cb);
+            it.slot = f_c - first;
+            it.direct = first == f_c && S1 <= f_hi;  // no other CTA meets this sequence
+            return it;
+        } else {
+            return persistent_item(prm, tb, I);
+        }
+    };
 
     if (threadIdx.x == 0) {
-        items[0] = blockIdx.x;
-        items[1] = (int)blockIdx.x < total ? atomicAdd(prm.work_counter, 1) : total;
+        if constexpr (Flat) {
+            items[0] = 0;
+            items[1] = 1;
+        } else {
+            items[0] = blockIdx.x;
+            items[1] = (int)blockIdx.x < total ? atomicAdd(prm.work_counter, 1) : total;
+        }
         *sm_abort = 0;
     }
     __syncthreads();
@@ -208,11 +348,11 @@ __global__ void __launch_bounds__(NW * 32, 1)
             if (is_k > known) return;
             const int I = items[is_k & 3];
             if (I >= total) return;
-            const PersistentItem it = persistent_item(prm, tb, I);
+            const PersistentItem it = item_at(I);
             is_nblk = it.nblk;
             is_kvh = it.kvh;
             is_j = warp;
-            is_bt = prm.block_tables + (size_t)it.b * prm.max_blocks_per_seq + it.p * (it.part / kBlockSize);
+            is_bt = prm.block_tables + (size_t)it.b * prm.max_blocks_per_seq + it.blk0;
             is_dec = true;
         }
         // the warp's t-th block of the item; block ids 32 at a time, only
@@ -251,11 +391,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
     for (int k = 0;; ++k) {
         const int I = items[k & 3];
         if (I >= total) break;  // the same for every warp
-        const PersistentItem it = persistent_item(prm, tb, I);
+        const PersistentItem it = item_at(I);
         // thread 0 draws the index of item k + 2 now; it is published at this item's barrier
         int drawn = total;
-        if (threadIdx.x == 0 && items[(k + 1) & 3] < total) drawn = atomicAdd(prm.work_counter, 1);
-        const int blk0 = it.p * (it.part / kBlockSize);
+        if constexpr (Flat) {
+            drawn = k + 2;
+        } else {
+            if (threadIdx.x == 0 && items[(k + 1) & 3] < total) drawn = atomicAdd(prm.work_counter, 1);
+        }
+        const int blk0 = it.blk0;
 
         float o[S::kSteps][4];
 #pragma unroll
@@ -337,8 +481,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
             continue;
         }
         if (it.nblk == 0) continue;
-        const int n_part = (it.L + it.part - 1) / it.part;
-        const bool direct = n_part == 1;
+        const bool direct = it.direct;
         if constexpr (NW == 1) {
             // one warp: o / l straight from the MMA fragments (lane (g, c)
             // holds heads 2c, 2c + 1); a partition whose blocks all had
@@ -348,7 +491,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
             const float f0 = w0 * (1.f / L0), f1 = w1 * (1.f / L1);
             const bool has0 = 2 * c < G, has1 = 2 * c + 1 < G;  // padding heads are not written
             const size_t head0 = (size_t)it.b * H + it.kvh * G + 2 * c;
-            const size_t pi0 = head0 * prm.max_partitions + it.p, pi1 = pi0 + prm.max_partitions;
+            const size_t pi0 = head0 * prm.max_partitions + it.slot, pi1 = pi0 + prm.max_partitions;
 #pragma unroll
             for (int mt = 0; mt < S::kSteps; ++mt) {
                 const int d = 16 * mt + g;
@@ -416,7 +559,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
                 for (int w = 0; w < NW; ++w) f[w] *= inv;
                 const size_t head = (size_t)it.b * H + it.kvh * G + h;
-                const size_t pi = head * prm.max_partitions + it.p;
+                const size_t pi = head * prm.max_partitions + it.slot;
 #pragma unroll
                 for (int kk = 0; kk < kSlice / 8; ++kk) {
                     const int d = warp * kSlice + 8 * kk + 2 * qd;
@@ -466,7 +609,7 @@ int persistent_smem_bytes(int head_dim, int warps, int stages) {
 }
 
 namespace {
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, bool Flat>
 cudaError_t launch_persistent_t(const PartitionParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                                 cudaStream_t stream) {
     const int smem = PersistentShape<D, NW, NS>::kSmemBytes + persistent_seq_cache_bytes(prm.num_seqs);
@@ -475,11 +618,11 @@ cudaError_t launch_persistent_t(const PartitionParams& prm, const CUtensorMap& t
     static_assert(kSmemMax <= 227 * 1024, "shared memory budget of one CTA with the table cache");
     static std::atomic<unsigned long long> done{0};
     cudaError_t e = once_per_device(done, [] {
-        cudaError_t r = cudaFuncSetAttribute(pa_partition_persistent_kernel<D, NW, NS>,
+        cudaError_t r = cudaFuncSetAttribute(pa_partition_persistent_kernel<D, NW, NS, Flat>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
         if (r != cudaSuccess) return r;
         // all of an SM's shared memory, so that the dependent reduce CTAs fit beside these
-        return cudaFuncSetAttribute(pa_partition_persistent_kernel<D, NW, NS>,
+        return cudaFuncSetAttribute(pa_partition_persistent_kernel<D, NW, NS, Flat>,
                                     cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     });
     if (e != cudaSuccess) return e;
@@ -491,7 +634,7 @@ cudaError_t launch_persistent_t(const PartitionParams& prm, const CUtensorMap& t
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, pa_partition_persistent_kernel<D, NW, NS>, tk, tv, prm);
+    e = cudaLaunchKernelEx(&cfg, pa_partition_persistent_kernel<D, NW, NS, Flat>, tk, tv, prm);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -499,16 +642,26 @@ cudaError_t launch_persistent_t(const PartitionParams& prm, const CUtensorMap& t
 
 cudaError_t launch_partition_persistent(int head_dim, int warps, int stages, const PartitionParams& prm,
                                         const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t stream) {
-    if (!prm.work_offsets || !prm.work_counter || !prm.seq_order || !prm.part_sizes || grid <= 0)
+    // the flat split needs no work list, but its tables must fit the CTA's cache
+    const bool flat = prm.flat != 0;
+    if (flat ? (prm.num_seqs > kPersistentSeqCache || prm.max_partitions < 1)
+             : (!prm.work_offsets || !prm.work_counter || !prm.seq_order || !prm.part_sizes))
         return cudaErrorInvalidValue;
-#define PA_PLAUNCH_CASE(W_, S_)                                                              \
-    if (warps == W_ && stages == S_) {                                                      \
-        switch (head_dim) {                                                                 \
-            case 64: return launch_persistent_t<64, W_, S_>(prm, tk, tv, grid, stream);     \
-            case 128: return launch_persistent_t<128, W_, S_>(prm, tk, tv, grid, stream);   \
-            case 256: return launch_persistent_t<256, W_, S_>(prm, tk, tv, grid, stream);   \
-            default: return cudaErrorInvalidValue;                                          \
-        }                                                                                   \
+    if (grid <= 0) return cudaErrorInvalidValue;
+#define PA_PLAUNCH_CASE(W_, S_)                                                                       \
+    if (warps == W_ && stages == S_) {                                                               \
+        switch (head_dim) {                                                                          \
+            case 64:                                                                                 \
+                return flat ? launch_persistent_t<64, W_, S_, true>(prm, tk, tv, grid, stream)        \
+                            : launch_persistent_t<64, W_, S_, false>(prm, tk, tv, grid, stream);      \
+            case 128:                                                                                \
+                return flat ? launch_persistent_t<128, W_, S_, true>(prm, tk, tv, grid, stream)       \
+                            : launch_persistent_t<128, W_, S_, false>(prm, tk, tv, grid, stream);     \
+            case 256:                                                                                \
+                return flat ? launch_persistent_t<256, W_, S_, true>(prm, tk, tv, grid, stream)       \
+                            : launch_persistent_t<256, W_, S_, false>(prm, tk, tv, grid, stream);     \
+            default: return cudaErrorInvalidValue;                                                   \
+        }                                                                                            \
     }
     PA_FOR_EACH_PERSISTENT_SHAPE(PA_PLAUNCH_CASE)
 #undef PA_PLAUNCH_CASE

@@ -143,8 +143,9 @@ def test_plan_fused_mode_keeps_partials_and_tickets_and_launches_once():
     _, split = plan(a, mode=pb.PA_MODE_SPLIT, partition_size=512)
     assert rc == 0 and fused["mode"] == pb.PA_MODE_FUSED and fused["launch_reduce"] == 0
     assert fused["grid_x"] == split["grid_x"] == 200 and fused["partition_size"] == 512
-    # the split partials plus one 4-byte ticket per (sequence, kv head), 256-byte aligned
-    assert fused["workspace_bytes"] == split["workspace_bytes"] + 256
+    # the split partials, a slot the size of the pooled claim counters (8 bytes per
+    # (sequence, kv head)), then one 4-byte ticket per (sequence, kv head), each 256-byte aligned
+    assert fused["workspace_bytes"] == split["workspace_bytes"] + 256 + 256
     rc, one = plan(args(max_seq_len=512, num_blocks=128), mode=pb.PA_MODE_FUSED)
     assert rc == 0 and one["grid_x"] == 1 and one["workspace_bytes"] == 0   # one partition: written directly
 
@@ -307,3 +308,57 @@ def test_one_wave_pooled_plan_for_every_kv_head_count(hkv, L):
     fixed = _plan_heads(hkv, L, flags=pb.PA_FLAG_DETERMINISTIC)
     assert fixed["pooled"] == 0 and fixed["grid_x"] == pl["grid_x"] and fixed["partition_size"] == pl["partition_size"]
     assert fixed["workspace_bytes"] + 256 == pl["workspace_bytes"]
+
+
+def _partials(a, P, begin, count, m=FAKE, l=FAKE, acc=FAKE, mode=0):
+    o = pb.pa_decode_opts(mode, 0, 0, 0, None, None)
+    return pb.lib.pa_decode_partials(ctypes.byref(a), ctypes.byref(o), P, begin, count, m, l, acc, None)
+
+
+def test_partials_and_merge_check_their_arguments_before_any_cuda_call():
+    a = args(max_seq_len=102400, out=None)  # the output is not used by the partials call
+    for P, begin, count in ((500, 0, 4), (0, 0, 4), (512, -1, 4), (512, 0, 0), (1 << 20, 4096, 4)):
+        assert _partials(a, P, begin, count) == pb.PA_ERR_INVALID_ARG, (P, begin, count)
+    assert _partials(a, 512, 0, 100, mode=pb.PA_MODE_FUSED) == pb.PA_ERR_INVALID_ARG
+    assert _partials(a, 512, 0, 100, m=None) == pb.PA_ERR_INVALID_ARG
+    assert _partials(a, 512, 0, 100, acc=FAKE + 4) == pb.PA_ERR_INVALID_ARG  # tmp_out not 16-byte aligned
+    assert _partials(args(D=96, out=None), 512, 0, 100) == pb.PA_ERR_UNSUPPORTED
+
+    def merge(num_seqs=1, H=24, D=256, max_seq_len=102400, P=512, R=2, pps=100, out=FAKE, acc=FAKE):
+        return pb.lib.pa_merge_partials(out, FAKE, FAKE, acc, FAKE, num_seqs, H, D, max_seq_len, P, R, pps, None)
+
+    assert merge(pps=99) == pb.PA_ERR_INVALID_ARG          # 2 x 99 partitions of 512 miss the last tokens
+    assert merge(P=500) == pb.PA_ERR_INVALID_ARG
+    assert merge(R=0) == pb.PA_ERR_INVALID_ARG
+    assert merge(D=96) == pb.PA_ERR_UNSUPPORTED
+    assert merge(out=None) == pb.PA_ERR_INVALID_ARG
+    assert merge(acc=FAKE + 8) == pb.PA_ERR_INVALID_ARG
+    assert merge(num_seqs=0, out=None) == pb.PA_OK              # nothing to do
+
+
+def test_partials_and_merge_fail_cleanly_without_a_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _partials(args(max_seq_len=102400, out=None), 512, 0, 100) == pb.PA_ERR_CUDA
+    assert pb.lib.pa_merge_partials(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 24, 256, 102400, 512, 2, 100,
+                                    None) == pb.PA_ERR_CUDA
+
+
+def test_plan_flat_mode_one_cta_per_sm_and_its_workspace():
+    a = args(num_seqs=8, max_seq_len=8192, num_blocks=8192)
+    rc, fl = plan(a, mode=pb.PA_MODE_FLAT)
+    assert rc == 0 and fl["mode"] == pb.PA_MODE_FLAT and fl["launch_reduce"] == 1
+    assert (fl["grid_x"], fl["grid_y"], fl["grid_z"], fl["threads"]) == (152, 1, 1, 128)
+    assert fl["max_partitions"] == 38 and fl["partition_size"] == 0
+    rows = 8 * 24 * 38
+    part = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 256 * 4 + 255) // 256 * 256
+    assert fl["workspace_bytes"] == part + 256  # + one partial count per sequence
+    rc, one = plan(args(num_seqs=3, max_seq_len=4096, Hkv=4, num_blocks=2000), mode=pb.PA_MODE_FLAT)
+    assert rc == 0 and one["grid_x"] == 152
+    # at most 256 sequences: the lengths and prefix sums live in each CTA's shared memory
+    assert plan(args(num_seqs=256, max_seq_len=64, num_blocks=2000), mode=pb.PA_MODE_FLAT)[0] == 0
+    assert plan(args(num_seqs=257, max_seq_len=64, num_blocks=2000), mode=pb.PA_MODE_FLAT)[0] == pb.PA_ERR_UNSUPPORTED
+    # 8 kv heads: 19 CTAs each; one kv head: 152
+    assert plan(args(num_seqs=2, H=32, Hkv=8), mode=pb.PA_MODE_FLAT)[1]["max_partitions"] == 19
+    assert plan(args(num_seqs=2, H=8, Hkv=1), mode=pb.PA_MODE_FLAT)[1]["max_partitions"] == 152
