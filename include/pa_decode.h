@@ -199,6 +199,8 @@ typedef struct {
     int stages;            /* shared-memory stages per warp of the partition CTA */
     int max_partitions;    /* partials kept per (sequence, head) in the workspace */
     int pooled;            /* 1 if the partition CTAs claim chunks of blocks (PA_FLAG_POOLED) */
+    int coop;              /* FUSED: 1 if the grid is launched cooperatively and the CTAs of a
+                              (sequence, kv head) merge in parallel after a group barrier */
 } pa_decode_plan_t;
 
 /* Decode attention with a library-owned workspace.

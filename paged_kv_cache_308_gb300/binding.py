@@ -70,6 +70,7 @@ class pa_decode_plan_t(ctypes.Structure):
         ("smem_bytes", ctypes.c_int), ("launch_reduce", ctypes.c_int), ("reduce_grid_x", ctypes.c_int),
         ("reduce_grid_y", ctypes.c_int), ("reduce_grid_z", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
         ("stages", ctypes.c_int), ("max_partitions", ctypes.c_int), ("pooled", ctypes.c_int),
+        ("coop", ctypes.c_int),
     ]
 
     def as_dict(self):

@@ -44,15 +44,16 @@ size_t claims_bytes(long long num_seqs, long long num_kv_heads) {
     return align_up(static_cast<size_t>(num_seqs) * num_kv_heads * 8, kWsAlign);
 }
 
-// The fused combine also keeps one u32 ticket per (sequence, kv head).  The
-// tickets sit after a slot the size of the claim counters, so that a pooled
+// The fused combine also keeps two u32 words per (sequence, kv head): the
+// ticket (or, merging in parallel, the arrivals) and the departures.  They
+// sit after a slot the size of the claim counters, so that a pooled split
 // call of the same shape on the same workspace (which arms those counters)
 // never touches them.
 size_t fused_workspace_bytes(long long num_seqs, long long num_heads, long long num_kv_heads,
                              long long max_partitions, long long head_dim) {
     if (max_partitions <= 1) return 0;
     return split_workspace_bytes(num_seqs, num_heads, max_partitions, head_dim) +
-           claims_bytes(num_seqs, num_kv_heads) + align_up(static_cast<size_t>(num_seqs) * num_kv_heads * 4, kWsAlign);
+           claims_bytes(num_seqs, num_kv_heads) + align_up(static_cast<size_t>(num_seqs) * num_kv_heads * 8, kWsAlign);
 }
 
 // SM count of the current device, cached per device.
@@ -204,7 +205,7 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     bool one_wave = false;
     const int req_mode = o ? o->mode : PA_MODE_AUTO;
     if (!(o && o->partition_size > 0) && !(o && (o->warps || o->stages)) && a->num_seqs == 1 &&
-        (req_mode == PA_MODE_AUTO || req_mode == PA_MODE_SPLIT)) {
+        (req_mode == PA_MODE_AUTO || req_mode == PA_MODE_SPLIT || req_mode == PA_MODE_FUSED)) {
         const int per_head = num_sms / a->num_kv_heads;  // partitions of the sequence
         if (per_head >= 2) {
             const long long p1 = ((a->max_seq_len + per_head - 1) / per_head + bs - 1) / bs * bs;
@@ -279,6 +280,18 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     }
     plan->launch_reduce =
         ((mode == PA_MODE_SPLIT || mode == PA_MODE_PERSISTENT || flat) && plan->max_partitions > 1) ? 1 : 0;
+    // FUSED on a grid the device holds at once merges in parallel after a
+    // group barrier (a cooperative launch), when the staged slice of the
+    // merge fits the CTA's stage area; otherwise the last CTA of a group merges
+    if (mode == PA_MODE_FUSED && plan->grid_x > 1) {
+        long long per_sm = kSmemPerSm / (plan->smem_bytes + 1024);
+        if (per_sm > 2048 / plan->threads) per_sm = 2048 / plan->threads;
+        if (per_sm > 32) per_sm = 32;
+        const long long ctas = (long long)plan->grid_x * plan->grid_y * plan->grid_z;
+        const long long stage_area = (long long)warps * stages * 2 * pa::kBlockSize * a->head_dim * 2;
+        plan->coop = ctas <= per_sm * num_sms &&
+                     pa::fused_barrier_bytes(plan->grid_x, a->num_heads / a->num_kv_heads, a->head_dim) <= stage_area;
+    }
     // Pooled: on request, and by default for the one-wave plan, where every
     // CTA is resident from the start and the SMs' unequal shares of HBM
     // bandwidth would otherwise set the finish (GB300, 102400 tokens: 66.8 ->
@@ -287,7 +300,10 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     const int flags = o ? o->flags : 0;
     const bool want_pool =
         (flags & PA_FLAG_POOLED) || (one_wave && !(flags & PA_FLAG_DETERMINISTIC));
-    plan->pooled = want_pool && !(flags & PA_FLAG_DETERMINISTIC) && mode == PA_MODE_SPLIT && plan->launch_reduce &&
+    // (the claim counters are re-armed by the reduce kernel, or by the last
+    // CTA to leave a fused group's barrier)
+    plan->pooled = want_pool && !(flags & PA_FLAG_DETERMINISTIC) &&
+                   ((mode == PA_MODE_SPLIT && plan->launch_reduce) || (mode == PA_MODE_FUSED && plan->coop)) &&
                    plan->partition_size >= pa::pool_min_partition(warps, stages);
     if (mode == PA_MODE_FUSED)
         plan->workspace_bytes =
@@ -298,7 +314,7 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         plan->reduce_grid_z = a->head_dim / reduce_slice(a->head_dim, (long long)a->num_seqs * a->num_heads, num_sms);
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim);
     }
-    if (plan->pooled)  // + the claim counters
+    if (plan->pooled && mode == PA_MODE_SPLIT)  // + the claim counters (inside FUSED's layout already)
         plan->workspace_bytes += claims_bytes(a->num_seqs, a->num_kv_heads);
     if (mode == PA_MODE_PERSISTENT)  // + the work list and item counter, the order, the partition sizes
         plan->workspace_bytes = split_workspace_bytes(a->num_seqs, a->num_heads, plan->max_partitions, a->head_dim) +
@@ -413,6 +429,7 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     prm.wait_limit = (o && o->wait_limit) ? o->wait_limit : pa::kDefaultWaitLimit;
     prm.force_timeout = (o && (o->flags & PA_FLAG_FORCE_TIMEOUT)) ? 1 : 0;
     prm.trace = g_trace;
+    prm.coop = fused && plan.coop ? 1 : 0;
 
     if (listed) {
         pa::ScanParams sp;
@@ -433,11 +450,20 @@ int run(const pa_decode_args* a, const pa_decode_opts* o, void* ws, size_t ws_by
     if (o && o->event_partition_begin &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_begin), stream) != cudaSuccess)
         return PA_ERR_CUDA;
-    const cudaError_t le =
+    cudaError_t le =
         persistent ? pa::launch_partition_persistent(a->head_dim, plan.threads / 32, plan.stages, prm, tk, tv,
                                                      plan.grid_x, stream)
                    : pa::launch_partition(a->head_dim, plan.threads / 32, plan.stages, prm, tk, tv,
                                           dim3(plan.grid_x, plan.grid_y, plan.grid_z), stream);
+    if (le == cudaErrorCooperativeLaunchTooLarge && prm.coop) {
+        // the device holds fewer CTAs at once than the plan assumed: the last
+        // CTA of each group merges instead, with fixed partitions
+        cudaGetLastError();
+        prm.coop = 0;
+        prm.claims = nullptr;
+        le = pa::launch_partition(a->head_dim, plan.threads / 32, plan.stages, prm, tk, tv,
+                                  dim3(plan.grid_x, plan.grid_y, plan.grid_z), stream);
+    }
     if (le != cudaSuccess) return PA_ERR_CUDA;
     if (o && o->event_partition_end &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_end), stream) != cudaSuccess)

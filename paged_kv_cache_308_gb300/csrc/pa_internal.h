@@ -115,6 +115,10 @@ struct PartitionParams {
     // first block (null when there is one CTA per kv head: no partials).
     int flat = 0;
     int* part_counts = nullptr;
+    // Fused combine on a co-resident (cooperatively launched) grid: the CTAs
+    // of a (sequence, kv head) meet at a group barrier and merge in parallel
+    // (tickets then holds an arrival and a departure word per group).
+    int coop = 0;
 };
 
 struct ReduceParams {
@@ -160,9 +164,16 @@ struct ScanParams {
 // -1 for a shape that is not compiled.
 int partition_smem_bytes(int head_dim, int warps, int stages);
 
-// prm.claims selects the pooled form of the kernel.
+// prm.claims selects the pooled form of the kernel.  With prm.coop the grid
+// is launched cooperatively (every CTA resident at once); a grid larger than
+// the device holds at once returns cudaErrorCooperativeLaunchTooLarge without
+// launching anything.
 cudaError_t launch_partition(int head_dim, int warps, int stages, const PartitionParams& prm,
                              const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, dim3 grid, cudaStream_t stream);
+
+// Bytes of the stage area the fused combine's parallel merge needs for n
+// partitions of a group of `group` heads (defined in pa_kernels.cu).
+long long fused_barrier_bytes(int n, int group, int head_dim);
 
 // Both kernels are launched as programmatic dependents of the preceding work
 // on the stream, so their start-up overlaps its tail; each waits on the

@@ -91,7 +91,7 @@ __device__ __forceinline__ void fused_combine(const PartitionParams& prm, int b,
     using S = PartitionShape<D, NW, NS>;
     __threadfence();
     __syncthreads();
-    unsigned int* tk = prm.tickets + (size_t)b * prm.num_kv_heads + kvh;
+    unsigned int* tk = prm.tickets + 2 * ((size_t)b * prm.num_kv_heads + kvh);
     if (threadIdx.x == 0) *s_last = atomicAdd(tk, 1u) == (unsigned)(n - 1);
     __syncthreads();
     if (!*s_last) return;
@@ -227,6 +227,103 @@ __device__ __forceinline__ void fused_combine(const PartitionParams& prm, int b,
         o[0] = __floats2half2_rn(a.x * inv, a.y * inv);
         o[1] = __floats2half2_rn(a.z * inv, a.w * inv);
     }
+}
+
+// Parallel merge after a group barrier (FUSED on a co-resident grid, the
+// cooperative form).  The n partition CTAs of a (sequence, kv head) publish
+// their partials, count themselves in the group's arrival word and wait --
+// a bounded wait -- until all n have; then CTA `slot` merges its own slice
+// [slot E / n, (slot + 1) E / n) of the group's E = G * D outputs.  Its loads
+// go out in one round: the weights w_p = l_p 2^(m_p - M) / sum_q l_q 2^(m_q - M)
+// of the heads the slice touches (one warp per head) and the slice's columns
+// of every partial, into the idle stage area; then each thread sums w_p O_p
+// over p in partition order for its outputs, so the bits do not depend on
+// timing.  Every CTA then counts itself in the departure word; the last one
+// resets both words (and re-arms a pooled claim counter), so every call
+// leaves them zero.  merge = false (an aborted CTA): arrive and depart only.
+// The host uses this form only when the staged slice fits the stage area.
+template <int D, int NW, int NS>
+__device__ __forceinline__ void fused_barrier_merge(const PartitionParams& prm, int b, int kvh, int slot, int n,
+                                                    uint8_t* smem, int* s_flag, bool merge) {
+    using S = PartitionShape<D, NW, NS>;
+    unsigned int* word = prm.tickets + 2 * ((size_t)b * prm.num_kv_heads + kvh);  // arrivals, departures
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        atomicAdd(word, 1u);
+        bool ok = false;
+        if (merge) {
+            for (unsigned it = 0; it < prm.wait_limit; ++it) {
+                unsigned v;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(word) : "memory");
+                if (v >= (unsigned)n) {
+                    ok = true;
+                    break;
+                }
+            }
+            if (!ok) atomicOr(&g_status, PA_DEV_TIMEOUT);
+        }
+        *s_flag = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (*s_flag) {
+        __threadfence();
+        const int G = prm.group, E = G * D;
+        const int e0 = (int)((long long)slot * E / n), e1 = (int)((long long)(slot + 1) * E / n);
+        const int es = e1 - e0;
+        if (es > 0) {
+            const int hA = e0 / D, nh = (e1 - 1) / D - hA + 1;  // the heads the slice touches
+            const size_t head0 = (size_t)b * prm.num_heads + (size_t)kvh * G;
+            float* wts = reinterpret_cast<float*>(smem);  // [nh][n]
+            float* acc = wts + ((nh * n + 3) & ~3);       // [n][es]
+            const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+            for (int hh = warp; hh < nh; hh += NW) {
+                const size_t row = (head0 + hA + hh) * prm.max_partitions;
+                float M = -INFINITY;
+                for (int p = lane; p < n; p += 32) M = fmaxf(M, __ldcg(prm.max_logits + row + p));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+                float W = 0.f;
+                for (int p = lane; p < n; p += 32) {
+                    const float w = __ldcg(prm.exp_sums + row + p) * exp2f(__ldcg(prm.max_logits + row + p) - M);
+                    wts[hh * n + p] = w;
+                    W += w;
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(kFull, W, off);
+                const float inv = 1.f / W;
+                for (int p = lane; p < n; p += 32) wts[hh * n + p] *= inv;
+            }
+            for (int x = threadIdx.x; x < n * es; x += NW * 32) {
+                const int p = x / es, e = e0 + x % es;
+                acc[x] = __ldcg(prm.tmp_out + ((head0 + e / D) * prm.max_partitions + p) * D + e % D);
+            }
+            __syncthreads();
+            for (int i = threadIdx.x; i < es; i += NW * 32) {
+                const int e = e0 + i, hh = e / D - hA;
+                float o = 0.f;
+                for (int p = 0; p < n; ++p) o += wts[hh * n + p] * acc[p * es + i];
+                prm.out[head0 * D + e] = __float2half_rn(o);
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(word + 1, 1u) == (unsigned)(n - 1)) {
+        // every CTA of the group is past the barrier and done claiming
+        atomicExch(word, 0u);
+        atomicExch(word + 1, 0u);
+        if (prm.claims) prm.claims[(size_t)b * prm.num_kv_heads + kvh] = (unsigned long long)kClaimTag << 32;
+    }
+}
+
+// Bytes of the idle stage area the parallel merge stages for up to n
+// partitions of one group (the host checks that this fits before it picks
+// that form).  A slice holds es <= ceil(E / n) outputs and touches nh <=
+// es / head_dim + 2 heads, so the weights take nh n <= group + 3 n floats
+// (+3 to align the columns) and the columns n es <= E + n floats: a bound
+// that grows with n, so it covers every group of a plan.
+__host__ __device__ constexpr long long barrier_merge_bytes(int n, int group, int head_dim) {
+    return 4ll * ((long long)group + (long long)group * head_dim + 4ll * n + 3);
 }
 
 // Pooled == false: CTA p takes the blocks of partition p, dealt round-robin
@@ -522,9 +619,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
         // A fused combine counts every partition's ticket, so an aborted CTA
         // still takes its own; the last one resets the count (the output is
         // not written and the status word already reports the failure).
-        if (prm.tickets && n_part > 1 && threadIdx.x == 0) {
-            unsigned int* tk = prm.tickets + (size_t)b * prm.num_kv_heads + kvh;
-            if (atomicAdd(tk, 1u) == (unsigned)(n_part - 1)) atomicExch(tk, 0u);
+        if (prm.tickets && n_part > 1) {
+            if (prm.coop) {
+                fused_barrier_merge<D, NW, NS>(prm, b, kvh, slot, n_part, smem, sm_abort + 1, false);
+            } else if (threadIdx.x == 0) {
+                unsigned int* tk = prm.tickets + 2 * ((size_t)b * prm.num_kv_heads + kvh);
+                if (atomicAdd(tk, 1u) == (unsigned)(n_part - 1)) atomicExch(tk, 0u);
+            }
         }
         return;
     }
@@ -648,7 +749,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
     }
     // spare words of the control area: the ticket result, then an 8-byte copy barrier
-    if (fused) fused_combine<D, NW, NS>(prm, b, kvh, n_part, smem, sm_abort + 1, smem_addr(sm_abort + 2));
+    if (fused) {
+        if (prm.coop)
+            fused_barrier_merge<D, NW, NS>(prm, b, kvh, slot, n_part, smem, sm_abort + 1, true);
+        else
+            fused_combine<D, NW, NS>(prm, b, kvh, n_part, smem, sm_abort + 1, smem_addr(sm_abort + 2));
+    }
     PA_TRACE_MARK(4);
 }
 
@@ -788,13 +894,23 @@ cudaError_t launch_partition_t(const PartitionParams& prm, const CUtensorMap& tk
                                cudaStream_t stream) {
     const int smem = PartitionShape<D, NW, NS>::kSmemBytes;
     static std::atomic<unsigned long long> done{0};
+    static int resident[64];  // CTAs one SM holds at once, per device (for the cooperative form)
     cudaError_t e = once_per_device(done, [&] {
         cudaError_t r = cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS, Pooled>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (r != cudaSuccess) return r;
         // all of an SM's shared memory, so that the dependent reduce CTAs fit beside these
-        return cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS, Pooled>,
-                                    cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+        r = cudaFuncSetAttribute(pa_partition_kernel<D, NW, NS, Pooled>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+        if (r != cudaSuccess) return r;
+        int dev = 0, per_sm = 0, sms = 0;
+        if ((r = cudaGetDevice(&dev)) != cudaSuccess) return r;
+        if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_partition_kernel<D, NW, NS, Pooled>,
+                                                               NW * 32, smem)) != cudaSuccess)
+            return r;
+        if ((r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return r;
+        if (dev >= 0 && dev < 64) resident[dev] = per_sm * sms;
+        return cudaSuccess;
     });
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -802,10 +918,28 @@ cudaError_t launch_partition_t(const PartitionParams& prm, const CUtensorMap& tk
     cfg.blockDim = dim3(NW * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cudaLaunchAttribute attr[2] = {pdl_attribute(), {}};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (prm.coop) {
+        // every CTA resident at once, or no launch at all: the CTAs of a group wait for each other
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        const long long ctas = (long long)grid.x * grid.y * grid.z;
+        if (dev < 0 || dev >= 64 || ctas > resident[dev]) return cudaErrorCooperativeLaunchTooLarge;
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg.numAttrs = 2;
+    }
     e = cudaLaunchKernelEx(&cfg, pa_partition_kernel<D, NW, NS, Pooled>, tk, tv, prm);
+    if (e != cudaSuccess && prm.coop) {
+        // a cooperative launch that the runtime will not combine with the
+        // programmatic dependency: launch it as a plain stream successor
+        cudaGetLastError();
+        attr[0] = attr[1];
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, pa_partition_kernel<D, NW, NS, Pooled>, tk, tv, prm);
+    }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -886,6 +1020,8 @@ cudaError_t launch_reduce(int head_dim, int width, const ReduceParams& prm, dim3
         default: return cudaErrorInvalidValue;
     }
 }
+
+long long fused_barrier_bytes(int n, int group, int head_dim) { return barrier_merge_bytes(n, group, head_dim); }
 
 cudaError_t disarm_claims(unsigned long long* claims, size_t count, cudaStream_t stream) {
     return cudaMemsetAsync(claims, 0, count * sizeof(unsigned long long), stream);

@@ -139,7 +139,8 @@ def test_permuted_block_table_is_bit_identical(dev, opt):
     assert torch.equal(a, run(_permuted_pool(w, 12), **opt))
 
 
-@pytest.mark.parametrize("opt", [dict(flags=pb.PA_FLAG_DETERMINISTIC), dict(mode="fused")],
+@pytest.mark.parametrize("opt", [dict(flags=pb.PA_FLAG_DETERMINISTIC),
+                                 dict(mode="fused", flags=pb.PA_FLAG_DETERMINISTIC)],
                          ids=["one_wave_deterministic", "fused"])
 def test_permuted_block_table_is_bit_identical_on_one_long_sequence(dev, opt):
     # the plan the benchmark times for one long sequence (one wave of one
@@ -287,9 +288,10 @@ def _fused_call(w, out, ws, stream=None, **extra):
 
 
 def _tickets(w, ws, plan_split_bytes):
-    # after the partials and a slot the size of the pooled claim counters
+    # after the partials and a slot the size of the pooled claim counters: two
+    # 4-byte words per (sequence, kv head)
     off = plan_split_bytes + (8 * len(w.seq_lens_host) * w.num_kv_heads + 255) // 256 * 256
-    return ws[off:off + 4 * len(w.seq_lens_host) * w.num_kv_heads]
+    return ws[off:off + 8 * len(w.seq_lens_host) * w.num_kv_heads]
 
 
 def test_fused_combine_is_deterministic_and_leaves_tickets_zero(dev):
@@ -336,7 +338,7 @@ def test_pooled_then_fused_on_one_caller_workspace(dev):
         assert (_claims(ws[:pooled["workspace_bytes"]], pooled, w) == CLAIM_ARMED).all()
         out = run(w, workspace=ws, mode="fused", partition_size=512)
         assert_parity(out, ref, f"fused after pooled {k}")
-        tickets = ws[fused["workspace_bytes"] - (len(w.seq_lens_host) * w.num_kv_heads * 4 + 255) // 256 * 256:]
+        tickets = ws[fused["workspace_bytes"] - (len(w.seq_lens_host) * w.num_kv_heads * 8 + 255) // 256 * 256:]
         assert torch.count_nonzero(tickets) == 0
 
 
@@ -605,3 +607,76 @@ def test_flat_split_many_short_sequences_and_graph_replay(dev):
     assert pb.pa_get_device_status() == 0
     assert_parity(out, oracle_ref(w), "flat graph replay with new lengths")
 
+
+
+# ---- fused combine on a co-resident grid: a group barrier, then every CTA merges its slice ----
+
+@pytest.mark.parametrize("lens,opt,pooled", [
+    ([102400], dict(), True),                                        # the one-wave plan, pooled
+    ([102400], dict(flags=pb.PA_FLAG_DETERMINISTIC), False),
+    ([2048], dict(partition_size=256), False),
+    ([3000, 17, 1029, 513, 128, 1, 0], dict(partition_size=128, warps=1, stages=2), False),
+    ([5000, 700, 64], dict(partition_size=512, warps=2, stages=2), False),
+    ([7000, 4000], dict(partition_size=1024, warps=4, stages=2), False),
+], ids=["one_wave_pooled", "one_wave_fixed", "b1_l2048_P256", "ragged_P128", "P512_2x2", "P1024_4x2"])
+def test_fused_parallel_merge(dev, lens, opt, pooled):
+    w = W.make_workload("coop", lens, num_blocks=sum((L + 15) // 16 for L in lens) + 9, seed=60 + len(lens),
+                        device=dev, tail_fill=float("nan"))
+    out = torch.empty_like(w.q)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len,
+                             mode="fused", **opt)
+    assert plan["coop"] == 1 and plan["launch_reduce"] == 0 and plan["pooled"] == int(pooled)
+    ws = pb.alloc_workspace(plan, dev)
+    ref = oracle_ref(w, THREADS)
+    outs = []
+    for k in range(3):  # the group words are left zero, the pooled counters re-armed
+        outs.append(run(w, workspace=ws, mode="fused", **opt))
+        assert_parity(outs[-1], ref, f"fused parallel merge, call {k}")
+        assert torch.count_nonzero(_tickets(w, ws, _split_bytes(w, plan))) == 0
+        if pooled:
+            assert (_claims_at(ws, _split_bytes(w, plan), w) == CLAIM_ARMED).all()
+    if not pooled:
+        assert all(torch.equal(outs[0], o) for o in outs[1:])
+    # the same merge as the reduce kernel up to rounding
+    split = run(w, mode="split", **{k: v for k, v in opt.items() if k != "flags"})
+    assert (outs[0].float() - split.float()).abs().max().item() < 2e-3
+    # captured and replayed
+    g = torch.cuda.CUDAGraph()
+    res = torch.empty_like(w.q)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        pb.decode_workload(w, out=res, stream=torch.cuda.current_stream(), workspace=ws, mode="fused", **opt)
+    for _ in range(3):
+        res.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert pb.pa_get_device_status() == 0
+        assert_parity(res, ref, "fused parallel merge, graph replay")
+
+
+def test_fused_parallel_merge_after_forced_timeout(dev):
+    w = W.make_workload("coopto", [20000, 3000], num_blocks=1500, seed=61, device=dev)
+    kw = dict(mode="fused", partition_size=512)
+    out = torch.empty_like(w.q)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len, **kw)
+    assert plan["coop"] == 1
+    ws = pb.alloc_workspace(plan, dev)
+    pb.pa_get_device_status()
+    pb.decode_workload(w, workspace=ws, flags=pb.PA_FLAG_FORCE_TIMEOUT, **kw)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() & pb.PA_DEV_TIMEOUT
+    assert torch.count_nonzero(_tickets(w, ws, _split_bytes(w, plan))) == 0  # every group left them zero
+    assert_parity(run(w, workspace=ws, **kw), oracle_ref(w), "fused after a forced timeout")
+
+
+def _split_bytes(w, plan):
+    """Bytes of the partials in a fused plan's workspace (before the claim and ticket slots)."""
+    n = len(w.seq_lens_host) * w.num_kv_heads
+    return plan["workspace_bytes"] - (n * 8 + 255) // 256 * 256 - (n * 8 + 255) // 256 * 256
+
+
+def _claims_at(ws, split_bytes, w):
+    n = len(w.seq_lens_host) * w.num_kv_heads
+    return ws[split_bytes:split_bytes + 8 * n].view(torch.int64)

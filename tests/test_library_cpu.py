@@ -74,8 +74,9 @@ def test_plan_long_context_runs_one_wave_of_one_cta_per_sm():
     assert (fixed["reduce_grid_x"], fixed["reduce_grid_y"], fixed["reduce_grid_z"]) == (24, 1, 8)
     assert fixed["workspace_bytes"] == ws_bytes(1, 24, 200, 256)
     assert fixed["workspace_bytes"] == pb.pa_decode_workspace_size(1, 102400, 24, 256, 512)
+    # FUSED takes the same one-wave decomposition (its CTAs merge after a group barrier)
     rc, fused = plan(args(), mode=pb.PA_MODE_FUSED)
-    assert rc == 0 and fused["partition_size"] == 512
+    assert rc == 0 and fused["partition_size"] == 2704 and fused["coop"] == 1
 
 
 def test_plan_modes():
@@ -139,7 +140,7 @@ def test_plan_persistent_mode_has_a_fixed_grid_and_a_work_list():
 
 def test_plan_fused_mode_keeps_partials_and_tickets_and_launches_once():
     a = args(max_seq_len=102400)
-    rc, fused = plan(a, mode=pb.PA_MODE_FUSED)
+    rc, fused = plan(a, mode=pb.PA_MODE_FUSED, partition_size=512)
     _, split = plan(a, mode=pb.PA_MODE_SPLIT, partition_size=512)
     assert rc == 0 and fused["mode"] == pb.PA_MODE_FUSED and fused["launch_reduce"] == 0
     assert fused["grid_x"] == split["grid_x"] == 200 and fused["partition_size"] == 512
@@ -362,3 +363,20 @@ def test_plan_flat_mode_one_cta_per_sm_and_its_workspace():
     # 8 kv heads: 19 CTAs each; one kv head: 152
     assert plan(args(num_seqs=2, H=32, Hkv=8), mode=pb.PA_MODE_FLAT)[1]["max_partitions"] == 19
     assert plan(args(num_seqs=2, H=8, Hkv=1), mode=pb.PA_MODE_FLAT)[1]["max_partitions"] == 152
+
+
+def test_plan_fused_merges_in_parallel_on_a_grid_the_device_holds():
+    # one long sequence: the one-wave plan (one 4-warp CTA per SM), pooled, cooperative
+    rc, fw = plan(args(max_seq_len=102400), mode=pb.PA_MODE_FUSED)
+    assert rc == 0 and fw["coop"] == 1 and fw["pooled"] == 1 and fw["launch_reduce"] == 0
+    assert (fw["grid_x"], fw["grid_y"], fw["threads"]) == (38, 4, 128)
+    o = pb.pa_decode_opts(pb.PA_MODE_FUSED, 0, pb.PA_FLAG_DETERMINISTIC, 0, None, None)
+    pl = pb.pa_decode_plan_t()
+    assert pb.lib.pa_decode_plan(ctypes.byref(args(max_seq_len=102400)), ctypes.byref(o), SMS, ctypes.byref(pl)) == 0
+    assert pl.coop == 1 and pl.pooled == 0
+    # 6400 partitions of 16 tokens x 4 kv heads: more CTAs than the SMs hold, so the last CTA merges
+    rc, big = plan(args(max_seq_len=102400), mode=pb.PA_MODE_FUSED, partition_size=16)
+    assert rc == 0 and big["coop"] == 0 and big["pooled"] == 0
+    # the split and the other modes never take the cooperative form
+    for mode in (pb.PA_MODE_SPLIT, pb.PA_MODE_SINGLE, pb.PA_MODE_PERSISTENT, pb.PA_MODE_FLAT, pb.PA_MODE_AUTO):
+        assert plan(args(max_seq_len=102400), mode=mode)[1]["coop"] == 0
