@@ -505,13 +505,17 @@ def run_gpu(args):
         pb.pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
                      w.head_dim, w.block_size, w.scale, stream, max_seq_len=w.max_seq_len)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
+    step()  # the first warm-up step sets the kernels' attributes and allocates the workspace
     torch.cuda.synchronize()
     assert pb.pa_get_device_status() == 0
 
     sampler = ClockSampler(local)
     sampler.start()
+    # the other warm-up steps run right before the timed region: starting the
+    # clock sampler leaves the GPU idle for a moment, and the first calls
+    # after an idle spell run slower
+    for _ in range(max(args.warmup, 3) - 1):
+        step()
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
