@@ -15,11 +15,13 @@
 //     block-table entries of the current and the next 32 blocks in registers;
 //   - warps 14 and 15 (MMA, one lane each): warp 14 issues S(j) = Q K(j)^T
 //     (M 128, N 64, K = head_dim, Q read from TMEM so only K comes from
-//     shared memory) into the TMEM score buffer as soon as every row has
-//     read S(j-1) out of it, warp 15 O += P(j) V(j) (M 128, N = head_dim,
-//     K 64) with P read from one of two TMEM P buffers.  The tensor cores
-//     take few MMAs ahead of their issuer, so two issuing threads keep them
-//     busy while either waits; S(j+1) runs while the rows work on tile j;
+//     shared memory) into TMEM score buffer j % 2 as soon as the P.V that
+//     last read that buffer has completed, warp 15 O += P(j) V(j) (M 128,
+//     N = head_dim, K 64) with P(j) read from the same buffer, where the rows
+//     wrote it (fp16) over S(j).  The tensor cores take few MMAs ahead of
+//     their issuer, so two issuing threads keep them busy while either waits;
+//     with two score buffers S(j+1) is issued right behind S(j) and runs
+//     while the rows work on tile j, with no hand-over from the rows first;
 // * keys are walked in tiles of 64 (4 blocks of 16: paged context blocks
 //   through the block table, then the chunk's own blocks), K tiles in a
 //   3-slot ring and V tiles in a 2-slot ring, all with the 128-byte swizzle:
@@ -51,10 +53,9 @@ enum : int {
     kTcBarKEmpty = kTcBarKFull + kTcMaxSlots,   // K slot read by its S MMA (commit)
     kTcBarVFull = kTcBarKEmpty + kTcMaxSlots,   // V slot landed (as K)
     kTcBarVEmpty = kTcBarVFull + kTcMaxSlots,   // V slot read by its P.V MMA (commit)
-    kTcBarSDone = kTcBarVEmpty + kTcMaxSlots,   // the score buffer holds S(j) (commit)
-    kTcBarSFree = kTcBarSDone + 1,            // every row warp has read S(j) into registers
-    kTcBarPReady = kTcBarSFree + 1,           // P buffer b written by all 4 row warps, 2
-    kTcBarPVDone = kTcBarPReady + 2,          // the P.V reading P buffer b completed (commit), 2
+    kTcBarSDone = kTcBarVEmpty + kTcMaxSlots,   // score buffer b holds S(j) (commit), 2
+    kTcBarPReady = kTcBarSDone + 2,           // P(j) written over S(j) in buffer b by all 4 row warps, 2
+    kTcBarPVDone = kTcBarPReady + 2,          // the P.V reading buffer b completed (commit), 2
     kTcBarQReady = kTcBarPVDone + 2,          // Q rows stored in TMEM by the 4 row warps
     kTcBarSDrain = kTcBarQReady + 1,          // every S MMA completed (final commit)
     kTcBarPVDrain = kTcBarSDrain + 1,         // every P.V MMA completed (final commit)
@@ -75,8 +76,8 @@ struct PrefixTcShape {
     // at most two CTAs per SM, so that their TMEM allocations always fit in
     // the SM's 512 columns (an allocation never has to wait for another CTA)
     static constexpr int kSmemBytes = kSmemNeed > 80 * 1024 ? kSmemNeed : 80 * 1024;
-    // O (D columns), Q (D / 2 columns of fp16 pairs), one score buffer (64),
-    // two P buffers (32 columns of fp16 pairs each)
+    // O (D columns), Q (D / 2 columns of fp16 pairs), two score buffers of
+    // 64 columns (each also takes its tile's P, 32 columns of fp16 pairs)
     static constexpr int kTmemUsed = D + D / 2 + 2 * kTcKeys;
     static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
     static_assert(kTmemUsed <= 512, "tensor memory columns of one SM");
@@ -198,7 +199,7 @@ __device__ __forceinline__ float tc_ex2(float x) {  // the PTX ex2.approx instru
 // P(j) ready, V(j) landed, K(j+1) landed, P.V(j) issued), 4 and 8-11 by the
 // load warp (V(j) issued, loop top, K(j+1) slot free, K(j+1) issued, V(j)
 // slot free), 5-6 by warp 0 (scores j in, P(j) out), 7 by warp 3 (P(j) out),
-// 14-15 by the S warp (K(j) landed, S(j-1) read by the rows).
+// 14-15 by the S warp (K(j) landed, score buffer j % 2 free).
 #ifdef PA_TRACE
 #define PA_TC_MARK(j, e)                                                                                          \
     do {                                                                                                          \
@@ -328,7 +329,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
     if (t == 0) {
         *sm_abort = 0;
         for (int i = 0; i < kTcBars; ++i) {
-            const bool by_rows = i == kTcBarSFree || i == kTcBarPReady || i == kTcBarPReady + 1 || i == kTcBarQReady;
+            const bool by_rows = i == kTcBarPReady || i == kTcBarPReady + 1 || i == kTcBarQReady;
             const bool by_k_loads = i < kTcBarKEmpty, by_v_loads = i >= kTcBarVFull && i < kTcBarVEmpty;
             mbar_init(bar(i), by_rows ? kTcSoftmaxWarps : by_k_loads ? kTcKLoadWarps : by_v_loads ? kTcVLoadWarps : 1);
         }
@@ -348,8 +349,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
     const uint32_t tmem = *tslot;
     const uint32_t tO = tmem;                    // D columns
     const uint32_t tQ = tO + D;                  // D / 2 columns (fp16 pairs)
-    const uint32_t tS = tQ + D / 2;              // the score buffer, 64 columns
-    const uint32_t tP0 = tS + kTcKeys;           // two P buffers of 32 columns (fp16 pairs)
+    const uint32_t tS = tQ + D / 2;              // two score buffers of 64 columns; P(j) over S(j)
     const unsigned limit = prm.force_timeout ? 0u : prm.wait_limit;
 
     if (warp >= kTcLoadWarp0 && warp < kTcSWarp) {
@@ -488,24 +488,28 @@ __global__ void __maxnreg__(kTcMaxRegs)
             ok = tc_warp_wait(bar(kTcBarQReady), 0, limit, sm_abort);
             for (int j = 0; ok && j < ntiles; ++j) {
                 if (lane == 0) PA_TC_MARK(j, 0);
-                // K(j) landed; every row has read S(j-1) out of the score buffer
+                // K(j) landed; score buffer j % 2 is free once P.V(j-2), the
+                // last reader of the P written there, has completed
                 if (!(ok = tc_warp_wait(bar(kTcBarKFull + j % S::kKSlots), (j / S::kKSlots) & 1, limit, sm_abort)))
                     break;
                 if (lane == 0) PA_TC_MARK(j, 14);
-                if (j >= 1 && !(ok = tc_warp_wait(bar(kTcBarSFree), (j - 1) & 1, limit, sm_abort))) break;
+                if (j >= 2 &&
+                    !(ok = tc_warp_wait(bar(kTcBarPVDone + (j & 1)), ((j - 2) >> 1) & 1, limit, sm_abort)))
+                    break;
                 if (lane == 0) PA_TC_MARK(j, 15);
                 tc_fence_after();
                 if (lane == 0) {
-                    // S(j) = Q K(j)^T into the score buffer, Q (A) from TMEM 8
+                    // S(j) = Q K(j)^T into score buffer j % 2, Q (A) from TMEM 8
                     // columns per 16 head_dim elements; a descriptor's low field is
                     // the start address / 16, so stepping through a buffer adds
                     // offset / 16
                     const uint64_t kd = kdesc0 + (uint64_t)((j % S::kKSlots) * (S::kTileBytes >> 4));
+                    const uint32_t sb = tS + (uint32_t)(j & 1) * kTcKeys;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k)
-                        tc_mma_ts(tS, tQ + k * 8, kd + (uint64_t)(((k >> 2) * S::kChunkStride + (k & 3) * 32) >> 4), idS,
+                        tc_mma_ts(sb, tQ + k * 8, kd + (uint64_t)(((k >> 2) * S::kChunkStride + (k & 3) * 32) >> 4), idS,
                                   k > 0);
-                    tc_commit(bar(kTcBarSDone));
+                    tc_commit(bar(kTcBarSDone + (j & 1)));
                     tc_commit(bar(kTcBarKEmpty + j % S::kKSlots));
                     PA_TC_MARK(j, 1);
                 }
@@ -538,12 +542,12 @@ __global__ void __maxnreg__(kTcMaxRegs)
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    // O += P(j) V(j), P in buffer j % 2, one MMA per block of 16
-                    // keys (V block: 64-column chunks 2 KB apart, 8-key groups
-                    // 1 KB apart); P buffer j % 2 and V slot j % kVSlots are free
-                    // when they complete
+                    // O += P(j) V(j), P over S(j) in score buffer j % 2, one MMA
+                    // per block of 16 keys (V block: 64-column chunks 2 KB apart,
+                    // 8-key groups 1 KB apart); score buffer j % 2 and V slot
+                    // j % kVSlots are free when they complete
                     const uint64_t vd = vdesc0 + (uint64_t)((j % S::kVSlots) * (S::kTileBytes >> 4));
-                    const uint32_t a = tP0 + (j & 1) * (kTcKeys / 2);
+                    const uint32_t a = tS + (uint32_t)(j & 1) * kTcKeys;
 #pragma unroll
                     for (int k = 0; k < kTcKeys / 16; ++k)
                         tc_mma_ts(tO, a + k * 8, vd + (uint64_t)((k * S::kBlockBytes) >> 4), idO, (j > 0 || k > 0));
@@ -605,15 +609,12 @@ __global__ void __maxnreg__(kTcMaxRegs)
         float m = -INFINITY, l = 0.f;  // reference max (scaled, log2 domain) and exp sum
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            if (!(ok = tc_warp_wait(bar(kTcBarSDone), j & 1, limit, sm_abort))) break;
+            const uint32_t sb = tS + (uint32_t)(j & 1) * kTcKeys + lane_off;  // this row of score buffer j % 2
+            if (!(ok = tc_warp_wait(bar(kTcBarSDone + (j & 1)), (j >> 1) & 1, limit, sm_abort))) break;
             tc_fence_after();
             if (t == 0) PA_TC_MARK(j, 5);
             uint32_t sv[2][32];
-            tc_ld32x2(tS + lane_off, sv[0], tS + lane_off + 32, sv[1]);
-            // S(j) is in registers: the score buffer may take S(j+1)
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kTcBarSFree));
+            tc_ld32x2(sb, sv[0], sb + 32, sv[1]);
             // visibility: every key of a tile made only of full context blocks
             // is visible; otherwise mask per key
             const bool full_ctx = 4 * j + 3 < nctx - (C % kBlockSize != 0 ? 1 : 0);
@@ -665,13 +666,10 @@ __global__ void __maxnreg__(kTcMaxRegs)
                 pk[c] = half2_bits(__floats2half2_rn(p0, p1));
             }
             l = l * alpha + (rs0 + rs1);
-            // P(j) to its own buffer once P.V(j-2), its last reader, has
-            // completed (this warp waited for P.V(j-4) two tiles ago, so the
-            // parity wait is unambiguous)
-            if (j >= 2 && !(ok = tc_warp_wait(bar(kTcBarPVDone + (j & 1)), ((j - 2) >> 1) & 1, limit, sm_abort)))
-                break;
-            tc_fence_after();
-            tc_st32(tP0 + (j & 1) * (kTcKeys / 2) + lane_off, pk);
+            // P(j) over S(j), which is in registers now: the S MMA of this
+            // buffer was issued after P.V(j-2), the buffer's previous reader,
+            // had completed, and the next one waits for P.V(j)
+            tc_st32(sb, pk);
             if (j > 0 && __any_sync(kFull, move)) {
                 // O is written by P.V(j-1): wait for it, then rescale this row
                 // (P.V(j-3) was waited for one tile ago)
