@@ -12,6 +12,7 @@ import pytest
 import torch
 
 from paged_kv_cache_308_gb300 import binding as pb
+from paged_kv_cache_308_gb300 import split_kv
 from paged_kv_cache_308_gb300 import workloads as W
 from parity_helpers import assert_parity, oracle_ref
 
@@ -19,7 +20,8 @@ pytestmark = pytest.mark.gpu
 
 MODES = [dict(), dict(mode="single"), dict(mode="split"), dict(mode="fused"), dict(mode="persistent"),
          dict(mode="split", partition_size=32), dict(mode="fused", partition_size=64),
-         dict(mode="persistent", partition_size=48), dict(mode="persistent", warps=2, stages=2)]
+         dict(mode="persistent", partition_size=48), dict(mode="persistent", warps=2, stages=2),
+         dict(mode="flat"), dict(mode="flat", warps=1, stages=2), dict(mode="flat", warps=2, stages=2)]
 
 
 def draw_case(i):
@@ -39,7 +41,7 @@ def dev():
     return torch.device("cuda:0")
 
 
-@pytest.mark.parametrize("i", range(36))
+@pytest.mark.parametrize("i", range(48))
 def test_random_case(dev, i):
     c = draw_case(i)
     blocks = sum((L + 15) // 16 for L in c["lens"]) + 3
@@ -83,3 +85,30 @@ def test_random_pooled_case(dev, i):
         for b, L in enumerate(c["lens"]):
             if L == 0:
                 assert torch.count_nonzero(out[b]) == 0, f"pooled case {i}: empty sequence {b} not zero"
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_split_kv_case(dev, i):
+    # the partitions spread over R sources (one pa_decode_partials call each,
+    # into its slot of the gathered buffer), then pa_merge_partials
+    c = draw_case(200 + i)
+    r = random.Random(300 + i)
+    P = 16 * r.choice([1, 2, 5, 16, 32, 64])
+    R = r.choice([1, 2, 3, 4])
+    blocks = sum((L + 15) // 16 for L in c["lens"]) + 3
+    w = W.make_workload(f"randskv{i}", c["lens"], num_heads=c["num_heads"], num_kv_heads=c["num_kv_heads"],
+                        head_dim=c["head_dim"], num_blocks=blocks, seed=c["seed"], device=dev,
+                        tail_fill=float("nan"))
+    ranges = [split_kv.partition_range(k, R, w.max_seq_len, P) for k in range(R)]
+    count = ranges[0][1]
+    gm, gl, gacc = split_kv.alloc_partials(w.num_seqs, w.num_heads, w.head_dim, count, dev, sources=R)
+    for k, (begin, n) in enumerate(ranges):
+        pb.pa_decode_partials(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads,
+                              w.head_dim, w.block_size, w.scale, P, begin, n, gm[k], gl[k], gacc[k],
+                              max_seq_len=w.max_seq_len)
+    out = torch.full_like(w.q, float("nan"))
+    pb.pa_merge_partials(out, gm, gl, gacc, w.seq_lens, w.num_heads, w.head_dim, P, R, count,
+                         max_seq_len=w.max_seq_len)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    assert_parity(out, oracle_ref(w), f"split-KV case {i}: {c} P={P} R={R}")
