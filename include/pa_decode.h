@@ -87,15 +87,22 @@ enum {
     PA_MODE_FUSED = 3,  /* partitions as SPLIT, one launch: the last CTA of each (sequence, kv head)
                            to finish (an atomic ticket; nobody waits) merges the partials in
                            partition order ("docs" commit page, the cross-partition level of the
-                           reduction hierarchy, here without any CTA waiting on another).  The
-                           workspace also holds one 4-byte ticket per (sequence, kv head), after
-                           the partials and a slot the size of the pooled claim counters, so a
-                           pooled call of the same shape on the same workspace leaves them
-                           alone.  The tickets must be zero before the first FUSED call on a
-                           workspace, and again after the workspace served a call of another
-                           shape or a PERSISTENT call (whose tables cover that slot): zero
-                           plan.workspace_bytes, e.g. with cudaMemsetAsync.  Every FUSED call
-                           leaves them zero, also after a device error */
+                           reduction hierarchy).  When the device holds the whole grid at once
+                           (plan.coop) the grid is launched cooperatively: the CTAs of each
+                           (sequence, kv head) meet at a bounded group barrier and each merges
+                           its own slice of the outputs; otherwise the last CTA to finish merges
+                           (an atomic ticket; nobody waits).  For one long sequence FUSED takes
+                           the one-wave plan (pooled unless PA_FLAG_DETERMINISTIC).  The
+                           workspace also holds two 4-byte words per (sequence, kv head) (the
+                           ticket or arrivals, and the departures), after the partials and a
+                           slot of 8 bytes per (sequence, kv head) for the pooled claim
+                           counters, so a pooled SPLIT call of the same shape on the same
+                           workspace leaves them alone.  The words must be zero before the first
+                           FUSED call on a workspace, and again after the workspace served a
+                           call of another shape or a PERSISTENT or FLAT call (whose tables may
+                           cover that slot): zero plan.workspace_bytes, e.g. with
+                           cudaMemsetAsync.  Every FUSED call leaves them zero, also after a
+                           device error */
     PA_MODE_PERSISTENT = 4, /* a fixed grid of (SMs x CTAs per SM) takes the items of a work list
                               that a small kernel builds on the device from a device counter,
                               longest partitions first.  Each sequence gets its own partition size:
