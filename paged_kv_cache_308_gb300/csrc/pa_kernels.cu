@@ -824,7 +824,9 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
         // single-partition, empty and invalid sequences were finished by the partition kernel
         return;
     }
-    const int n = prm.part_counts ? prm.part_counts[b] : (L + part - 1) / part;
+    // (a flat split's count comes from the workspace: clamped to the row, so a
+    // stale word could never send the reads past it)
+    const int n = prm.part_counts ? min(prm.part_counts[b], prm.max_partitions) : (L + part - 1) / part;
     if (!Merge && n <= 1) return;
 
     __shared__ float4 red_acc[kGroups][kLanes];
