@@ -85,8 +85,9 @@ struct PartitionParams {
     // Diagnostic builds (-DPA_TRACE) only: per-CTA records of
     // {sm id, entry, first block ready, main loop done, exit} in globaltimer ns.
     unsigned long long* trace;
-    // Fused combine: one ticket per (sequence, kv head), zero before the call
-    // and left zero after it; null when a separate reduce kernel merges.
+    // Fused combine: two words per (sequence, kv head) (the ticket or the
+    // arrivals, then the departures), zero before the call and left zero
+    // after it; null when a separate reduce kernel merges.
     unsigned int* tickets;
     // Persistent schedule: the sequences in schedule order (seq_order), the
     // exclusive prefix sums of their work items in that order (num_seqs + 1

@@ -692,7 +692,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
             if (lane == 0) mbar_arrive(bar(kTcBarPReady + (j & 1)));
         }
         PA_TC_PHASE(3);
-        // the last two P.Vs (one per P buffer) complete before O is read
+        // the last two P.Vs (one per score buffer) complete before O is read
         if (ok && ntiles >= 2)
             ok = tc_warp_wait(bar(kTcBarPVDone + ((ntiles - 2) & 1)), ((ntiles - 2) >> 1) & 1, limit, sm_abort);
         if (ok) ok = tc_warp_wait(bar(kTcBarPVDone + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, limit, sm_abort);

@@ -145,7 +145,7 @@ def test_plan_fused_mode_keeps_partials_and_tickets_and_launches_once():
     assert rc == 0 and fused["mode"] == pb.PA_MODE_FUSED and fused["launch_reduce"] == 0
     assert fused["grid_x"] == split["grid_x"] == 200 and fused["partition_size"] == 512
     # the split partials, a slot the size of the pooled claim counters (8 bytes per
-    # (sequence, kv head)), then one 4-byte ticket per (sequence, kv head), each 256-byte aligned
+    # (sequence, kv head)), then two 4-byte group words per (sequence, kv head), each 256-byte aligned
     assert fused["workspace_bytes"] == split["workspace_bytes"] + 256 + 256
     rc, one = plan(args(max_seq_len=512, num_blocks=128), mode=pb.PA_MODE_FUSED)
     assert rc == 0 and one["grid_x"] == 1 and one["workspace_bytes"] == 0   # one partition: written directly
