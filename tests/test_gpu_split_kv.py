@@ -165,3 +165,30 @@ def test_argument_errors(dev):
     w.seq_lens[0] = 3001
     pb.pa_merge_partials(out, gm, gl, gacc, w.seq_lens, w.num_heads, w.head_dim, 512, 2, count, max_seq_len=3000)
     assert pb.pa_get_device_status() & pb.PA_DEV_BAD_SEQ_LEN
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_split_kv_decode_through_nccl(dev):
+    # the whole host path -- ranges, partials, an NCCL all-gather of the local
+    # buffers, the merge -- in a process group of one rank on this GPU
+    import os
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()))
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=dev)
+    try:
+        w = W.make_workload("nccl", [5000, 0, 17, 12000], num_blocks=1200, seed=35, device=dev,
+                            tail_fill=float("nan"))
+        out = torch.full_like(w.q, float("nan"))
+        split_kv.split_kv_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                                 w.num_kv_heads, w.head_dim, w.block_size, w.scale, 512, max_seq_len=w.max_seq_len)
+        torch.cuda.synchronize()
+        assert pb.pa_get_device_status() == 0
+        assert_parity(out, oracle_ref(w), "split_kv_decode over NCCL")
+    finally:
+        dist.destroy_process_group()
