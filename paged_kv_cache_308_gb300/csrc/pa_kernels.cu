@@ -797,16 +797,23 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
             return (size_t)p;
         }
     };
-    // A thread's first partial is read together with the length, so the two
-    // latencies overlap: the row holds max_partitions entries, so the reads
-    // stay inside the workspace, and a value past the sequence's partitions
-    // is never used.
-    float mp0 = 0.f, lp0 = 0.f;
-    float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (pg < prm.max_partitions) {
-        mp0 = ml[at(pg)];
-        lp0 = el[at(pg)];
-        t0 = tp[at(pg) * (D / 4)];
+    // A thread's first kPre partials are read together with the length, so
+    // their latencies overlap: the row holds max_partitions entries, so the
+    // reads stay inside the workspace, and a value past the sequence's
+    // partitions is never used.
+    constexpr int kPre = 2;
+    float mp0[kPre], lp0[kPre];
+    float4 t0[kPre];
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+        const int p = pg + i * kGroups;
+        mp0[i] = lp0[i] = 0.f;
+        t0[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p < prm.max_partitions) {
+            mp0[i] = ml[at(p)];
+            lp0[i] = el[at(p)];
+            t0[i] = tp[at(p) * (D / 4)];
+        }
     }
     const int L = prm.seq_lens[b];
     const int part = prm.part_sizes ? prm.part_sizes[b] : prm.partition_size;
@@ -846,9 +853,11 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
         acc.w = acc.w * alpha + beta * t.w;
         m = mn;
     };
-    if (pg < n) fold(mp0, lp0, t0);
+#pragma unroll
+    for (int i = 0; i < kPre; ++i)
+        if (pg + i * kGroups < n) fold(mp0[i], lp0[i], t0[i]);
 #pragma unroll 4
-    for (int p = pg + kGroups; p < n; p += kGroups) fold(ml[at(p)], el[at(p)], tp[at(p) * (D / 4)]);
+    for (int p = pg + kPre * kGroups; p < n; p += kGroups) fold(ml[at(p)], el[at(p)], tp[at(p) * (D / 4)]);
     red_acc[pg][col] = acc;
     if (col == 0) {
         red_m[pg] = m;
