@@ -264,9 +264,22 @@ def graph_calls_per_s(pb, w, dev, per_graph=20, replays=25):
     return per_graph * replays / (e0.elapsed_time(e1) / 1e3)
 
 
+def queue_ahead(stream, calls):
+    """Queue a GPU spin on `stream` long enough for the host to queue the
+    next `calls` calls behind it (about 15 us of host time each, 0.3-50 ms),
+    so a timed region that starts after it opens on a full queue: the
+    region then holds the calls' device time, not the host's launch latency
+    of its first call.  (The host's costs are in the end-to-end figure.)"""
+    if hasattr(torch.cuda, "_sleep"):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(min(50e-3, max(3e-4, calls * 15e-6)) * 2.0e9))  # ~2 GHz SM clock
+
+
 def time_steps(fn, steps, stream):
+    """Seconds of device time for `steps` back-to-back calls of `fn`."""
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
+    queue_ahead(stream, steps)
     s.record(stream)
     for _ in range(steps):
         fn()
