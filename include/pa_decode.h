@@ -331,6 +331,38 @@ int pa_prefix(void* out, const void* q, const void* k_new, const void* v_new, co
  * options only flags, wait_limit and the two timing events apply). */
 int pa_prefix_ex(const pa_prefix_args* args, const pa_decode_opts* opts, pa_stream_t stream);
 
+/* Chunked prefill with the last wave's query tiles split by key range.
+ * The tensor-core prefill kernel runs one CTA per SM per (query tile, kv
+ * head, sequence), and every CTA walks all of its sequence's keys, so the
+ * CTAs take about the same time and a grid of N of them on S SMs runs in
+ * ceil(N / S) rounds.  When the last round is partly empty, its trailing
+ * query tiles (`units`, counted in the grid's order: tile fastest, then kv
+ * head, then sequence) each run as `parts` CTAs, CTA p walking the p-th of
+ * `parts` consecutive ranges of the tile's key tiles and leaving, per row,
+ * the online-softmax state (m, l, O relative to 2^m) in the workspace; a
+ * second kernel then merges a row's parts with the log-sum-exp rule of the
+ * decode reduce ("docs" commit page, Phase 2; the alpha/beta fold of the
+ * "paged_attention_v2_triton.py" commit page).  The result is the same
+ * attention as pa_prefix_ex up to the rounding order of the sums.
+ * Split: NULL or parts == 0 takes the library's plan (a model of the rounds
+ * on this device, for grids of at most 4 rounds of one CTA per SM; it may
+ * split nothing); parts in [1, 64] with units in
+ * [0, N] forces that split.  The workspace (caller-owned device memory,
+ * 256-byte aligned, contents need no initialisation) must hold
+ * pa_prefix_split_workspace_size bytes for the same arguments and split;
+ * the call allocates nothing.  With PA_FLAG_PREFIX_WARP_MMA nothing is split
+ * and this is pa_prefix_ex.  Errors as pa_prefix_ex, plus PA_ERR_INVALID_ARG
+ * for a workspace that is missing, too small or misaligned, or a split out
+ * of range. */
+typedef struct {
+    int parts; /* key ranges per split query tile; 0 = the library's plan */
+    int units; /* trailing query tiles that are split (with parts > 0) */
+} pa_prefix_split_opts;
+
+int pa_prefix_split_workspace_size(const pa_prefix_args* args, const pa_prefix_split_opts* split, size_t* bytes);
+int pa_prefix_split(const pa_prefix_args* args, const pa_decode_opts* opts, const pa_prefix_split_opts* split,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
 /* Size of the fixed device scratch that pa_decode_noalloc uses (16 MiB). */
 #define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -89,6 +89,10 @@ class pa_prefix_args(ctypes.Structure):
     ]
 
 
+class pa_prefix_split_opts(ctypes.Structure):
+    _fields_ = [("parts", ctypes.c_int), ("units", ctypes.c_int)]
+
+
 class PaDecodeError(RuntimeError):
     def __init__(self, code: int, what: str = ""):
         self.code = code
@@ -123,6 +127,12 @@ def _load() -> ctypes.CDLL:
     lib.pa_prefix.argtypes = [vp] * 9 + [i32] * 5 + [i64, i32, i32, i32, i32, f32, vp]
     lib.pa_prefix_ex.restype = i32
     lib.pa_prefix_ex.argtypes = [ctypes.POINTER(pa_prefix_args), ctypes.POINTER(pa_decode_opts), vp]
+    lib.pa_prefix_split_workspace_size.restype = i32
+    lib.pa_prefix_split_workspace_size.argtypes = [ctypes.POINTER(pa_prefix_args), ctypes.POINTER(pa_prefix_split_opts),
+                                                   ctypes.POINTER(ctypes.c_size_t)]
+    lib.pa_prefix_split.restype = i32
+    lib.pa_prefix_split.argtypes = [ctypes.POINTER(pa_prefix_args), ctypes.POINTER(pa_decode_opts),
+                                    ctypes.POINTER(pa_prefix_split_opts), vp, ctypes.c_size_t, vp]
     lib.pa_decode_partials.restype = i32
     lib.pa_decode_partials.argtypes = [ctypes.POINTER(pa_decode_args), ctypes.POINTER(pa_decode_opts), i32, i32, i32,
                                        vp, vp, vp, vp]
@@ -297,10 +307,8 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, num_head
         raise PaDecodeError(rc, "pa_decode_noalloc")
 
 
-def pa_prefix(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_heads,
-              num_kv_heads, head_dim, block_size, scale, stream=None, *, max_context_len: int, max_query_len: int,
-              **opt) -> None:
-    """Chunked-prefill attention (see include/pa_decode.h); options as for pa_decode_ex."""
+def _prefix_args(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_heads,
+                 num_kv_heads, head_dim, block_size, scale, max_context_len, max_query_len) -> pa_prefix_args:
     for name, t, dt in (("out", out, torch.float16), ("q", q, torch.float16), ("k_new", k_new, torch.float16),
                         ("v_new", v_new, torch.float16), ("k_cache", k_cache, torch.float16),
                         ("v_cache", v_cache, torch.float16), ("block_tables", block_tables, torch.int32),
@@ -308,12 +316,20 @@ def pa_prefix(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens
                         ("query_start_loc", query_start_loc, torch.int32)):
         if t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
             raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
-    args = pa_prefix_args(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+    return pa_prefix_args(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
                           v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
                           query_start_loc.data_ptr(), int(context_lens.shape[0]), int(q.shape[0]),
                           int(block_tables.shape[1]), int(max_context_len), int(max_query_len),
                           int(k_cache.shape[0]), int(num_heads), int(num_kv_heads), int(head_dim), int(block_size),
                           float(scale))
+
+
+def pa_prefix(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_heads,
+              num_kv_heads, head_dim, block_size, scale, stream=None, *, max_context_len: int, max_query_len: int,
+              **opt) -> None:
+    """Chunked-prefill attention (see include/pa_decode.h); options as for pa_decode_ex."""
+    args = _prefix_args(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                        num_heads, num_kv_heads, head_dim, block_size, scale, max_context_len, max_query_len)
     if opt:
         rc = lib.pa_prefix_ex(ctypes.byref(args), ctypes.byref(make_opts(**opt)), _stream_handle(stream))
     else:
@@ -324,6 +340,54 @@ def pa_prefix(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens
                            _stream_handle(stream))
     if rc != PA_OK:
         raise PaDecodeError(rc, "pa_prefix")
+
+
+def pa_prefix_split(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_heads,
+                    num_kv_heads, head_dim, block_size, scale, stream=None, *, max_context_len: int,
+                    max_query_len: int, workspace: Optional[torch.Tensor] = None, parts: int = 0, units: int = 0,
+                    **opt) -> None:
+    """Chunked prefill with the last wave's query tiles split by key range
+    (see include/pa_decode.h).  `workspace`: a CUDA uint8 tensor of at least
+    prefix_split_workspace_size(...) bytes; None allocates one here (the
+    call itself allocates nothing).  parts/units force a split (0: the
+    library's plan)."""
+    args = _prefix_args(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                        num_heads, num_kv_heads, head_dim, block_size, scale, max_context_len, max_query_len)
+    split = pa_prefix_split_opts(int(parts), int(units))
+    if workspace is None:
+        nbytes = ctypes.c_size_t(0)
+        rc = lib.pa_prefix_split_workspace_size(ctypes.byref(args), ctypes.byref(split), ctypes.byref(nbytes))
+        if rc != PA_OK:
+            raise PaDecodeError(rc, "pa_prefix_split_workspace_size")
+        workspace = torch.empty(max(int(nbytes.value), 1), dtype=torch.uint8, device=out.device)
+    rc = lib.pa_prefix_split(ctypes.byref(args), ctypes.byref(make_opts(**opt)), ctypes.byref(split),
+                             workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    if rc != PA_OK:
+        raise PaDecodeError(rc, "pa_prefix_split")
+
+
+def prefix_split_workspace_size(w, parts: int = 0, units: int = 0) -> int:
+    """Bytes of workspace pa_prefix_split needs for a workloads.PrefixWorkload."""
+    out = torch.empty_like(w.q)
+    args = _prefix_args(out, w.q, w.k_new, w.v_new, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                        w.query_start_loc, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, w.scale,
+                        w.max_context_len, w.max_query_len)
+    nbytes = ctypes.c_size_t(0)
+    rc = lib.pa_prefix_split_workspace_size(ctypes.byref(args), ctypes.byref(pa_prefix_split_opts(parts, units)),
+                                            ctypes.byref(nbytes))
+    if rc != PA_OK:
+        raise PaDecodeError(rc, "pa_prefix_split_workspace_size")
+    return int(nbytes.value)
+
+
+def prefix_split_workload(w, out: Optional[torch.Tensor] = None, stream=None, **kw) -> torch.Tensor:
+    """pa_prefix_split on a workloads.PrefixWorkload (tensors on the GPU)."""
+    if out is None:
+        out = torch.empty_like(w.q)
+    pa_prefix_split(out, w.q, w.k_new, w.v_new, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                    w.query_start_loc, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, w.scale, stream,
+                    max_context_len=w.max_context_len, max_query_len=w.max_query_len, **kw)
+    return out
 
 
 def prefix_workload(w, out: Optional[torch.Tensor] = None, stream=None, **opt) -> torch.Tensor:

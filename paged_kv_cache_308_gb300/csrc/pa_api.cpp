@@ -692,7 +692,81 @@ int validate_prefix(const pa_prefix_args* a, const pa_decode_opts* o) {
     return PA_OK;
 }
 
-int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t stream) {
+// Key split of the tensor-core prefill kernel's last round (pa_prefix_split).
+// Every CTA of that kernel walks all keys of its sequence, so with one CTA
+// per SM a grid of N CTAs on S SMs takes about ceil(N / S) rounds of T.  When
+// the last round holds R = N mod S CTAs, splitting those R tiles into k key
+// ranges gives R k CTAs of about (T - f) / k + f each, in ceil(R k / S)
+// rounds, plus a merge.  T = f + tiles * t_tile with f ~ 7 us of fixed cost
+// per CTA and t_tile ~ 0.9 us per 64-key tile (GB300, head_dim 256; per-CTA
+// phase traces), tiles from the longest context and chunk.  The k in [2, 8]
+// with the shortest last rounds is taken if it saves at least 5 % of T.  On
+// 4 x 8192 cached tokens with chunks of 512 (400 CTAs, 96 in the last round)
+// the model takes k = 3, the fastest of the measured splits (us per call:
+// none 381.6, k = 3 373.1, k = 2 401.2, k = 4 385.2, k = 5 400.5, k = 6 394.2;
+// the last 248 tiles in 3: 410.8; every tile in 2: 453.4): a part costs more
+// than (T - f) / k + f, since it also writes its rows in fp32 for the merge.
+struct PrefixSplit {
+    int parts = 0, whole = 0, units = 0, tiles_per_seq = 0;
+};
+
+constexpr double kPrefixFixedUs = 7.0, kPrefixTileUs = 0.9, kPrefixMergeUs = 3.0;
+constexpr long long kPrefixSplitMaxRounds = 4;
+
+int plan_prefix_split(const pa_prefix_args* a, const pa_prefix_split_opts* split, int num_sms, PrefixSplit* sp) {
+    *sp = PrefixSplit{};
+    const int tile_tokens = pa::kPrefixTileRows / (a->num_heads / a->num_kv_heads);
+    sp->tiles_per_seq = (a->max_query_len + tile_tokens - 1) / tile_tokens;
+    const long long n = (long long)sp->tiles_per_seq * a->num_kv_heads * a->num_seqs;
+    if (split && split->parts != 0) {
+        if (split->parts < 1 || split->parts > 64 || split->units < 0 || split->units > n) return PA_ERR_INVALID_ARG;
+        if ((long long)split->units * split->parts + (n - split->units) >= (1ll << 31)) return PA_ERR_INVALID_ARG;
+        if (split->units == 0) return PA_OK;
+        sp->parts = split->parts;
+        sp->units = split->units;
+        sp->whole = static_cast<int>(n - split->units);
+        return PA_OK;
+    }
+    // Only a grid of a few rounds has a clean partial last round: with more,
+    // the CTAs of a ragged batch differ in length and already fill it (the
+    // 16-sequence mixed batch, 21 rounds: 528 -> 542 us when split).
+    if (num_sms <= 0 || n <= num_sms || n > kPrefixSplitMaxRounds * num_sms) return PA_OK;
+    const long long r = n % num_sms;
+    if (r == 0) return PA_OK;
+    const long long tiles = ((a->max_context_len + pa::kBlockSize - 1) / pa::kBlockSize +
+                             (a->max_query_len + pa::kBlockSize - 1) / pa::kBlockSize + 3) / 4;
+    const double t = kPrefixFixedUs + tiles * kPrefixTileUs;
+    double best = t;  // the last round of whole tiles
+    int best_k = 0;
+    for (int k = 2; k <= 8; ++k) {
+        const long long rounds = (r * k + num_sms - 1) / num_sms;
+        const double tk = rounds * ((t - kPrefixFixedUs) / k + kPrefixFixedUs) + kPrefixMergeUs;
+        if (tk < best) {
+            best = tk;
+            best_k = k;
+        }
+    }
+    if (best_k == 0 || best > 0.95 * t) return PA_OK;
+    sp->parts = best_k;
+    sp->units = static_cast<int>(r);
+    sp->whole = static_cast<int>(n - r);
+    return PA_OK;
+}
+
+size_t prefix_split_o_bytes(const PrefixSplit& sp, int head_dim) {
+    return align_up((size_t)sp.units * sp.parts * pa::kPrefixTileRows * head_dim * 4, kWsAlign);
+}
+
+size_t prefix_split_bytes(const PrefixSplit& sp, int head_dim) {
+    if (!sp.parts) return 0;
+    return prefix_split_o_bytes(sp, head_dim) +
+           align_up((size_t)sp.units * sp.parts * pa::kPrefixTileRows * 2 * 4, kWsAlign);
+}
+
+// split_call: pa_prefix_split (the key split of `split`, or the plan's,
+// into workspace `ws`); otherwise pa_prefix / pa_prefix_ex.
+int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t stream, bool split_call = false,
+               const pa_prefix_split_opts* split = nullptr, void* ws = nullptr, size_t ws_bytes = 0) {
     int rc = validate_prefix(a, o);
     if (rc) return rc;
     if (a->num_seqs == 0 || a->num_tokens == 0) return PA_OK;
@@ -704,6 +778,16 @@ int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t st
     ca.block_size = a->block_size;
     // tensor-core (tcgen05) kernel by default; the warp-level MMA kernel on request
     const bool warp_mma = o && (o->flags & PA_FLAG_PREFIX_WARP_MMA);
+    // the key split and its workspace are checked before any CUDA call but
+    // the SM count (which only the library's own plan reads)
+    PrefixSplit sp;
+    if (split_call && !warp_mma) {
+        int num_sms = 0;
+        if (!(split && split->parts) && query_sm_count(&num_sms) != PA_OK) return PA_ERR_CUDA;
+        if ((rc = plan_prefix_split(a, split, num_sms, &sp))) return rc;
+        if (sp.parts && (!ws || ws_bytes < prefix_split_bytes(sp, a->head_dim) || !aligned(ws, kWsAlign)))
+            return PA_ERR_INVALID_ARG;
+    }
     // K cache, V cache, K new, V new; the tcgen05 kernel copies V a whole block per box
     CUtensorMap maps[4];
     if ((rc = make_cache_map(&maps[0], a->k_cache, &ca)) ||
@@ -738,7 +822,15 @@ int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t st
     if (!prm.status) return PA_ERR_CUDA;
     prm.trace = g_trace;
     const int tile_tokens = (warp_mma ? 64 : 128) / prm.group;
-    const dim3 grid((a->max_query_len + tile_tokens - 1) / tile_tokens, a->num_kv_heads, a->num_seqs);
+    dim3 grid((a->max_query_len + tile_tokens - 1) / tile_tokens, a->num_kv_heads, a->num_seqs);
+    if (sp.parts) {  // a 1-D grid of units (see PrefixParams::split_parts)
+        prm.split_whole = sp.whole;
+        prm.split_parts = sp.parts;
+        prm.tiles_per_seq = sp.tiles_per_seq;
+        prm.split_o = static_cast<float*>(ws);
+        prm.split_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + prefix_split_o_bytes(sp, a->head_dim));
+        grid = dim3(sp.whole + sp.units * sp.parts, 1, 1);
+    }
     if (o && o->event_partition_begin &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_begin), stream) != cudaSuccess)
         return PA_ERR_CUDA;
@@ -748,6 +840,7 @@ int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t st
     if (o && o->event_partition_end &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_end), stream) != cudaSuccess)
         return PA_ERR_CUDA;
+    if (sp.parts && pa::launch_prefix_merge(a->head_dim, prm, sp.units, stream) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
 }
 
@@ -835,6 +928,24 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
 
 int pa_prefix_ex(const pa_prefix_args* args, const pa_decode_opts* opts, pa_stream_t stream) {
     return run_prefix(args, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_prefix_split_workspace_size(const pa_prefix_args* args, const pa_prefix_split_opts* split, size_t* bytes) {
+    if (!bytes) return PA_ERR_INVALID_ARG;
+    *bytes = 0;
+    int rc = validate_prefix(args, nullptr);
+    if (rc) return rc;
+    int num_sms = 0;
+    if (!(split && split->parts) && query_sm_count(&num_sms) != PA_OK) return PA_ERR_CUDA;
+    PrefixSplit sp;
+    if ((rc = plan_prefix_split(args, split, num_sms, &sp))) return rc;
+    *bytes = prefix_split_bytes(sp, args->head_dim);
+    return PA_OK;
+}
+
+int pa_prefix_split(const pa_prefix_args* args, const pa_decode_opts* opts, const pa_prefix_split_opts* split,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+    return run_prefix(args, opts, reinterpret_cast<cudaStream_t>(stream), true, split, workspace, workspace_bytes);
 }
 
 int pa_prefix(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache, const void* v_cache,

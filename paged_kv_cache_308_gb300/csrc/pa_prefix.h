@@ -19,6 +19,18 @@ struct PrefixParams {
     unsigned wait_limit;
     int force_timeout;
     unsigned int* status;           // device status word (PA_DEV_* bits are OR-ed in)
+    // Key split of the last wave (tcgen05 kernel; split_parts == 0: off, and
+    // the grid is (query tiles, kv heads, sequences)).  Otherwise the grid is
+    // 1-D over units numbered as that grid's CTAs (tile fastest, then kv head,
+    // then sequence; tiles_per_seq tiles per kv head): CTAs [0, split_whole)
+    // run units [0, split_whole) whole, and CTA split_whole + r * split_parts + p
+    // runs part p of the key tiles of unit split_whole + r, leaving its rows'
+    // unnormalised partial in split_o / split_ml for pa_prefix_merge_kernel.
+    int split_whole = 0;
+    int split_parts = 0;
+    int tiles_per_seq = 0;
+    float* split_o = nullptr;       // [R][split_parts][128 rows][D]: O relative to 2^m
+    float* split_ml = nullptr;      // [R][split_parts][128 rows][2]: m (scaled, log2), l
     // Diagnostic builds (-DPA_TRACE) only: the tcgen05 kernel records
     // SM clock stamps of its pipeline events, kPrefixTraceIters x 16 per CTA
     // (the last of the kPrefixTraceIters records holds the CTA's phases in
@@ -38,5 +50,10 @@ cudaError_t launch_prefix(int head_dim, const PrefixParams& prm, const CUtensorM
 int prefix_tc_smem_bytes(int head_dim);
 cudaError_t launch_prefix_tc(int head_dim, const PrefixParams& prm, const CUtensorMap* maps, dim3 grid,
                              cudaStream_t stream);
+// Rows rounded up by the tcgen05 kernel's tiles (the MMA M), for the split workspace.
+constexpr int kPrefixTileRows = 128;
+// The merge of a key split: the fp16 output rows of its `units` split units
+// from their parts' partials (a programmatic dependent of the tcgen05 kernel).
+cudaError_t launch_prefix_merge(int head_dim, const PrefixParams& prm, int units, cudaStream_t stream);
 
 }  // namespace pa

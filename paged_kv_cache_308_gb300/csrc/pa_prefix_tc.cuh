@@ -291,7 +291,20 @@ __global__ void __maxnreg__(kTcMaxRegs)
     const uint32_t bar0 = smem_addr(bars);
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
-    const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    // The CTA's unit: a query tile of one (sequence, kv head), whole or, in a
+    // key split (PrefixParams::split_parts), part `part` of its key tiles.
+    int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, part = -1, unit_r = 0;
+    if (prm.split_parts > 0) {
+        int w = blockIdx.x;
+        if (w >= prm.split_whole) {
+            unit_r = (w - prm.split_whole) / prm.split_parts;
+            part = (w - prm.split_whole) - unit_r * prm.split_parts;
+            w = prm.split_whole + unit_r;
+        }
+        tile = w % prm.tiles_per_seq;
+        kvh = (w / prm.tiles_per_seq) % prm.num_kv_heads;
+        b = w / (prm.tiles_per_seq * prm.num_kv_heads);
+    }
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     PA_TC_PHASE(0);
     PA_TC_PHASE(7);
@@ -312,6 +325,14 @@ __global__ void __maxnreg__(kTcMaxRegs)
     const int nctx = (C + kBlockSize - 1) / kBlockSize;         // context blocks
     const int nblocks = nctx + tlast / kBlockSize + 1;          // + chunk blocks up to tlast
     const int ntiles = (nblocks + 3) / 4;
+    // key tiles [jb, jb + n) of the walk: all of them, or the part's share
+    // (iteration j of the loops below takes key tile jb + j; the rings and
+    // barrier phases count iterations)
+    int jb = 0, n = ntiles;
+    if (part >= 0) {
+        jb = (int)((long long)part * ntiles / prm.split_parts);
+        n = (int)((long long)(part + 1) * ntiles / prm.split_parts) - jb;
+    }
     const int32_t* bt = prm.block_tables + (size_t)b * prm.max_blocks_per_seq;
 
     // The row threads read their Q rows into registers after the setup
@@ -398,18 +419,19 @@ __global__ void __maxnreg__(kTcMaxRegs)
         };
         auto chunk_token = [&](int blk, int p) { return p == -2 ? prm.num_tokens : q0 + (blk - nctx) * kBlockSize; };
         auto issue = [&](int j) {
+            const int jt = jb + j;  // j picks the ring slot, jt the keys
             if (!is_k) {
                 // blocks i, i + kTcVLoadWarps, ... of the tile, each in one box
                 // laid out [chunk][16 rows][128 B]
                 int phys[kVBlocks];
 #pragma unroll
-                for (int x = 0; x < kVBlocks; ++x) phys[x] = lookup(4 * j + i + x * kTcVLoadWarps);
+                for (int x = 0; x < kVBlocks; ++x) phys[x] = lookup(4 * jt + i + x * kTcVLoadWarps);
                 if (lane == 0) {
                     const uint32_t full = bar(full0 + j % slots);
                     mbar_arrive_expect_tx(full, kVBlocks * S::kBlockBytes);
 #pragma unroll
                     for (int x = 0; x < kVBlocks; ++x) {
-                        const int bi = i + x * kTcVLoadWarps, blk = 4 * j + bi;
+                        const int bi = i + x * kTcVLoadWarps, blk = 4 * jt + bi;
                         const int p = checked(blk, phys[x]);
                         const uint32_t dst = smem_addr(vs + (j % S::kVSlots) * S::kTileBytes) + bi * S::kBlockBytes;
                         if (p >= 0)
@@ -421,7 +443,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
                 __syncwarp();
                 return;
             }
-            const int blk = 4 * j + i;
+            const int blk = 4 * jt + i;
             const int phys = lookup(blk);
             if (lane == 0) {
                 const uint32_t full = bar(full0 + j % slots);
@@ -445,10 +467,11 @@ __global__ void __maxnreg__(kTcMaxRegs)
             }
             __syncwarp();
         };
-        cur.nxt = fetch(0);
+        cur.group = ((4 * jb) >> 5) - 1;  // the first lookup takes the group read ahead here
+        cur.nxt = fetch(cur.group + 1);
         bool ok = true;
         int issued = 0;
-        for (int j = 0; j < ntiles; ++j) {
+        for (int j = 0; j < n; ++j) {
             // slot j % slots last held tile j - slots: free once the MMA that
             // read it has completed
             if (j >= slots &&
@@ -486,7 +509,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
             constexpr uint32_t idS = tc_idesc(kTcRows, kTcKeys, 0);
             const uint64_t kdesc0 = tc_desc(smem_addr(ks), 16, 1024);
             ok = tc_warp_wait(bar(kTcBarQReady), 0, limit, sm_abort);
-            for (int j = 0; ok && j < ntiles; ++j) {
+            for (int j = 0; ok && j < n; ++j) {
                 if (lane == 0) PA_TC_MARK(j, 0);
                 // K(j) landed; score buffer j % 2 is free once P.V(j-2), the
                 // last reader of the P written there, has completed
@@ -518,7 +541,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
         } else {
             constexpr uint32_t idO = tc_idesc(kTcRows, D, 1);
             const uint64_t vdesc0 = tc_desc(smem_addr(vs), kBlockSize * 128, 1024);
-            for (int j = 0; j < ntiles; ++j) {
+            for (int j = 0; j < n; ++j) {
                 if (lane == 0) PA_TC_MARK(j, 12);
                 // rows have written P(j) (and rescaled O if they had to); V(j) landed
                 if (!(ok = tc_warp_wait(bar(kTcBarPReady + (j & 1)), (j >> 1) & 1, limit, sm_abort))) break;
@@ -526,7 +549,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
                 if (!(ok = tc_warp_wait(bar(kTcBarVFull + j % S::kVSlots), (j / S::kVSlots) & 1, limit, sm_abort))) break;
                 if (lane == 0) PA_TC_MARK(j, 3);
                 uint8_t* vt = vs + (j % S::kVSlots) * S::kTileBytes;
-                if (j == partial_tile) {
+                if (jb + j == partial_tile) {
                     // V rows of cache slots past the context may hold anything: p is
                     // 0 there, but 0 * NaN is not; clear them before P.V reads them
                     const int i = (nctx - 1) % 4, first = C % kBlockSize;
@@ -608,7 +631,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
         PA_TC_PHASE(2);
         float m = -INFINITY, l = 0.f;  // reference max (scaled, log2 domain) and exp sum
         bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
+        for (int j = 0; j < n; ++j) {
             const uint32_t sb = tS + (uint32_t)(j & 1) * kTcKeys + lane_off;  // this row of score buffer j % 2
             if (!(ok = tc_warp_wait(bar(kTcBarSDone + (j & 1)), (j >> 1) & 1, limit, sm_abort))) break;
             tc_fence_after();
@@ -617,7 +640,8 @@ __global__ void __maxnreg__(kTcMaxRegs)
             tc_ld32x2(sb, sv[0], sb + 32, sv[1]);
             // visibility: every key of a tile made only of full context blocks
             // is visible; otherwise mask per key
-            const bool full_ctx = 4 * j + 3 < nctx - (C % kBlockSize != 0 ? 1 : 0);
+            const int jt = jb + j;
+            const bool full_ctx = 4 * jt + 3 < nctx - (C % kBlockSize != 0 ? 1 : 0);
             if (!full_ctx) {
                 // visible slots of each 16-key block of the tile for this row:
                 // a context block shows its keys below C, a chunk block the
@@ -626,9 +650,9 @@ __global__ void __maxnreg__(kTcMaxRegs)
                 int nvis[4];
 #pragma unroll
                 for (int qb = 0; qb < 4; ++qb) {
-                    const int blk = 4 * j + qb;
-                    const int n = blk < nctx ? C - blk * kBlockSize : my_tok + 1 - (blk - nctx) * kBlockSize;
-                    nvis[qb] = min(max(n, 0), kBlockSize);
+                    const int blk = 4 * jt + qb;
+                    const int vis = blk < nctx ? C - blk * kBlockSize : my_tok + 1 - (blk - nctx) * kBlockSize;
+                    nvis[qb] = min(max(vis, 0), kBlockSize);
                 }
                 const uint32_t hidden = __float_as_uint(sl2 >= 0.f ? -INFINITY : INFINITY);
 #pragma unroll
@@ -693,13 +717,38 @@ __global__ void __maxnreg__(kTcMaxRegs)
         }
         PA_TC_PHASE(3);
         // the last two P.Vs (one per score buffer) complete before O is read
-        if (ok && ntiles >= 2)
-            ok = tc_warp_wait(bar(kTcBarPVDone + ((ntiles - 2) & 1)), ((ntiles - 2) >> 1) & 1, limit, sm_abort);
-        if (ok) ok = tc_warp_wait(bar(kTcBarPVDone + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, limit, sm_abort);
+        if (ok && n >= 2)
+            ok = tc_warp_wait(bar(kTcBarPVDone + ((n - 2) & 1)), ((n - 2) >> 1) & 1, limit, sm_abort);
+        if (ok && n >= 1) ok = tc_warp_wait(bar(kTcBarPVDone + ((n - 1) & 1)), ((n - 1) >> 1) & 1, limit, sm_abort);
         if (!ok) {
             if (lane == 0) {
                 *sm_abort = 1;
                 atomicOr(prm.status, PA_DEV_TIMEOUT);
+            }
+        } else if (part >= 0) {
+            tc_fence_after();
+            // a part of a key split: the row's partial (m, l and O relative to
+            // 2^m, fp32) for the merge; a part without key tiles leaves m = -inf
+            // and l = 0, which the merge skips without reading its O
+            const size_t slot = ((size_t)unit_r * prm.split_parts + part) * kTcRows + t;
+            if (row_real) {
+                prm.split_ml[2 * slot] = m;
+                prm.split_ml[2 * slot + 1] = l;
+            }
+            float4* orow = reinterpret_cast<float4*>(prm.split_o + slot * D);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 64) {
+                uint32_t ov[2][32];
+                tc_ld32x2(tO + lane_off + c0, ov[0], tO + lane_off + c0 + 32, ov[1]);
+                if (row_real && n > 0) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4)
+                            orow[(c0 + 32 * h + c) / 4] =
+                                make_float4(__uint_as_float(ov[h][c]), __uint_as_float(ov[h][c + 1]),
+                                            __uint_as_float(ov[h][c + 2]), __uint_as_float(ov[h][c + 3]));
+                }
             }
         } else {
             tc_fence_after();
@@ -733,6 +782,60 @@ __global__ void __maxnreg__(kTcMaxRegs)
     __syncthreads();  // every role done: no copy or MMA in flight past this point
     PA_TC_PHASE(5);
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(S::kTmemCols));
+}
+
+// Merge of a key split (PrefixParams::split_parts): every row of split unit
+// r had its keys walked in split_parts ranges, each leaving (m_p, l_p, O_p)
+// with O_p and l_p relative to 2^m_p (m in the scaled log2 domain).  The
+// output is the log-sum-exp merge of the decode path's reduce, here over the
+// key ranges of one query tile: with M = max_p m_p and w_p = 2^(m_p - M),
+//     out = sum_p w_p O_p / sum_p w_p l_p,
+// folded in part order.  A part with m_p = -inf saw no key of the row and
+// weighs nothing (its O is not read).  Grid (split units, row groups); a
+// thread takes 4 columns of one row.
+template <int D>
+__global__ void __launch_bounds__(256) pa_prefix_merge_kernel(const PrefixParams prm) {
+    constexpr int kCols = D / 4;               // float4 columns of a row
+    constexpr int kRowsPerCta = 256 / kCols;   // 4 at head_dim 256
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int r = blockIdx.x, w = prm.split_whole + r;
+    const int tile = w % prm.tiles_per_seq, kvh = (w / prm.tiles_per_seq) % prm.num_kv_heads;
+    const int b = w / (prm.tiles_per_seq * prm.num_kv_heads);
+    const int G = prm.group, H = prm.num_heads, tile_tokens = kTcRows / G;
+    // the same checks as the kernel that wrote the partials: a unit it left
+    // is left here too
+    const int C = __ldg(prm.context_lens + b);
+    const int q0 = __ldg(prm.query_start_loc + b), q1 = __ldg(prm.query_start_loc + b + 1);
+    const int qlen = q1 - q0;
+    if (C < 0 || C > prm.max_context_len || C > prm.max_blocks_per_seq * kBlockSize || qlen < 0 ||
+        qlen > prm.max_query_len || q0 < 0 || q1 > prm.num_tokens)
+        return;
+    const int row = blockIdx.y * kRowsPerCta + (int)threadIdx.x / kCols, col = (int)threadIdx.x % kCols;
+    const int ti = row / G, tok = tile * tile_tokens + ti;
+    if (ti >= tile_tokens || tok >= qlen) return;
+    const int k = prm.split_parts;
+    const size_t slot0 = (size_t)r * k * kTcRows + row;  // part p: slot0 + p * kTcRows
+    float M = -INFINITY;
+    for (int p = 0; p < k; ++p) M = fmaxf(M, prm.split_ml[2 * (slot0 + (size_t)p * kTcRows)]);
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < k; ++p) {
+        const size_t slot = slot0 + (size_t)p * kTcRows;
+        const float mp = prm.split_ml[2 * slot];
+        if (mp == -INFINITY) continue;
+        const float wp = exp2f(mp - M);
+        den += wp * prm.split_ml[2 * slot + 1];
+        const float4 o = reinterpret_cast<const float4*>(prm.split_o + slot * D)[col];
+        acc.x += wp * o.x;
+        acc.y += wp * o.y;
+        acc.z += wp * o.z;
+        acc.w += wp * o.w;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __half2* dst = reinterpret_cast<__half2*>(prm.out + ((size_t)(q0 + tok) * H + kvh * G + row % G) * D + 4 * col);
+    dst[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+    dst[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
 }
 
 int prefix_tc_smem_bytes(int head_dim) {
@@ -773,6 +876,33 @@ cudaError_t launch_prefix_tc(int head_dim, const PrefixParams& prm, const CUtens
         case 64: return launch_prefix_tc_t<64>(prm, maps, grid, stream);
         case 128: return launch_prefix_tc_t<128>(prm, maps, grid, stream);
         case 256: return launch_prefix_tc_t<256>(prm, maps, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+namespace {
+template <int D>
+cudaError_t launch_prefix_merge_t(const PrefixParams& prm, int units, cudaStream_t stream) {
+    constexpr int kRowsPerCta = 256 / (D / 4);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units, kTcRows / kRowsPerCta, 1);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, pa_prefix_merge_kernel<D>, prm);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_prefix_merge(int head_dim, const PrefixParams& prm, int units, cudaStream_t stream) {
+    static_assert(kPrefixTileRows == kTcRows, "split workspace rows");
+    switch (head_dim) {
+        case 64: return launch_prefix_merge_t<64>(prm, units, stream);
+        case 128: return launch_prefix_merge_t<128>(prm, units, stream);
+        case 256: return launch_prefix_merge_t<256>(prm, units, stream);
         default: return cudaErrorInvalidValue;
     }
 }

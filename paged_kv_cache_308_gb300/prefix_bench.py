@@ -6,7 +6,10 @@ microseconds per call, useful TFLOP/s (score and P.V multiply-adds over the
 visible keys only, see workloads.PrefixWorkload.flops) and the fraction of
 the measured dense 16-bit tensor-core peak.
 
-    python -m paged_kv_cache_308_gb300.prefix_bench [--impl tcgen05|warp_mma|both] [--iters N] [workload ...]
+    python -m paged_kv_cache_308_gb300.prefix_bench [--impl tcgen05|tcgen05_split|warp_mma|all] [--iters N] [workload ...]
+
+tcgen05_split is pa_prefix_split (the last round's query tiles split by key
+range) under the library's plan.
 """
 from __future__ import annotations
 
@@ -19,7 +22,7 @@ import torch
 from . import binding as pb
 from . import workloads as W
 
-IMPLS = {"tcgen05": 0, "warp_mma": pb.PA_FLAG_PREFIX_WARP_MMA}
+IMPLS = {"tcgen05": 0, "tcgen05_split": 0, "warp_mma": pb.PA_FLAG_PREFIX_WARP_MMA}
 FALLBACK_TENSOR_TFLOPS = 1900.0
 
 
@@ -33,19 +36,25 @@ def tensor_peak():
         return FALLBACK_TENSOR_TFLOPS, "fallback"
 
 
-def time_prefix(w, flags: int, iters: int, warmup: int, stream=None) -> float:
-    """Mean seconds per pa_prefix_ex call over `iters` back-to-back calls."""
+def time_prefix(w, flags: int, iters: int, warmup: int, stream=None, split: bool = False) -> float:
+    """Mean seconds per call over `iters` back-to-back calls: pa_prefix_ex, or
+    with `split` pa_prefix_split under the library's plan (workspace kept)."""
     stream = stream or torch.cuda.current_stream()
     out = torch.empty_like(w.q)
+    if split:
+        ws = torch.empty(max(1, pb.prefix_split_workspace_size(w)), dtype=torch.uint8, device=out.device)
+        call = lambda: pb.prefix_split_workload(w, out, stream=stream, workspace=ws, flags=flags)
+    else:
+        call = lambda: pb.prefix_workload(w, out, stream=stream, flags=flags)
     for _ in range(warmup):
-        pb.prefix_workload(w, out, stream=stream, flags=flags)
+        call()
     torch.cuda.synchronize()
     if pb.pa_get_device_status() != 0:
         raise RuntimeError("prefix kernel reported a device error")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(iters):
-        pb.prefix_workload(w, out, stream=stream, flags=flags)
+        call()
     e1.record(stream)
     e1.synchronize()
     if pb.pa_get_device_status() != 0:
@@ -59,7 +68,7 @@ def measure(names, impls, iters: int, warmup: int, device) -> list:
     for name in names:
         w = W.make_prefix_config(name, device=device)
         for impl in impls:
-            t = time_prefix(w, IMPLS[impl], iters, warmup)
+            t = time_prefix(w, IMPLS[impl], iters, warmup, split=impl == "tcgen05_split")
             tf = w.flops / t / 1e12
             rows.append({"workload": name, "kernel": impl, "us_per_call": t * 1e6, "tflops": tf,
                          "frac_of_tensor_peak": tf / peak, "peak_tflops": peak, "peak_kind": kind,
@@ -71,12 +80,12 @@ def measure(names, impls, iters: int, warmup: int, device) -> list:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--impl", choices=["tcgen05", "warp_mma", "both"], default="both")
+    ap.add_argument("--impl", choices=["tcgen05", "tcgen05_split", "warp_mma", "all"], default="all")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("workloads", nargs="*", default=W.PREFIX_CONFIG_NAMES)
     args = ap.parse_args()
-    impls = list(IMPLS) if args.impl == "both" else [args.impl]
+    impls = list(IMPLS) if args.impl == "all" else [args.impl]
     for row in measure(args.workloads, impls, args.iters, args.warmup, torch.device("cuda:0")):
         print(json.dumps(row), flush=True)
 

@@ -380,3 +380,48 @@ def test_plan_fused_merges_in_parallel_on_a_grid_the_device_holds():
     # the split and the other modes never take the cooperative form
     for mode in (pb.PA_MODE_SPLIT, pb.PA_MODE_SINGLE, pb.PA_MODE_PERSISTENT, pb.PA_MODE_FLAT, pb.PA_MODE_AUTO):
         assert plan(args(max_seq_len=102400), mode=mode)[1]["coop"] == 0
+
+
+def prefix_args(B=4, ctx=8192, ql=512, H=24, Hkv=4, D=256):
+    mbps = (ctx + 15) // 16
+    return pb.pa_prefix_args(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, B * ql, mbps, ctx, ql,
+                             B * mbps, H, Hkv, D, 16, 1 / 16)
+
+
+def split_size(a, parts, units):
+    n = ctypes.c_size_t(123)
+    rc = pb.lib.pa_prefix_split_workspace_size(ctypes.byref(a), ctypes.byref(pb.pa_prefix_split_opts(parts, units)),
+                                               ctypes.byref(n))
+    return rc, n.value
+
+
+def test_prefix_split_workspace_size_of_a_forced_split():
+    # rows of 128 (the MMA M) per part: O in fp32, then (m, l), each 256-byte aligned
+    a = prefix_args()
+    r = lambda x: (x + 255) // 256 * 256
+    for parts, units in ((3, 96), (1, 1), (64, 400), (2, 7)):
+        rc, n = split_size(a, parts, units)
+        assert rc == pb.PA_OK
+        rows = parts * units * 128
+        assert n == r(rows * 256 * 4) + r(rows * 2 * 4), (parts, units)
+    assert split_size(a, 5, 0) == (pb.PA_OK, 0)  # nothing split
+
+
+@pytest.mark.parametrize("parts,units", [(65, 1), (-1, 1), (2, 401), (2, -1)])
+def test_prefix_split_rejects_a_split_out_of_range(parts, units):
+    # 25 query tiles x 4 kv heads x 4 sequences = 400 units
+    rc, n = split_size(prefix_args(), parts, units)
+    assert rc == pb.PA_ERR_INVALID_ARG and n == 0
+
+
+def test_prefix_split_fails_cleanly_without_a_device():
+    a = prefix_args()
+    # the library's own plan needs the SM count: no device, an error, no crash
+    assert split_size(a, 0, 0)[0] == pb.PA_ERR_CUDA
+    o = pb.make_opts()
+    sp = pb.pa_prefix_split_opts(3, 96)
+    # a forced split checks its workspace before any CUDA call
+    rc = pb.lib.pa_prefix_split(ctypes.byref(a), ctypes.byref(o), ctypes.byref(sp), None, 0, None)
+    assert rc == pb.PA_ERR_INVALID_ARG
+    rc = pb.lib.pa_prefix_split(ctypes.byref(a), ctypes.byref(o), ctypes.byref(sp), FAKE + 16, 1 << 30, None)
+    assert rc == pb.PA_ERR_INVALID_ARG  # misaligned
