@@ -610,6 +610,9 @@ def run_gpu(args):
                 per_config[name]["single"] = measure_variant(pb, wc, stream, dev, peak, n_var, mode="single")
                 per_config[name]["split_p512"] = measure_variant(pb, wc, stream, dev, peak, n_var, mode="split",
                                                                  partition_size=512)
+            if name == "b4_l32768_peaked":  # equal lengths: the caller may say so (one-wave plan)
+                per_config[name]["uniform_lengths_flag"] = measure_variant(pb, wc, stream, dev, peak, n_var,
+                                                                           flags=pb.PA_FLAG_UNIFORM_LENGTHS)
             del wc
             torch.cuda.empty_cache()
         # chunked prefill over the paged cache (both kernels), TFLOP/s

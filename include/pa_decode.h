@@ -150,8 +150,18 @@ enum {
                                     The planner's one-wave plan for one long sequence is pooled
                                     without this flag.  Source of the split it refines: "docs"
                                     commit page, GQA-aware grid and partition paragraphs */
-    PA_FLAG_DETERMINISTIC = 8    /* never pool (not even the one-wave plan): each partial covers
+    PA_FLAG_DETERMINISTIC = 8,   /* never pool (not even the one-wave plan): each partial covers
                                     fixed blocks, so repeated calls give identical bits */
+    PA_FLAG_UNIFORM_LENGTHS = 16 /* AUTO/SPLIT/FUSED without a partition size or CTA shape: the
+                                    caller states that the batch's sequences are all about
+                                    max_seq_len long.  The planner then gives the batch the
+                                    one-wave decomposition it gives a single sequence: one 4-warp
+                                    CTA per SM, floor(SMs / (kv heads x sequences)) partitions per
+                                    sequence of ceil(max_seq_len / that) tokens (rounded up to
+                                    whole blocks), when that is at least 2; fixed partitions.
+                                    Any lengths stay correct; a batch in which a few sequences are
+                                    much longer than the rest runs slower than without the flag
+                                    (their partitions get only their share of the SMs) */
 };
 
 /* All inputs of one decode call (device pointers; see the layouts above). */

@@ -202,14 +202,27 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     // (GB300, 4 kv heads, head_dim 256, against 512-token partitions: 102400
     // tokens 70.5 -> 68.9 us, 262144: 174.4 -> 161.6, 524288: 343.9 -> 305.0;
     // below ~2048 tokens per partition the two are within a few per cent).
+    //
+    // A batch whose sequences the caller states are all about max_seq_len long
+    // (PA_FLAG_UNIFORM_LENGTHS) takes the same decomposition: SMs / (kv heads x
+    // sequences) partitions per sequence, for any partition length.  Measured
+    // per call against the 512-token grid (GB300, 4 kv heads, head_dim 256,
+    // fixed partitions): 4 x 4096 tokens 14.5 -> 12.5 us, 4 x 16384 52.1 ->
+    // 46.0, 4 x 32768 85.7 -> 82.6, 2 x 65536 86.2 -> 82.4, 8 x 8192 51.7 ->
+    // 46.2, 16 x 16384 163.9 -> 158.4.  Without the statement the host cannot
+    // tell such a batch from one whose longest sequence stands alone (4 x
+    // [32768, 100, 100, 100]: 30.8 -> 47.1 us) or from lengths spread below
+    // the longest (8 x U[1, 8192]: 27.7 -> 37.7), so batches keep the grid.
     bool one_wave = false;
     const int req_mode = o ? o->mode : PA_MODE_AUTO;
-    if (!(o && o->partition_size > 0) && !(o && (o->warps || o->stages)) && a->num_seqs == 1 &&
-        (req_mode == PA_MODE_AUTO || req_mode == PA_MODE_SPLIT || req_mode == PA_MODE_FUSED)) {
-        const int per_head = num_sms / a->num_kv_heads;  // partitions of the sequence
-        if (per_head >= 2) {
-            const long long p1 = ((a->max_seq_len + per_head - 1) / per_head + bs - 1) / bs * bs;
-            if (p1 >= kOneWaveMinPartition) {
+    const bool uniform = o && (o->flags & PA_FLAG_UNIFORM_LENGTHS);
+    if (!(o && o->partition_size > 0) && !(o && (o->warps || o->stages)) && (a->num_seqs == 1 || uniform) &&
+        a->num_seqs > 0 && (req_mode == PA_MODE_AUTO || req_mode == PA_MODE_SPLIT || req_mode == PA_MODE_FUSED)) {
+        // partitions of each sequence
+        const long long per_seq = (long long)num_sms / ((long long)a->num_kv_heads * a->num_seqs);
+        if (per_seq >= 2) {
+            const long long p1 = ((a->max_seq_len + per_seq - 1) / per_seq + bs - 1) / bs * bs;
+            if (p1 >= (a->num_seqs == 1 ? kOneWaveMinPartition : bs)) {
                 part = static_cast<int>(p1);
                 one_wave = true;
             }
@@ -292,14 +305,16 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         plan->coop = ctas <= per_sm * num_sms &&
                      pa::fused_barrier_bytes(plan->grid_x, a->num_heads / a->num_kv_heads, a->head_dim) <= stage_area;
     }
-    // Pooled: on request, and by default for the one-wave plan, where every
-    // CTA is resident from the start and the SMs' unequal shares of HBM
-    // bandwidth would otherwise set the finish (GB300, 102400 tokens: 66.8 ->
-    // 65.4 us per call; 262144: 158.5 -> 156.0).  Plans of several waves stay
-    // fixed: a later wave's CTAs would find only their first chunks left.
+    // Pooled: on request, and by default for the one-wave plan of one
+    // sequence, where every CTA is resident from the start and the SMs'
+    // unequal shares of HBM bandwidth would otherwise set the finish (GB300,
+    // 102400 tokens: 66.8 -> 65.4 us per call; 262144: 158.5 -> 156.0).  The
+    // one-wave plan of a uniform batch stays fixed (pooled: 4 x 32768 82.6 ->
+    // 81.8 us, 2 x 65536 82.4 -> 83.1).  Plans of several waves stay fixed: a
+    // later wave's CTAs would find only their first chunks left.
     const int flags = o ? o->flags : 0;
     const bool want_pool =
-        (flags & PA_FLAG_POOLED) || (one_wave && !(flags & PA_FLAG_DETERMINISTIC));
+        (flags & PA_FLAG_POOLED) || (one_wave && a->num_seqs == 1 && !(flags & PA_FLAG_DETERMINISTIC));
     // (the claim counters are re-armed by the reduce kernel, or by the last
     // CTA to leave a fused group's barrier)
     plan->pooled = want_pool && !(flags & PA_FLAG_DETERMINISTIC) &&

@@ -680,3 +680,33 @@ def _split_bytes(w, plan):
 def _claims_at(ws, split_bytes, w):
     n = len(w.seq_lens_host) * w.num_kv_heads
     return ws[split_bytes:split_bytes + 8 * n].view(torch.int64)
+
+
+@pytest.mark.parametrize("lens", [[4000] * 4, [4000, 100, 3000, 0], [1, 17, 4000], [2048] * 8])
+def test_uniform_lengths_flag(dev, lens):
+    # the batch's one-wave plan (PA_FLAG_UNIFORM_LENGTHS) on uniform batches and,
+    # where the statement is wrong, on ragged ones: correct either way
+    w = W.make_workload("uniform", lens, num_blocks=sum((L + 15) // 16 for L in lens) + 5, seed=len(lens) + lens[0],
+                        device=dev, tail_fill=float("nan"))
+    flags = pb.PA_FLAG_UNIFORM_LENGTHS
+    plan = pb.pa_decode_plan(torch.empty_like(w.q), w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                             w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, w.scale,
+                             max_seq_len=w.max_seq_len, flags=flags)
+    assert plan["threads"] == 128 and plan["grid_x"] * plan["grid_y"] * plan["grid_z"] <= 152
+    out = pb.decode_workload(w, flags=flags)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    assert_parity(out, oracle_ref(w), f"uniform-lengths plan {lens}")
+    assert all(torch.count_nonzero(out[b]) == 0 for b, L in enumerate(lens) if L == 0)
+    # fixed partitions: repeats give the same bits
+    again = pb.decode_workload(w, flags=flags)
+    torch.cuda.synchronize()
+    assert torch.equal(out, again)
+
+
+def test_uniform_lengths_flag_on_the_peaked_workload(dev):
+    w = W.make_config("b4_l32768_peaked", device=dev)
+    out = pb.decode_workload(w, flags=pb.PA_FLAG_UNIFORM_LENGTHS)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    assert_parity(out, oracle_ref(w), "b4_l32768_peaked, uniform-lengths plan")

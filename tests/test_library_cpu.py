@@ -425,3 +425,43 @@ def test_prefix_split_fails_cleanly_without_a_device():
     assert rc == pb.PA_ERR_INVALID_ARG
     rc = pb.lib.pa_prefix_split(ctypes.byref(a), ctypes.byref(o), ctypes.byref(sp), FAKE + 16, 1 << 30, None)
     assert rc == pb.PA_ERR_INVALID_ARG  # misaligned
+
+
+def plan_flags(a, flags, partition_size=0, warps=0, stages=0, mode=0):
+    o = pb.pa_decode_opts(mode, partition_size, flags, 0, None, None, warps, stages)
+    pl = pb.pa_decode_plan_t()
+    rc = pb.lib.pa_decode_plan(ctypes.byref(a), ctypes.byref(o), SMS, ctypes.byref(pl))
+    return rc, pl.as_dict()
+
+
+@pytest.mark.parametrize("B,L,per_seq,P", [(4, 32768, 9, 3648), (4, 4096, 9, 464), (2, 65536, 19, 3456),
+                                           (16, 16384, 2, 8192), (8, 8192, 4, 2048)])
+def test_uniform_lengths_flag_gives_a_batch_the_one_wave_plan(B, L, per_seq, P):
+    # floor(152 / (4 kv heads x B)) partitions per sequence of ceil(L / that)
+    # tokens, rounded up to whole blocks; one 4-warp CTA per SM; fixed partitions
+    a = args(num_seqs=B, max_seq_len=L, num_blocks=B * L // 16)
+    rc, pl = plan_flags(a, pb.PA_FLAG_UNIFORM_LENGTHS)
+    assert rc == pb.PA_OK
+    assert pl["partition_size"] == P and (pl["grid_x"], pl["grid_y"], pl["grid_z"]) == (per_seq, 4, B)
+    assert pl["threads"] == 128 and pl["stages"] == 2 and pl["pooled"] == 0 and pl["launch_reduce"] == 1
+    assert pl["grid_x"] * pl["grid_y"] * pl["grid_z"] <= SMS
+    # without the statement a batch keeps the 512-token grid
+    rc, pl = plan_flags(a, 0)
+    assert pl["partition_size"] in (256, 512)
+
+
+def test_uniform_lengths_flag_leaves_other_plans_alone():
+    # too many sequences for two partitions each (152 // (4 x 32) = 1): the grid
+    rc, pl = plan_flags(args(num_seqs=32, max_seq_len=4096, num_blocks=8192), pb.PA_FLAG_UNIFORM_LENGTHS)
+    assert rc == pb.PA_OK and pl["partition_size"] == 512 and pl["grid_x"] == 8
+    # a caller's partition size or CTA shape wins over the flag
+    a = args(num_seqs=4, max_seq_len=32768, num_blocks=8192)
+    assert plan_flags(a, pb.PA_FLAG_UNIFORM_LENGTHS, partition_size=1024)[1]["partition_size"] == 1024
+    rc, pl = plan_flags(a, pb.PA_FLAG_UNIFORM_LENGTHS, warps=2, stages=2)
+    assert pl["partition_size"] == 512 and pl["threads"] == 64
+    # one sequence: the flag changes nothing (the one-wave rule already holds, pooled)
+    one = args()
+    assert plan_flags(one, pb.PA_FLAG_UNIFORM_LENGTHS)[1] == plan_flags(one, 0)[1]
+    # with PA_FLAG_POOLED the batch's one wave is pooled
+    rc, pl = plan_flags(a, pb.PA_FLAG_UNIFORM_LENGTHS | pb.PA_FLAG_POOLED)
+    assert pl["pooled"] == 1 and pl["partition_size"] == 3648
