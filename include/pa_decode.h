@@ -187,10 +187,12 @@ typedef struct {
 typedef struct {
     int mode;                    /* PA_MODE_* */
     int partition_size;          /* tokens per partition in SPLIT mode, multiple of block_size; 0 = chosen
-                                    by the planner: 512 (256 when that gives fewer CTAs than SMs; for
-                                    one long sequence, as many partitions per kv head as SMs allow,
-                                    one wave of one 4-warp CTA per SM, when that exceeds 2048 tokens;
-                                    that plan is pooled, see PA_FLAG_POOLED) */
+                                    by the planner: 512 (256 when that gives fewer CTAs than SMs); for
+                                    one sequence, as many partitions per kv head as SMs allow, one wave
+                                    of one 4-warp CTA per SM, when those partitions exceed 2048 tokens
+                                    (pooled, see PA_FLAG_POOLED) or the sequence is 513..4096 tokens
+                                    long (fixed partitions); for a batch, the same with
+                                    PA_FLAG_UNIFORM_LENGTHS */
     int flags;                   /* PA_FLAG_* */
     unsigned int wait_limit;     /* polls before a copy wait gives up; 0 = library default (2^20) */
     void* event_partition_begin; /* optional cudaEvent_t recorded on `stream` right before ... */
@@ -264,7 +266,9 @@ int pa_decode_plan(const pa_decode_args* args, const pa_decode_opts* opts, int n
  * the "docs" commit page (max score, exp sum, weighted V per partition, fp32),
  * sized once for reuse as the "qwen3_6_scripts/paged_attn.py" commit page's
  * buffer-reuse paragraphs advise.  partition_size 0 gives an upper bound for the
- * automatic partition size (its pooled claim counters included).  A pooled SPLIT
+ * automatic partition size, one-wave plans included (PA_FLAG_UNIFORM_LENGTHS
+ * too; it asks the device's SM count, and assumes 1024 SMs without a device),
+ * and its pooled claim counters.  A pooled SPLIT
  * needs 256-byte-aligned num_seqs * num_kv_heads * 8 bytes more; FUSED that much
  * plus 256-byte-aligned num_seqs * num_kv_heads * 4; PERSISTENT has its own
  * partition count and tables (work list, order, sizes).  pa_decode_plan gives

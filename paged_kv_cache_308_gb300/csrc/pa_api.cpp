@@ -13,6 +13,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pa_internal.h"
@@ -22,6 +23,9 @@ namespace {
 
 constexpr int kDefaultPartition = 512;
 constexpr int kOneWaveMinPartition = 2048;  // see make_plan
+constexpr int kOneWaveShortMaxLen = 4096;    // see make_plan
+// SM count assumed by pa_decode_workspace_size when no device answers (above any GPU's)
+constexpr int kMaxSmsBound = 1024;
 // PA_MODE_PERSISTENT CTA shapes: 4 x 2 when the scan apportions the partitions
 // (about one item per CTA), 1 x 2 for a caller's partition size (many items)
 constexpr int kPersistentWarps = 4, kPersistentWarpsFixedSize = 1, kPersistentStages = 2;
@@ -202,6 +206,11 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     // (GB300, 4 kv heads, head_dim 256, against 512-token partitions: 102400
     // tokens 70.5 -> 68.9 us, 262144: 174.4 -> 161.6, 524288: 343.9 -> 305.0;
     // below ~2048 tokens per partition the two are within a few per cent).
+    // A short sequence (512 < L <= 4096 tokens) takes it too: the call is
+    // bound by latency, and one round of copies per CTA on every SM beats
+    // fewer CTAs with several (device time per call: 2048 tokens 8.27 ->
+    // 6.48 us with 64-token partitions, 4096: 8.41 -> 7.61; 8192 lost,
+    // 8.85 -> 9.29, so the grid stays in between).
     //
     // A batch whose sequences the caller states are all about max_seq_len long
     // (PA_FLAG_UNIFORM_LENGTHS) takes the same decomposition: SMs / (kv heads x
@@ -222,7 +231,8 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         const long long per_seq = (long long)num_sms / ((long long)a->num_kv_heads * a->num_seqs);
         if (per_seq >= 2) {
             const long long p1 = ((a->max_seq_len + per_seq - 1) / per_seq + bs - 1) / bs * bs;
-            if (p1 >= (a->num_seqs == 1 ? kOneWaveMinPartition : bs)) {
+            const bool short_seq = a->max_seq_len > kDefaultPartition && a->max_seq_len <= kOneWaveShortMaxLen;
+            if (p1 >= (a->num_seqs == 1 ? kOneWaveMinPartition : bs) || (a->num_seqs == 1 && short_seq)) {
                 part = static_cast<int>(p1);
                 one_wave = true;
             }
@@ -1006,9 +1016,18 @@ int pa_merge_partials(void* out, const float* max_logits, const float* exp_sums,
 
 size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, int head_dim, int partition_size) {
     if (num_seqs <= 0 || max_seq_len <= 0 || num_heads <= 0 || head_dim <= 0) return 0;
-    // 0: the smallest partition the automatic choice takes (the most partials)
-    const int part = partition_size > 0 ? partition_size : kDefaultPartition / 2;
-    return split_workspace_bytes(num_seqs, num_heads, (max_seq_len + part - 1) / part, head_dim);
+    if (partition_size > 0)
+        return split_workspace_bytes(num_seqs, num_heads, (max_seq_len + partition_size - 1) / partition_size,
+                                     head_dim);
+    // 0: the most partials an automatic plan makes per (sequence, head):
+    // partitions of kDefaultPartition / 2 tokens, or a one-wave plan's (one
+    // CTA per SM, so at most SMs partitions, each of at least one block)
+    long long parts = (max_seq_len + kDefaultPartition / 2 - 1) / (kDefaultPartition / 2);
+    int num_sms = 0;
+    if (query_sm_count(&num_sms) != PA_OK || num_sms <= 0) num_sms = kMaxSmsBound;
+    const long long one_wave = (max_seq_len + pa::kBlockSize - 1) / pa::kBlockSize;
+    parts = std::max(parts, std::min(one_wave, (long long)num_sms));
+    return split_workspace_bytes(num_seqs, num_heads, static_cast<int>(parts), head_dim);
 }
 
 int pa_get_device_status(pa_stream_t stream, int* status) {

@@ -96,10 +96,14 @@ def test_plan_modes():
 def test_plan_halves_the_partition_when_the_grid_is_smaller_than_the_gpu():
     o = pb.pa_decode_opts(0, 0, 0, 0, None, None)
     pl = pb.pa_decode_plan_t()
-    # one 2048-token sequence: 4 partitions x 4 kv heads = 16 CTAs < 152 SMs
-    assert pb.lib.pa_decode_plan(ctypes.byref(args(max_seq_len=2048, num_blocks=128)), ctypes.byref(o), 152,
-                                 ctypes.byref(pl)) == 0
+    # two 2048-token sequences: 4 partitions x 4 kv heads x 2 = 32 CTAs < 152 SMs
+    assert pb.lib.pa_decode_plan(ctypes.byref(args(num_seqs=2, max_seq_len=2048, num_blocks=256)), ctypes.byref(o),
+                                 152, ctypes.byref(pl)) == 0
     assert pl.partition_size == 256 and pl.grid_x == 8
+    # one 8192-token sequence (between the short and the long one-wave rules): 256 too
+    assert pb.lib.pa_decode_plan(ctypes.byref(args(max_seq_len=8192, num_blocks=512)), ctypes.byref(o), 152,
+                                 ctypes.byref(pl)) == 0
+    assert pl.partition_size == 256 and pl.grid_x == 32
     # 64 of them give 1024 CTAs at the default size, which stays
     a = args(num_seqs=64, max_seq_len=2048, num_blocks=64 * 128)
     assert pb.lib.pa_decode_plan(ctypes.byref(a), ctypes.byref(o), 152, ctypes.byref(pl)) == 0
@@ -465,3 +469,17 @@ def test_uniform_lengths_flag_leaves_other_plans_alone():
     # with PA_FLAG_POOLED the batch's one wave is pooled
     rc, pl = plan_flags(a, pb.PA_FLAG_UNIFORM_LENGTHS | pb.PA_FLAG_POOLED)
     assert pl["pooled"] == 1 and pl["partition_size"] == 3648
+
+
+@pytest.mark.parametrize("L,P,parts", [(2048, 64, 32), (4096, 112, 37), (513, 16, 33), (3000, 80, 38)])
+def test_short_sequence_runs_one_wave_of_one_block_deep_ctas(L, P, parts):
+    # 512 < L <= 4096 tokens: ceil(L / 38) tokens rounded up to whole blocks,
+    # one 4-warp CTA per SM, fixed partitions (too short to pool)
+    rc, pl = plan_flags(args(max_seq_len=L, num_blocks=(L + 15) // 16), 0)
+    assert rc == pb.PA_OK
+    assert pl["partition_size"] == P and (pl["grid_x"], pl["grid_y"]) == (parts, 4)
+    assert pl["threads"] == 128 and pl["stages"] == 2 and pl["pooled"] == 0 and pl["launch_reduce"] == 1
+    assert pb.pa_decode_workspace_size(1, L, 24, 256, 0) >= pl["workspace_bytes"]
+    # 512 tokens or fewer: one partition, no reduce
+    rc, pl = plan_flags(args(max_seq_len=512, num_blocks=32), 0)
+    assert pl["launch_reduce"] == 0 and pl["grid_x"] == 1
