@@ -190,9 +190,10 @@ typedef struct {
                                     by the planner: 512 (256 when that gives fewer CTAs than SMs); for
                                     one sequence, as many partitions per kv head as SMs allow, one wave
                                     of one 4-warp CTA per SM, when those partitions exceed 2048 tokens
-                                    (pooled, see PA_FLAG_POOLED) or the sequence is 513..4096 tokens
-                                    long (fixed partitions); for a batch, the same with
-                                    PA_FLAG_UNIFORM_LENGTHS */
+                                    (pooled, see PA_FLAG_POOLED); for any batch whose longest sequence
+                                    is over 512 tokens, the same one wave when its partitions come to
+                                    at most 128 tokens (fixed); for a batch with
+                                    PA_FLAG_UNIFORM_LENGTHS, the one wave at any partition length */
     int flags;                   /* PA_FLAG_* */
     unsigned int wait_limit;     /* polls before a copy wait gives up; 0 = library default (2^20) */
     void* event_partition_begin; /* optional cudaEvent_t recorded on `stream` right before ... */

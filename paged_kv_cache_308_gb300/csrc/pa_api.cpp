@@ -23,7 +23,7 @@ namespace {
 
 constexpr int kDefaultPartition = 512;
 constexpr int kOneWaveMinPartition = 2048;  // see make_plan
-constexpr int kOneWaveShortMaxLen = 4096;    // see make_plan
+constexpr int kOneWaveShortMaxPartition = 128;  // see make_plan
 // SM count assumed by pa_decode_workspace_size when no device answers (above any GPU's)
 constexpr int kMaxSmsBound = 1024;
 // PA_MODE_PERSISTENT CTA shapes: 4 x 2 when the scan apportions the partitions
@@ -206,11 +206,8 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     // (GB300, 4 kv heads, head_dim 256, against 512-token partitions: 102400
     // tokens 70.5 -> 68.9 us, 262144: 174.4 -> 161.6, 524288: 343.9 -> 305.0;
     // below ~2048 tokens per partition the two are within a few per cent).
-    // A short sequence (512 < L <= 4096 tokens) takes it too: the call is
-    // bound by latency, and one round of copies per CTA on every SM beats
-    // fewer CTAs with several (device time per call: 2048 tokens 8.27 ->
-    // 6.48 us with 64-token partitions, 4096: 8.41 -> 7.61; 8192 lost,
-    // 8.85 -> 9.29, so the grid stays in between).
+    // A short call is bound by latency: one round of copies per CTA on every
+    // SM beats fewer CTAs with several (below).
     //
     // A batch whose sequences the caller states are all about max_seq_len long
     // (PA_FLAG_UNIFORM_LENGTHS) takes the same decomposition: SMs / (kv heads x
@@ -222,19 +219,31 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     // tell such a batch from one whose longest sequence stands alone (4 x
     // [32768, 100, 100, 100]: 30.8 -> 47.1 us) or from lengths spread below
     // the longest (8 x U[1, 8192]: 27.7 -> 37.7), so batches keep the grid.
-    bool one_wave = false;
+    //
+    // Short sequences (longer than one 512-token partition) take the one wave
+    // too, in any batch, when its partitions hold at most one round of copies
+    // of a 4-warp CTA (kOneWaveShortMaxPartition tokens): every CTA then ends
+    // after one round whatever the lengths, so an uneven batch costs nothing
+    // that the grid would save.  Device time per call against AUTO's grid:
+    // 2048 tokens 8.27 -> 6.48 us, 4096: 8.41 -> 7.61 (8192, with 224-token
+    // partitions, lost: 8.85 -> 9.29); 2 x 2048 8.72 -> 7.40, [2048, 40]
+    // 8.40 -> 7.40, 4 x 1024 9.27 -> 8.07, [1024, 50, 300, 700] 9.06 -> 7.80.
+    bool one_wave = false, pool_one_wave = false;
     const int req_mode = o ? o->mode : PA_MODE_AUTO;
     const bool uniform = o && (o->flags & PA_FLAG_UNIFORM_LENGTHS);
-    if (!(o && o->partition_size > 0) && !(o && (o->warps || o->stages)) && (a->num_seqs == 1 || uniform) &&
-        a->num_seqs > 0 && (req_mode == PA_MODE_AUTO || req_mode == PA_MODE_SPLIT || req_mode == PA_MODE_FUSED)) {
+    if (!(o && o->partition_size > 0) && !(o && (o->warps || o->stages)) && a->num_seqs > 0 &&
+        (req_mode == PA_MODE_AUTO || req_mode == PA_MODE_SPLIT || req_mode == PA_MODE_FUSED)) {
         // partitions of each sequence
         const long long per_seq = (long long)num_sms / ((long long)a->num_kv_heads * a->num_seqs);
         if (per_seq >= 2) {
             const long long p1 = ((a->max_seq_len + per_seq - 1) / per_seq + bs - 1) / bs * bs;
-            const bool short_seq = a->max_seq_len > kDefaultPartition && a->max_seq_len <= kOneWaveShortMaxLen;
-            if (p1 >= (a->num_seqs == 1 ? kOneWaveMinPartition : bs) || (a->num_seqs == 1 && short_seq)) {
+            const bool long_one = a->num_seqs == 1 && p1 >= kOneWaveMinPartition;
+            const bool stated = a->num_seqs > 1 && uniform;
+            const bool short_seq = a->max_seq_len > kDefaultPartition && p1 <= kOneWaveShortMaxPartition;
+            if (long_one || stated || short_seq) {
                 part = static_cast<int>(p1);
                 one_wave = true;
+                pool_one_wave = long_one;
             }
         }
     }
@@ -315,8 +324,9 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         plan->coop = ctas <= per_sm * num_sms &&
                      pa::fused_barrier_bytes(plan->grid_x, a->num_heads / a->num_kv_heads, a->head_dim) <= stage_area;
     }
-    // Pooled: on request, and by default for the one-wave plan of one
-    // sequence, where every CTA is resident from the start and the SMs'
+    // Pooled: on request, and by default for the one-wave plan of one long
+    // sequence (short ones measured no gain: 4096 tokens 7.61 -> 7.54 us,
+    // 2048 6.48 -> 6.50), where every CTA is resident from the start and the SMs'
     // unequal shares of HBM bandwidth would otherwise set the finish (GB300,
     // 102400 tokens: 66.8 -> 65.4 us per call; 262144: 158.5 -> 156.0).  The
     // one-wave plan of a uniform batch stays fixed (pooled: 4 x 32768 82.6 ->
@@ -324,7 +334,7 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     // later wave's CTAs would find only their first chunks left.
     const int flags = o ? o->flags : 0;
     const bool want_pool =
-        (flags & PA_FLAG_POOLED) || (one_wave && a->num_seqs == 1 && !(flags & PA_FLAG_DETERMINISTIC));
+        (flags & PA_FLAG_POOLED) || (pool_one_wave && !(flags & PA_FLAG_DETERMINISTIC));
     // (the claim counters are re-armed by the reduce kernel, or by the last
     // CTA to leave a fused group's barrier)
     plan->pooled = want_pool && !(flags & PA_FLAG_DETERMINISTIC) &&

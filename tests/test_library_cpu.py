@@ -96,10 +96,10 @@ def test_plan_modes():
 def test_plan_halves_the_partition_when_the_grid_is_smaller_than_the_gpu():
     o = pb.pa_decode_opts(0, 0, 0, 0, None, None)
     pl = pb.pa_decode_plan_t()
-    # two 2048-token sequences: 4 partitions x 4 kv heads x 2 = 32 CTAs < 152 SMs
-    assert pb.lib.pa_decode_plan(ctypes.byref(args(num_seqs=2, max_seq_len=2048, num_blocks=256)), ctypes.byref(o),
+    # two 8192-token sequences: 16 partitions x 4 kv heads x 2 = 128 CTAs < 152 SMs
+    assert pb.lib.pa_decode_plan(ctypes.byref(args(num_seqs=2, max_seq_len=8192, num_blocks=1024)), ctypes.byref(o),
                                  152, ctypes.byref(pl)) == 0
-    assert pl.partition_size == 256 and pl.grid_x == 8
+    assert pl.partition_size == 256 and pl.grid_x == 32
     # one 8192-token sequence (between the short and the long one-wave rules): 256 too
     assert pb.lib.pa_decode_plan(ctypes.byref(args(max_seq_len=8192, num_blocks=512)), ctypes.byref(o), 152,
                                  ctypes.byref(pl)) == 0
@@ -471,15 +471,22 @@ def test_uniform_lengths_flag_leaves_other_plans_alone():
     assert pl["pooled"] == 1 and pl["partition_size"] == 3648
 
 
-@pytest.mark.parametrize("L,P,parts", [(2048, 64, 32), (4096, 112, 37), (513, 16, 33), (3000, 80, 38)])
-def test_short_sequence_runs_one_wave_of_one_block_deep_ctas(L, P, parts):
-    # 512 < L <= 4096 tokens: ceil(L / 38) tokens rounded up to whole blocks,
-    # one 4-warp CTA per SM, fixed partitions (too short to pool)
-    rc, pl = plan_flags(args(max_seq_len=L, num_blocks=(L + 15) // 16), 0)
+@pytest.mark.parametrize("B,L,P,parts", [(1, 2048, 64, 32), (1, 4096, 112, 37), (1, 513, 16, 33), (1, 3000, 80, 38),
+                                          (1, 4864, 128, 38), (2, 2048, 112, 19), (4, 1024, 128, 8),
+                                          (3, 1500, 128, 12)])
+def test_short_sequence_runs_one_wave_of_one_block_deep_ctas(B, L, P, parts):
+    # longest sequence over 512 tokens and one-wave partitions of at most 128
+    # tokens (one round of copies for a 4-warp CTA): floor(152 / (4 B))
+    # partitions of ceil(L / that) tokens rounded up to whole blocks, one
+    # 4-warp CTA per SM, fixed partitions, in any batch
+    rc, pl = plan_flags(args(num_seqs=B, max_seq_len=L, num_blocks=B * ((L + 15) // 16)), 0)
     assert rc == pb.PA_OK
-    assert pl["partition_size"] == P and (pl["grid_x"], pl["grid_y"]) == (parts, 4)
+    assert pl["partition_size"] == P and (pl["grid_x"], pl["grid_y"], pl["grid_z"]) == (parts, 4, B)
     assert pl["threads"] == 128 and pl["stages"] == 2 and pl["pooled"] == 0 and pl["launch_reduce"] == 1
-    assert pb.pa_decode_workspace_size(1, L, 24, 256, 0) >= pl["workspace_bytes"]
+    assert pb.pa_decode_workspace_size(B, L, 24, 256, 0) >= pl["workspace_bytes"]
+    # longer partitions keep the grid (one 5000-token sequence: 144-token ones)
+    rc, pl = plan_flags(args(max_seq_len=5000, num_blocks=313), 0)
+    assert pl["partition_size"] == 256
     # 512 tokens or fewer: one partition, no reduce
     rc, pl = plan_flags(args(max_seq_len=512, num_blocks=32), 0)
     assert pl["launch_reduce"] == 0 and pl["grid_x"] == 1
