@@ -75,12 +75,14 @@ int query_sm_count(int* num_sms) {
 }
 
 // Head_dim slice of one reduce CTA: the widest slice that still gives the
-// reduce grid about four CTAs per SM, so a large batch runs few, wide CTAs
+// reduce grid about two CTAs per SM, so a large batch runs few, wide CTAs
 // (short launch and latency chains) and a single long sequence runs narrow
-// ones (more loads in flight per partial).
+// ones (more loads in flight per partial).  Two rather than four CTAs per
+// SM: b8_u8192 27.33 -> 27.05 us per call (128-wide slices instead of 64),
+// b4_l32768_peaked 85.26 -> 85.41 (64 instead of 32), the rest unchanged.
 int reduce_slice(int head_dim, long long pairs, int num_sms) {
     for (int w = head_dim; w > pa::kReduceMinSlice; w /= 2)
-        if (pairs * (head_dim / w) >= 4ll * num_sms) return w;
+        if (pairs * (head_dim / w) >= 2ll * num_sms) return w;
     return pa::kReduceMinSlice;
 }
 
