@@ -112,3 +112,33 @@ def test_random_split_kv_case(dev, i):
     torch.cuda.synchronize()
     assert pb.pa_get_device_status() == 0
     assert_parity(out, oracle_ref(w), f"split-KV case {i}: {c} P={P} R={R}")
+
+
+def draw_short_case(i):
+    # AUTO's short one-wave plans: longest sequence 513..4864 tokens, small
+    # batches (partitions of at most 128 tokens, one copy round per CTA);
+    # every other case states uniform lengths, right or wrong
+    r = random.Random(5000 + i)
+    hkv = r.choice([1, 2, 4, 8])
+    g = r.choice([1, 2, 4, 6, 8])
+    d = r.choice([64, 128, 256])
+    b = r.choice([1, 1, 2, 3, 4])
+    longest = r.randint(513, 4864)
+    lens = [longest] + [r.choice([0, 1, 17, r.randint(1, longest), longest]) for _ in range(b - 1)]
+    r.shuffle(lens)
+    opt = dict(flags=pb.PA_FLAG_UNIFORM_LENGTHS) if i % 2 else dict()
+    return dict(lens=lens, num_heads=hkv * g, num_kv_heads=hkv, head_dim=d, opt=opt, seed=500 + i)
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_short_auto_case(dev, i):
+    c = draw_short_case(i)
+    blocks = sum((L + 15) // 16 for L in c["lens"]) + 3
+    w = W.make_workload(f"short{i}", c["lens"], num_heads=c["num_heads"], num_kv_heads=c["num_kv_heads"],
+                        head_dim=c["head_dim"], num_blocks=blocks, seed=c["seed"], device=dev,
+                        tail_fill=float("nan"))
+    out = pb.decode_workload(w, **c["opt"])
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    assert_parity(out, oracle_ref(w), f"short case {i}: {c}")
+    assert all(torch.count_nonzero(out[b]) == 0 for b, L in enumerate(c["lens"]) if L == 0)
