@@ -91,8 +91,8 @@ enum {
                            (plan.coop) the grid is launched cooperatively: the CTAs of each
                            (sequence, kv head) meet at a bounded group barrier and each merges
                            its own slice of the outputs; otherwise the last CTA to finish merges
-                           (an atomic ticket; nobody waits).  For one long sequence FUSED takes
-                           the one-wave plan (pooled unless PA_FLAG_DETERMINISTIC).  The
+                           (an atomic ticket; nobody waits).  For one sequence FUSED takes
+                           the one-wave plan (pooled as for SPLIT).  The
                            workspace also holds two 4-byte words per (sequence, kv head) (the
                            ticket or arrivals, and the departures), after the partials and a
                            slot of 8 bytes per (sequence, kv head) for the pooled claim
@@ -188,12 +188,12 @@ typedef struct {
     int mode;                    /* PA_MODE_* */
     int partition_size;          /* tokens per partition in SPLIT mode, multiple of block_size; 0 = chosen
                                     by the planner: 512 (256 when that gives fewer CTAs than SMs); for
-                                    one sequence, as many partitions per kv head as SMs allow, one wave
-                                    of one 4-warp CTA per SM, when those partitions exceed 2048 tokens
-                                    (pooled, see PA_FLAG_POOLED); for any batch whose longest sequence
-                                    is over 512 tokens, the same one wave when its partitions come to
-                                    at most 128 tokens (fixed); for a batch with
-                                    PA_FLAG_UNIFORM_LENGTHS, the one wave at any partition length */
+                                    one sequence over 512 tokens, as many partitions per kv head as SMs
+                                    allow, one wave of one 4-warp CTA per SM (pooled from 2048-token
+                                    partitions on, see PA_FLAG_POOLED; fixed below); for a batch whose
+                                    longest sequence is over 512 tokens, the same one wave when its
+                                    partitions come to at most 128 tokens (fixed), or at any length
+                                    with PA_FLAG_UNIFORM_LENGTHS */
     int flags;                   /* PA_FLAG_* */
     unsigned int wait_limit;     /* polls before a copy wait gives up; 0 = library default (2^20) */
     void* event_partition_begin; /* optional cudaEvent_t recorded on `stream` right before ... */

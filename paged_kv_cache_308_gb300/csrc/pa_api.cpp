@@ -22,7 +22,7 @@
 namespace {
 
 constexpr int kDefaultPartition = 512;
-constexpr int kOneWaveMinPartition = 2048;  // see make_plan
+constexpr int kOneWavePoolMinPartition = 2048;  // see make_plan
 constexpr int kOneWaveShortMaxPartition = 128;  // see make_plan
 // SM count assumed by pa_decode_workspace_size when no device answers (above any GPU's)
 constexpr int kMaxSmsBound = 1024;
@@ -202,14 +202,18 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
                                a->num_kv_heads * a->num_seqs;
         if (ctas < num_sms) part = kDefaultPartition / 2;
     }
-    // One long sequence: its grid is known exactly, so it runs as ONE wave of
-    // one 4-warp CTA per SM (partitions x kv heads = SMs).  Fewer, longer CTAs
-    // pay a CTA's start-up and merge once per SM and leave fewer partials
-    // (GB300, 4 kv heads, head_dim 256, against 512-token partitions: 102400
-    // tokens 70.5 -> 68.9 us, 262144: 174.4 -> 161.6, 524288: 343.9 -> 305.0;
-    // below ~2048 tokens per partition the two are within a few per cent).
-    // A short call is bound by latency: one round of copies per CTA on every
-    // SM beats fewer CTAs with several (below).
+    // One sequence longer than one partition: its grid is known exactly, so
+    // it runs as ONE wave of one 4-warp CTA per SM (partitions x kv heads =
+    // SMs).  Fewer, longer CTAs pay a CTA's start-up and merge once per SM and
+    // leave fewer partials (GB300, 4 kv heads, head_dim 256, device time per
+    // call against AUTO's grid: 102400 tokens 70.5 -> 68.9 us, 262144: 174.4
+    // -> 161.6, 524288: 343.9 -> 305.0; 65536: 47.1 -> 45.5, 24000: 17.9 ->
+    // 14.1, 12000: 11.6 -> 9.7, 6000: 8.6 -> 8.3, 2048: 8.3 -> 6.5; the one
+    // length measured slower was 8192, 8.8 -> 9.2).  From 2048-token
+    // partitions on it is pooled (below); shorter ones measured no gain from
+    // pooling (16384 tokens: 11.3 fixed, 13.7 pooled).  A short call is bound
+    // by latency: one round of copies per CTA on every SM beats fewer CTAs
+    // with several (below).
     //
     // A batch whose sequences the caller states are all about max_seq_len long
     // (PA_FLAG_UNIFORM_LENGTHS) takes the same decomposition: SMs / (kv heads x
@@ -239,13 +243,13 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         const long long per_seq = (long long)num_sms / ((long long)a->num_kv_heads * a->num_seqs);
         if (per_seq >= 2) {
             const long long p1 = ((a->max_seq_len + per_seq - 1) / per_seq + bs - 1) / bs * bs;
-            const bool long_one = a->num_seqs == 1 && p1 >= kOneWaveMinPartition;
+            const bool one_seq = a->num_seqs == 1 && a->max_seq_len > kDefaultPartition;
             const bool stated = a->num_seqs > 1 && uniform;
             const bool short_seq = a->max_seq_len > kDefaultPartition && p1 <= kOneWaveShortMaxPartition;
-            if (long_one || stated || short_seq) {
+            if (one_seq || stated || short_seq) {
                 part = static_cast<int>(p1);
                 one_wave = true;
-                pool_one_wave = long_one;
+                pool_one_wave = one_seq && p1 >= kOneWavePoolMinPartition;
             }
         }
     }

@@ -63,9 +63,10 @@ def test_plan_long_context_runs_one_wave_of_one_cta_per_sm():
     assert pl["pooled"] == 1  # + one 8-byte claim counter per kv head, in its own 256-byte slot
     assert pl["workspace_bytes"] == ws_bytes(1, 24, 38, 256) + 256
     assert pl["workspace_bytes"] <= pb.pa_decode_workspace_size(1, 102400, 24, 256, 0)
-    # below 2048 tokens per partition, and for batches, the 512-token default stays
+    # below 2048 tokens per partition the one wave has fixed partitions
     rc, short = plan(args(max_seq_len=65536, num_blocks=4096))
-    assert rc == 0 and short["partition_size"] == 512 and short["grid_x"] == 128
+    assert rc == 0 and short["partition_size"] == 1728 and short["grid_x"] == 38 and short["pooled"] == 0
+    # batches keep the 512-token default
     rc, batch = plan(args(num_seqs=2, num_blocks=12800))
     assert rc == 0 and batch["partition_size"] == 512 and batch["grid_x"] == 200
     # an explicit partition size or mode keeps the old plan
@@ -99,10 +100,6 @@ def test_plan_halves_the_partition_when_the_grid_is_smaller_than_the_gpu():
     # two 8192-token sequences: 16 partitions x 4 kv heads x 2 = 128 CTAs < 152 SMs
     assert pb.lib.pa_decode_plan(ctypes.byref(args(num_seqs=2, max_seq_len=8192, num_blocks=1024)), ctypes.byref(o),
                                  152, ctypes.byref(pl)) == 0
-    assert pl.partition_size == 256 and pl.grid_x == 32
-    # one 8192-token sequence (between the short and the long one-wave rules): 256 too
-    assert pb.lib.pa_decode_plan(ctypes.byref(args(max_seq_len=8192, num_blocks=512)), ctypes.byref(o), 152,
-                                 ctypes.byref(pl)) == 0
     assert pl.partition_size == 256 and pl.grid_x == 32
     # 64 of them give 1024 CTAs at the default size, which stays
     a = args(num_seqs=64, max_seq_len=2048, num_blocks=64 * 128)
@@ -304,13 +301,15 @@ def _plan_heads(num_kv_heads, max_seq_len, flags=0, num_heads=None):
 def test_one_wave_pooled_plan_for_every_kv_head_count(hkv, L):
     pl = _plan_heads(hkv, L)
     per_head = SMS // hkv
-    if -(-L // per_head) < 2048:  # partitions shorter than 2048 tokens keep the 512-token plan
-        assert pl["partition_size"] == 512 and pl["pooled"] == 0
-        return
-    # one 4-warp CTA per SM at most, partitions of whole blocks covering the sequence, pooled
-    assert pl["threads"] == 128 and pl["stages"] == 2 and pl["pooled"] == 1
+    # one 4-warp CTA per SM at most, partitions of whole blocks covering the sequence,
+    # pooled from 2048-token partitions on
+    assert pl["threads"] == 128 and pl["stages"] == 2
     assert pl["grid_x"] * pl["grid_y"] <= SMS and pl["grid_y"] == hkv
     assert pl["partition_size"] % 16 == 0 and pl["partition_size"] * pl["grid_x"] >= L
+    if -(-L // per_head) < 2048:
+        assert pl["pooled"] == 0
+        return
+    assert pl["pooled"] == 1
     fixed = _plan_heads(hkv, L, flags=pb.PA_FLAG_DETERMINISTIC)
     assert fixed["pooled"] == 0 and fixed["grid_x"] == pl["grid_x"] and fixed["partition_size"] == pl["partition_size"]
     assert fixed["workspace_bytes"] + 256 == pl["workspace_bytes"]
@@ -473,20 +472,20 @@ def test_uniform_lengths_flag_leaves_other_plans_alone():
 
 
 @pytest.mark.parametrize("B,L,P,parts", [(1, 2048, 64, 32), (1, 4096, 112, 37), (1, 513, 16, 33), (1, 3000, 80, 38),
-                                          (1, 4864, 128, 38), (2, 2048, 112, 19), (4, 1024, 128, 8),
-                                          (3, 1500, 128, 12)])
+                                          (1, 4864, 128, 38), (1, 8192, 224, 37), (1, 16384, 432, 38),
+                                          (2, 2048, 112, 19), (4, 1024, 128, 8), (3, 1500, 128, 12)])
 def test_short_sequence_runs_one_wave_of_one_block_deep_ctas(B, L, P, parts):
-    # longest sequence over 512 tokens and one-wave partitions of at most 128
-    # tokens (one round of copies for a 4-warp CTA): floor(152 / (4 B))
-    # partitions of ceil(L / that) tokens rounded up to whole blocks, one
-    # 4-warp CTA per SM, fixed partitions, in any batch
+    # one sequence over 512 tokens, or a batch whose one-wave partitions hold
+    # at most 128 tokens (one round of copies for a 4-warp CTA):
+    # floor(152 / (4 B)) partitions of ceil(L / that) tokens rounded up to
+    # whole blocks, one 4-warp CTA per SM, fixed partitions
     rc, pl = plan_flags(args(num_seqs=B, max_seq_len=L, num_blocks=B * ((L + 15) // 16)), 0)
     assert rc == pb.PA_OK
     assert pl["partition_size"] == P and (pl["grid_x"], pl["grid_y"], pl["grid_z"]) == (parts, 4, B)
     assert pl["threads"] == 128 and pl["stages"] == 2 and pl["pooled"] == 0 and pl["launch_reduce"] == 1
     assert pb.pa_decode_workspace_size(B, L, 24, 256, 0) >= pl["workspace_bytes"]
-    # longer partitions keep the grid (one 5000-token sequence: 144-token ones)
-    rc, pl = plan_flags(args(max_seq_len=5000, num_blocks=313), 0)
+    # in a batch, longer partitions keep the grid (two 5000-token sequences)
+    rc, pl = plan_flags(args(num_seqs=2, max_seq_len=5000, num_blocks=626), 0)
     assert pl["partition_size"] == 256
     # 512 tokens or fewer: one partition, no reduce
     rc, pl = plan_flags(args(max_seq_len=512, num_blocks=32), 0)
