@@ -188,12 +188,13 @@ typedef struct {
     int mode;                    /* PA_MODE_* */
     int partition_size;          /* tokens per partition in SPLIT mode, multiple of block_size; 0 = chosen
                                     by the planner: 512 (256 when that gives fewer CTAs than SMs); for
-                                    one sequence over 512 tokens, as many partitions per kv head as SMs
+                                    one sequence over 128 tokens, as many partitions per kv head as SMs
                                     allow, one wave of one 4-warp CTA per SM (pooled from 2048-token
                                     partitions on, see PA_FLAG_POOLED; fixed below); for a batch whose
-                                    longest sequence is over 512 tokens, the same one wave when its
+                                    longest sequence is over 128 tokens, the same one wave when its
                                     partitions come to at most 128 tokens (fixed), or at any length
-                                    with PA_FLAG_UNIFORM_LENGTHS */
+                                    with PA_FLAG_UNIFORM_LENGTHS.  AUTO runs SINGLE when the longest
+                                    sequence fits one partition of the plan, e.g. up to 128 tokens */
     int flags;                   /* PA_FLAG_* */
     unsigned int wait_limit;     /* polls before a copy wait gives up; 0 = library default (2^20) */
     void* event_partition_begin; /* optional cudaEvent_t recorded on `stream` right before ... */

@@ -23,6 +23,7 @@ namespace {
 
 constexpr int kDefaultPartition = 512;
 constexpr int kOneWavePoolMinPartition = 2048;  // see make_plan
+constexpr int kOneWaveMinLen = 128;              // see make_plan
 constexpr int kOneWaveShortMaxPartition = 128;  // see make_plan
 // SM count assumed by pa_decode_workspace_size when no device answers (above any GPU's)
 constexpr int kMaxSmsBound = 1024;
@@ -202,7 +203,13 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
                                a->num_kv_heads * a->num_seqs;
         if (ctas < num_sms) part = kDefaultPartition / 2;
     }
-    // One sequence longer than one partition: its grid is known exactly, so
+    // Up to kOneWaveMinLen tokens (one round of copies for a 4-warp CTA)
+    // SINGLE needs no reduce and wins (64 tokens: 3.6 us against 5.6); above
+    // it a one-wave plan does, since SINGLE adds about a microsecond per copy
+    // round (512 tokens: 8.55 -> 5.87 us, 400: 7.81 -> 5.86, 300: 6.54 ->
+    // 5.83, 200: 5.81 -> 5.67; batches 4 x 300 6.6 -> 6.0, 8 x 400 7.9 -> 6.8).
+    //
+    // One sequence over kOneWaveMinLen tokens: its grid is known exactly, so
     // it runs as ONE wave of one 4-warp CTA per SM (partitions x kv heads =
     // SMs).  Fewer, longer CTAs pay a CTA's start-up and merge once per SM and
     // leave fewer partials (GB300, 4 kv heads, head_dim 256, device time per
@@ -243,9 +250,9 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
         const long long per_seq = (long long)num_sms / ((long long)a->num_kv_heads * a->num_seqs);
         if (per_seq >= 2) {
             const long long p1 = ((a->max_seq_len + per_seq - 1) / per_seq + bs - 1) / bs * bs;
-            const bool one_seq = a->num_seqs == 1 && a->max_seq_len > kDefaultPartition;
+            const bool one_seq = a->num_seqs == 1 && a->max_seq_len > kOneWaveMinLen;
             const bool stated = a->num_seqs > 1 && uniform;
-            const bool short_seq = a->max_seq_len > kDefaultPartition && p1 <= kOneWaveShortMaxPartition;
+            const bool short_seq = a->max_seq_len > kOneWaveMinLen && p1 <= kOneWaveShortMaxPartition;
             if (one_seq || stated || short_seq) {
                 part = static_cast<int>(p1);
                 one_wave = true;

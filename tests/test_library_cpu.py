@@ -86,8 +86,10 @@ def test_plan_modes():
     assert pl["launch_reduce"] == 0 and pl["workspace_bytes"] == 0
     rc, pl = plan(args(max_seq_len=1000, num_blocks=128), mode=pb.PA_MODE_SINGLE)
     assert pl["partition_size"] == 1008                                   # rounded up to whole blocks
+    rc, pl = plan(args(max_seq_len=128, num_blocks=128))
+    assert rc == 0 and pl["mode"] == pb.PA_MODE_SINGLE                    # one copy round: no reduce
     rc, pl = plan(args(max_seq_len=512, num_blocks=128))
-    assert rc == 0 and pl["mode"] == pb.PA_MODE_SINGLE                    # one partition: no reduce
+    assert rc == 0 and pl["mode"] == pb.PA_MODE_SPLIT and pl["partition_size"] == 16   # the one wave
     rc, pl = plan(args(max_seq_len=513, num_blocks=128), mode=pb.PA_MODE_SPLIT, partition_size=64)
     assert rc == 0 and pl["grid_x"] == math.ceil(513 / 64) and pl["launch_reduce"] == 1
     rc, pl = plan(args(num_seqs=0))
@@ -148,7 +150,7 @@ def test_plan_fused_mode_keeps_partials_and_tickets_and_launches_once():
     # the split partials, a slot the size of the pooled claim counters (8 bytes per
     # (sequence, kv head)), then two 4-byte group words per (sequence, kv head), each 256-byte aligned
     assert fused["workspace_bytes"] == split["workspace_bytes"] + 256 + 256
-    rc, one = plan(args(max_seq_len=512, num_blocks=128), mode=pb.PA_MODE_FUSED)
+    rc, one = plan(args(max_seq_len=128, num_blocks=128), mode=pb.PA_MODE_FUSED)
     assert rc == 0 and one["grid_x"] == 1 and one["workspace_bytes"] == 0   # one partition: written directly
 
 
@@ -472,6 +474,7 @@ def test_uniform_lengths_flag_leaves_other_plans_alone():
 
 
 @pytest.mark.parametrize("B,L,P,parts", [(1, 2048, 64, 32), (1, 4096, 112, 37), (1, 513, 16, 33), (1, 3000, 80, 38),
+                                          (1, 129, 16, 9), (1, 512, 16, 32), (4, 300, 48, 7), (8, 400, 112, 4),
                                           (1, 4864, 128, 38), (1, 8192, 224, 37), (1, 16384, 432, 38),
                                           (2, 2048, 112, 19), (4, 1024, 128, 8), (3, 1500, 128, 12)])
 def test_short_sequence_runs_one_wave_of_one_block_deep_ctas(B, L, P, parts):
@@ -487,6 +490,6 @@ def test_short_sequence_runs_one_wave_of_one_block_deep_ctas(B, L, P, parts):
     # in a batch, longer partitions keep the grid (two 5000-token sequences)
     rc, pl = plan_flags(args(num_seqs=2, max_seq_len=5000, num_blocks=626), 0)
     assert pl["partition_size"] == 256
-    # 512 tokens or fewer: one partition, no reduce
-    rc, pl = plan_flags(args(max_seq_len=512, num_blocks=32), 0)
+    # 128 tokens or fewer: one partition, no reduce
+    rc, pl = plan_flags(args(max_seq_len=128, num_blocks=8), 0)
     assert pl["launch_reduce"] == 0 and pl["grid_x"] == 1
