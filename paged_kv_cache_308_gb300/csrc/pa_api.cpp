@@ -197,50 +197,45 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     int part = (o && o->partition_size > 0) ? o->partition_size : kDefaultPartition;
     if (!(o && o->partition_size > 0) && a->max_seq_len > kDefaultPartition) {
         // Short work: when partitions of the default size would give fewer CTAs
-        // than SMs, halve them so that twice as many SMs stream the cache
-        // (b1_l2048: 13.7 -> 10.5 us; smaller partitions cost more in the reduce).
+        // than SMs, halve them so that twice as many SMs stream the cache (an
+        // early measurement on 2048 tokens, which now take a one-wave plan:
+        // 13.7 -> 10.5 us; smaller partitions cost more in the reduce).
         const long long ctas = (long long)((a->max_seq_len + kDefaultPartition - 1) / kDefaultPartition) *
                                a->num_kv_heads * a->num_seqs;
         if (ctas < num_sms) part = kDefaultPartition / 2;
     }
-    // Up to kOneWaveMinLen tokens (one round of copies for a 4-warp CTA)
-    // SINGLE needs no reduce and wins (64 tokens: 3.6 us against 5.6); above
-    // it a one-wave plan does, since SINGLE adds about a microsecond per copy
-    // round (512 tokens: 8.55 -> 5.87 us, 400: 7.81 -> 5.86, 300: 6.54 ->
-    // 5.83, 200: 5.81 -> 5.67; batches 4 x 300 6.6 -> 6.0, 8 x 400 7.9 -> 6.8).
+    // One-wave plans: one 4-warp CTA per SM, floor(SMs / (kv heads x
+    // sequences)) partitions per sequence of ceil(max_seq_len / that) tokens
+    // (whole blocks).  Device time per call on GB300 (4 kv heads, head_dim
+    // 256) against the grid of 512- or 256-token partitions:
     //
-    // One sequence over kOneWaveMinLen tokens: its grid is known exactly, so
-    // it runs as ONE wave of one 4-warp CTA per SM (partitions x kv heads =
-    // SMs).  Fewer, longer CTAs pay a CTA's start-up and merge once per SM and
-    // leave fewer partials (GB300, 4 kv heads, head_dim 256, device time per
-    // call against AUTO's grid: 102400 tokens 70.5 -> 68.9 us, 262144: 174.4
-    // -> 161.6, 524288: 343.9 -> 305.0; 65536: 47.1 -> 45.5, 24000: 17.9 ->
-    // 14.1, 12000: 11.6 -> 9.7, 6000: 8.6 -> 8.3, 2048: 8.3 -> 6.5; the one
-    // length measured slower was 8192, 8.8 -> 9.2).  From 2048-token
-    // partitions on it is pooled (below); shorter ones measured no gain from
-    // pooling (16384 tokens: 11.3 fixed, 13.7 pooled).  A short call is bound
-    // by latency: one round of copies per CTA on every SM beats fewer CTAs
-    // with several (below).
-    //
-    // A batch whose sequences the caller states are all about max_seq_len long
-    // (PA_FLAG_UNIFORM_LENGTHS) takes the same decomposition: SMs / (kv heads x
-    // sequences) partitions per sequence, for any partition length.  Measured
-    // per call against the 512-token grid (GB300, 4 kv heads, head_dim 256,
-    // fixed partitions): 4 x 4096 tokens 14.5 -> 12.5 us, 4 x 16384 52.1 ->
-    // 46.0, 4 x 32768 85.7 -> 82.6, 2 x 65536 86.2 -> 82.4, 8 x 8192 51.7 ->
-    // 46.2, 16 x 16384 163.9 -> 158.4.  Without the statement the host cannot
-    // tell such a batch from one whose longest sequence stands alone (4 x
-    // [32768, 100, 100, 100]: 30.8 -> 47.1 us) or from lengths spread below
-    // the longest (8 x U[1, 8192]: 27.7 -> 37.7), so batches keep the grid.
-    //
-    // Short sequences (longer than one 512-token partition) take the one wave
-    // too, in any batch, when its partitions hold at most one round of copies
-    // of a 4-warp CTA (kOneWaveShortMaxPartition tokens): every CTA then ends
-    // after one round whatever the lengths, so an uneven batch costs nothing
-    // that the grid would save.  Device time per call against AUTO's grid:
-    // 2048 tokens 8.27 -> 6.48 us, 4096: 8.41 -> 7.61 (8192, with 224-token
-    // partitions, lost: 8.85 -> 9.29); 2 x 2048 8.72 -> 7.40, [2048, 40]
-    // 8.40 -> 7.40, 4 x 1024 9.27 -> 8.07, [1024, 50, 300, 700] 9.06 -> 7.80.
+    // * Up to kOneWaveMinLen tokens (one round of copies for a 4-warp CTA)
+    //   SINGLE needs no reduce and wins (64 tokens: 3.6 us against 5.6).
+    //   Above it SINGLE adds about a microsecond per copy round (512 tokens:
+    //   8.55 -> 5.87 us, 400: 7.81 -> 5.86, 300: 6.54 -> 5.83, 200: 5.81 ->
+    //   5.67).
+    // * One sequence over kOneWaveMinLen tokens: its grid is known exactly.
+    //   Fewer, longer CTAs pay a CTA's start-up and merge once per SM and
+    //   leave fewer partials (102400 tokens 70.5 -> 68.9 us, 262144: 174.4 ->
+    //   161.6, 524288: 343.9 -> 305.0; 65536: 47.1 -> 45.5, 24000: 17.9 ->
+    //   14.1, 12000: 11.6 -> 9.7, 6000: 8.6 -> 8.3, 2048: 8.3 -> 6.5; the one
+    //   length measured slower was 8192, 8.8 -> 9.2).  From 2048-token
+    //   partitions on it is pooled (below); shorter ones measured no gain
+    //   from pooling (16384 tokens: 11.3 fixed, 13.7 pooled).
+    // * Any batch whose partitions come to at most one round of copies
+    //   (kOneWaveShortMaxPartition tokens): every CTA ends after one round
+    //   whatever the lengths, so an uneven batch loses nothing the grid would
+    //   save (2 x 2048 8.72 -> 7.40, [2048, 40] 8.40 -> 7.40, 4 x 1024 9.27 ->
+    //   8.07, [1024, 50, 300, 700] 9.06 -> 7.80, 4 x 300 6.6 -> 6.0, 8 x 400
+    //   7.9 -> 6.8).
+    // * A batch whose sequences the caller states are all about max_seq_len
+    //   long (PA_FLAG_UNIFORM_LENGTHS), at any partition length (4 x 4096
+    //   14.5 -> 12.5 us, 4 x 16384 52.1 -> 46.0, 4 x 32768 85.7 -> 82.6, 2 x
+    //   65536 86.2 -> 82.4, 8 x 8192 51.7 -> 46.2, 16 x 16384 163.9 -> 158.4).
+    //   Without the statement the host cannot tell such a batch from one
+    //   whose longest sequence stands alone (4 x [32768, 100, 100, 100]: 30.8
+    //   -> 47.1 us) or whose lengths spread below the longest (8 x U[1, 8192]:
+    //   27.7 -> 37.7), so other batches keep the grid.
     bool one_wave = false, pool_one_wave = false;
     const int req_mode = o ? o->mode : PA_MODE_AUTO;
     const bool uniform = o && (o->flags & PA_FLAG_UNIFORM_LENGTHS);
