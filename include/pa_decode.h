@@ -191,10 +191,11 @@ typedef struct {
                                     one sequence over 128 tokens, as many partitions per kv head as SMs
                                     allow, one wave of one 4-warp CTA per SM (pooled from 2048-token
                                     partitions on, see PA_FLAG_POOLED; fixed below); for a batch whose
-                                    longest sequence is over 128 tokens, the same one wave when its
-                                    partitions come to at most 128 tokens (fixed), or at any length
-                                    with PA_FLAG_UNIFORM_LENGTHS.  AUTO runs SINGLE when the longest
-                                    sequence fits one partition of the plan, e.g. up to 128 tokens */
+                                    longest sequence is over 256 tokens, the same one wave when it gives
+                                    at least 4 partitions per sequence of at most 128 tokens (fixed),
+                                    or at any length with PA_FLAG_UNIFORM_LENGTHS.  AUTO runs SINGLE
+                                    when the longest sequence fits one partition of the plan, e.g.
+                                    up to 128 tokens, or up to 512 in larger batches */
     int flags;                   /* PA_FLAG_* */
     unsigned int wait_limit;     /* polls before a copy wait gives up; 0 = library default (2^20) */
     void* event_partition_begin; /* optional cudaEvent_t recorded on `stream` right before ... */

@@ -24,6 +24,7 @@ namespace {
 constexpr int kDefaultPartition = 512;
 constexpr int kOneWavePoolMinPartition = 2048;  // see make_plan
 constexpr int kOneWaveMinLen = 128;              // see make_plan
+constexpr int kOneWaveShortMinParts = 4;         // see make_plan
 constexpr int kOneWaveShortMaxPartition = 128;  // see make_plan
 // SM count assumed by pa_decode_workspace_size when no device answers (above any GPU's)
 constexpr int kMaxSmsBound = 1024;
@@ -222,12 +223,17 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     //   length measured slower was 8192, 8.8 -> 9.2).  From 2048-token
     //   partitions on it is pooled (below); shorter ones measured no gain
     //   from pooling (16384 tokens: 11.3 fixed, 13.7 pooled).
-    // * Any batch whose partitions come to at most one round of copies
+    // * A batch whose partitions come to at most one round of copies
     //   (kOneWaveShortMaxPartition tokens): every CTA ends after one round
     //   whatever the lengths, so an uneven batch loses nothing the grid would
     //   save (2 x 2048 8.72 -> 7.40, [2048, 40] 8.40 -> 7.40, 4 x 1024 9.27 ->
     //   8.07, [1024, 50, 300, 700] 9.06 -> 7.80, 4 x 300 6.6 -> 6.0, 8 x 400
-    //   7.9 -> 6.8).
+    //   7.9 -> 6.8), when it gives at least kOneWaveShortMinParts partitions
+    //   per sequence of sequences over 256 tokens (SINGLE would need three
+    //   copy rounds or more).  Below that, SINGLE, with no reduce, won (8 x
+    //   256 5.89 against 6.29 us, 16 x 200 5.99 against 6.95, 12 x 300 6.65
+    //   against 7.40, 16 x 129 5.33 against 6.77); the reduce's cost grows
+    //   with the batch.
     // * A batch whose sequences the caller states are all about max_seq_len
     //   long (PA_FLAG_UNIFORM_LENGTHS), at any partition length (4 x 4096
     //   14.5 -> 12.5 us, 4 x 16384 52.1 -> 46.0, 4 x 32768 85.7 -> 82.6, 2 x
@@ -247,7 +253,8 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
             const long long p1 = ((a->max_seq_len + per_seq - 1) / per_seq + bs - 1) / bs * bs;
             const bool one_seq = a->num_seqs == 1 && a->max_seq_len > kOneWaveMinLen;
             const bool stated = a->num_seqs > 1 && uniform;
-            const bool short_seq = a->max_seq_len > kOneWaveMinLen && p1 <= kOneWaveShortMaxPartition;
+            const bool short_seq = a->num_seqs > 1 && per_seq >= kOneWaveShortMinParts &&
+                                   a->max_seq_len > 2 * kOneWaveMinLen && p1 <= kOneWaveShortMaxPartition;
             if (one_seq || stated || short_seq) {
                 part = static_cast<int>(p1);
                 one_wave = true;

@@ -493,3 +493,11 @@ def test_short_sequence_runs_one_wave_of_one_block_deep_ctas(B, L, P, parts):
     # 128 tokens or fewer: one partition, no reduce
     rc, pl = plan_flags(args(max_seq_len=128, num_blocks=8), 0)
     assert pl["launch_reduce"] == 0 and pl["grid_x"] == 1
+
+
+@pytest.mark.parametrize("B,L", [(16, 200), (8, 256), (12, 300), (16, 129), (64, 512)])
+def test_larger_short_batches_keep_single_pass(B, L):
+    # fewer than 4 one-wave partitions per sequence, or sequences of at most
+    # 256 tokens: SINGLE (no reduce) measured faster than a one-wave split
+    rc, pl = plan_flags(args(num_seqs=B, max_seq_len=L, num_blocks=B * ((L + 15) // 16)), 0)
+    assert rc == pb.PA_OK and pl["mode"] == pb.PA_MODE_SINGLE and pl["launch_reduce"] == 0
