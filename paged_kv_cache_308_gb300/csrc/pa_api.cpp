@@ -82,6 +82,15 @@ int query_sm_count(int* num_sms) {
 // ones (more loads in flight per partial).  Two rather than four CTAs per
 // SM: b8_u8192 27.33 -> 27.05 us per call (128-wide slices instead of 64),
 // b4_l32768_peaked 85.26 -> 85.41 (64 instead of 32), the rest unchanged.
+// 4-warp CTAs per SM in a one-wave plan: enough to keep about 128 KB of
+// K/V copies in flight per SM whatever the head_dim (a 4 x 2 CTA keeps 8
+// blocks of K and V, 512 * head_dim bytes), since one SM's copies are
+// latency-bound.  With one CTA per SM, 102400 tokens at head_dim 128 (32/8
+// heads) streamed 5.1 TB/s and 131072 at head_dim 64 2.7 TB/s, against
+// 6.3 TB/s at 256.  Registers and shared memory allow it: at head_dim 128 a
+// CTA takes about 19K registers and 66 KB, at 64 about 14K and 34 KB.
+int one_wave_ctas_per_sm(int head_dim) { return head_dim >= 256 ? 1 : head_dim >= 128 ? 2 : 4; }
+
 int reduce_slice(int head_dim, long long pairs, int num_sms) {
     for (int w = head_dim; w > pa::kReduceMinSlice; w /= 2)
         if (pairs * (head_dim / w) >= 2ll * num_sms) return w;
@@ -247,8 +256,9 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
     const bool uniform = o && (o->flags & PA_FLAG_UNIFORM_LENGTHS);
     if (!(o && o->partition_size > 0) && !(o && (o->warps || o->stages)) && a->num_seqs > 0 &&
         (req_mode == PA_MODE_AUTO || req_mode == PA_MODE_SPLIT || req_mode == PA_MODE_FUSED)) {
-        // partitions of each sequence
-        const long long per_seq = (long long)num_sms / ((long long)a->num_kv_heads * a->num_seqs);
+        // partitions of each sequence: one wave of one_wave_slots CTAs
+        const long long per_seq =
+            (long long)num_sms * one_wave_ctas_per_sm(a->head_dim) / ((long long)a->num_kv_heads * a->num_seqs);
         if (per_seq >= 2) {
             const long long p1 = ((a->max_seq_len + per_seq - 1) / per_seq + bs - 1) / bs * bs;
             const bool one_seq = a->num_seqs == 1 && a->max_seq_len > kOneWaveMinLen;
@@ -1045,13 +1055,14 @@ size_t pa_decode_workspace_size(int num_seqs, int max_seq_len, int num_heads, in
         return split_workspace_bytes(num_seqs, num_heads, (max_seq_len + partition_size - 1) / partition_size,
                                      head_dim);
     // 0: the most partials an automatic plan makes per (sequence, head):
-    // partitions of kDefaultPartition / 2 tokens, or a one-wave plan's (one
-    // CTA per SM, so at most SMs partitions, each of at least one block)
+    // partitions of kDefaultPartition / 2 tokens, or a one-wave plan's (at
+    // most 4 CTAs per SM, so at most 4 x SMs partitions, each of at least
+    // one block)
     long long parts = (max_seq_len + kDefaultPartition / 2 - 1) / (kDefaultPartition / 2);
     int num_sms = 0;
     if (query_sm_count(&num_sms) != PA_OK || num_sms <= 0) num_sms = kMaxSmsBound;
     const long long one_wave = (max_seq_len + pa::kBlockSize - 1) / pa::kBlockSize;
-    parts = std::max(parts, std::min(one_wave, (long long)num_sms));
+    parts = std::max(parts, std::min(one_wave, (long long)num_sms * one_wave_ctas_per_sm(head_dim)));
     return split_workspace_bytes(num_seqs, num_heads, static_cast<int>(parts), head_dim);
 }
 

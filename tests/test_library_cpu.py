@@ -501,3 +501,16 @@ def test_larger_short_batches_keep_single_pass(B, L):
     # 256 tokens: SINGLE (no reduce) measured faster than a one-wave split
     rc, pl = plan_flags(args(num_seqs=B, max_seq_len=L, num_blocks=B * ((L + 15) // 16)), 0)
     assert rc == pb.PA_OK and pl["mode"] == pb.PA_MODE_SINGLE and pl["launch_reduce"] == 0
+
+
+@pytest.mark.parametrize("H,Hkv,D,L,per_seq,P,pooled", [(32, 8, 128, 102400, 38, 2704, 1), (32, 4, 64, 131072, 152, 864, 0),
+                                                         (16, 2, 256, 102400, 76, 1360, 0), (8, 8, 128, 65536, 38, 1728, 0)])
+def test_one_wave_keeps_copies_in_flight_at_every_head_dim(H, Hkv, D, L, per_seq, P, pooled):
+    # 256 / head_dim 4-warp CTAs per SM (1 at 256, 2 at 128, 4 at 64): about
+    # 128 KB of K/V copies in flight per SM whatever the head_dim
+    a = args(max_seq_len=L, H=H, Hkv=Hkv, D=D, num_blocks=(L + 15) // 16)
+    rc, pl = plan_flags(a, 0)
+    assert rc == pb.PA_OK
+    assert (pl["grid_x"], pl["grid_y"]) == (per_seq, Hkv) and pl["partition_size"] == P and pl["pooled"] == pooled
+    assert pl["grid_x"] * pl["grid_y"] == SMS * (256 // D) or pl["grid_x"] * P >= L
+    assert pb.pa_decode_workspace_size(1, L, H, D, 0) >= pl["workspace_bytes"]
