@@ -114,7 +114,9 @@ enum {
                               log-sum-exp reduce.  The host never reads the lengths, so the call is
                               graph-safe.  The workspace also holds the work list, the counter,
                               the order and the sizes (rewritten by every call) */
-    PA_MODE_FLAT = 5    /* one wave of one CTA per SM, num_SMs / num_kv_heads CTAs per kv head:
+    PA_MODE_FLAT = 5    /* one wave of 256 / head_dim CTAs per SM (one at head_dim 256, so that
+                           about 128 KB of copies are in flight per SM), that many times num_SMs /
+                           num_kv_heads CTAs per kv head:
                            every CTA reads the lengths on the device and streams an equal share
                            (to within one block) of the batch's concatenated blocks, one partial
                            per sequence its share meets, then the log-sum-exp reduce; no ragged

@@ -310,9 +310,11 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
                                                                   pa::persistent_seq_cache_bytes(a->num_seqs)
                                                             : pa::partition_smem_bytes(a->head_dim, warps, stages);
     if (flat) {
-        // one CTA per SM: C CTAs per kv head, each streaming an equal share
+        // one wave (one CTA per SM at head_dim 256, more below it, as for the
+        // one-wave plans): C CTAs per kv head, each streaming an equal share
         // of the batch's blocks (the share is fixed on the device)
-        const int C = num_sms / a->num_kv_heads > 0 ? num_sms / a->num_kv_heads : 1;
+        const int slots = num_sms * one_wave_ctas_per_sm(a->head_dim);
+        const int C = slots / a->num_kv_heads > 0 ? slots / a->num_kv_heads : 1;
         plan->grid_x = C * a->num_kv_heads;
         plan->grid_y = plan->grid_z = 1;
         plan->partition_size = 0;
