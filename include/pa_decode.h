@@ -149,7 +149,7 @@ enum {
                                     resets them to zero instead).  Stale bytes left by other calls
                                     are therefore tolerated: this library's partials (bounded by
                                     the fp16 inputs), tickets and work lists never hold the tag.
-                                    The planner's one-wave plan for one long sequence is pooled
+                                    The planner's one-wave plan for one sequence is pooled from 2048-token partitions on
                                     without this flag.  Source of the split it refines: "docs"
                                     commit page, GQA-aware grid and partition paragraphs */
     PA_FLAG_DETERMINISTIC = 8,   /* never pool (not even the one-wave plan): each partial covers
