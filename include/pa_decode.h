@@ -149,9 +149,10 @@ enum {
                                     resets them to zero instead).  Stale bytes left by other calls
                                     are therefore tolerated: this library's partials (bounded by
                                     the fp16 inputs), tickets and work lists never hold the tag.
-                                    The planner's one-wave plan for one sequence is pooled from 2048-token partitions on
-                                    without this flag.  Source of the split it refines: "docs"
-                                    commit page, GQA-aware grid and partition paragraphs */
+                                    The planner's one-wave plan for one sequence is pooled without
+                                    this flag from 2048-token partitions on.  Source of the split it
+                                    refines: "docs" commit page, GQA-aware grid and partition
+                                    paragraphs */
     PA_FLAG_DETERMINISTIC = 8,   /* never pool (not even the one-wave plan): each partial covers
                                     fixed blocks, so repeated calls give identical bits */
     PA_FLAG_UNIFORM_LENGTHS = 16 /* AUTO/SPLIT/FUSED without a partition size or CTA shape: the
