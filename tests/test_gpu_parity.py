@@ -710,3 +710,19 @@ def test_uniform_lengths_flag_on_the_peaked_workload(dev):
     torch.cuda.synchronize()
     assert pb.pa_get_device_status() == 0
     assert_parity(out, oracle_ref(w), "b4_l32768_peaked, uniform-lengths plan")
+
+
+@pytest.mark.parametrize("H,Hkv,D,L,pooled", [(32, 8, 128, 102400, 1), (32, 4, 64, 131072, 0), (64, 8, 128, 50000, 0)])
+def test_one_wave_at_smaller_head_dims(dev, H, Hkv, D, L, pooled):
+    # the one-wave plan runs 256 / head_dim CTAs per SM (2 at 128, 4 at 64);
+    # at 32/8 heads and 102400 tokens its 2704-token partitions are pooled
+    w = W.make_workload("hd", [L], num_heads=H, num_kv_heads=Hkv, head_dim=D, num_blocks=(L + 15) // 16 + 4,
+                        seed=H + D, device=dev, scale=D ** -0.5, tail_fill=float("nan"))
+    plan = pb.pa_decode_plan(torch.empty_like(w.q), w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                             w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, w.scale,
+                             max_seq_len=w.max_seq_len)
+    assert plan["grid_x"] * plan["grid_y"] == 152 * (256 // D) and plan["pooled"] == pooled
+    out = pb.decode_workload(w)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    assert_parity(out, oracle_ref(w), f"one wave, H={H} Hkv={Hkv} D={D} L={L}")
