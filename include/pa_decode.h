@@ -158,10 +158,11 @@ enum {
     PA_FLAG_UNIFORM_LENGTHS = 16 /* AUTO/SPLIT/FUSED without a partition size or CTA shape: the
                                     caller states that the batch's sequences are all about
                                     max_seq_len long.  The planner then gives the batch the
-                                    one-wave decomposition it gives a single sequence: one 4-warp
-                                    CTA per SM, floor(SMs / (kv heads x sequences)) partitions per
-                                    sequence of ceil(max_seq_len / that) tokens (rounded up to
-                                    whole blocks), when that is at least 2; fixed partitions.
+                                    one-wave decomposition it gives a single sequence: 256 /
+                                    head_dim 4-warp CTAs per SM (one at head_dim 256), floor(SMs x
+                                    that / (kv heads x sequences)) partitions per sequence of
+                                    ceil(max_seq_len / that) tokens (rounded up to whole blocks),
+                                    when that is at least 2; fixed partitions.
                                     Any lengths stay correct; a batch in which a few sequences are
                                     much longer than the rest runs slower than without the flag
                                     (their partitions get only their share of the SMs) */
@@ -191,8 +192,9 @@ typedef struct {
     int mode;                    /* PA_MODE_* */
     int partition_size;          /* tokens per partition in SPLIT mode, multiple of block_size; 0 = chosen
                                     by the planner: 512 (256 when that gives fewer CTAs than SMs); for
-                                    one sequence over 128 tokens, as many partitions per kv head as SMs
-                                    allow, one wave of one 4-warp CTA per SM (pooled from 2048-token
+                                    one sequence over 128 tokens, one wave of 256 / head_dim 4-warp
+                                    CTAs per SM (one at head_dim 256), as many partitions per kv head
+                                    as that gives (pooled from 2048-token
                                     partitions on, see PA_FLAG_POOLED; fixed below); for a batch whose
                                     longest sequence is over 256 tokens, the same one wave when it gives
                                     at least 4 partitions per sequence of at most 128 tokens (fixed),
@@ -211,15 +213,17 @@ typedef struct {
 
 /* What a call will launch (filled by pa_decode_plan; host-only, no CUDA calls). */
 typedef struct {
-    int mode;              /* PA_MODE_SINGLE, PA_MODE_SPLIT, PA_MODE_FUSED or PA_MODE_PERSISTENT */
+    int mode;              /* PA_MODE_SINGLE, _SPLIT, _FUSED, _PERSISTENT or _FLAT */
     int partition_size;    /* tokens per CTA (SINGLE: max_seq_len rounded up to block_size;
-                              PERSISTENT: 0 = apportioned per sequence on the device) */
+                              PERSISTENT: 0 = apportioned per sequence on the device; FLAT: 0,
+                              each CTA's share is fixed on the device) */
     int grid_x, grid_y, grid_z;          /* partition kernel: partitions, kv heads, sequences
-                                            (PERSISTENT: the fixed grid, 1, 1) */
+                                            (PERSISTENT and FLAT: the fixed grid, 1, 1) */
     int threads;           /* threads per partition CTA */
     int smem_bytes;        /* dynamic shared memory per partition CTA */
     int launch_reduce;     /* 1 if the reduce kernel runs */
-    int reduce_grid_x, reduce_grid_y, reduce_grid_z; /* heads, sequences, head_dim/32 */
+    int reduce_grid_x, reduce_grid_y, reduce_grid_z; /* heads, sequences, head_dim / slice
+                                                        width (32..256, about 2 CTAs per SM) */
     size_t workspace_bytes; /* caller workspace pa_decode_ex needs (0 when there are no partials) */
     int stages;            /* shared-memory stages per warp of the partition CTA */
     int max_partitions;    /* partials kept per (sequence, head) in the workspace */
