@@ -198,7 +198,6 @@ __device__ __forceinline__ void fused_combine(const PartitionParams& prm, int b,
         float m = -INFINITY, wsum = 0.f;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
         auto fold = [&](float mp, float lp, float4 t) {
-            if (mp == -INFINITY) return;  // an empty partial weighs nothing (its O is not used)
             const float mn = fmaxf(m, mp);
             const float alpha = exp2f(m - mn);  // 0 on the first partition (m = -inf)
             const float beta = lp * exp2f(mp - mn);
@@ -844,7 +843,6 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
     float m = -INFINITY, wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     auto fold = [&](float mp, float lp, const float4& t) {
-        if (mp == -INFINITY) return;  // an empty partial weighs nothing (its O is not used)
         const float mn = fmaxf(m, mp);
         const float alpha = exp2f(m - mn);  // 0 on the first partition (m = -inf)
         const float beta = lp * exp2f(mp - mn);

@@ -192,28 +192,3 @@ def test_split_kv_decode_through_nccl(dev):
         assert_parity(out, oracle_ref(w), "split_kv_decode over NCCL")
     finally:
         dist.destroy_process_group()
-
-
-def test_merge_skips_an_empty_partial(dev):
-    # synthetic partials (max in base 2, exp sum, normalised weighted V) of one
-    # source; partition 2 is empty (-inf, 0, and a NaN O that must not be read):
-    # the merge is the log-sum-exp merge of the other three
-    H, D, P, n = 2, 64, 16, 4
-    rng = np.random.default_rng(41)
-    m = rng.normal(0, 3, (1, 1, H, n)).astype(np.float32)
-    l = rng.uniform(0.5, 20, (1, 1, H, n)).astype(np.float32)
-    acc = rng.normal(0, 1, (1, 1, H, n, D)).astype(np.float32)
-    m[..., 2], l[..., 2], acc[..., 2, :] = -np.inf, 0.0, np.nan
-    keep = [0, 1, 3]
-    mk, lk, ak = m[0, 0][:, keep].astype(np.float64), l[0, 0][:, keep].astype(np.float64), acc[0, 0][:, keep].astype(np.float64)
-    w = lk * np.exp2(mk - mk.max(axis=1, keepdims=True))
-    want = (w[..., None] * ak).sum(axis=1) / w.sum(axis=1, keepdims=True)
-    gm, gl, gacc = (torch.from_numpy(x).to(dev) for x in (m, l, acc))
-    seq_lens = torch.tensor([n * P], dtype=torch.int32, device=dev)
-    out = torch.full((1, H, D), float("nan"), dtype=torch.float16, device=dev)
-    pb.pa_merge_partials(out, gm, gl, gacc, seq_lens, H, D, P, 1, n, max_seq_len=n * P)
-    torch.cuda.synchronize()
-    assert pb.pa_get_device_status() == 0
-    got = out[0].float().cpu().numpy()
-    assert np.all(np.isfinite(got))
-    assert np.all(np.abs(got - want) <= 2e-3 + 1e-2 * np.abs(want)), np.abs(got - want).max()
