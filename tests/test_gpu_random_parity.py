@@ -142,3 +142,30 @@ def test_random_short_auto_case(dev, i):
     assert pb.pa_get_device_status() == 0
     assert_parity(out, oracle_ref(w), f"short case {i}: {c}")
     assert all(torch.count_nonzero(out[b]) == 0 for b, L in enumerate(c["lens"]) if L == 0)
+
+
+def draw_large_case(i):
+    # AUTO at realistic sizes: one-wave plans at 1, 2 or 4 CTAs per SM
+    # (head_dim 256, 128, 64), pooled and fixed, and the grid for batches
+    r = random.Random(9000 + i)
+    hkv = r.choice([1, 2, 4, 8])
+    g = r.choice([1, 4, 6, 8])
+    d = r.choice([64, 128, 256])
+    b = r.choice([1, 1, 2, 4, 16, 48])
+    cap = max(16, (400_000_000 // (4 * hkv * d)) // b)  # about 400 MB of K/V at most
+    lens = [min(cap, int(round(2 ** r.uniform(10, 17)))) for _ in range(b)]
+    return dict(lens=lens, num_heads=hkv * g, num_kv_heads=hkv, head_dim=d, seed=900 + i)
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_random_large_auto_case(dev, i):
+    c = draw_large_case(i)
+    blocks = sum((L + 15) // 16 for L in c["lens"]) + 3
+    w = W.make_workload(f"large{i}", c["lens"], num_heads=c["num_heads"], num_kv_heads=c["num_kv_heads"],
+                        head_dim=c["head_dim"], num_blocks=blocks, seed=c["seed"], device=dev,
+                        scale=c["head_dim"] ** -0.5, tail_fill=float("nan"))
+    out = pb.decode_workload(w)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    assert_parity(out, oracle_ref(w), f"large case {i}: B={len(c['lens'])} max={max(c['lens'])} "
+                                      f"H={c['num_heads']}/{c['num_kv_heads']} D={c['head_dim']}")
