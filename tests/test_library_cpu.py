@@ -514,3 +514,24 @@ def test_one_wave_keeps_copies_in_flight_at_every_head_dim(H, Hkv, D, L, per_seq
     assert (pl["grid_x"], pl["grid_y"]) == (per_seq, Hkv) and pl["partition_size"] == P and pl["pooled"] == pooled
     assert pl["grid_x"] * pl["grid_y"] == SMS * (256 // D) or pl["grid_x"] * P >= L
     assert pb.pa_decode_workspace_size(1, L, H, D, 0) >= pl["workspace_bytes"]
+
+
+def test_workspace_bound_covers_every_automatic_plan_property():
+    # pa_decode_workspace_size(..., 0) is documented as an upper bound for any
+    # automatic plan (one-wave plans, PA_FLAG_UNIFORM_LENGTHS and the pooled
+    # counters included): random shapes, AUTO and SPLIT, with and without flags
+    import random
+    r = random.Random(11)
+    for _ in range(3000):
+        hkv = r.choice([1, 2, 4, 8])
+        H = hkv * r.choice([1, 2, 3, 4, 6, 8])
+        D = r.choice([64, 128, 256])
+        B = r.choice([1, 1, 2, 3, 4, 8, 16, 64, 300])
+        L = r.choice([1, 16, 100, 129, 257, 512, 513, 2048, 4864, 8192, 30000, 102400, 524288, r.randint(1, 200000)])
+        flags = r.choice([0, pb.PA_FLAG_UNIFORM_LENGTHS, pb.PA_FLAG_POOLED, pb.PA_FLAG_DETERMINISTIC])
+        mode = r.choice([0, pb.PA_MODE_SPLIT])
+        a = args(num_seqs=B, max_seq_len=L, H=H, Hkv=hkv, D=D, num_blocks=max(1, min(B * ((L + 15) // 16), (1 << 31) // (hkv * 16) - 1)))
+        rc, pl = plan_flags(a, flags, mode=mode)
+        if rc != pb.PA_OK:
+            continue
+        assert pb.pa_decode_workspace_size(B, L, H, D, 0) >= pl["workspace_bytes"], (B, L, H, hkv, D, flags, mode, pl)
