@@ -726,3 +726,37 @@ def test_one_wave_at_smaller_head_dims(dev, H, Hkv, D, L, pooled):
     torch.cuda.synchronize()
     assert pb.pa_get_device_status() == 0
     assert_parity(out, oracle_ref(w), f"one wave, H={H} Hkv={Hkv} D={D} L={L}")
+
+
+@pytest.mark.parametrize("lens,flags", [([2048, 700, 1500], 0), ([4000] * 4, pb.PA_FLAG_UNIFORM_LENGTHS),
+                                        ([3000], 0), ([90000], 0)])
+def test_one_wave_plans_replay_from_a_graph_with_new_lengths(dev, lens, flags):
+    # the host never reads the lengths: a captured one-wave call (short batch,
+    # uniform-lengths batch, short and long single sequences) replays with
+    # other lengths under the same bound and matches the oracle
+    w = W.make_workload("owgraph", lens, num_blocks=sum((L + 15) // 16 for L in lens) + 5, seed=len(lens) + lens[0],
+                        device=dev, tail_fill=float("nan"))
+    out = torch.full_like(w.q, float("nan"))
+    kw = dict(max_seq_len=w.max_seq_len, flags=flags)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, **kw)
+    assert plan["threads"] == 128 and plan["launch_reduce"] == 1
+    ws = pb.alloc_workspace(plan, dev)
+    args = (out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads, w.num_kv_heads, w.head_dim,
+            w.block_size, w.scale)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pb.pa_decode_ex(*args, s, workspace=ws, **kw)  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pb.pa_decode_ex(*args, torch.cuda.current_stream(), workspace=ws, **kw)
+    for new in ([L // 3 for L in lens], [max(0, L - 17) for L in lens], lens):
+        w.seq_lens.copy_(torch.tensor(new, dtype=torch.int32, device=dev))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert pb.pa_get_device_status() == 0
+        assert_parity(out, oracle_ref(w), f"graph replay, lengths {new}")
