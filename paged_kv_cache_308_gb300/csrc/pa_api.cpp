@@ -196,6 +196,66 @@ void choose_shape(const pa_decode_args* a, const pa_decode_plan_t* plan, int num
     *stages = kShapes[pick].stages;
 }
 
+// One-wave plans: 256 / head_dim 4-warp CTAs per SM (one_wave_ctas_per_sm),
+// floor(SMs x that / (kv heads x sequences)) partitions per sequence of
+// ceil(max_seq_len / that) tokens (whole blocks).  Device time per call on GB300 (4 kv heads, head_dim
+// 256) against the grid of 512- or 256-token partitions:
+//
+// * Up to kOneWaveMinLen tokens (one round of copies for a 4-warp CTA)
+//   SINGLE needs no reduce and wins (64 tokens: 3.6 us against 5.6).
+//   Above it SINGLE adds about a microsecond per copy round (512 tokens:
+//   8.55 -> 5.87 us, 400: 7.81 -> 5.86, 300: 6.54 -> 5.83, 200: 5.81 ->
+//   5.67).
+// * One sequence over kOneWaveMinLen tokens: its grid is known exactly.
+//   Fewer, longer CTAs pay a CTA's start-up and merge once per SM and
+//   leave fewer partials (102400 tokens 70.5 -> 68.9 us, 262144: 174.4 ->
+//   161.6, 524288: 343.9 -> 305.0; 65536: 47.1 -> 45.5, 24000: 17.9 ->
+//   14.1, 12000: 11.6 -> 9.7, 6000: 8.6 -> 8.3, 2048: 8.3 -> 6.5; the one
+//   length measured slower was 8192, 8.8 -> 9.2).  From 2048-token
+//   partitions on it is pooled (below); shorter ones measured no gain
+//   from pooling (16384 tokens: 11.3 fixed, 13.7 pooled).
+// * A batch whose partitions come to at most one round of copies
+//   (kOneWaveShortMaxPartition tokens): every CTA ends after one round
+//   whatever the lengths, so an uneven batch loses nothing the grid would
+//   save (2 x 2048 8.72 -> 7.40, [2048, 40] 8.40 -> 7.40, 4 x 1024 9.27 ->
+//   8.07, [1024, 50, 300, 700] 9.06 -> 7.80, 4 x 300 6.6 -> 6.0, 8 x 400
+//   7.9 -> 6.8), when it gives at least kOneWaveShortMinParts partitions
+//   per sequence of sequences over 256 tokens (SINGLE would need three
+//   copy rounds or more).  Below that, SINGLE, with no reduce, won (8 x
+//   256 5.89 against 6.29 us, 16 x 200 5.99 against 6.95, 12 x 300 6.65
+//   against 7.40, 16 x 129 5.33 against 6.77); the reduce's cost grows
+//   with the batch.
+// * A batch whose sequences the caller states are all about max_seq_len
+//   long (PA_FLAG_UNIFORM_LENGTHS), at any partition length (4 x 4096
+//   14.5 -> 12.5 us, 4 x 16384 52.1 -> 46.0, 4 x 32768 85.7 -> 82.6, 2 x
+//   65536 86.2 -> 82.4, 8 x 8192 51.7 -> 46.2, 16 x 16384 163.9 -> 158.4).
+//   Without the statement the host cannot tell such a batch from one
+//   whose longest sequence stands alone (4 x [32768, 100, 100, 100]: 30.8
+//   -> 47.1 us) or whose lengths spread below the longest (8 x U[1, 8192]:
+//   27.7 -> 37.7), so other batches keep the grid.
+// Returns true and sets *part (and *pool) when the call takes a one-wave
+// plan; the caller has left partition_size and the CTA shape to the library.
+bool one_wave_partition(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, int* part, bool* pool) {
+    const int req_mode = o ? o->mode : PA_MODE_AUTO;
+    if (a->num_seqs <= 0 || !(req_mode == PA_MODE_AUTO || req_mode == PA_MODE_SPLIT || req_mode == PA_MODE_FUSED))
+        return false;
+    // partitions of each sequence: one wave of 256 / head_dim CTAs per SM
+    const long long per_seq =
+        (long long)num_sms * one_wave_ctas_per_sm(a->head_dim) / ((long long)a->num_kv_heads * a->num_seqs);
+    if (per_seq < 2) return false;
+    const int bs = a->block_size;
+    const long long p1 = ((a->max_seq_len + per_seq - 1) / per_seq + bs - 1) / bs * bs;
+    const bool uniform = o && (o->flags & PA_FLAG_UNIFORM_LENGTHS);
+    const bool one_seq = a->num_seqs == 1 && a->max_seq_len > kOneWaveMinLen;
+    const bool stated = a->num_seqs > 1 && uniform;
+    const bool short_seq = a->num_seqs > 1 && per_seq >= kOneWaveShortMinParts &&
+                           a->max_seq_len > 2 * kOneWaveMinLen && p1 <= kOneWaveShortMaxPartition;
+    if (!(one_seq || stated || short_seq)) return false;
+    *part = static_cast<int>(p1);
+    *pool = one_seq && p1 >= kOneWavePoolMinPartition;
+    return true;
+}
+
 int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_decode_plan_t* plan) {
     int rc = validate(a, o);
     if (rc) return rc;
@@ -214,64 +274,10 @@ int make_plan(const pa_decode_args* a, const pa_decode_opts* o, int num_sms, pa_
                                a->num_kv_heads * a->num_seqs;
         if (ctas < num_sms) part = kDefaultPartition / 2;
     }
-    // One-wave plans: one 4-warp CTA per SM, floor(SMs / (kv heads x
-    // sequences)) partitions per sequence of ceil(max_seq_len / that) tokens
-    // (whole blocks).  Device time per call on GB300 (4 kv heads, head_dim
-    // 256) against the grid of 512- or 256-token partitions:
-    //
-    // * Up to kOneWaveMinLen tokens (one round of copies for a 4-warp CTA)
-    //   SINGLE needs no reduce and wins (64 tokens: 3.6 us against 5.6).
-    //   Above it SINGLE adds about a microsecond per copy round (512 tokens:
-    //   8.55 -> 5.87 us, 400: 7.81 -> 5.86, 300: 6.54 -> 5.83, 200: 5.81 ->
-    //   5.67).
-    // * One sequence over kOneWaveMinLen tokens: its grid is known exactly.
-    //   Fewer, longer CTAs pay a CTA's start-up and merge once per SM and
-    //   leave fewer partials (102400 tokens 70.5 -> 68.9 us, 262144: 174.4 ->
-    //   161.6, 524288: 343.9 -> 305.0; 65536: 47.1 -> 45.5, 24000: 17.9 ->
-    //   14.1, 12000: 11.6 -> 9.7, 6000: 8.6 -> 8.3, 2048: 8.3 -> 6.5; the one
-    //   length measured slower was 8192, 8.8 -> 9.2).  From 2048-token
-    //   partitions on it is pooled (below); shorter ones measured no gain
-    //   from pooling (16384 tokens: 11.3 fixed, 13.7 pooled).
-    // * A batch whose partitions come to at most one round of copies
-    //   (kOneWaveShortMaxPartition tokens): every CTA ends after one round
-    //   whatever the lengths, so an uneven batch loses nothing the grid would
-    //   save (2 x 2048 8.72 -> 7.40, [2048, 40] 8.40 -> 7.40, 4 x 1024 9.27 ->
-    //   8.07, [1024, 50, 300, 700] 9.06 -> 7.80, 4 x 300 6.6 -> 6.0, 8 x 400
-    //   7.9 -> 6.8), when it gives at least kOneWaveShortMinParts partitions
-    //   per sequence of sequences over 256 tokens (SINGLE would need three
-    //   copy rounds or more).  Below that, SINGLE, with no reduce, won (8 x
-    //   256 5.89 against 6.29 us, 16 x 200 5.99 against 6.95, 12 x 300 6.65
-    //   against 7.40, 16 x 129 5.33 against 6.77); the reduce's cost grows
-    //   with the batch.
-    // * A batch whose sequences the caller states are all about max_seq_len
-    //   long (PA_FLAG_UNIFORM_LENGTHS), at any partition length (4 x 4096
-    //   14.5 -> 12.5 us, 4 x 16384 52.1 -> 46.0, 4 x 32768 85.7 -> 82.6, 2 x
-    //   65536 86.2 -> 82.4, 8 x 8192 51.7 -> 46.2, 16 x 16384 163.9 -> 158.4).
-    //   Without the statement the host cannot tell such a batch from one
-    //   whose longest sequence stands alone (4 x [32768, 100, 100, 100]: 30.8
-    //   -> 47.1 us) or whose lengths spread below the longest (8 x U[1, 8192]:
-    //   27.7 -> 37.7), so other batches keep the grid.
+    // one-wave plans (see one_wave_partition)
     bool one_wave = false, pool_one_wave = false;
-    const int req_mode = o ? o->mode : PA_MODE_AUTO;
-    const bool uniform = o && (o->flags & PA_FLAG_UNIFORM_LENGTHS);
-    if (!(o && o->partition_size > 0) && !(o && (o->warps || o->stages)) && a->num_seqs > 0 &&
-        (req_mode == PA_MODE_AUTO || req_mode == PA_MODE_SPLIT || req_mode == PA_MODE_FUSED)) {
-        // partitions of each sequence: one wave of one_wave_slots CTAs
-        const long long per_seq =
-            (long long)num_sms * one_wave_ctas_per_sm(a->head_dim) / ((long long)a->num_kv_heads * a->num_seqs);
-        if (per_seq >= 2) {
-            const long long p1 = ((a->max_seq_len + per_seq - 1) / per_seq + bs - 1) / bs * bs;
-            const bool one_seq = a->num_seqs == 1 && a->max_seq_len > kOneWaveMinLen;
-            const bool stated = a->num_seqs > 1 && uniform;
-            const bool short_seq = a->num_seqs > 1 && per_seq >= kOneWaveShortMinParts &&
-                                   a->max_seq_len > 2 * kOneWaveMinLen && p1 <= kOneWaveShortMaxPartition;
-            if (one_seq || stated || short_seq) {
-                part = static_cast<int>(p1);
-                one_wave = true;
-                pool_one_wave = one_seq && p1 >= kOneWavePoolMinPartition;
-            }
-        }
-    }
+    if (!(o && o->partition_size > 0) && !(o && (o->warps || o->stages)))
+        one_wave = one_wave_partition(a, o, num_sms, &part, &pool_one_wave);
     const int split_parts = (a->max_seq_len + part - 1) / part;
     int mode = o ? o->mode : PA_MODE_AUTO;
     if (mode == PA_MODE_AUTO) {
