@@ -4,7 +4,8 @@ Each case draws a batch of sequences with context lengths (0, inside a block,
 on a block boundary, a few blocks) and chunk lengths (1 to a few query
 tiles), a GQA ratio and a head_dim, and runs both prefix kernels (tcgen05 and
 warp-level MMA) through the C ABI; every output element is compared with the
-oracle.  The draws come from a fixed seed.
+oracle.  A second sweep runs the key split (pa_prefix_split) with random
+forced splits.  The draws come from a fixed seed.
 """
 import os
 import random
@@ -52,3 +53,25 @@ def test_random_prefix_case(dev, i, flags):
                                   host_bits(w.query_start_loc), w.num_heads, w.num_kv_heads, w.head_dim,
                                   w.block_size, w.scale, threads=THREADS)
     assert_parity(out, ref, f"prefix case {i}: {c}")
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_prefix_split_case(dev, i):
+    # the key split (pa_prefix_split) on the same kind of draws, with a forced
+    # split: a random number of key ranges for a random run of trailing tiles
+    c = draw_case(100 + i)
+    r = random.Random(3000 + i)
+    w = W.make_prefix_workload(f"psplit{i}", c["ctx"], c["ql"], num_heads=c["num_heads"],
+                               num_kv_heads=c["num_kv_heads"], head_dim=c["head_dim"], seed=c["seed"], device=dev,
+                               tail_fill=float("nan"))
+    tile_tokens = 128 // (w.num_heads // w.num_kv_heads)
+    n = -(-w.max_query_len // tile_tokens) * w.num_kv_heads * len(c["ql"])
+    parts, units = r.randint(1, 9), r.randint(1, n)
+    out = pb.prefix_split_workload(w, parts=parts, units=units)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    ref = oracle.prefix_attention(host_bits(w.q), host_bits(w.k_new), host_bits(w.v_new), host_bits(w.k_cache),
+                                  host_bits(w.v_cache), host_bits(w.block_tables), host_bits(w.context_lens),
+                                  host_bits(w.query_start_loc), w.num_heads, w.num_kv_heads, w.head_dim,
+                                  w.block_size, w.scale, threads=THREADS)
+    assert_parity(out, ref, f"prefix split case {i}: {c} parts={parts} units={units} of {n}")
