@@ -155,7 +155,7 @@ enum {
                                     paragraphs */
     PA_FLAG_DETERMINISTIC = 8,   /* never pool (not even the one-wave plan): each partial covers
                                     fixed blocks, so repeated calls give identical bits */
-    PA_FLAG_UNIFORM_LENGTHS = 16 /* AUTO/SPLIT/FUSED without a partition size or CTA shape: the
+    PA_FLAG_UNIFORM_LENGTHS = 16, /* AUTO/SPLIT/FUSED without a partition size or CTA shape: the
                                     caller states that the batch's sequences are all about
                                     max_seq_len long.  The planner then gives the batch the
                                     one-wave decomposition it gives a single sequence: 256 /
@@ -166,6 +166,12 @@ enum {
                                     Any lengths stay correct; a batch in which a few sequences are
                                     much longer than the rest runs slower than without the flag
                                     (their partitions get only their share of the SMs) */
+    PA_FLAG_PREFIX_GRID = 32     /* pa_prefix_ex / pa_prefix_split, tcgen05 kernel: one CTA per
+                                    query tile (and key-split part) instead of the default
+                                    persistent form, in which a grid of the CTAs the SMs hold at
+                                    once claims the tiles in grid order from a device counter and
+                                    each CTA's copy rings run on from one tile to the next.  Both
+                                    forms compute every tile alike, so they give the same bits */
 };
 
 /* All inputs of one decode call (device pointers; see the layouts above). */
@@ -302,7 +308,8 @@ const char* pa_status_string(int status);
 /* Free the library-owned workspaces of every device (synchronises them, then
  * restores the current device).  The counterpart of the allocate-once cache of
  * the "qwen3_6_scripts/paged_attn.py" commit page's buffer-reuse paragraphs: the
- * next pa_decode allocates again.  Never frees caller memory. */
+ * next pa_decode allocates again.  Also frees the persistent prefill's counter
+ * (the next pa_prefix allocates it again).  Never frees caller memory. */
 void pa_release_workspace(void);
 
 /* Chunked-prefill ("prefix") attention over the paged cache.
@@ -320,8 +327,17 @@ void pa_release_workspace(void);
  * caches and block table as for pa_decode.  max_context_len and max_query_len
  * are host-side bounds that size the grid.  The new tokens' K/V are read from
  * k_new/v_new, not from the cache (the caller appends them afterwards).
- * Same support, alignment, ownership and error rules as pa_decode; allocates
- * nothing.  Device-detected bad lengths set PA_DEV_BAD_SEQ_LEN. */
+ * Same support, alignment, ownership and error rules as pa_decode.
+ * Device-detected bad lengths set PA_DEV_BAD_SEQ_LEN.
+ * The tensor-core kernel runs in a persistent form by default: a grid of the
+ * CTAs the SMs hold at once claims the query tiles in grid order from a
+ * library-owned device counter (256 bytes per device, allocated and zeroed by
+ * the first such call on the device, re-armed by every call, freed by
+ * pa_release_workspace), and each CTA's copy rings run on from one tile to
+ * the next.  A call made while its stream is being captured before that
+ * counter exists runs the grid form (one CTA per query tile), which
+ * PA_FLAG_PREFIX_GRID also selects; both give the same bits.  Calls on
+ * different streams that overlap in time share (and race on) the counter. */
 typedef struct {
     void* out;
     const void* q;
@@ -374,7 +390,9 @@ int pa_prefix_ex(const pa_prefix_args* args, const pa_decode_opts* opts, pa_stre
  * [0, N] forces that split.  The workspace (caller-owned device memory,
  * 256-byte aligned, contents need no initialisation) must hold
  * pa_prefix_split_workspace_size bytes for the same arguments and split;
- * the call allocates nothing.  With PA_FLAG_PREFIX_WARP_MMA nothing is split
+ * the call allocates nothing but the persistent form's counter (see
+ * pa_prefix), whose parts are units like the whole tiles.  With
+ * PA_FLAG_PREFIX_WARP_MMA nothing is split
  * and this is pa_prefix_ex.  Errors as pa_prefix_ex, plus PA_ERR_INVALID_ARG
  * for a workspace that is missing, too small or misaligned, or a split out
  * of range. */

@@ -44,6 +44,7 @@ PA_FLAG_PREFIX_WARP_MMA = 2
 PA_FLAG_POOLED = 4
 PA_FLAG_DETERMINISTIC = 8
 PA_FLAG_UNIFORM_LENGTHS = 16
+PA_FLAG_PREFIX_GRID = 32
 
 
 class pa_decode_args(ctypes.Structure):

@@ -831,6 +831,38 @@ size_t prefix_split_bytes(const PrefixSplit& sp, int head_dim) {
            align_up((size_t)sp.units * sp.parts * pa::kPrefixTileRows * 2 * 4, kWsAlign);
 }
 
+// The persistent prefill's claim counter and finish count, one pair per
+// device, zeroed once here; each call's last CTA re-arms them.
+std::mutex g_sched_mutex;
+unsigned int* g_sched[kMaxDevices];
+
+bool prefix_sched_ready() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_sched_mutex);
+    return g_sched[dev] != nullptr;
+}
+
+int ensure_prefix_sched(unsigned int** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_sched_mutex);
+    if (!g_sched[dev]) {
+        void* p = nullptr;
+        if (cudaMalloc(&p, 256) != cudaSuccess) {
+            cudaGetLastError();
+            return PA_ERR_OOM;
+        }
+        if (cudaMemset(p, 0, 256) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+            cudaFree(p);
+            return PA_ERR_CUDA;
+        }
+        g_sched[dev] = static_cast<unsigned int*>(p);
+    }
+    *out = g_sched[dev];
+    return PA_OK;
+}
+
 // split_call: pa_prefix_split (the key split of `split`, or the plan's,
 // into workspace `ws`); otherwise pa_prefix / pa_prefix_ex.
 int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t stream, bool split_call = false,
@@ -891,6 +923,7 @@ int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t st
     prm.trace = g_trace;
     const int tile_tokens = (warp_mma ? 64 : 128) / prm.group;
     dim3 grid((a->max_query_len + tile_tokens - 1) / tile_tokens, a->num_kv_heads, a->num_seqs);
+    prm.tiles_per_seq = static_cast<int>(grid.x);
     if (sp.parts) {  // a 1-D grid of units (see PrefixParams::split_parts)
         prm.split_whole = sp.whole;
         prm.split_parts = sp.parts;
@@ -898,6 +931,23 @@ int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t st
         prm.split_o = static_cast<float*>(ws);
         prm.split_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + prefix_split_o_bytes(sp, a->head_dim));
         grid = dim3(sp.whole + sp.units * sp.parts, 1, 1);
+    }
+    if (!warp_mma && !(o && (o->flags & PA_FLAG_PREFIX_GRID))) {
+        // the persistent form: the same units, claimed by a grid the SMs hold
+        // at once.  Its counter is allocated by the first such call on the
+        // device; a call made while the stream is being captured before that
+        // keeps the grid form (allocating would break the capture).
+        int num_sms = 0;
+        if (query_sm_count(&num_sms) != PA_OK) return PA_ERR_CUDA;
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return PA_ERR_CUDA;
+        if (cap == cudaStreamCaptureStatusNone || prefix_sched_ready()) {
+            if ((rc = ensure_prefix_sched(&prm.sched))) return rc;
+            const long long units = (long long)grid.x * grid.y * grid.z;
+            const long long slots = (long long)num_sms * pa::prefix_tc_ctas_per_sm(a->head_dim);
+            prm.total_units = static_cast<int>(units);
+            grid = dim3(static_cast<unsigned>(units < slots ? units : slots), 1, 1);
+        }
     }
     if (o && o->event_partition_begin &&
         cudaEventRecord(static_cast<cudaEvent_t>(o->event_partition_begin), stream) != cudaSuccess)
@@ -1104,6 +1154,15 @@ void pa_release_workspace(void) {
         }
         g_ws[d] = nullptr;
         g_ws_bytes[d] = 0;
+    }
+    std::lock_guard<std::mutex> lock_sched(g_sched_mutex);
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (!g_sched[d]) continue;
+        if (cudaSetDevice(d) == cudaSuccess) {
+            cudaDeviceSynchronize();
+            cudaFree(g_sched[d]);
+        }
+        g_sched[d] = nullptr;
     }
     if (have_cur) cudaSetDevice(cur);
 }

@@ -31,6 +31,12 @@ struct PrefixParams {
     int tiles_per_seq = 0;
     float* split_o = nullptr;       // [R][split_parts][128 rows][D]: O relative to 2^m
     float* split_ml = nullptr;      // [R][split_parts][128 rows][2]: m (scaled, log2), l
+    // Persistent form of the tcgen05 kernel (sched != nullptr): a fixed grid
+    // whose CTAs claim the total_units units (numbered as the CTAs above,
+    // tiles_per_seq set in either form) from the counter sched[0]; sched[1]
+    // counts the CTAs that finished, and the last one re-arms both to zero.
+    unsigned int* sched = nullptr;
+    int total_units = 0;
     // Diagnostic builds (-DPA_TRACE) only: the tcgen05 kernel records
     // SM clock stamps of its pipeline events, kPrefixTraceIters x 16 per CTA
     // (the last of the kPrefixTraceIters records holds the CTA's phases in
@@ -48,6 +54,8 @@ cudaError_t launch_prefix(int head_dim, const PrefixParams& prm, const CUtensorM
 // The tcgen05 version: 128-row tiles (floor(128 / G) tokens); its V maps are
 // whole-block views (3-D cache, 4-D chunk) whose box is one block.
 int prefix_tc_smem_bytes(int head_dim);
+// CTAs of the tcgen05 kernel one SM holds at once (shared and tensor memory).
+int prefix_tc_ctas_per_sm(int head_dim);
 cudaError_t launch_prefix_tc(int head_dim, const PrefixParams& prm, const CUtensorMap* maps, dim3 grid,
                              cudaStream_t stream);
 // Rows rounded up by the tcgen05 kernel's tiles (the MMA M), for the split workspace.

@@ -6,10 +6,11 @@ microseconds per call, useful TFLOP/s (score and P.V multiply-adds over the
 visible keys only, see workloads.PrefixWorkload.flops) and the fraction of
 the measured dense 16-bit tensor-core peak.
 
-    python -m paged_kv_cache_308_gb300.prefix_bench [--impl tcgen05|tcgen05_split|warp_mma|all] [--iters N] [workload ...]
+    python -m paged_kv_cache_308_gb300.prefix_bench [--impl NAME|all] [--iters N] [workload ...]
 
 tcgen05_split is pa_prefix_split (the last round's query tiles split by key
-range) under the library's plan.
+range) under the library's plan; both run the tcgen05 kernel's default
+persistent form, the _grid variants its grid form (PA_FLAG_PREFIX_GRID).
 """
 from __future__ import annotations
 
@@ -22,7 +23,11 @@ import torch
 from . import binding as pb
 from . import workloads as W
 
-IMPLS = {"tcgen05": 0, "tcgen05_split": 0, "warp_mma": pb.PA_FLAG_PREFIX_WARP_MMA}
+# name: (option flags, through pa_prefix_split)
+IMPLS = {"tcgen05": (0, False), "tcgen05_split": (0, True),
+         "tcgen05_grid": (pb.PA_FLAG_PREFIX_GRID, False),
+         "tcgen05_split_grid": (pb.PA_FLAG_PREFIX_GRID, True),
+         "warp_mma": (pb.PA_FLAG_PREFIX_WARP_MMA, False)}
 FALLBACK_TENSOR_TFLOPS = 1900.0
 
 
@@ -68,7 +73,8 @@ def measure(names, impls, iters: int, warmup: int, device) -> list:
     for name in names:
         w = W.make_prefix_config(name, device=device)
         for impl in impls:
-            t = time_prefix(w, IMPLS[impl], iters, warmup, split=impl == "tcgen05_split")
+            flags, split = IMPLS[impl]
+            t = time_prefix(w, flags, iters, warmup, split=split)
             tf = w.flops / t / 1e12
             rows.append({"workload": name, "kernel": impl, "us_per_call": t * 1e6, "tflops": tf,
                          "frac_of_tensor_peak": tf / peak, "peak_tflops": peak, "peak_kind": kind,
@@ -80,7 +86,7 @@ def measure(names, impls, iters: int, warmup: int, device) -> list:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--impl", choices=["tcgen05", "tcgen05_split", "warp_mma", "all"], default="all")
+    ap.add_argument("--impl", choices=list(IMPLS) + ["all"], default="all")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("workloads", nargs="*", default=W.PREFIX_CONFIG_NAMES)

@@ -29,8 +29,10 @@ def dev():
     return torch.device("cuda:0")
 
 
-# the tcgen05 (tensor-memory) kernel is the default; the warp-level MMA kernel on request
-IMPLS = {"tcgen05": {}, "warp_mma": {"flags": pb.PA_FLAG_PREFIX_WARP_MMA}}
+# the tcgen05 (tensor-memory) kernel is the default (its persistent form), its
+# grid form and the warp-level MMA kernel on request
+IMPLS = {"tcgen05": {}, "tcgen05_grid": {"flags": pb.PA_FLAG_PREFIX_GRID},
+         "warp_mma": {"flags": pb.PA_FLAG_PREFIX_WARP_MMA}}
 
 
 @pytest.fixture(params=list(IMPLS))
