@@ -139,3 +139,38 @@ def test_persistent_replays_from_a_cuda_graph(dev):
         g.replay()
         _check(out)
         assert torch.equal(out, ref)
+
+
+_CAPTURE_FIRST = r"""
+import sys, torch
+sys.path.insert(0, {root!r})
+from paged_kv_cache_308_gb300 import binding as pb, workloads as W
+dev = torch.device("cuda:0")
+w = W.make_prefix_workload("p", [900, 40], [70, 33], num_blocks=80, seed=23, device=dev)
+ref = pb.prefix_workload(w, flags=pb.PA_FLAG_PREFIX_GRID)  # kernel attributes set; no counter yet
+torch.cuda.synchronize()
+out = torch.full_like(w.q, float("nan"))
+s = torch.cuda.Stream(device=dev)
+s.wait_stream(torch.cuda.current_stream(dev))
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):
+    pb.prefix_workload(w, out=out, stream=s)  # captured before the counter exists: the grid form
+g.replay()
+torch.cuda.synchronize()
+assert pb.pa_get_device_status() == 0
+assert torch.equal(out, ref)
+fresh = pb.prefix_workload(w)  # outside a capture: allocates the counter, persistent form
+torch.cuda.synchronize()
+assert torch.equal(fresh, ref)
+print("ok")
+"""
+
+
+def test_capture_before_the_counter_exists_keeps_the_grid_form(dev):
+    # a fresh process: the counter is per process and device, and this one has it already
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _CAPTURE_FIRST.format(root=root)], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
