@@ -535,3 +535,23 @@ def test_workspace_bound_covers_every_automatic_plan_property():
         if rc != pb.PA_OK:
             continue
         assert pb.pa_decode_workspace_size(B, L, H, D, 0) >= pl["workspace_bytes"], (B, L, H, hkv, D, flags, mode, pl)
+
+
+def test_many_short_pairs_take_2x2_ctas():
+    # at least 64 (sequence, kv head) pairs of at most 16K tokens in 512-token
+    # partitions, head_dim >= 128: 2x2 CTAs; the named batches keep their shapes
+    def shape(B, L, Hkv=4, H=24, D=256, **kw):
+        rc, pl = plan(args(num_seqs=B, max_seq_len=L, num_blocks=B * L // 16 + 10, Hkv=Hkv, H=H, D=D), **kw)
+        assert rc == 0
+        return pl["partition_size"], (pl["threads"] // 32, pl["stages"])
+    assert shape(32, 4096) == (512, (2, 2))
+    assert shape(16, 16384) == (512, (2, 2))
+    assert shape(100, 1500) == (512, (2, 2))
+    assert shape(8, 8192, Hkv=8, H=32, D=128) == (512, (2, 2))
+    # below the pair count, above the length, or a caller's partition size: the wave model's choice
+    assert shape(15, 8192) == (512, (1, 3))
+    assert shape(16, 16385) == (512, (1, 3))
+    assert shape(32, 4096, mode=pb.PA_MODE_SPLIT, partition_size=256) == (256, (1, 3))
+    assert shape(4, 32768) == (512, (1, 3))      # b4_l32768_peaked
+    assert shape(64, 32768) == (512, (1, 2))     # b64_loguniform
+    assert shape(8, 8192) == (512, (2, 2))       # b8_u8192 (the wave model's pick)
