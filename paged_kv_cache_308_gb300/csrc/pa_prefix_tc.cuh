@@ -372,7 +372,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
     PA_TC_PHASE(0);
     PA_TC_PHASE(7);
     const int G = prm.group, H = prm.num_heads;
-    TcUnit u0;  // grid form: the CTA's unit
+    TcUnit u0{};  // grid form: the CTA's unit
     if (!persist) {
         u0 = tc_unit(prm, c0, t == 0);
         if (!u0.run) return;
@@ -460,6 +460,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
             if (id >= 0) sm_units[s] = d;
             mbar_arrive(bar(kTcBarUnitFull + s));
         }
+        __syncwarp();  // lane 0's slot writes are visible to the warp
         id = __shfl_sync(kFull, id, 0);
         if (persist && u > 0 && id >= 0) {
             // the claimed tile's Q rows (per token, the G heads' rows are
