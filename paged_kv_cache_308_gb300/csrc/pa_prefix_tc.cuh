@@ -72,8 +72,9 @@ struct PrefixTcShape {
     static constexpr int kTileBytes = kTcKeys * D * 2;          // K or V of one key tile
     static constexpr int kChunkStride = kTcKeys * 128;          // one 64-column chunk of a K tile
     static constexpr int kBlockBytes = kBlockSize * D * 2;      // one block of a V tile: [chunk][16][128 B]
-    // barriers, TMEM address, abort flag, 2 unit ids, 2 decoded units
-    static constexpr int kCtrlBytes = kTcBars * 8 + 16 + 128;
+    // barriers, TMEM address, abort flag, 2 unit ids, 2 decoded units, the
+    // row warps' copies of their current unit
+    static constexpr int kCtrlBytes = kTcBars * 8 + 16 + 128 + 4 * 64;
     // ring slots: 7 tiles of 32 KB fill the shared memory at head_dim 256
     static constexpr int kKSlots = 4;
     static constexpr int kVSlots = D == 256 ? 3 : 4;
@@ -355,6 +356,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
     volatile int* sm_abort = reinterpret_cast<volatile int*>(tslot + 1);
     volatile int* sm_unit = reinterpret_cast<volatile int*>(tslot + 2);  // 2 unit id slots
     TcUnit* sm_units = reinterpret_cast<TcUnit*>(tslot + 4);             // their decoded units
+    TcUnit* rows_units = reinterpret_cast<TcUnit*>(reinterpret_cast<uint8_t*>(sm_units) + 128);  // one per row warp
     const uint32_t bar0 = smem_addr(bars);
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -802,8 +804,11 @@ __global__ void __maxnreg__(kTcMaxRegs)
         if (rc >= 0) load_q(cur);
         PA_TC_PHASE(2);
         for (int g = 0, uq = 0; ok && rc >= 0; ++uq) {
+            // the fields the epilogue needs wait in shared memory, not in
+            // registers, while the tile loop runs
+            if (lane == 0) rows_units[warp] = cur;
+            __syncwarp();
             const int my_tok = cur.t0 + ti;  // chunk token index of the row
-            const bool row_real = ti < kTcRows / G && my_tok < cur.qlen;
             const int n = cur.n, jb = cur.jb, nctx = cur.nctx, C = cur.C;
             float m = -INFINITY, l = 0.f;  // reference max (scaled, log2 domain) and exp sum
             for (int j = 0; j < n; ++j) {
@@ -897,9 +902,11 @@ __global__ void __maxnreg__(kTcMaxRegs)
             // Where this row's result goes (the unit's fields are dead after
             // the next unit is taken): the fp16 output row, or the part's
             // partial slot of a key split
-            const int part = cur.part;
-            const size_t slot = part >= 0 ? ((size_t)cur.unit_r * prm.split_parts + part) * kTcRows + t : 0;
-            __half* orow_h = prm.out + ((size_t)(cur.q0 + my_tok) * H + cur.kvh * G + (t % G)) * D;
+            const TcUnit cu = rows_units[warp];
+            const bool row_real = ti < kTcRows / G && cu.t0 + ti < cu.qlen;
+            const int part = cu.part;
+            const size_t slot = part >= 0 ? ((size_t)cu.unit_r * prm.split_parts + part) * kTcRows + t : 0;
+            __half* orow_h = prm.out + ((size_t)(cu.q0 + cu.t0 + ti) * H + cu.kvh * G + (t % G)) * D;
             // The next unit's Q goes into TMEM while this unit's last P.Vs run:
             // its S MMAs then start while the rows store this unit's O.
             TcUnit nxt;
