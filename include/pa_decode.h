@@ -372,12 +372,12 @@ int pa_prefix(void* out, const void* q, const void* k_new, const void* v_new, co
 int pa_prefix_ex(const pa_prefix_args* args, const pa_decode_opts* opts, pa_stream_t stream);
 
 /* Chunked prefill with the last wave's query tiles split by key range.
- * The tensor-core prefill kernel runs one CTA per SM per (query tile, kv
- * head, sequence), and every CTA walks all of its sequence's keys, so the
- * CTAs take about the same time and a grid of N of them on S SMs runs in
+ * The tensor-core prefill kernel works on one (query tile, kv head,
+ * sequence) at a time per SM, and every tile walks all of its sequence's
+ * keys, so the tiles take about the same time and N of them on S SMs run in
  * ceil(N / S) rounds.  When the last round is partly empty, its trailing
  * query tiles (`units`, counted in the grid's order: tile fastest, then kv
- * head, then sequence) each run as `parts` CTAs, CTA p walking the p-th of
+ * head, then sequence) each run as `parts` units, part p walking the p-th of
  * `parts` consecutive ranges of the tile's key tiles and leaving, per row,
  * the online-softmax state (m, l, O relative to 2^m) in the workspace; a
  * second kernel then merges a row's parts with the log-sum-exp rule of the
