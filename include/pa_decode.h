@@ -327,8 +327,10 @@ void pa_release_workspace(void);
  * caches and block table as for pa_decode.  max_context_len and max_query_len
  * are host-side bounds that size the grid.  The new tokens' K/V are read from
  * k_new/v_new, not from the cache (the caller appends them afterwards).
- * Same support, alignment, ownership and error rules as pa_decode.
- * Device-detected bad lengths set PA_DEV_BAD_SEQ_LEN.
+ * Same support, alignment, ownership and error rules as pa_decode; a call
+ * whose query tiles (of floor(128 / G) tokens) x kv heads x sequences reach
+ * 2^31 returns PA_ERR_UNSUPPORTED.  Device-detected bad lengths set
+ * PA_DEV_BAD_SEQ_LEN.
  * The tensor-core kernel runs in a persistent form by default: a grid of the
  * CTAs the SMs hold at once claims the query tiles in grid order from a
  * library-owned device counter (256 bytes per device, allocated and zeroed by

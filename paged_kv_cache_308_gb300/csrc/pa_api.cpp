@@ -765,6 +765,11 @@ int validate_prefix(const pa_prefix_args* a, const pa_decode_opts* o) {
     if ((long long)a->max_context_len > (long long)a->max_blocks_per_seq * a->block_size) return PA_ERR_INVALID_ARG;
     if (a->num_blocks * a->num_kv_heads * a->block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     if (a->num_tokens > 0 && a->max_query_len == 0) return PA_ERR_INVALID_ARG;
+    // the kernels number their units (query tiles x kv heads x sequences,
+    // tiles of at least 128 / G tokens) in 32 bits
+    const long long tile_tokens = 128 / (a->num_heads / a->num_kv_heads);
+    if ((a->max_query_len + tile_tokens - 1) / tile_tokens * a->num_kv_heads * a->num_seqs >= (1ll << 31))
+        return PA_ERR_UNSUPPORTED;
     if (a->num_seqs == 0 || a->num_tokens == 0) return PA_OK;
     if (!a->out || !a->q || !a->k_new || !a->v_new || !a->k_cache || !a->v_cache || !a->block_tables ||
         !a->context_lens || !a->query_start_loc)

@@ -555,3 +555,17 @@ def test_many_short_pairs_take_2x2_ctas():
     assert shape(4, 32768) == (512, (1, 3))      # b4_l32768_peaked
     assert shape(64, 32768) == (512, (1, 2))     # b64_loguniform
     assert shape(8, 8192) == (512, (2, 2))       # b8_u8192 (the wave model's pick)
+
+
+def test_prefix_refuses_a_unit_count_past_32_bits():
+    # 200 query tiles of 128 tokens x 256 kv heads x 65535 sequences: 3.4e9 units,
+    # refused before any CUDA call
+    a = pb.pa_prefix_args(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 65535, 65535 * 25600, 0, 0, 25600,
+                          0, 256, 256, 128, 16, 1 / 16)
+    assert pb.lib.pa_prefix_ex(ctypes.byref(a), None, None) == pb.PA_ERR_UNSUPPORTED
+    n = ctypes.c_size_t(7)
+    assert pb.lib.pa_prefix_split_workspace_size(ctypes.byref(a), None, ctypes.byref(n)) == pb.PA_ERR_UNSUPPORTED
+    # one sequence fewer tiles: accepted up to the device (none here)
+    b = prefix_args()
+    assert pb.lib.pa_prefix_split_workspace_size(ctypes.byref(b), ctypes.byref(pb.pa_prefix_split_opts(3, 96)),
+                                                 ctypes.byref(n)) == pb.PA_OK
