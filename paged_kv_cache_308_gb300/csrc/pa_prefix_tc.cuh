@@ -3,9 +3,12 @@
 //
 // Same operation and inputs as pa_prefix_kernel (see pa_prefix_kernel.cuh).
 // Mapping:
-// * one CTA per (query tile, kv head, sequence); the tile is 128 rows of
-//   (new token, GQA head) pairs = floor(128 / G) tokens.  Three roles in
-//   separate warps, handing over only through mbarriers:
+// * a unit of work is a (query tile, kv head, sequence); the tile is 128 rows
+//   of (new token, GQA head) pairs = floor(128 / G) tokens.  By default a grid
+//   of the CTAs the SMs hold at once claims the units from a device counter
+//   (the persistent form; the grid form runs one CTA per unit), and each CTA's
+//   rings and barrier phases run on from one unit to the next.  Three roles
+//   in separate warps, handing over only through mbarriers:
 //   - warps 0-3 (softmax): thread t owns row t (= TMEM lane t); it turns its
 //     score row into P (fp16) with the online-softmax update and rescales
 //     its O row in TMEM when its max moves;
@@ -24,7 +27,8 @@
 //     while the rows work on tile j, with no hand-over from the rows first;
 // * keys are walked in tiles of 64 (4 blocks of 16: paged context blocks
 //   through the block table, then the chunk's own blocks), K tiles in a
-//   3-slot ring and V tiles in a 2-slot ring, all with the 128-byte swizzle:
+//   4-slot ring and V tiles in a 3-slot ring (4 below head_dim 256), all with
+//   the 128-byte swizzle:
 //   a K block as one 16-row box per 64 head_dim columns (the S operand needs
 //   the 64 keys of a tile contiguous per column chunk), a V block as a single
 //   box laid out [chunk][16 rows][128 B] (one P.V MMA per block reads it);
