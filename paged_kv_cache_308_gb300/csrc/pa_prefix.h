@@ -54,7 +54,7 @@ cudaError_t launch_prefix(int head_dim, const PrefixParams& prm, const CUtensorM
 // The tcgen05 version: 128-row tiles (floor(128 / G) tokens); its V maps are
 // whole-block views (3-D cache, 4-D chunk) whose box is one block.
 int prefix_tc_smem_bytes(int head_dim);
-// CTAs of the tcgen05 kernel one SM holds at once (shared and tensor memory).
+// CTAs of the tcgen05 kernel one SM holds at once (shared and tensor memory, registers).
 int prefix_tc_ctas_per_sm(int head_dim);
 cudaError_t launch_prefix_tc(int head_dim, const PrefixParams& prm, const CUtensorMap* maps, dim3 grid,
                              cudaStream_t stream);

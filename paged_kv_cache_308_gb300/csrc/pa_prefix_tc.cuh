@@ -1083,7 +1083,9 @@ constexpr int tc_ctas_per_sm() {
     constexpr int by_smem = (228 * 1024) / (PrefixTcShape<D>::kSmemBytes + 1024);
     constexpr int by_tmem = 512 / PrefixTcShape<D>::kTmemCols;
     constexpr int by_threads = 2048 / kTcThreads;
-    return by_smem < by_tmem ? (by_smem < by_threads ? by_smem : by_threads) : (by_tmem < by_threads ? by_tmem : by_threads);
+    constexpr int by_regs = 65536 / (kTcThreads * kTcMaxRegs);  // the kernel may use all kTcMaxRegs
+    constexpr int a = by_smem < by_tmem ? by_smem : by_tmem, b = by_threads < by_regs ? by_threads : by_regs;
+    return a < b ? a : b;
 }
 }  // namespace
 
