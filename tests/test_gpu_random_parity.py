@@ -169,3 +169,22 @@ def test_random_large_auto_case(dev, i):
     assert pb.pa_get_device_status() == 0
     assert_parity(out, oracle_ref(w), f"large case {i}: B={len(c['lens'])} max={max(c['lens'])} "
                                       f"H={c['num_heads']}/{c['num_kv_heads']} D={c['head_dim']}")
+
+
+@pytest.mark.parametrize("B,L,H,Hkv,D", [(64, 4096, 24, 4, 256), (16, 16384, 32, 8, 128)])
+def test_many_short_pairs_run_2x2_ctas(dev, B, L, H, Hkv, D):
+    # at least 64 (sequence, kv head) pairs of at most 16K tokens: AUTO picks
+    # 2x2 CTAs over 512-token partitions; ragged lengths, NaN past each end
+    g = torch.Generator().manual_seed(B * L + D)
+    lens = torch.randint(1, L + 1, (B,), generator=g).tolist()
+    w = W.make_workload(f"pairs_{B}x{L}", lens, num_heads=H, num_kv_heads=Hkv, head_dim=D,
+                        num_blocks=sum((x + 15) // 16 for x in lens) + 3, seed=B + D, device=dev,
+                        scale=D ** -0.5, tail_fill=float("nan"))
+    out = torch.empty_like(w.q)
+    plan = pb.pa_decode_plan(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.num_heads,
+                             w.num_kv_heads, w.head_dim, w.block_size, w.scale, max_seq_len=w.max_seq_len)
+    assert (plan["mode"], plan["partition_size"], plan["threads"] // 32, plan["stages"]) == (pb.PA_MODE_SPLIT, 512, 2, 2)
+    out = pb.decode_workload(w)
+    torch.cuda.synchronize()
+    assert pb.pa_get_device_status() == 0
+    assert_parity(out, oracle_ref(w), f"{B} x U[1, {L}] H={H}/{Hkv} D={D}")
