@@ -333,13 +333,16 @@ void pa_release_workspace(void);
  * PA_DEV_BAD_SEQ_LEN.
  * The tensor-core kernel runs in a persistent form by default: a grid of the
  * CTAs the SMs hold at once claims the query tiles in grid order from a
- * library-owned device counter (256 bytes per device, allocated and zeroed by
- * the first such call on the device, re-armed by every call, freed by
- * pa_release_workspace), and each CTA's copy rings run on from one tile to
- * the next.  A call made while its stream is being captured before that
- * counter exists runs the grid form (one CTA per query tile), which
- * PA_FLAG_PREFIX_GRID also selects; both give the same bits.  Calls on
- * different streams that overlap in time share (and race on) the counter. */
+ * library-owned device counter, and each CTA's copy rings run on from one
+ * tile to the next.  There is one counter (256 bytes) per device and stream,
+ * allocated and zeroed on the stream by the first such call on it, re-armed
+ * by every call and freed by pa_release_workspace; calls on one stream never
+ * overlap, so they never share it while running.  A call made while its
+ * stream is being captured before that stream's counter exists runs the grid
+ * form (one CTA per query tile), which PA_FLAG_PREFIX_GRID also selects; both
+ * give the same bits.  A captured call keeps the counter of the stream it was
+ * captured on: replays of that graph must not overlap one another or other
+ * calls on that stream. */
 typedef struct {
     void* out;
     const void* q;

@@ -14,7 +14,9 @@
 #include <string.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "pa_internal.h"
 #include "pa_prefix.h"
@@ -854,34 +856,38 @@ size_t prefix_split_bytes(const PrefixSplit& sp, int head_dim) {
 }
 
 // The persistent prefill's claim counter and finish count, one pair per
-// device, zeroed once here; each call's last CTA re-arms them.
+// (device, stream), zeroed on the stream when first used; each call's last
+// CTA re-arms them.  Calls on one stream never overlap, so no two running
+// grids share a pair.
 std::mutex g_sched_mutex;
-unsigned int* g_sched[kMaxDevices];
+std::map<std::pair<int, uintptr_t>, unsigned int*> g_sched;
 
-bool prefix_sched_ready() {
+bool prefix_sched_ready(cudaStream_t stream) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
     std::lock_guard<std::mutex> lock(g_sched_mutex);
-    return g_sched[dev] != nullptr;
+    return g_sched.count({dev, reinterpret_cast<uintptr_t>(stream)}) != 0;
 }
 
-int ensure_prefix_sched(unsigned int** out) {
+int ensure_prefix_sched(cudaStream_t stream, unsigned int** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_sched_mutex);
-    if (!g_sched[dev]) {
+    const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
+    auto it = g_sched.find(key);
+    if (it == g_sched.end()) {
         void* p = nullptr;
         if (cudaMalloc(&p, 256) != cudaSuccess) {
             cudaGetLastError();
             return PA_ERR_OOM;
         }
-        if (cudaMemset(p, 0, 256) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        if (cudaMemsetAsync(p, 0, 256, stream) != cudaSuccess) {
             cudaFree(p);
             return PA_ERR_CUDA;
         }
-        g_sched[dev] = static_cast<unsigned int*>(p);
+        it = g_sched.emplace(key, static_cast<unsigned int*>(p)).first;
     }
-    *out = g_sched[dev];
+    *out = it->second;
     return PA_OK;
 }
 
@@ -957,14 +963,14 @@ int run_prefix(const pa_prefix_args* a, const pa_decode_opts* o, cudaStream_t st
     if (!warp_mma && !(o && (o->flags & PA_FLAG_PREFIX_GRID))) {
         // the persistent form: the same units, claimed by a grid the SMs hold
         // at once.  Its counter is allocated by the first such call on the
-        // device; a call made while the stream is being captured before that
+        // stream; a call made while the stream is being captured before that
         // keeps the grid form (allocating would break the capture).
         int num_sms = 0;
         if (query_sm_count(&num_sms) != PA_OK) return PA_ERR_CUDA;
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return PA_ERR_CUDA;
-        if (cap == cudaStreamCaptureStatusNone || prefix_sched_ready()) {
-            if ((rc = ensure_prefix_sched(&prm.sched))) return rc;
+        if (cap == cudaStreamCaptureStatusNone || prefix_sched_ready(stream)) {
+            if ((rc = ensure_prefix_sched(stream, &prm.sched))) return rc;
             const long long units = (long long)grid.x * grid.y * grid.z;
             const long long slots = (long long)num_sms * pa::prefix_tc_ctas_per_sm(a->head_dim);
             prm.total_units = static_cast<int>(units);
@@ -1178,14 +1184,13 @@ void pa_release_workspace(void) {
         g_ws_bytes[d] = 0;
     }
     std::lock_guard<std::mutex> lock_sched(g_sched_mutex);
-    for (int d = 0; d < kMaxDevices; ++d) {
-        if (!g_sched[d]) continue;
-        if (cudaSetDevice(d) == cudaSuccess) {
+    for (const auto& e : g_sched) {
+        if (cudaSetDevice(e.first.first) == cudaSuccess) {
             cudaDeviceSynchronize();
-            cudaFree(g_sched[d]);
+            cudaFree(e.second);
         }
-        g_sched[d] = nullptr;
     }
+    g_sched.clear();
     if (have_cur) cudaSetDevice(cur);
 }
 

@@ -174,3 +174,27 @@ def test_capture_before_the_counter_exists_keeps_the_grid_form(dev):
     r = subprocess.run([sys.executable, "-c", _CAPTURE_FIRST.format(root=root)], capture_output=True, text=True,
                        timeout=300)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
+def test_concurrent_calls_on_two_streams(dev):
+    # each stream has its own counter: two persistent calls in flight at once,
+    # on different workloads, both give the grid form's bits
+    a = W.make_prefix_workload("a", [3000, 17, 250], [300, 41, 129], num_blocks=240, seed=31, device=dev)
+    b = W.make_prefix_workload("b", [900, 0, 4000, 64], [64, 200, 90, 7], num_blocks=340, seed=32, device=dev)
+    ref_a, ref_b = _plain(a, flags=GRID), _plain(b, flags=GRID)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    out_a, out_b = torch.empty_like(a.q), torch.empty_like(b.q)
+    for s in (s1, s2):
+        s.wait_stream(torch.cuda.current_stream(dev))
+    for _ in range(5):
+        out_a.fill_(float("nan"))
+        out_b.fill_(float("nan"))
+        s1.wait_stream(torch.cuda.current_stream(dev))
+        s2.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s1):
+            pb.prefix_workload(a, out=out_a, stream=s1)
+        with torch.cuda.stream(s2):
+            pb.prefix_workload(b, out=out_b, stream=s2)
+        torch.cuda.synchronize()
+        assert pb.pa_get_device_status() == 0
+        assert torch.equal(out_a, ref_a) and torch.equal(out_b, ref_b)
