@@ -569,3 +569,14 @@ def test_prefix_refuses_a_unit_count_past_32_bits():
     b = prefix_args()
     assert pb.lib.pa_prefix_split_workspace_size(ctypes.byref(b), ctypes.byref(pb.pa_prefix_split_opts(3, 96)),
                                                  ctypes.byref(n)) == pb.PA_OK
+
+
+def test_binding_constants_match_the_header():
+    # every PA_MODE_*, PA_FLAG_*, PA_ERR_* and PA_DEV_* enumerator of the header
+    # exists in the binding with the same value
+    import re
+    text = re.sub(r"/\*.*?\*/", "", open(pb.HEADER_PATH).read(), flags=re.S)
+    consts = {k: int(v) for k, v in re.findall(r"\b(PA_(?:MODE|FLAG|ERR|DEV)_[A-Z0-9_]+)\s*=\s*(-?\d+)", text)}
+    assert {"PA_FLAG_PREFIX_GRID", "PA_FLAG_UNIFORM_LENGTHS", "PA_MODE_FLAT", "PA_DEV_TIMEOUT"} <= set(consts)
+    for k, v in consts.items():
+        assert getattr(pb, k) == v, k
